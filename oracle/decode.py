@@ -1,0 +1,208 @@
+"""Float64 CPU oracle for single-token decode attention over a paged KV cache.
+
+TEST INFRASTRUCTURE ONLY. Nothing in the product path imports, calls or links
+this module: only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` use it. It shares no code with the CUDA path.
+
+What it computes is the plain definition, written out without blocking,
+fusion or reordering:
+
+  for each sequence b, query head h, logical token j < ctx_b:
+      phys  = block_tables[b, j // P]                 (paged addressing)
+      slot  = j %  P
+      K_j   = k_cache[phys, slot, h // G, :]           (contiguous grouping, G = Hq / Hkv)
+      V_j   = v_cache[phys, slot, h // G, :]
+      s_j   = scale * <q[b, h], K_j>
+  m = max_j s_j;  Z = sum_j exp(s_j - m)
+  out[b, h] = sum_j exp(s_j - m) V_j / Z,   lse[b, h] = m + ln Z   (natural log)
+
+Sources (web pages this library follows):
+  * "From MHA to MLA: KV Caches and Attention Kernels" (g-u-n.github.io),
+    section 2 (head mapping h -> h // G), section 3 (grouped decode: masked
+    rows, online softmax whose end result is the expression above, LSE),
+    section 4 (Flash-Decoding: per-split normalized output O_s and L_s and the
+    weighted combine), section 5 (paged addressing: logical page n // P,
+    offset n - page * P, physical page from the block table), section 6
+    (absorbed MLA: score = content dot + rope dot, value = latent only).
+  * "L2 讲解：paged decode attention 与 GQA" (kzhou003.github.io gpu-kernel-drills),
+    section ④ (page loop: num_pages = cdiv(ctx, PAGE), phys looked up per
+    page, last page masked) and the pitfalls list (contiguous grouping).
+  * FlashMLA-ETAP README, "Supported configurations" and "Usage": K and V share
+    one 576-wide cache tensor, head_dim_v = 512, lse is float32 log-sum-exp.
+
+Inputs are the 16-bit bit patterns produced by the shared input generator; the
+oracle widens them exactly to float64 itself.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+FP16 = "fp16"
+BF16 = "bf16"
+
+
+# --------------------------------------------------------------------------------------
+# exact widening of stored 16-bit values
+# --------------------------------------------------------------------------------------
+def widen(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """16-bit patterns -> float64, exactly (fp16 via numpy's float16; bf16 = high half of a float32)."""
+    bits = np.asarray(bits, dtype=np.uint16)
+    if dtype == FP16:
+        return bits.view(np.float16).astype(np.float64)
+    if dtype == BF16:
+        return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    raise ValueError(dtype)
+
+
+# --------------------------------------------------------------------------------------
+# paged addressing ("From MHA to MLA", section 5; drill page, section ④)
+# --------------------------------------------------------------------------------------
+def num_pages(ctx: int, page_size: int) -> int:
+    """cdiv(ctx, PAGE): how many block-table entries a sequence of ``ctx`` tokens uses."""
+    return (int(ctx) + page_size - 1) // page_size
+
+
+def token_locations(block_table_row: np.ndarray, ctx: int, page_size: int):
+    """(physical block, slot) of logical tokens 0..ctx-1.
+
+    Logical token n lives on logical page n // P at offset n - (n // P) * P; the
+    block table maps the logical page to a physical block. Only the first
+    cdiv(ctx, P) table entries are read.
+    """
+    phys = []
+    slots = []
+    for n in range(int(ctx)):
+        logical_page = n // page_size
+        offset = n - logical_page * page_size
+        phys.append(int(block_table_row[logical_page]))
+        slots.append(offset)
+    return np.asarray(phys, dtype=np.int64), np.asarray(slots, dtype=np.int64)
+
+
+def gather_tokens(cache: np.ndarray, block_table_row: np.ndarray, ctx: int, page_size: int):
+    """Rows of ``cache[num_blocks, P, ...]`` for logical tokens 0..ctx-1, in token order."""
+    phys, slots = token_locations(block_table_row, ctx, page_size)
+    return cache[phys, slots]
+
+
+# --------------------------------------------------------------------------------------
+# attention over one gathered sequence ("From MHA to MLA", sections 2-3)
+# --------------------------------------------------------------------------------------
+def attend(q_rows: np.ndarray, keys: np.ndarray, values: np.ndarray, scale: float):
+    """softmax(scale * q K^T) V and its natural-log LSE, in float64.
+
+    q_rows [n, Dqk], keys [L, Dqk], values [L, Dv] (L >= 1) -> out [n, Dv], lse [n].
+    """
+    q_rows = np.asarray(q_rows, dtype=np.float64)
+    keys = np.asarray(keys, dtype=np.float64)
+    values = np.asarray(values, dtype=np.float64)
+    s = float(scale) * (q_rows @ keys.T)          # [n, L] scaled logits
+    m = s.max(axis=1)                              # row maximum
+    e = np.exp(s - m[:, None])
+    z = e.sum(axis=1)                              # softmax denominator
+    out = (e @ values) / z[:, None]
+    lse = m + np.log(z)
+    return out, lse
+
+
+# --------------------------------------------------------------------------------------
+# GQA / MQA / MHA paged decode
+# --------------------------------------------------------------------------------------
+def kv_head_of(h: int, num_q_heads: int, num_kv_heads: int) -> int:
+    """Contiguous grouping: query head h reads KV head h // G, G = Hq / Hkv."""
+    if num_q_heads % num_kv_heads:
+        raise ValueError("H_q must be divisible by H_kv")
+    return h // (num_q_heads // num_kv_heads)
+
+
+def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale, page_size, dtype,
+                 rows=None):
+    """Oracle for GQA/MQA/MHA decode over a paged cache.
+
+    q [B, Hq, D] (16-bit bits), k_cache/v_cache [NB, P, Hkv, D] (bits),
+    block_tables [B, max_blocks] int32, context_lens [B] int32 (>= 1).
+    rows: optional list of (b, h) pairs to evaluate (others left NaN).
+    Returns out [B, Hq, Dv] float64 and lse [B, Hq] float64.
+    """
+    B, Hq, _ = q.shape
+    Hkv = k_cache.shape[2]
+    Dv = v_cache.shape[3]
+    out = np.full((B, Hq, Dv), np.nan)
+    lse = np.full((B, Hq), np.nan)
+    wanted = None if rows is None else {(int(b), int(h)) for b, h in rows}
+    for b in range(B):
+        ctx = int(context_lens[b])
+        if ctx < 1:
+            raise ValueError("context length must be >= 1")
+        heads_by_kv = {}
+        for h in range(Hq):
+            if wanted is not None and (b, h) not in wanted:
+                continue
+            heads_by_kv.setdefault(kv_head_of(h, Hq, Hkv), []).append(h)
+        for kvh, heads in heads_by_kv.items():
+            keys = widen(gather_tokens(k_cache[:, :, kvh, :], block_tables[b], ctx, page_size), dtype)
+            vals = widen(gather_tokens(v_cache[:, :, kvh, :], block_tables[b], ctx, page_size), dtype)
+            o, l = attend(widen(q[b, heads, :], dtype), keys, vals, scale)
+            out[b, heads] = o
+            lse[b, heads] = l
+    return out, lse
+
+
+# --------------------------------------------------------------------------------------
+# absorbed MLA decode ("From MHA to MLA", section 6; FlashMLA-ETAP "Supported configurations")
+# --------------------------------------------------------------------------------------
+def mla_decode(q, kv_cache, block_tables, context_lens, scale, page_size, dtype,
+               head_dim_v=512, rows=None):
+    """Oracle for absorbed-MLA decode: every query head attends to one shared latent record.
+
+    q [B, Hq, Dqk] (content dims then rope dims), kv_cache [NB, P, Dqk] (bits).
+    Score = scale * (content dot + rope dot) = scale * <q, kv[:Dqk]>; value = kv[:head_dim_v].
+    """
+    B, Hq, Dqk = q.shape
+    out = np.full((B, Hq, head_dim_v), np.nan)
+    lse = np.full((B, Hq), np.nan)
+    wanted = None if rows is None else {(int(b), int(h)) for b, h in rows}
+    for b in range(B):
+        ctx = int(context_lens[b])
+        if ctx < 1:
+            raise ValueError("context length must be >= 1")
+        heads = [h for h in range(Hq) if wanted is None or (b, h) in wanted]
+        if not heads:
+            continue
+        record = widen(gather_tokens(kv_cache, block_tables[b], ctx, page_size), dtype)  # [L, Dqk]
+        qb = widen(q[b, heads, :], dtype)
+        content = float(scale) * (qb[:, :head_dim_v] @ record[:, :head_dim_v].T)
+        rope = float(scale) * (qb[:, head_dim_v:] @ record[:, head_dim_v:Dqk].T)
+        s = content + rope
+        m = s.max(axis=1)
+        e = np.exp(s - m[:, None])
+        z = e.sum(axis=1)
+        out[b, heads] = (e @ record[:, :head_dim_v]) / z[:, None]
+        lse[b, heads] = m + np.log(z)
+    return out, lse
+
+
+# --------------------------------------------------------------------------------------
+# Flash-Decoding split and combine ("From MHA to MLA", section 4)
+# --------------------------------------------------------------------------------------
+def attend_interval(q_rows, keys, values, scale, begin, end):
+    """Stage 1 of Flash-Decoding for one split: normalized O_s and L_s over tokens [begin, end)."""
+    return attend(q_rows, keys[begin:end], values[begin:end], scale)
+
+
+def combine_splits(partial_out: np.ndarray, partial_lse: np.ndarray):
+    """Combine S locally normalized split results of one head.
+
+    partial_out [S, Dv], partial_lse [S] -> out [Dv], lse.
+    L = max_s L_s + ln sum_s exp(L_s - max);  out = sum_s exp(L_s - L) O_s.
+    A split with L_s = -inf (no keys) carries zero weight and is skipped.
+    """
+    partial_out = np.asarray(partial_out, dtype=np.float64)
+    partial_lse = np.asarray(partial_lse, dtype=np.float64)
+    keep = np.isfinite(partial_lse)
+    po, pl = partial_out[keep], partial_lse[keep]
+    mx = pl.max()
+    w = np.exp(pl - mx)
+    denom = w.sum()
+    out = (w[:, None] * po).sum(axis=0) / denom
+    return out, mx + np.log(denom)

@@ -1,0 +1,334 @@
+"""Pins for the float64 oracle: values and invariants the pages and the mathematics fix.
+
+Each test would fail on a plausible mistake in the oracle (wrong page index or
+slot, interleaved instead of contiguous grouping, a dropped scale, log2 instead
+of ln, a transposed operand, reading unused table entries or stale slots,
+using the rope dims as value dims, a wrong combine weight).
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_61_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+NAN16 = {synth.FP16: 0x7E00, synth.BF16: 0x7FC0}
+
+
+def _small_case(dtype=synth.FP16, seed=3, batch=3, hq=8, hkv=2, d=64, ctx=(37, 1, 50)):
+    return synth.make_gqa_case(batch=batch, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                               dtype=dtype, context_lens=list(ctx), table_layout="permutation",
+                               num_blocks=24, max_blocks_per_seq=5, seed=seed)
+
+
+def _run(case, **kw):
+    return oracle.paged_decode(case.q, case.k_cache, case.v_cache, case.block_tables,
+                               case.context_lens, case.scale, case.page_size, case.dtype, **kw)
+
+
+# ---------------------------------------------------------------- paged addressing
+def _read_worked_example():
+    ranges, meta = [], {}
+    with open(os.path.join(GOLDEN, "worked_example_ctx37.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            if line.startswith("range"):
+                ranges.append(tuple(int(x) for x in line.split()[1:]))
+            else:
+                k, v = (s.strip() for s in line.split("="))
+                meta[k] = [int(x) for x in v.split()]
+    return meta, ranges
+
+
+def test_worked_example_ctx37_mapping():
+    meta, ranges = _read_worked_example()
+    ctx, page = meta["ctx"][0], meta["page_size"][0]
+    assert oracle.num_pages(ctx, page) == meta["num_pages"][0] == 3
+    # entries after the third are garbage that would break the gather if it were read
+    row = np.array(meta["table_prefix"] + [10 ** 9, -7, 2 ** 31 - 1], dtype=np.int64)
+    phys, slots = oracle.token_locations(row, ctx, page)
+    expect_phys, expect_slots = [], []
+    for t0, t1, blk, s0, s1 in ranges:
+        assert t1 - t0 == s1 - s0
+        expect_phys += [blk] * (t1 - t0 + 1)
+        expect_slots += list(range(s0, s1 + 1))
+    assert phys.tolist() == expect_phys and slots.tolist() == expect_slots
+
+
+def test_worked_example_gather_reads_only_three_entries():
+    meta, _ = _read_worked_example()
+    nb, page = 10, 16
+    cache = np.arange(nb * page, dtype=np.int64).reshape(nb, page)  # label = block*16 + slot
+    row = np.array(meta["table_prefix"] + [10 ** 9], dtype=np.int64)  # entry 3 is out of range
+    got = oracle.gather_tokens(cache, row, 37, page)
+    assert got.tolist() == ([9 * 16 + s for s in range(16)] + [3 * 16 + s for s in range(16)]
+                            + [7 * 16 + s for s in range(5)])
+
+
+def test_unused_entries_and_stale_slots_never_matter():
+    case = _small_case()
+    out0, lse0 = _run(case)
+    poisoned = synth.DecodeCase(**{**case.__dict__})
+    k, v, tab = case.k_cache.copy(), case.v_cache.copy(), case.block_tables.copy()
+    used = set()
+    for b, ctx in enumerate(case.context_lens):
+        npg = oracle.num_pages(ctx, case.page_size)
+        used.update(int(x) for x in tab[b, :npg])
+        last = int(tab[b, npg - 1])
+        fill = int(ctx) - (npg - 1) * case.page_size
+        k[last, fill:] = NAN16[case.dtype]
+        v[last, fill:] = NAN16[case.dtype]
+        tab[b, npg:] = 10 ** 8          # would raise IndexError if read
+    for blk in range(case.num_blocks):
+        if blk not in used:
+            k[blk] = NAN16[case.dtype]
+            v[blk] = NAN16[case.dtype]
+    poisoned.k_cache, poisoned.v_cache, poisoned.block_tables = k, v, tab
+    out1, lse1 = _run(poisoned)
+    assert np.isfinite(out1).all() and np.isfinite(lse1).all()
+    np.testing.assert_array_equal(out0, out1)
+    np.testing.assert_array_equal(lse0, lse1)
+
+
+def test_block_permutation_invariance():
+    case = _small_case(dtype=synth.BF16)
+    out0, lse0 = _run(case)
+    rng = np.random.default_rng(11)
+    perm = rng.permutation(case.num_blocks)
+    moved = synth.DecodeCase(**{**case.__dict__})
+    moved.k_cache = np.empty_like(case.k_cache)
+    moved.v_cache = np.empty_like(case.v_cache)
+    moved.k_cache[perm] = case.k_cache
+    moved.v_cache[perm] = case.v_cache
+    moved.block_tables = perm[case.block_tables].astype(np.int32)
+    out1, lse1 = _run(moved)
+    np.testing.assert_array_equal(out0, out1)
+    np.testing.assert_array_equal(lse0, lse1)
+
+
+# ---------------------------------------------------------------- softmax closed forms
+def test_ctx1_gives_first_value_row():
+    case = _small_case(ctx=(1, 1, 1))
+    out, lse = _run(case)
+    G = case.group
+    for b in range(case.batch):
+        blk = int(case.block_tables[b, 0])
+        for h in range(case.num_q_heads):
+            kvh = h // G
+            v0 = oracle.widen(case.v_cache[blk, 0, kvh], case.dtype)
+            k0 = oracle.widen(case.k_cache[blk, 0, kvh], case.dtype)
+            qv = oracle.widen(case.q[b, h], case.dtype)
+            np.testing.assert_array_equal(out[b, h], v0)
+            assert lse[b, h] == pytest.approx(case.scale * math.fsum(qv * k0), abs=1e-12)
+
+
+def test_equal_keys_give_mean_value_and_log_length():
+    case = _small_case(ctx=(37, 16, 5))
+    G = case.group
+    k = case.k_cache.copy()
+    k[:] = case.k_cache[0, 0]                     # every key row identical (per kv head)
+    case.k_cache = k
+    out, lse = _run(case)
+    for b, ctx in enumerate(case.context_lens):
+        for h in range(case.num_q_heads):
+            kvh = h // G
+            s = case.scale * math.fsum(oracle.widen(case.q[b, h], case.dtype)
+                                       * oracle.widen(k[0, 0, kvh], case.dtype))
+            assert lse[b, h] == pytest.approx(s + math.log(int(ctx)), abs=1e-12)
+            rows = [oracle.widen(case.v_cache[case.block_tables[b, j // 16], j % 16, kvh], case.dtype)
+                    for j in range(int(ctx))]
+            np.testing.assert_allclose(out[b, h], np.mean(rows, axis=0), rtol=0, atol=1e-12)
+
+
+def test_constant_values_give_that_value():
+    case = _small_case()
+    v = np.empty_like(case.v_cache)
+    for kvh in range(case.num_kv_heads):
+        v[:, :, kvh, :] = case.q[0, kvh]          # any fixed 16-bit row per kv head
+    case.v_cache = v
+    out, _ = _run(case)
+    G = case.group
+    for b in range(case.batch):
+        for h in range(case.num_q_heads):
+            np.testing.assert_allclose(out[b, h], oracle.widen(case.q[0, h // G], case.dtype),
+                                       rtol=0, atol=1e-12)
+
+
+def test_needle_selects_one_token():
+    case = _small_case(ctx=(37, 20, 50))
+    one = synth.float32_to_bits(np.float32(1.0), case.dtype)
+    sixteen = synth.float32_to_bits(np.float32(16.0), case.dtype)
+    case.q[:] = one
+    for target in (0, 15, 16, 36):
+        k = np.zeros_like(case.k_cache)
+        b = 0
+        blk = int(case.block_tables[b, target // 16])
+        k[blk, target % 16] = sixteen
+        case.k_cache = k
+        out, lse = _run(case)
+        for h in range(case.num_q_heads):
+            v = oracle.widen(case.v_cache[blk, target % 16, h // case.group], case.dtype)
+            np.testing.assert_allclose(out[b, h], v, rtol=0, atol=1e-30)
+            assert lse[b, h] == pytest.approx(case.scale * 16 * case.head_dim_qk, abs=1e-9)
+
+
+# ---------------------------------------------------------------- head grouping
+def test_gqa_equals_mha_with_repeated_kv_heads():
+    case = _small_case(hq=8, hkv=2)
+    out_gqa, lse_gqa = _run(case)
+    mha = synth.DecodeCase(**{**case.__dict__})
+    mha.k_cache = np.repeat(case.k_cache, case.group, axis=2)
+    mha.v_cache = np.repeat(case.v_cache, case.group, axis=2)
+    mha.num_kv_heads = case.num_q_heads
+    out_mha, lse_mha = _run(mha)
+    # same arithmetic; only the BLAS blocking differs (4 rows per call vs 1)
+    np.testing.assert_allclose(out_gqa, out_mha, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse_gqa, lse_mha, rtol=0, atol=1e-13)
+    # the interleaved convention (kv head = h % Hkv) is a different operator on this input
+    inter = synth.DecodeCase(**{**case.__dict__})
+    order = [h % case.num_kv_heads for h in range(case.num_q_heads)]
+    inter.k_cache = case.k_cache[:, :, order, :]
+    inter.v_cache = case.v_cache[:, :, order, :]
+    inter.num_kv_heads = case.num_q_heads
+    out_int, _ = _run(inter)
+    assert np.abs(out_int - out_gqa).max() > 1e-3
+
+
+def test_mqa_is_single_kv_head_special_case():
+    case = _small_case(hq=8, hkv=1)
+    out, lse = _run(case)
+    for b, ctx in enumerate(case.context_lens):
+        keys = oracle.widen(oracle.gather_tokens(case.k_cache[:, :, 0], case.block_tables[b], ctx, 16), case.dtype)
+        vals = oracle.widen(oracle.gather_tokens(case.v_cache[:, :, 0], case.block_tables[b], ctx, 16), case.dtype)
+        o, l = oracle.attend(oracle.widen(case.q[b], case.dtype), keys, vals, case.scale)
+        np.testing.assert_allclose(out[b], o, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[b], l, rtol=0, atol=1e-13)
+
+
+def test_rejects_indivisible_heads_and_empty_context():
+    with pytest.raises(ValueError):
+        oracle.kv_head_of(0, 6, 4)
+    case = _small_case(ctx=(5, 0, 3))
+    with pytest.raises(ValueError):
+        _run(case)
+
+
+# ---------------------------------------------------------------- textbook cross-check
+def _torch_reference(case):
+    """softmax(scale q K^T) V and logsumexp with torch float64 on a gather built from torch ops."""
+    P = case.page_size
+    out = torch.empty(case.batch, case.num_q_heads, case.head_dim_v, dtype=torch.float64)
+    lse = torch.empty(case.batch, case.num_q_heads, dtype=torch.float64)
+    tdt = torch.float16 if case.dtype == synth.FP16 else torch.bfloat16
+    q = torch.from_numpy(case.q.view(np.int16)).view(tdt).double()
+    k = torch.from_numpy(case.k_cache.view(np.int16)).view(tdt).double()
+    v = torch.from_numpy(case.v_cache.view(np.int16)).view(tdt).double()
+    kf = k.reshape(-1, case.num_kv_heads, case.head_dim_qk)
+    vf = v.reshape(-1, case.num_kv_heads, case.head_dim_v)
+    for b in range(case.batch):
+        n = torch.arange(int(case.context_lens[b]))
+        rowidx = torch.from_numpy(case.block_tables[b].astype(np.int64))[n // P] * P + n % P
+        for h in range(case.num_q_heads):
+            kvh = h * case.num_kv_heads // case.num_q_heads
+            logits = case.scale * (kf[rowidx, kvh] @ q[b, h])
+            out[b, h] = torch.softmax(logits, dim=0) @ vf[rowidx, kvh]
+            lse[b, h] = torch.logsumexp(logits, dim=0)
+    return out.numpy(), lse.numpy()
+
+
+@pytest.mark.parametrize("dtype", [synth.FP16, synth.BF16])
+def test_matches_torch_float64_softmax(dtype):
+    case = _small_case(dtype=dtype, ctx=(37, 1, 80), hq=8, hkv=2)
+    out, lse = _run(case)
+    ref_out, ref_lse = _torch_reference(case)
+    np.testing.assert_allclose(out, ref_out, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, rtol=0, atol=1e-12)
+
+
+def test_tiny_workload_matches_torch_float64():
+    case = synth.workload("gqa_tiny")
+    out, lse = _run(case)
+    ref_out, ref_lse = _torch_reference(case)
+    np.testing.assert_allclose(out, ref_out, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, rtol=0, atol=1e-12)
+
+
+def test_row_subset_matches_full():
+    case = _small_case()
+    out, lse = _run(case)
+    rows = [(0, 3), (2, 7), (1, 0)]
+    o2, l2 = _run(case, rows=rows)
+    for b, h in rows:
+        np.testing.assert_allclose(o2[b, h], out[b, h], rtol=0, atol=1e-13)
+        assert l2[b, h] == pytest.approx(lse[b, h], abs=1e-13)
+    assert np.isnan(o2[0, 0]).all()
+
+
+# ---------------------------------------------------------------- split-KV combine
+def test_split_combine_equals_whole():
+    rng = np.random.default_rng(5)
+    L, D = 300, 32
+    q = rng.standard_normal((4, D))
+    keys = rng.standard_normal((L, D))
+    vals = rng.standard_normal((L, D))
+    whole_o, whole_l = oracle.attend(q, keys, vals, 0.3)
+    for cuts in ([0, 150, 300], [0, 1, 2, 299, 300], [0, 17, 64, 200, 233, 300]):
+        parts = [oracle.attend_interval(q, keys, vals, 0.3, a, b) for a, b in zip(cuts[:-1], cuts[1:])]
+        for r in range(q.shape[0]):
+            po = np.stack([p[0][r] for p in parts])
+            pl = np.array([p[1][r] for p in parts])
+            o, l = oracle.combine_splits(po, pl)
+            np.testing.assert_allclose(o, whole_o[r], rtol=0, atol=1e-12)
+            assert l == pytest.approx(whole_l[r], abs=1e-12)
+
+
+def test_combine_weights_by_split_mass_and_skips_empty():
+    # two splits with LSE ln 1 and ln 3: weights 1/4 and 3/4; an empty split (-inf) is ignored
+    po = np.array([[1.0, 0.0], [0.0, 1.0], [np.nan, np.nan]])
+    pl = np.array([0.0, math.log(3.0), -math.inf])
+    o, l = oracle.combine_splits(po, pl)
+    np.testing.assert_allclose(o, [0.25, 0.75], rtol=0, atol=1e-15)
+    assert l == pytest.approx(math.log(4.0), abs=1e-15)
+
+
+# ---------------------------------------------------------------- MLA
+def _small_mla(hq=16, ctx=(70, 1, 129), seed=4):
+    return synth.make_mla_case(batch=len(ctx), num_q_heads=hq, dtype=synth.BF16,
+                               context_lens=list(ctx), seed=seed)
+
+
+def test_mla_equals_generic_with_one_kv_head():
+    case = _small_mla()
+    out, lse = oracle.mla_decode(case.q, case.kv_cache, case.block_tables, case.context_lens,
+                                 case.scale, case.page_size, case.dtype)
+    k = case.kv_cache[:, :, None, :]
+    v = case.kv_cache[:, :, None, :512]
+    out2, lse2 = oracle.paged_decode(case.q, k, v, case.block_tables, case.context_lens,
+                                     case.scale, case.page_size, case.dtype)
+    np.testing.assert_allclose(out, out2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse2, rtol=0, atol=1e-12)
+
+
+def test_mla_rope_only_needle_returns_latent_of_target():
+    case = _small_mla(hq=4, ctx=(100,))
+    kv = case.kv_cache.copy()
+    q = case.q.copy()
+    q[..., :512] = 0                                   # no content score at all
+    q[..., 512:] = synth.float32_to_bits(np.float32(1.0), case.dtype)
+    kv[..., 512:] = 0
+    target = 77
+    blk = int(case.block_tables[0, target // 64])
+    kv[blk, target % 64, 512:] = synth.float32_to_bits(np.float32(16.0), case.dtype)
+    out, lse = oracle.mla_decode(q, kv, case.block_tables, case.context_lens, case.scale,
+                                 case.page_size, case.dtype)
+    want = oracle.widen(kv[blk, target % 64, :512], case.dtype)
+    for h in range(4):
+        np.testing.assert_allclose(out[0, h], want, rtol=0, atol=1e-30)
+        assert lse[0, h] == pytest.approx(case.scale * 16 * 64, abs=1e-9)
+    assert out.shape[-1] == 512
