@@ -1,0 +1,193 @@
+/*
+ * pda.h - paged decode attention for GB300 (sm_103a), C ABI.
+ *
+ * One new query token per sequence attends to that sequence's cached keys and
+ * values, which live in a paged pool addressed through a block table:
+ *
+ *   for sequence b, query head h, logical token j < context_lens[b]:
+ *     phys = block_tables[b][j / P], slot = j % P                  (paging)
+ *     K_j  = k_cache[phys][slot][h / G][:], V_j likewise (G = Hq / Hkv, contiguous grouping)
+ *     s_j  = scale * <q[b][h], K_j>
+ *   out[b][h] = sum_j softmax(s)_j V_j,   lse[b][h] = ln sum_j exp(s_j)   (natural log, fp32)
+ *
+ * Sources: "From MHA to MLA: KV Caches and Attention Kernels" (g-u-n.github.io),
+ * sections 2-6 (GQA head mapping, grouped-head decode, Flash-Decoding split and
+ * combine, paged addressing, absorbed MLA); "L2 讲解：paged decode attention 与
+ * GQA" (kzhou003.github.io gpu-kernel-drills), sections ③-⑤ (grid over
+ * (batch, KV head), page loop, masking of the partial last page); FlashMLA-ETAP
+ * README, sections "Usage" and "Supported configurations" (per-step scheduling
+ * metadata, 576/512 latent layout, page size 64, fp32 lse).
+ *
+ * Conventions for every call:
+ *  - The caller owns every buffer and the stream. Device pointers are CUDA
+ *    device (or managed) memory of the current device; "host" pointers are
+ *    ordinary host memory.
+ *  - Tensors are dense and row-major with the shapes given below; 16-bit
+ *    tensors (q, caches, out) start on a 16-byte boundary, the workspace on a
+ *    256-byte boundary.
+ *  - Decode calls allocate nothing. They are asynchronous on `stream` (NULL =
+ *    the legacy default stream) and return as soon as the work is enqueued.
+ *  - Arguments are validated on the host; a failed check returns a status and
+ *    enqueues nothing. pda_last_error() gives a one-line reason for the last
+ *    failure on the calling thread. No C++ exception crosses this boundary.
+ *  - A workspace may be used by one call at a time: two calls that overlap on
+ *    the GPU (different streams, same workspace) race.
+ */
+#ifndef PDA_H_
+#define PDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PDA_API __attribute__((visibility("default")))
+#else
+#define PDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without including the CUDA headers. */
+typedef struct CUstream_st* pda_stream_t;
+
+typedef enum pda_status {
+  PDA_OK = 0,
+  PDA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, ctx < 1, plan/kind mismatch */
+  PDA_ERR_UNSUPPORTED = 2,  /* a shape or dtype this build has no kernel for */
+  PDA_ERR_WORKSPACE = 3,    /* workspace missing or too small for the plan */
+  PDA_ERR_CUDA = 4          /* a CUDA runtime call failed (launch, copy, device query) */
+} pda_status;
+
+typedef enum pda_dtype { PDA_FP16 = 0, PDA_BF16 = 1 } pda_dtype;
+typedef enum pda_kind { PDA_KIND_GQA = 0, PDA_KIND_MLA = 1 } pda_kind;
+
+/* Shape of one decode problem. The plan keeps a copy. */
+typedef struct pda_problem {
+  int32_t kind;               /* pda_kind */
+  int32_t dtype;              /* pda_dtype of q, the caches and out */
+  int32_t batch;              /* B >= 0 sequences (B == 0: every call is a no-op) */
+  int32_t num_q_heads;        /* Hq */
+  int32_t num_kv_heads;       /* Hkv, Hq % Hkv == 0 ("H_q must be divisible by H_kv"); MLA: 1 */
+  int32_t head_dim_qk;        /* GQA: 64 or 128; MLA: 576 (512 latent + 64 rope) */
+  int32_t head_dim_v;         /* GQA: == head_dim_qk; MLA: 512 (V = first 512 dims of the record) */
+  int32_t page_size;          /* tokens per physical block P; GQA: 16; MLA: 64 */
+  int32_t max_blocks_per_seq; /* columns of block_tables */
+  int64_t num_blocks;         /* physical blocks in the cache pool */
+  int32_t num_sms;            /* SMs to plan for; 0 = query the current device */
+  int32_t force_num_ctas;     /* 0 = automatic; > 0 = split the work over exactly this many CTAs */
+} pda_problem;
+
+typedef struct pda_plan pda_plan;  /* opaque, owned by the library */
+
+/*
+ * Plan one decode step (FlashMLA-ETAP "Usage": scheduling metadata is computed
+ * once per step, whenever the context lengths change, and reused by every
+ * layer's attention call).
+ *
+ * The work of a step is the list of (sequence, KV head, page) tiles; the plan
+ * divides it into equal contiguous ranges, one per CTA, sized from the SM
+ * count. A (sequence, KV head) whose pages land in more than one range is
+ * computed as Flash-Decoding splits ("From MHA to MLA", section 4) and
+ * combined on the GPU by the last CTA that finishes one of its splits.
+ *
+ * context_lens_host: [B] int32 on the host, every entry in
+ * [1, max_blocks_per_seq * page_size]. The device context_lens passed to the
+ * decode call MUST hold the same values.
+ * Returns PDA_OK and *plan, or an error status (and *plan == NULL).
+ */
+PDA_API pda_status pda_plan_create(pda_plan** plan, const pda_problem* problem,
+                           const int32_t* context_lens_host);
+
+/* Frees a plan (NULL is ignored). */
+PDA_API void pda_plan_destroy(pda_plan* plan);
+
+/* Bytes of device workspace the decode call needs for this plan (>= 256). */
+PDA_API size_t pda_plan_workspace_bytes(const pda_plan* plan);
+
+/* CTAs the decode call launches. */
+PDA_API int32_t pda_plan_num_ctas(const pda_plan* plan);
+
+/* Number of Flash-Decoding splits of sequence b: the largest number of CTAs that
+ * share one of its (KV head or head group) segments. 1 = computed by one CTA. */
+PDA_API int32_t pda_plan_num_splits(const pda_plan* plan, int32_t b);
+
+/*
+ * Zero a workspace before its first use with any plan. The decode calls leave
+ * the workspace's counters at zero when they complete, so this is needed once
+ * per workspace allocation, not once per call. Asynchronous on `stream`.
+ */
+PDA_API pda_status pda_workspace_init(const pda_plan* plan, void* workspace, pda_stream_t stream);
+
+/*
+ * Read and clear the device error word of a workspace (synchronizes `stream`).
+ * *code = 0: no error; bit 0: a block-table entry of a read page was outside
+ * [0, num_blocks) (that page was read as zeros); bit 1: a pipeline wait timed
+ * out and the kernel abandoned its work.
+ */
+PDA_API pda_status pda_read_device_error(void* workspace, pda_stream_t stream, int32_t* code);
+
+/*
+ * GQA / MQA / MHA paged decode ("From MHA to MLA", sections 3-5; drill page,
+ * sections ③-⑤).
+ *   q             device [B, Hq, D]            dtype
+ *   k_cache       device [num_blocks, P, Hkv, D] dtype
+ *   v_cache       device [num_blocks, P, Hkv, D] dtype
+ *   block_tables  device [B, max_blocks_per_seq] int32; only the first
+ *                 ceil(ctx_b / P) entries of row b are read
+ *   context_lens  device [B] int32, equal to the plan's host copy
+ *   scale         softmax scale applied to q.k (e.g. 1/sqrt(D)); finite
+ *   out           device [B, Hq, D] dtype (written; rows of other sequences untouched)
+ *   lse           device [B, Hq] float32 natural-log LSE of the scaled logits, or NULL
+ *   plan          from pda_plan_create with kind PDA_KIND_GQA
+ *   workspace     device, pda_plan_workspace_bytes(plan) bytes, zeroed once
+ * Slots past ctx in a sequence's last page and blocks not referenced by the
+ * first ceil(ctx/P) table entries are never used, whatever they hold.
+ */
+PDA_API pda_status paged_decode_attn(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, const int32_t* context_lens,
+                             float scale, void* out, float* lse, const pda_plan* plan,
+                             void* workspace, pda_stream_t stream);
+
+/*
+ * Absorbed MLA decode ("From MHA to MLA", section 6; FlashMLA-ETAP "Usage"):
+ * every query head attends to one shared record per token of
+ * head_dim_qk = 576 values (512 latent then 64 rope). Scores use all 576,
+ * values are the first 512.
+ *   q             device [B, Hq, 576] dtype (absorbed content query then rope query)
+ *   kv_cache      device [num_blocks, 64, 576] dtype (one KV head)
+ *   block_tables, context_lens, scale, plan (kind PDA_KIND_MLA), workspace: as above
+ *   out           device [B, Hq, 512] dtype
+ *   lse           device [B, Hq] float32 or NULL
+ */
+PDA_API pda_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_tables,
+                      const int32_t* context_lens, float scale, void* out, float* lse,
+                      const pda_plan* plan, void* workspace, pda_stream_t stream);
+
+/*
+ * Flash-Decoding combine on its own ("From MHA to MLA", section 4): for each
+ * of `rows` rows, merge `num_splits` locally normalized partial outputs:
+ *   L = max_s L_s + ln sum_s exp(L_s - max_s L_s),   out = sum_s exp(L_s - L) O_s
+ * Splits with L_s = -inf carry no weight.
+ *   partial_out  device [rows, num_splits, head_dim_v] float32
+ *   partial_lse  device [rows, num_splits] float32 (natural log)
+ *   out          device [rows, head_dim_v] in out_dtype (pda_dtype)
+ *   lse          device [rows] float32, or NULL
+ * head_dim_v: a multiple of 4, at most 1024. rows >= 0, num_splits >= 1.
+ */
+PDA_API pda_status pda_combine_splits(const float* partial_out, const float* partial_lse, int32_t rows,
+                              int32_t num_splits, int32_t head_dim_v, void* out,
+                              int32_t out_dtype, float* lse, pda_stream_t stream);
+
+/* Static name of a status code. */
+PDA_API const char* pda_status_string(pda_status status);
+
+/* One-line description of the last failed call on this thread ("" if none). */
+PDA_API const char* pda_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PDA_H_ */

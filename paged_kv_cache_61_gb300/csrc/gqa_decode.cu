@@ -1,0 +1,642 @@
+// GQA / MQA / MHA paged decode attention for sm_103a.
+//
+// What it computes ("From MHA to MLA", sections 3-5; drill page "L2 讲解：paged
+// decode attention 与 GQA", sections ③-⑤): for each sequence b and KV head kvh,
+// the G = Hq/Hkv query heads kvh*G .. kvh*G+G-1 (contiguous grouping) attend to
+// the ctx_b cached tokens, gathered page by page through the block table, with
+// an online softmax; long sequences are split Flash-Decoding style and the
+// splits merged by their log-sum-exp.
+//
+// How (GB300 design, not the pages' Triton/Hopper kernels):
+//  * Persistent-free, equal-work CTAs: the plan gives every CTA the same number
+//    of (sequence, KV head, page) tiles in one flattened list, so one wave of
+//    CTAs covers any batch mix (uniform, one 32K sequence, varlen).
+//  * A producer warp walks the CTA's tiles, reads the block table 32 entries
+//    at a time and issues TMA tile loads (4-D map over [block, slot, kvh, d],
+//    coordinates (d, kvh, 0, phys): the 64-bit address is formed by the TMA
+//    unit, so no 32-bit product phys*stride exists) of each page's K and V into
+//    a ring of shared-memory stages with 128-byte swizzle.
+//  * Four consumer warps take pages round-robin. Each page is one m16n8k16
+//    tile in the transposed ("keys on M") orientation the FlashMLA-ETAP README
+//    describes for Hopper WGMMA, here on warp MMA: S^T[16 tokens x 8 heads] =
+//    K * Q^T, so a group of 4 heads wastes half an MMA instead of 3/4 of one.
+//    The online softmax runs down each column (head) with three shuffles;
+//    P^T is turned into the B fragment of O^T += V^T * P^T with movmatrix.
+//  * Stale slots of a partial last page are removed by selects on the scores
+//    and on the V^T fragments, never by multiplying, so whatever the slots
+//    hold (even NaN) cannot reach the output.
+//  * At the end of each (sequence, KV head) piece the warps merge their states
+//    in shared memory; a complete segment is written directly, a split piece
+//    writes (O_s, L_s) to its CTA's slot, and the last piece to arrive (atomic
+//    counter) combines all pieces ("From MHA to MLA", section 4) and resets the
+//    counter.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "pda_internal.h"
+#include "ptx.cuh"
+
+namespace pda {
+
+namespace {
+
+constexpr int kPage = 16;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 6;
+constexpr int kBoxBytes = kPage * 128;  // one TMA box: 16 tokens x 64 dims x 16 bit
+constexpr int kCtasPerSm = 3;
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct GqaParams {
+  const void* q;
+  void* out;
+  float* lse;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int32_t batch, num_q_heads, num_kv_heads, group, max_blocks;
+  int64_t num_blocks;
+  float scale_log2;
+  int64_t total_tiles, tiles_per_cta;
+  int32_t* err;
+  int32_t* counters;
+  float* part_lse;
+  float* part_out;
+};
+
+template <int D>
+struct Layout {
+  static constexpr int kDBlocks = D / 64;
+  static constexpr int kStageBytes = 2 * kDBlocks * kBoxBytes;
+  static constexpr int kMergeStride = D + 4;  // floats per head row; +4 spreads banks
+  static constexpr int kMergeWarpFloats = 8 * kMergeStride + 16;
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kMergeBytes = kConsumerWarps * kMergeWarpFloats * 4;
+  static constexpr int kBarBytes = 2 * kStages * 8 + 16;
+  static constexpr int kSmemBytes = 1024 + kRingBytes + kMergeBytes + kBarBytes;
+};
+
+__device__ __forceinline__ int pages_of(int ctx) { return (ctx + kPage - 1) / kPage; }
+
+// ------------------------------------------------------------------ tile walk
+// The CTA's tiles [g_lo, g_hi) of the flattened list (sequence-major, KV-head
+// next, page last) are visited as "portions": maximal runs inside one segment.
+struct Walker {
+  int b;
+  int np;           // pages of sequence b
+  int64_t start_b;  // flattened index of sequence b's first tile
+  int64_t g;        // next tile to visit
+};
+
+struct Portion {
+  int b, kvh, p0, p1, np;
+  int64_t seg_start;
+};
+
+// Warp-collective: find the sequence whose tiles contain flattened tile g.
+__device__ __forceinline__ void walker_init(Walker& w, const GqaParams& p, int64_t g, int lane) {
+  int64_t base = 0;
+  w.b = p.batch;
+  w.start_b = 0;
+  w.np = 1;
+  w.g = g;
+  for (int b0 = 0; b0 < p.batch; b0 += 32) {
+    const int b = b0 + lane;
+    const int np = b < p.batch ? pages_of(__ldg(p.context_lens + b)) : 0;
+    const int64_t width = int64_t(np) * p.num_kv_heads;
+    int64_t incl = width;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t t = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const int64_t excl = incl - width;
+    const unsigned hit = __ballot_sync(kFull, b < p.batch && base + excl <= g && g < base + incl);
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      w.b = b0 + src;
+      w.start_b = base + __shfl_sync(kFull, excl, src);
+      w.np = __shfl_sync(kFull, np, src);
+      return;
+    }
+    base += __shfl_sync(kFull, incl, 31);
+  }
+}
+
+__device__ __forceinline__ Portion walker_next(Walker& w, const GqaParams& p, int64_t g_hi) {
+  const int64_t off = w.g - w.start_b;
+  const int kvh = int(off / w.np);
+  const int p0 = int(off - int64_t(kvh) * w.np);
+  const int p1 = int(min(int64_t(w.np), int64_t(p0) + (g_hi - w.g)));
+  Portion pt{w.b, kvh, p0, p1, w.np, w.start_b + int64_t(kvh) * w.np};
+  w.g += p1 - p0;
+  if (p1 == w.np && kvh + 1 == p.num_kv_heads) {
+    w.start_b += int64_t(p.num_kv_heads) * w.np;
+    ++w.b;
+    if (w.b < p.batch && w.g < g_hi) w.np = pages_of(__ldg(p.context_lens + w.b));
+  }
+  return pt;
+}
+
+// Wait for a ring stage; gives up on timeout or when another warp aborted.
+__device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (ptx::globaltimer() - t0 > ptx::kWaitLimitNs) return false;
+  }
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
+  uint4 r;
+  r.x = ptx::Mma<T>::pack(v[0], v[1]);
+  r.y = ptx::Mma<T>::pack(v[2], v[3]);
+  r.z = ptx::Mma<T>::pack(v[4], v[5]);
+  r.w = ptx::Mma<T>::pack(v[6], v[7]);
+  return r;
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int D, typename T, int NHT>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+    gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const GqaParams p) {
+  using L = Layout<D>;
+  constexpr int kDB = L::kDBlocks;
+  constexpr int kWP = kConsumerWarps / NHT;  // consumer warps sharing one head subtile
+  constexpr int kKS = D / 16;                // k-steps of S^T and m-tiles of O^T
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = align1024(smem_raw);
+  float* merge = reinterpret_cast<float*>(ring + L::kRingBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + L::kRingBytes + L::kMergeBytes);
+  uint64_t* empty = full + kStages;
+  volatile int* flags = reinterpret_cast<volatile int*>(empty + kStages);  // [0] abort, [1] last
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t g_lo = int64_t(blockIdx.x) * p.tiles_per_cta;
+  const int64_t g_hi = min(p.total_tiles, g_lo + p.tiles_per_cta);
+  if (g_lo >= g_hi) return;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], NHT);
+    }
+    flags[0] = 0;
+    flags[1] = 0;
+    ptx::fence_mbarrier_init();
+  }
+  __syncthreads();
+
+  Walker walk;
+  walker_init(walk, p, g_lo, lane);
+
+  if (warp == kConsumerWarps) {
+    // ============================== producer warp ==============================
+    if (lane == 0) {
+      ptx::prefetch_tensormap(&tm_k);
+      ptx::prefetch_tensormap(&tm_v);
+    }
+    const uint64_t policy = ptx::policy_evict_first();
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t filled = 0;  // bit s: stage s was filled at least once
+    bool ok = true;
+    while (ok && walk.g < g_hi) {
+      const Portion pt = walker_next(walk, p, g_hi);
+      const int32_t* row = p.block_tables + int64_t(pt.b) * p.max_blocks;
+      int32_t next = (pt.p0 + lane < pt.p1) ? __ldg(row + pt.p0 + lane) : 0;
+      for (int base = pt.p0; ok && base < pt.p1; base += 32) {
+        const int32_t cur = next;
+        if (base + 32 < pt.p1) next = (base + 32 + lane < pt.p1) ? __ldg(row + base + 32 + lane) : 0;
+        const int n = min(32, pt.p1 - base);
+        for (int j = 0; j < n; ++j) {
+          const int32_t phys = __shfl_sync(kFull, cur, j);
+          int good = 1;
+          if (lane == 0) {
+            if (!wait_stage(&empty[stage], phase ^ 1, flags)) {
+              good = 0;
+            } else {
+              // An id outside the pool is flagged; TMA fills such a tile with zeros.
+              if (phys < 0 || int64_t(phys) >= p.num_blocks) atomicOr(p.err, 1);
+              ptx::mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
+              uint8_t* st = ring + stage * L::kStageBytes;
+#pragma unroll
+              for (int db = 0; db < kDB; ++db) {
+                ptx::tma_load_4d(st + db * kBoxBytes, &tm_k, &full[stage], db * 64, pt.kvh, 0,
+                                 phys, policy);
+                ptx::tma_load_4d(st + (kDB + db) * kBoxBytes, &tm_v, &full[stage], db * 64,
+                                 pt.kvh, 0, phys, policy);
+              }
+              filled |= 1u << stage;
+            }
+          }
+          ok = __shfl_sync(kFull, good, 0) != 0;
+          if (!ok) break;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      flags[0] = 1;
+      atomicOr(p.err, 2);
+    }
+    // Never leave with a copy in flight: wait (bounded) for each stage's last fill.
+    if (lane == 0) {
+      for (int s = 0; s < kStages; ++s) {
+        if (!(filled >> s & 1)) continue;
+        // stages before `stage` were last filled in `phase`, the rest in phase ^ 1
+        const uint32_t par = (s < stage) ? phase : (phase ^ 1);
+        const uint64_t t0 = ptx::globaltimer();
+        while (!ptx::mbar_try_wait(&full[s], par) && ptx::globaltimer() - t0 < ptx::kWaitLimitNs) {
+        }
+      }
+    }
+    return;
+  }
+
+  // ============================== consumer warps ==============================
+  const int hsub = warp % NHT;
+  const int pres = warp / NHT;
+  const int tid = threadIdx.x;  // 0..127 among consumers
+  const T* __restrict__ qg = static_cast<const T*>(p.q);
+  T* __restrict__ outg = static_cast<T*>(p.out);
+  float* mw = merge + warp * L::kMergeWarpFloats;
+  const int r0 = lane >> 2;            // token row (S^T) / d row (O^T) of this lane
+  const int cq = 2 * (lane & 3);       // first of the two head columns of this lane
+  // ldmatrix lane roles
+  const int tok_k = (lane & 7) + ((lane >> 3) & 1) * 8;
+  const int chunk_k = lane >> 4;
+  const int tok_v = (lane & 7) + ((lane >> 4) & 1) * 8;
+  const int chunk_v = (lane >> 3) & 1;
+  const uint32_t ring_s = ptx::smem_addr(ring);
+
+  bool aborted = false;
+  int64_t k = 0;  // CTA-local index of the current portion's first tile
+  while (walk.g < g_hi) {
+    const Portion pt = walker_next(walk, p, g_hi);
+    const int ctx = __ldg(p.context_lens + pt.b);
+    const int npg = pt.p1 - pt.p0;
+
+    // Q^T as the B operand (k = head dim, n = head): lane holds head hsub*8 + lane/4.
+    const int jq = hsub * 8 + r0;
+    uint32_t qf[kKS][2];
+    {
+      const bool hv = jq < p.group;
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+          qg + (int64_t(pt.b) * p.num_q_heads + int64_t(pt.kvh) * p.group + (hv ? jq : 0)) * D);
+#pragma unroll
+      for (int ks = 0; ks < kKS; ++ks) {
+        qf[ks][0] = hv ? __ldg(qrow + (ks * 16 + cq) / 2) : 0u;
+        qf[ks][1] = hv ? __ldg(qrow + (ks * 16 + 8 + cq) / 2) : 0u;
+      }
+    }
+
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float acc[kKS][4];
+#pragma unroll
+    for (int mt = 0; mt < kKS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+
+    for (int i = pres; i < npg; i += kWP) {
+      const int64_t t = k + i;
+      const int stage = int(t % kStages);
+      const uint32_t par = uint32_t(t / kStages) & 1u;
+      if (!aborted && !wait_stage(&full[stage], par, flags)) {
+        aborted = true;
+        if (lane == 0) {
+          flags[0] = 1;
+          atomicOr(p.err, 2);
+        }
+      }
+      if (aborted) continue;
+      const int valid = min(kPage, ctx - (pt.p0 + i) * kPage);
+      const uint32_t kb = ring_s + stage * L::kStageBytes;
+      const uint32_t vb = kb + kDB * kBoxBytes;
+
+      // S^T = K * Q^T  (M = 16 tokens, N = 8 heads, K = D)
+      float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < kKS; ++ks) {
+        const int chunk = (ks & 3) * 2 + chunk_k;
+        const uint32_t addr = kb + (ks >> 2) * kBoxBytes + tok_k * 128 + ((chunk ^ (tok_k & 7)) << 4);
+        uint32_t a[4];
+        ptx::ldsm_x4(addr, a[0], a[1], a[2], a[3]);
+        ptx::Mma<T>::run(s, a, qf[ks][0], qf[ks][1]);
+      }
+      float x0 = s[0] * p.scale_log2, x1 = s[1] * p.scale_log2;
+      float x2 = s[2] * p.scale_log2, x3 = s[3] * p.scale_log2;
+      if (valid < kPage) {
+        if (r0 >= valid) x0 = x1 = -INFINITY;
+        if (r0 + 8 >= valid) x2 = x3 = -INFINITY;
+      }
+      // online softmax down each head column (log2 domain)
+      float c0 = fmaxf(x0, x2), c1 = fmaxf(x1, x3);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        c0 = fmaxf(c0, __shfl_xor_sync(kFull, c0, o));
+        c1 = fmaxf(c1, __shfl_xor_sync(kFull, c1, o));
+      }
+      const float mn0 = fmaxf(m0, c0), mn1 = fmaxf(m1, c1);
+      const float al0 = ptx::exp2_approx(m0 - mn0), al1 = ptx::exp2_approx(m1 - mn1);
+      const float p0 = ptx::exp2_approx(x0 - mn0), p1 = ptx::exp2_approx(x1 - mn1);
+      const float p2 = ptx::exp2_approx(x2 - mn0), p3 = ptx::exp2_approx(x3 - mn1);
+      l0 = l0 * al0 + (p0 + p2);
+      l1 = l1 * al1 + (p1 + p3);
+      m0 = mn0;
+      m1 = mn1;
+      if (__any_sync(kFull, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+        for (int mt = 0; mt < kKS; ++mt) {
+          acc[mt][0] *= al0;
+          acc[mt][1] *= al1;
+          acc[mt][2] *= al0;
+          acc[mt][3] *= al1;
+        }
+      }
+      // P^T as the B operand (k = token, n = head)
+      const uint32_t pb0 = ptx::movmatrix_trans(ptx::Mma<T>::pack(p0, p1));
+      const uint32_t pb1 = ptx::movmatrix_trans(ptx::Mma<T>::pack(p2, p3));
+      // token masks for the V^T fragments (tokens cq, cq+1 and cq+8, cq+9)
+      uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
+      if (valid < kPage) {
+        vm_lo = (cq < valid ? 0x0000ffffu : 0u) | (cq + 1 < valid ? 0xffff0000u : 0u);
+        vm_hi = (cq + 8 < valid ? 0x0000ffffu : 0u) | (cq + 9 < valid ? 0xffff0000u : 0u);
+      }
+      // O^T += V^T * P^T  (M = D in 16-row tiles, N = 8 heads, K = 16 tokens)
+#pragma unroll
+      for (int mt = 0; mt < kKS; ++mt) {
+        const int chunk = (mt & 3) * 2 + chunk_v;
+        const uint32_t addr = vb + (mt >> 2) * kBoxBytes + tok_v * 128 + ((chunk ^ (tok_v & 7)) << 4);
+        uint32_t a[4];
+        ptx::ldsm_x4_trans(addr, a[0], a[1], a[2], a[3]);
+        a[0] &= vm_lo;
+        a[1] &= vm_lo;
+        a[2] &= vm_hi;
+        a[3] &= vm_hi;
+        ptx::Mma<T>::run(acc[mt], a, pb0, pb1);
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&empty[stage]);
+    }
+    k += npg;
+
+    // ---- this warp's state -> shared memory
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l0 += __shfl_xor_sync(kFull, l0, o);
+      l1 += __shfl_xor_sync(kFull, l1, o);
+    }
+#pragma unroll
+    for (int mt = 0; mt < kKS; ++mt) {
+      const int d = mt * 16 + r0;
+      mw[cq * L::kMergeStride + d] = acc[mt][0];
+      mw[(cq + 1) * L::kMergeStride + d] = acc[mt][1];
+      mw[cq * L::kMergeStride + d + 8] = acc[mt][2];
+      mw[(cq + 1) * L::kMergeStride + d + 8] = acc[mt][3];
+    }
+    if (lane < 4) {
+      mw[8 * L::kMergeStride + cq] = m0;
+      mw[8 * L::kMergeStride + cq + 1] = m1;
+      mw[8 * L::kMergeStride + 8 + cq] = l0;
+      mw[8 * L::kMergeStride + 8 + cq + 1] = l1;
+    }
+    ptx::named_barrier_sync(1, kConsumerWarps * 32);
+
+    // ---- merge the warps of each head subtile; write final rows or this CTA's split slot
+    const bool whole = (pt.p0 == 0 && pt.p1 == pt.np);
+    const int slot = (pt.seg_start <= g_lo) ? 0 : 1;
+    const int64_t slot_row = (int64_t(blockIdx.x) * 2 + slot) * p.group;
+    constexpr int kChunks = D / 8;
+    for (int idx = tid; idx < p.group * kChunks; idx += kConsumerWarps * 32) {
+      const int j = idx / kChunks;
+      const int dc = idx - j * kChunks;
+      const int hs = j >> 3, n = j & 7;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < kWP; ++r)
+        mx = fmaxf(mx, merge[(hs + r * NHT) * L::kMergeWarpFloats + 8 * L::kMergeStride + n]);
+      float lsum = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int r = 0; r < kWP; ++r) {
+        const float* w = merge + (hs + r * NHT) * L::kMergeWarpFloats;
+        const float wm = w[8 * L::kMergeStride + n];
+        if (wm == -INFINITY) continue;  // this warp saw no page of the portion
+        const float f = ptx::exp2_approx(wm - mx);
+        lsum += w[8 * L::kMergeStride + 8 + n] * f;
+        const float4 a = *reinterpret_cast<const float4*>(w + n * L::kMergeStride + dc * 8);
+        const float4 b = *reinterpret_cast<const float4*>(w + n * L::kMergeStride + dc * 8 + 4);
+        o[0] += a.x * f; o[1] += a.y * f; o[2] += a.z * f; o[3] += a.w * f;
+        o[4] += b.x * f; o[5] += b.y * f; o[6] += b.z * f; o[7] += b.w * f;
+      }
+      const float inv = 1.f / lsum;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] *= inv;
+      const float lse_nat = (mx + log2f(lsum)) * kLn2;
+      if (whole) {
+        const int64_t orow = int64_t(pt.b) * p.num_q_heads + int64_t(pt.kvh) * p.group + j;
+        *reinterpret_cast<uint4*>(outg + orow * D + dc * 8) = pack8<T>(o);
+        if (dc == 0 && p.lse != nullptr) p.lse[orow] = lse_nat;
+      } else {
+        float* po = p.part_out + (slot_row + j) * D + dc * 8;
+        __stcg(reinterpret_cast<float4*>(po), make_float4(o[0], o[1], o[2], o[3]));
+        __stcg(reinterpret_cast<float4*>(po + 4), make_float4(o[4], o[5], o[6], o[7]));
+        if (dc == 0) __stcg(p.part_lse + slot_row + j, lse_nat);
+      }
+    }
+
+    if (!whole) {
+      // ---- split piece: count arrivals; the last piece combines all of them
+      __threadfence();
+      ptx::named_barrier_sync(1, kConsumerWarps * 32);
+      const int64_t c0 = pt.seg_start / p.tiles_per_cta;
+      const int64_t c1 = (pt.seg_start + pt.np - 1) / p.tiles_per_cta;
+      const int pieces = int(c1 - c0 + 1);
+      int32_t* counter = p.counters + int64_t(pt.b) * p.num_kv_heads + pt.kvh;
+      if (tid == 0) {
+        const int prev = aborted ? -1 : atomicAdd(counter, 1);
+        flags[1] = (prev == pieces - 1) ? 1 : 0;
+      }
+      ptx::named_barrier_sync(1, kConsumerWarps * 32);
+      if (flags[1]) {
+        __threadfence();
+        for (int idx = tid; idx < p.group * kChunks; idx += kConsumerWarps * 32) {
+          const int j = idx / kChunks;
+          const int dc = idx - j * kChunks;
+          float mx = -INFINITY;
+          for (int64_t c = c0; c <= c1; ++c) {
+            const int sl = (c == c0 && pt.seg_start > c * p.tiles_per_cta) ? 1 : 0;
+            mx = fmaxf(mx, __ldcg(p.part_lse + (c * 2 + sl) * p.group + j));
+          }
+          float den = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          for (int64_t c = c0; c <= c1; ++c) {
+            const int sl = (c == c0 && pt.seg_start > c * p.tiles_per_cta) ? 1 : 0;
+            const int64_t rowi = (c * 2 + sl) * p.group + j;
+            const float ls = __ldcg(p.part_lse + rowi);
+            if (ls == -INFINITY) continue;
+            const float wgt = ptx::exp2_approx((ls - mx) * kLog2e);
+            den += wgt;
+            const float4 a = __ldcg(reinterpret_cast<const float4*>(p.part_out + rowi * D + dc * 8));
+            const float4 b = __ldcg(reinterpret_cast<const float4*>(p.part_out + rowi * D + dc * 8 + 4));
+            o[0] += wgt * a.x; o[1] += wgt * a.y; o[2] += wgt * a.z; o[3] += wgt * a.w;
+            o[4] += wgt * b.x; o[5] += wgt * b.y; o[6] += wgt * b.z; o[7] += wgt * b.w;
+          }
+          const float inv = 1.f / den;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] *= inv;
+          const int64_t orow = int64_t(pt.b) * p.num_q_heads + int64_t(pt.kvh) * p.group + j;
+          *reinterpret_cast<uint4*>(outg + orow * D + dc * 8) = pack8<T>(o);
+          if (dc == 0 && p.lse != nullptr) p.lse[orow] = mx + logf(den);
+        }
+        if (tid == 0) atomicExch(counter, 0);
+      }
+    }
+    // the merge area is rewritten by the next portion
+    ptx::named_barrier_sync(1, kConsumerWarps * 32);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// Map over a paged cache [num_blocks, P, Hkv, D] (16-bit): dims (d, kvh, slot, block),
+// box (64, 1, P, 1), 128-byte swizzle.
+bool encode_cache_map(CUtensorMap* map, const void* base, int64_t num_blocks, int page, int hkv,
+                      int d, bool bf16) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[4] = {cuuint64_t(d), cuuint64_t(hkv), cuuint64_t(page),
+                              cuuint64_t(num_blocks)};
+  const cuuint64_t strides[3] = {cuuint64_t(d) * 2, cuuint64_t(hkv) * d * 2,
+                                 cuuint64_t(page) * hkv * d * 2};
+  const cuuint32_t box[4] = {64, 1, cuuint32_t(page), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, typename T, int NHT>
+int launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const GqaParams& prm, int grid,
+               cudaStream_t stream) {
+  auto kern = gqa_decode_kernel<D, T, NHT>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Layout<D>::kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  kern<<<grid, kThreads, Layout<D>::kSmemBytes, stream>>>(tk, tv, prm);
+  return cudaGetLastError();
+}
+
+template <int D, typename T>
+int launch_d(int nht, const CUtensorMap& tk, const CUtensorMap& tv, const GqaParams& prm, int grid,
+             cudaStream_t s) {
+  switch (nht) {
+    case 1: return launch_one<D, T, 1>(tk, tv, prm, grid, s);
+    case 2: return launch_one<D, T, 2>(tk, tv, prm, grid, s);
+    default: return launch_one<D, T, 4>(tk, tv, prm, grid, s);
+  }
+}
+
+}  // namespace
+
+bool gqa_supported(const pda_problem& p, std::string* why) {
+  if (p.head_dim_qk != p.head_dim_v || (p.head_dim_qk != 64 && p.head_dim_qk != 128)) {
+    *why = "GQA decode supports head_dim_qk == head_dim_v in {64, 128}";
+    return false;
+  }
+  if (p.page_size != kPage) {
+    *why = "GQA decode supports page_size 16";
+    return false;
+  }
+  const int g = p.num_q_heads / p.num_kv_heads;
+  if (g > 32) {
+    *why = "GQA decode supports up to 32 query heads per KV head";
+    return false;
+  }
+  if (p.num_blocks > INT32_MAX) {
+    *why = "num_blocks must fit in int32 (block-table entries are int32)";
+    return false;
+  }
+  return true;
+}
+
+int gqa_ctas_per_sm(const pda_problem&) { return kCtasPerSm; }
+
+int launch_gqa_decode(const Plan& plan, const GqaArgs& a, const Workspace& ws, void* stream) {
+  const pda_problem& pr = plan.prob;
+  const bool bf16 = pr.dtype == PDA_BF16;
+  CUtensorMap tk, tv;
+  if (!encode_cache_map(&tk, a.k_cache, pr.num_blocks, pr.page_size, pr.num_kv_heads,
+                        pr.head_dim_qk, bf16) ||
+      !encode_cache_map(&tv, a.v_cache, pr.num_blocks, pr.page_size, pr.num_kv_heads,
+                        pr.head_dim_v, bf16))
+    return -1;
+  GqaParams prm{};
+  prm.q = a.q;
+  prm.out = a.out;
+  prm.lse = a.lse;
+  prm.block_tables = a.block_tables;
+  prm.context_lens = a.context_lens;
+  prm.batch = pr.batch;
+  prm.num_q_heads = pr.num_q_heads;
+  prm.num_kv_heads = pr.num_kv_heads;
+  prm.group = plan.group;
+  prm.max_blocks = pr.max_blocks_per_seq;
+  prm.num_blocks = pr.num_blocks;
+  prm.scale_log2 = a.scale * kLog2e;
+  prm.total_tiles = plan.total_tiles;
+  prm.tiles_per_cta = plan.tiles_per_cta;
+  prm.err = ws.err;
+  prm.counters = ws.counters;
+  prm.part_lse = ws.part_lse;
+  prm.part_out = ws.part_out;
+  const int nht = plan.head_subtiles <= 1 ? 1 : (plan.head_subtiles <= 2 ? 2 : 4);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (pr.head_dim_qk == 64)
+    return bf16 ? launch_d<64, __nv_bfloat16>(nht, tk, tv, prm, plan.num_ctas, s)
+                : launch_d<64, __half>(nht, tk, tv, prm, plan.num_ctas, s);
+  return bf16 ? launch_d<128, __nv_bfloat16>(nht, tk, tv, prm, plan.num_ctas, s)
+              : launch_d<128, __half>(nht, tk, tv, prm, plan.num_ctas, s);
+}
+
+}  // namespace pda

@@ -1,0 +1,92 @@
+// Internal declarations shared by the host side (plan.cpp, api.cpp) and the kernel launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "pda.h"
+
+namespace pda {
+
+// Work decomposition shared by the GQA and MLA kernels.
+//
+// A "segment" is one (sequence b, KV head or head group) pair; it owns
+// num_pages(b) = ceil(ctx_b / P) page tiles. Segments are laid out b-major,
+// head-minor, so the step's tiles form one flattened list of `total_tiles`
+// entries. CTA i owns tiles [i*tiles_per_cta, min((i+1)*tiles_per_cta, total)).
+// A segment covered by several CTAs is a Flash-Decoding split: each piece
+// writes a normalized partial (O_s, L_s) into a per-CTA slot and the last piece
+// to finish merges them.
+struct Plan {
+  pda_problem prob{};
+  int32_t group = 1;            // query heads per segment (GQA: Hq/Hkv; MLA: Hq / head groups)
+  int32_t segs_per_seq = 1;     // segments per sequence (GQA: Hkv; MLA: head groups)
+  int32_t head_subtiles = 1;    // GQA: 8-head MMA column tiles per segment
+  int64_t total_tiles = 0;
+  int64_t tiles_per_cta = 0;
+  int32_t num_ctas = 0;
+  std::vector<int32_t> context_lens;  // host copy used for planning
+  std::vector<int32_t> splits;        // per sequence: max pieces over its segments
+  // workspace layout (byte offsets)
+  size_t ws_err = 0;        // int32 device error word
+  size_t ws_counters = 0;   // int32 [B * segs_per_seq]
+  size_t ws_part_lse = 0;   // float [num_ctas * 2 * group]
+  size_t ws_part_out = 0;   // float [num_ctas * 2 * group * head_dim_v]
+  size_t ws_bytes = 0;
+};
+
+// Error reporting (thread-local last error string).
+pda_status fail(pda_status s, const std::string& why);
+void clear_error();
+
+// Device workspace pointers derived from a plan.
+struct Workspace {
+  int32_t* err;
+  int32_t* counters;
+  float* part_lse;
+  float* part_out;
+};
+Workspace workspace_views(const Plan& plan, void* base);
+
+// Kernel launchers (return a CUDA error code as int; 0 = success).
+struct GqaArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  float scale;
+  void* out;
+  float* lse;
+};
+int launch_gqa_decode(const Plan& plan, const GqaArgs& args, const Workspace& ws, void* stream);
+
+struct MlaArgs {
+  const void* q;
+  const void* kv_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  float scale;
+  void* out;
+  float* lse;
+};
+int launch_mla_decode(const Plan& plan, const MlaArgs& args, const Workspace& ws, void* stream);
+
+int launch_combine(const float* partial_out, const float* partial_lse, int rows, int num_splits,
+                   int head_dim_v, void* out, int out_dtype, float* lse, void* stream);
+
+// Shape support queries (host-side, for validation before launch).
+bool gqa_supported(const pda_problem& p, std::string* why);
+bool mla_supported(const pda_problem& p, std::string* why);
+
+// CTA residency the planner assumes for each kernel (CTAs per SM).
+int gqa_ctas_per_sm(const pda_problem& p);
+int mla_ctas_per_sm(const pda_problem& p);
+int mla_heads_per_cta(const pda_problem& p);
+
+}  // namespace pda
+
+// The opaque handle of the C ABI is the planner's record.
+struct pda_plan : pda::Plan {};

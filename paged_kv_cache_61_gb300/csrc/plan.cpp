@@ -1,0 +1,190 @@
+// Host-side planning: validate a decode problem and divide its page tiles over CTAs.
+//
+// FlashMLA-ETAP "Usage": scheduling metadata is computed once per decoding step
+// from cache_seqlens and reused by every layer. "From MHA to MLA", section 4: a
+// production runtime picks the number of splits from batch size, head tiles,
+// context length and the number of SMs. Here every CTA receives the same number
+// of page tiles (to within one), so varlen batches and single long sequences
+// both keep every SM busy; the splits of a sequence follow from where the
+// equal ranges cut its segments.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <new>
+
+#include "pda_internal.h"
+
+namespace pda {
+
+namespace {
+
+thread_local std::string g_last_error;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+pda_status fail(pda_status s, const std::string& why) {
+  g_last_error = why;
+  return s;
+}
+
+void clear_error() { g_last_error.clear(); }
+
+Workspace workspace_views(const Plan& plan, void* base) {
+  char* b = static_cast<char*>(base);
+  return Workspace{reinterpret_cast<int32_t*>(b + plan.ws_err),
+                   reinterpret_cast<int32_t*>(b + plan.ws_counters),
+                   reinterpret_cast<float*>(b + plan.ws_part_lse),
+                   reinterpret_cast<float*>(b + plan.ws_part_out)};
+}
+
+}  // namespace pda
+
+using pda::fail;
+
+extern "C" PDA_API const char* pda_last_error(void) { return pda::g_last_error.c_str(); }
+
+extern "C" PDA_API const char* pda_status_string(pda_status s) {
+  switch (s) {
+    case PDA_OK: return "PDA_OK";
+    case PDA_ERR_INVALID_ARG: return "PDA_ERR_INVALID_ARG";
+    case PDA_ERR_UNSUPPORTED: return "PDA_ERR_UNSUPPORTED";
+    case PDA_ERR_WORKSPACE: return "PDA_ERR_WORKSPACE";
+    case PDA_ERR_CUDA: return "PDA_ERR_CUDA";
+  }
+  return "PDA_ERR_UNKNOWN";
+}
+
+extern "C" PDA_API pda_status pda_plan_create(pda_plan** out, const pda_problem* prob,
+                                      const int32_t* ctx_host) {
+  pda::clear_error();
+  if (out == nullptr) return fail(PDA_ERR_INVALID_ARG, "plan output pointer is NULL");
+  *out = nullptr;
+  if (prob == nullptr) return fail(PDA_ERR_INVALID_ARG, "problem is NULL");
+  const pda_problem& p = *prob;
+  if (p.kind != PDA_KIND_GQA && p.kind != PDA_KIND_MLA)
+    return fail(PDA_ERR_INVALID_ARG, "kind must be PDA_KIND_GQA or PDA_KIND_MLA");
+  if (p.dtype != PDA_FP16 && p.dtype != PDA_BF16)
+    return fail(PDA_ERR_INVALID_ARG, "dtype must be PDA_FP16 or PDA_BF16");
+  if (p.batch < 0) return fail(PDA_ERR_INVALID_ARG, "batch must be >= 0");
+  if (p.num_q_heads < 1 || p.num_kv_heads < 1)
+    return fail(PDA_ERR_INVALID_ARG, "head counts must be >= 1");
+  if (p.num_q_heads % p.num_kv_heads != 0)
+    return fail(PDA_ERR_INVALID_ARG, "H_q must be divisible by H_kv");
+  if (p.page_size < 1 || p.max_blocks_per_seq < 1 || p.num_blocks < 1)
+    return fail(PDA_ERR_INVALID_ARG, "page_size, max_blocks_per_seq and num_blocks must be >= 1");
+  if (p.head_dim_qk < 1 || p.head_dim_v < 1)
+    return fail(PDA_ERR_INVALID_ARG, "head dims must be >= 1");
+  if (p.num_sms < 0 || p.force_num_ctas < 0)
+    return fail(PDA_ERR_INVALID_ARG, "num_sms and force_num_ctas must be >= 0");
+  if (p.batch > 0 && ctx_host == nullptr)
+    return fail(PDA_ERR_INVALID_ARG, "context_lens_host is NULL");
+
+  std::string why;
+  if (p.kind == PDA_KIND_GQA ? !pda::gqa_supported(p, &why) : !pda::mla_supported(p, &why))
+    return fail(PDA_ERR_UNSUPPORTED, why);
+
+  const int64_t max_ctx = int64_t(p.max_blocks_per_seq) * p.page_size;
+  for (int32_t b = 0; b < p.batch; ++b) {
+    if (ctx_host[b] < 1)
+      return fail(PDA_ERR_INVALID_ARG, "context_lens[" + std::to_string(b) + "] < 1");
+    if (ctx_host[b] > max_ctx)
+      return fail(PDA_ERR_INVALID_ARG, "context_lens[" + std::to_string(b) +
+                                           "] exceeds max_blocks_per_seq * page_size");
+  }
+
+  int num_sms = p.num_sms;
+  if (num_sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(PDA_ERR_CUDA, "could not query the SM count of the current device");
+    }
+  }
+
+  pda_plan* plan = new (std::nothrow) pda_plan();
+  if (plan == nullptr) return fail(PDA_ERR_INVALID_ARG, "out of host memory");
+  plan->prob = p;
+  plan->prob.num_sms = num_sms;
+  plan->context_lens.assign(ctx_host, ctx_host + p.batch);
+
+  int ctas_per_sm;
+  int64_t min_tiles_per_cta;
+  if (p.kind == PDA_KIND_GQA) {
+    plan->group = p.num_q_heads / p.num_kv_heads;
+    plan->segs_per_seq = p.num_kv_heads;
+    plan->head_subtiles = (plan->group + 7) / 8;
+    ctas_per_sm = pda::gqa_ctas_per_sm(p);
+    min_tiles_per_cta = 4;
+  } else {
+    plan->group = pda::mla_heads_per_cta(p);
+    plan->segs_per_seq = p.num_q_heads / plan->group;
+    plan->head_subtiles = 1;
+    ctas_per_sm = pda::mla_ctas_per_sm(p);
+    min_tiles_per_cta = 2;
+  }
+
+  int64_t pages_total = 0;
+  for (int32_t b = 0; b < p.batch; ++b) pages_total += pda::cdiv(ctx_host[b], p.page_size);
+  plan->total_tiles = pages_total * plan->segs_per_seq;
+
+  if (plan->total_tiles > 0) {
+    int64_t q;
+    if (p.force_num_ctas > 0) {
+      q = pda::cdiv(plan->total_tiles, p.force_num_ctas);
+    } else {
+      const int64_t max_ctas = int64_t(num_sms) * ctas_per_sm;
+      q = std::max(min_tiles_per_cta, pda::cdiv(plan->total_tiles, max_ctas));
+    }
+    plan->tiles_per_cta = q;
+    plan->num_ctas = int32_t(pda::cdiv(plan->total_tiles, q));
+  }
+
+  // Splits per sequence: how many CTA ranges cut each of its segments.
+  plan->splits.assign(p.batch, 1);
+  int64_t start = 0;
+  for (int32_t b = 0; b < p.batch; ++b) {
+    const int64_t np = pda::cdiv(ctx_host[b], p.page_size);
+    int32_t worst = 1;
+    for (int32_t s = 0; s < plan->segs_per_seq; ++s) {
+      const int64_t s0 = start + s * np, s1 = s0 + np;
+      worst = std::max<int32_t>(worst, int32_t((s1 - 1) / plan->tiles_per_cta -
+                                               s0 / plan->tiles_per_cta + 1));
+    }
+    plan->splits[b] = worst;
+    start += np * plan->segs_per_seq;
+  }
+
+  size_t off = 0;
+  plan->ws_err = off;
+  off += 256;
+  plan->ws_counters = off;
+  off = pda::round_up(off + sizeof(int32_t) * size_t(p.batch) * plan->segs_per_seq, 256);
+  plan->ws_part_lse = off;
+  off = pda::round_up(off + sizeof(float) * size_t(plan->num_ctas) * 2 * plan->group, 256);
+  plan->ws_part_out = off;
+  off = pda::round_up(
+      off + sizeof(float) * size_t(plan->num_ctas) * 2 * plan->group * p.head_dim_v, 256);
+  plan->ws_bytes = off;
+
+  *out = plan;
+  return PDA_OK;
+}
+
+extern "C" PDA_API void pda_plan_destroy(pda_plan* plan) { delete plan; }
+
+extern "C" PDA_API size_t pda_plan_workspace_bytes(const pda_plan* plan) {
+  return plan ? plan->ws_bytes : 0;
+}
+
+extern "C" PDA_API int32_t pda_plan_num_ctas(const pda_plan* plan) { return plan ? plan->num_ctas : 0; }
+
+extern "C" PDA_API int32_t pda_plan_num_splits(const pda_plan* plan, int32_t b) {
+  if (plan == nullptr || b < 0 || b >= plan->prob.batch) return 0;
+  return plan->splits[b];
+}

@@ -1,0 +1,82 @@
+"""Helpers for GPU tests: move a synthetic case to the device and run it through the C ABI."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from paged_kv_cache_61_gb300 import pda, synth
+
+TOL_OUT = {synth.FP16: 2e-3, synth.BF16: 1e-2}   # max-abs error of out vs the float64 oracle
+TOL_LSE = 1e-3                                   # max-abs error of the fp32 LSE
+
+
+def torch_dtype(dtype: str):
+    return torch.float16 if dtype == synth.FP16 else torch.bfloat16
+
+
+def to_device_16(bits: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device)
+    return t.view(torch_dtype(dtype))
+
+
+def device_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def make_plan(case: synth.DecodeCase, force_num_ctas: int = 0) -> pda.Plan:
+    return pda.Plan(kind=pda.PDA_KIND_GQA if case.kind == "gqa" else pda.PDA_KIND_MLA,
+                    dtype=pda.PDA_FP16 if case.dtype == synth.FP16 else pda.PDA_BF16,
+                    batch=case.batch, num_q_heads=case.num_q_heads,
+                    num_kv_heads=case.num_kv_heads, head_dim_qk=case.head_dim_qk,
+                    head_dim_v=case.head_dim_v, page_size=case.page_size,
+                    max_blocks_per_seq=case.max_blocks_per_seq, num_blocks=case.num_blocks,
+                    context_lens=case.context_lens.tolist(), force_num_ctas=force_num_ctas)
+
+
+class DeviceCase:
+    """A case's inputs resident on the GPU plus output buffers and a zeroed workspace."""
+
+    def __init__(self, case: synth.DecodeCase, force_num_ctas: int = 0):
+        self.case = case
+        self.q = to_device_16(case.q, case.dtype)
+        if case.kind == "gqa":
+            self.k = to_device_16(case.k_cache, case.dtype)
+            self.v = to_device_16(case.v_cache, case.dtype)
+        else:
+            self.kv = to_device_16(case.kv_cache, case.dtype)
+        self.tables = torch.from_numpy(case.block_tables).cuda()
+        self.ctx = torch.from_numpy(case.context_lens).cuda()
+        self.out = torch.full((case.batch, case.num_q_heads, case.head_dim_v), float("nan"),
+                              dtype=torch_dtype(case.dtype), device="cuda")
+        self.lse = torch.full((case.batch, case.num_q_heads), float("nan"), dtype=torch.float32,
+                              device="cuda")
+        self.replan(force_num_ctas)
+
+    def replan(self, force_num_ctas: int = 0):
+        self.plan = make_plan(self.case, force_num_ctas)
+        self.ws = torch.zeros(max(256, self.plan.workspace_bytes), dtype=torch.uint8, device="cuda")
+        pda.workspace_init(self.plan, self.ws)
+
+    def run(self, out=None, lse="default"):
+        c = self.case
+        out = self.out if out is None else out
+        lse = self.lse if isinstance(lse, str) else lse
+        if c.kind == "gqa":
+            pda.paged_decode_attn(self.q, self.k, self.v, self.tables, self.ctx, c.scale, out, lse,
+                                  self.plan, self.ws)
+        else:
+            pda.mla_decode(self.q, self.kv, self.tables, self.ctx, c.scale, out, lse, self.plan,
+                           self.ws)
+        return out, lse
+
+
+def compare(case, out_gpu: torch.Tensor, lse_gpu: torch.Tensor, ref_out, ref_lse, rows=None):
+    """Max-abs errors of (out, lse) over all rows or the listed (b, h) rows."""
+    o = out_gpu.float().cpu().numpy().astype(np.float64)
+    l = lse_gpu.cpu().numpy().astype(np.float64)
+    if rows is None:
+        return float(np.abs(o - ref_out).max()), float(np.abs(l - ref_lse).max())
+    bs = [r[0] for r in rows]
+    hs = [r[1] for r in rows]
+    return (float(np.abs(o[bs, hs] - ref_out[bs, hs]).max()),
+            float(np.abs(l[bs, hs] - ref_lse[bs, hs]).max()))

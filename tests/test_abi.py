@@ -1,0 +1,132 @@
+"""The C-ABI library: it loads, exports every declared symbol and validates on the host.
+
+No compute call runs here: every call below returns before touching a GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_61_gb300 import build, pda
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    if not os.path.exists(pda.LIB_PATH):
+        build.build()
+    return pda.lib()
+
+
+def _declared_functions():
+    names = []
+    for header in os.listdir(os.path.join(ROOT, "include")):
+        if header.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", header)).read()
+            names += re.findall(r"PDA_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+    return names
+
+
+def test_every_declared_symbol_is_exported():
+    names = _declared_functions()
+    assert len(names) >= 12
+    handle = ctypes.CDLL(pda.LIB_PATH)
+    for name in names:
+        assert hasattr(handle, name), f"{name} declared in include/ but not exported"
+
+
+def test_status_strings():
+    assert pda.status_name(pda.PDA_OK) == "PDA_OK"
+    assert pda.status_name(pda.PDA_ERR_WORKSPACE) == "PDA_ERR_WORKSPACE"
+
+
+def _plan(**kw):
+    args = dict(kind=pda.PDA_KIND_GQA, dtype=pda.PDA_FP16, batch=2, num_q_heads=8, num_kv_heads=2,
+                head_dim_qk=64, head_dim_v=64, page_size=16, max_blocks_per_seq=4, num_blocks=8,
+                context_lens=[5, 64], num_sms=152)
+    args.update(kw)
+    return pda.Plan(**args)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(num_q_heads=6, num_kv_heads=4), pda.PDA_ERR_INVALID_ARG),      # H_q % H_kv != 0
+    (dict(context_lens=[0, 5]), pda.PDA_ERR_INVALID_ARG),                 # ctx < 1
+    (dict(context_lens=[65, 5]), pda.PDA_ERR_INVALID_ARG),                # ctx > max_blocks * P
+    (dict(dtype=7), pda.PDA_ERR_INVALID_ARG),
+    (dict(kind=9), pda.PDA_ERR_INVALID_ARG),
+    (dict(head_dim_qk=96, head_dim_v=96), pda.PDA_ERR_UNSUPPORTED),
+    (dict(page_size=32, context_lens=[5, 5]), pda.PDA_ERR_UNSUPPORTED),
+    (dict(num_q_heads=128, num_kv_heads=2), pda.PDA_ERR_UNSUPPORTED),     # G = 64
+    (dict(batch=-1), pda.PDA_ERR_INVALID_ARG),
+])
+def test_plan_rejects_bad_problems(kw, status):
+    with pytest.raises(pda.PdaError) as e:
+        _plan(**kw)
+    assert e.value.status == status
+    assert pda.lib().pda_last_error().decode() != ""
+
+
+def test_plan_properties():
+    p = _plan()
+    assert p.num_ctas >= 1
+    assert p.workspace_bytes >= 256 and p.workspace_bytes % 256 == 0
+    assert p.num_splits(0) >= 1 and p.num_splits(5) == 0
+    one = _plan(force_num_ctas=1)
+    assert one.num_ctas == 1 and one.num_splits(0) == one.num_splits(1) == 1
+
+
+def test_uniform_batch_split_counts():
+    # 64 sequences x 8 KV heads x 64 pages over 7 forced CTAs: each range holds
+    # ceil(32768/7) tiles, so no segment is cut by more than 2 ranges
+    p = _plan(batch=64, num_q_heads=32, num_kv_heads=8, head_dim_qk=128, head_dim_v=128,
+              max_blocks_per_seq=64, num_blocks=4096, context_lens=[1024] * 64, force_num_ctas=7)
+    assert p.num_ctas == 7
+    assert max(p.num_splits(b) for b in range(64)) == 2
+    # one long sequence is split across every CTA
+    p = _plan(batch=1, num_q_heads=32, num_kv_heads=8, head_dim_qk=128, head_dim_v=128,
+              max_blocks_per_seq=2048, num_blocks=2048, context_lens=[32768])
+    assert p.num_ctas > 100 and p.num_splits(0) > 10
+
+
+def test_empty_batch_is_a_no_op():
+    p = _plan(batch=0, context_lens=[])
+    assert p.num_ctas == 0
+    # all pointers NULL: nothing is enqueued, so this is safe without a GPU
+    pda.paged_decode_attn(0, 0, 0, 0, 0, 0.125, 0, None, p, 0, stream=0)
+
+
+@pytest.mark.parametrize("which", ["q", "k", "out", "ws", "misaligned_q", "scale", "kind"])
+def test_decode_rejects_bad_arguments_before_launch(which):
+    p = _plan()
+    args = dict(q=4096, k=8192, v=8192, tables=64, ctx=128, scale=0.125, out=4096, lse=None,
+                ws=1 << 20)
+    if which == "q":
+        args["q"] = 0
+    elif which == "k":
+        args["k"] = 0
+    elif which == "out":
+        args["out"] = 0
+    elif which == "ws":
+        args["ws"] = 0
+    elif which == "misaligned_q":
+        args["q"] = 4098
+    elif which == "scale":
+        args["scale"] = float("inf")
+    with pytest.raises(pda.PdaError) as e:
+        if which == "kind":
+            pda.mla_decode(args["q"], args["k"], args["tables"], args["ctx"], args["scale"],
+                           args["out"], None, p, args["ws"], stream=0)
+        else:
+            pda.paged_decode_attn(args["q"], args["k"], args["v"], args["tables"], args["ctx"],
+                                  args["scale"], args["out"], args["lse"], p, args["ws"], stream=0)
+    assert e.value.status in (pda.PDA_ERR_INVALID_ARG, pda.PDA_ERR_WORKSPACE)
+
+
+def test_combine_rejects_bad_sizes():
+    with pytest.raises(pda.PdaError):
+        pda.combine_splits(0, 0, 4, 0, 128, 0, pda.PDA_FP16, None, stream=0)
+    with pytest.raises(pda.PdaError):
+        pda.combine_splits(0, 0, 4, 2, 130, 0, pda.PDA_FP16, None, stream=0)
+    pda.combine_splits(0, 0, 0, 2, 128, 0, pda.PDA_FP16, None, stream=0)  # rows == 0: no-op
