@@ -16,7 +16,8 @@
 //    coordinates (d, kvh, 0, phys): the 64-bit address is formed by the TMA
 //    unit, so no 32-bit product phys*stride exists) of each page's K and V into
 //    a ring of shared-memory stages with 128-byte swizzle.
-//  * Four consumer warps take pages round-robin. Each page is one m16n8k16
+//  * Four consumer warps take pages round-robin (by CTA-local tile index, so a
+//    ring stage always has the same consumers). Each page is one m16n8k16
 //    tile in the transposed ("keys on M") orientation the FlashMLA-ETAP README
 //    describes for Hopper WGMMA, here on warp MMA: S^T[16 tokens x 8 heads] =
 //    K * Q^T, so a group of 4 heads wastes half an MMA instead of 3/4 of one.
@@ -46,9 +47,13 @@ namespace {
 constexpr int kPage = 16;
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 6;
+// Ring stages: a multiple of the consumer warps, so stage s is only ever read by
+// the warps whose tiles are t = s (mod kConsumerWarps / NHT), each of which takes
+// every fill of that stage in order (the parity waits rely on this).
+constexpr int kStages = 8;
 constexpr int kBoxBytes = kPage * 128;  // one TMA box: 16 tokens x 64 dims x 16 bit
-constexpr int kCtasPerSm = 3;
+constexpr int kCtasPerSm = 2;
+static_assert(kStages % kConsumerWarps == 0, "each stage needs a fixed set of consumer warps");
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -314,7 +319,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
     for (int mt = 0; mt < kKS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
 
-    for (int i = pres; i < npg; i += kWP) {
+    // This warp's tiles are those with CTA-local index t = pres (mod kWP).
+    const int first = int(((pres - k) % kWP + kWP) % kWP);
+    for (int i = first; i < npg; i += kWP) {
       const int64_t t = k + i;
       const int stage = int(t % kStages);
       const uint32_t par = uint32_t(t / kStages) & 1u;
