@@ -1,0 +1,449 @@
+#!/usr/bin/env python
+"""Benchmark of paged decode attention on GB300 (one JSON line on stdout, rank 0).
+
+Default workload: GQA paged decode, B=64, ctx=1024, Hq=32, Hkv=8, D=128, fp16,
+PAGE=16, randomly permuted block tables (the workload the drill page measures
+at 1520 GB/s on an RTX 5090). A step is one decode call: one pass of the whole
+hot path (block-table walk, TMA page stream, scores, online softmax, PV, split
+merge) over the batch. ``value`` is the achieved algorithmic HBM bandwidth:
+the K+V bytes of the attended tokens divided by the device time of a step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Multi-GPU (torchrun, one rank per GPU): every rank decodes its own batch of the
+same shape (weak scaling, no data-path collective); time = max over ranks.
+``--impl reference`` times the float64 CPU oracle on the host cores instead
+(rank 0 only), each step a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+if "reference" in sys.argv:
+    # the reference arm reports one core: keep numpy's BLAS on one thread
+    for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[_v] = "1"
+
+from paged_kv_cache_61_gb300 import synth, traffic  # noqa: E402
+
+DEFAULT_WORKLOAD = "gqa_b64_ctx1k"
+L2_BYTES = 129 * 2 ** 20
+KERNEL_SOURCES = {"gqa": ["gqa_decode.cu", "ptx.cuh"], "mla": ["mla_decode.cu", "ptx.cuh"]}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------- helpers
+def env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_hash(kind: str) -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, "paged_kv_cache_61_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kind: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel is unchanged since."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    rec = d.get(workload)
+    if not rec or rec.get("kernel_hash") != kernel_hash(kind):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms in a background process."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.lines = []
+        self.proc = None
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_stop(self):
+        self.t_stop = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.reader.join(timeout=2)
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append((t, float(parts[2]), float(parts[3]), parts[6:10]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        inside = [r for r in rows if self.t_start - 0.06 <= r[0] <= self.t_stop + 0.06]
+        use = inside or sorted(rows, key=lambda r: abs(r[0] - self.t_stop))[:3]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+# ---------------------------------------------------------------- workload accounting
+def accounting(case):
+    """Algorithmic bytes and FLOPs of one step (K+V of the attended tokens; 2 FLOP per MAC)."""
+    ctx = case.context_lens.tolist()
+    if case.kind == "gqa":
+        kv = traffic.gqa_kv_bytes(ctx, case.num_kv_heads, case.head_dim_qk, 2)
+    else:
+        kv = traffic.mla_kv_bytes(ctx, case.head_dim_qk, 2)
+    flops = traffic.decode_flops(ctx, case.num_q_heads, case.head_dim_qk, case.head_dim_v)
+    return kv, flops
+
+
+def workload_config(case, rotation_copies):
+    cfg = {"workload": case.name, "kind": case.kind, "batch": case.batch,
+           "num_q_heads": case.num_q_heads, "num_kv_heads": case.num_kv_heads,
+           "head_dim_qk": case.head_dim_qk, "head_dim_v": case.head_dim_v,
+           "page_size": case.page_size, "dtype": case.dtype,
+           "context_lens": ("all " + str(int(case.context_lens[0]))
+                            if (case.context_lens == case.context_lens[0]).all()
+                            else f"varlen sum {int(case.context_lens.sum())}"),
+           "seed": 0}
+    if rotation_copies:
+        cfg["l2"] = (f"inputs larger than L2: steps rotate over {rotation_copies} copies of the "
+                     f"cache ({rotation_copies} x {accounting(case)[0] / 1e6:.0f} MB)")
+    return cfg
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def oracle_sample(case, budget_s: float):
+    """Run the oracle on whole sequences until ~budget_s; return (kv_bytes_done, seconds)."""
+    import oracle
+    done_bytes, t0 = 0, time.perf_counter()
+    b = 0
+    while True:
+        rows = [(b, h) for h in range(case.num_q_heads)]
+        if case.kind == "gqa":
+            oracle.paged_decode(case.q, case.k_cache, case.v_cache, case.block_tables,
+                                case.context_lens, case.scale, case.page_size, case.dtype,
+                                rows=rows)
+            done_bytes += traffic.gqa_kv_bytes([case.context_lens[b]], case.num_kv_heads,
+                                               case.head_dim_qk, 2)
+        else:
+            oracle.mla_decode(case.q, case.kv_cache, case.block_tables, case.context_lens,
+                              case.scale, case.page_size, case.dtype, rows=rows)
+            done_bytes += traffic.mla_kv_bytes([case.context_lens[b]], case.head_dim_qk, 2)
+        b = (b + 1) % case.batch
+        if time.perf_counter() - t0 >= budget_s:
+            return done_bytes, time.perf_counter() - t0, b
+
+
+def cpu_baseline(workload: str, budget_s: float = 10.0):
+    """Time the oracle single-threaded in a fresh process (BLAS pinned to one thread)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; from paged_kv_cache_61_gb300 "
+            "import synth; c = synth.workload(%r); b, s, n = bench.oracle_sample(c, %r); "
+            "print(json.dumps([b, s, n]))") % (ROOT, workload, budget_s)
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       timeout=600)
+    if r.returncode != 0:
+        return {"value": None, "error": r.stderr.strip().splitlines()[-1:]}
+    done, secs, nseq = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": done / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"float64 numpy oracle, one thread, {max(nseq, 1)} whole sequences "
+                      f"(all heads) of {workload} in {secs:.1f} s"}
+
+
+def run_reference(args, workload):
+    """The reference arm: the oracle, as it stands, on the host cores."""
+    case = synth.workload(workload)
+    kv, flops = accounting(case)
+    per_step_budget = max(0.02, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(case, per_step_budget)
+    total_bytes, total_s = 0, 0.0
+    for _ in range(args.steps):
+        b, s, _n = oracle_sample(case, per_step_budget)
+        total_bytes += b
+        total_s += s
+    gbs = total_bytes / total_s / 1e9
+    value = gbs if case.kind == "gqa" else gbs * (flops / kv) / 1e3
+    unit = "GB/s" if case.kind == "gqa" else "TFLOP/s"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": kv / (gbs * 1e9) * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, seed 0)",
+            "config": workload_config(case, 0),
+            "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
+                             "sample": f"each step: whole sequences of {workload} for "
+                                       f"~{per_step_budget:.2f} s, one thread"},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+METRIC = "paged decode attn achieved HBM GB/s (% of GB300 peak), μs/step; MLA TFLOPS"
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_gpu(args, workload, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    from paged_kv_cache_61_gb300 import pda
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    case = synth.workload(workload, seed=rank)
+    kv_bytes, flops = accounting(case)
+    tdt = torch.float16 if case.dtype == synth.FP16 else torch.bfloat16
+
+    def dev16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(tdt)
+
+    copies = max(1, min(64, math.ceil(4 * L2_BYTES / kv_bytes)))
+    q = dev16(case.q)
+    if case.kind == "gqa":
+        k0, v0 = dev16(case.k_cache), dev16(case.v_cache)
+        caches = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(copies - 1)]
+    else:
+        kv0 = dev16(case.kv_cache)
+        caches = [(kv0, None)] + [(kv0.clone(), None) for _ in range(copies - 1)]
+    tables = torch.from_numpy(case.block_tables).cuda()
+    ctx = torch.from_numpy(case.context_lens).cuda()
+    out = torch.empty(case.batch, case.num_q_heads, case.head_dim_v, dtype=tdt, device="cuda")
+    lse = torch.empty(case.batch, case.num_q_heads, dtype=torch.float32, device="cuda")
+    plan = pda.Plan(kind=pda.PDA_KIND_GQA if case.kind == "gqa" else pda.PDA_KIND_MLA,
+                    dtype=pda.PDA_FP16 if case.dtype == synth.FP16 else pda.PDA_BF16,
+                    batch=case.batch, num_q_heads=case.num_q_heads,
+                    num_kv_heads=case.num_kv_heads, head_dim_qk=case.head_dim_qk,
+                    head_dim_v=case.head_dim_v, page_size=case.page_size,
+                    max_blocks_per_seq=case.max_blocks_per_seq, num_blocks=case.num_blocks,
+                    context_lens=case.context_lens.tolist())
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    pda.workspace_init(plan, ws, stream)
+
+    def step(i, q_=q, out_=out, lse_=lse, tables_=tables, ctx_=ctx):
+        kc, vc = caches[i % copies]
+        if case.kind == "gqa":
+            pda.paged_decode_attn(q_, kc, vc, tables_, ctx_, case.scale, out_, lse_, plan, ws,
+                                  stream)
+        else:
+            pda.mla_decode(q_, kc, tables_, ctx_, case.scale, out_, lse_, plan, ws, stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_start()
+    t_all0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step(i)
+        ends[i].record(stream)
+    t_all1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    if sampler:
+        sampler.mark_stop()
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = t_all0.elapsed_time(t_all1)
+    ms_per_step = total_ms / args.steps
+    if dist is not None:
+        t = torch.tensor([ms_per_step], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    clocks = sampler.stop() if sampler else None
+    if rank != 0:
+        return
+
+    # ---- end to end through the C ABI: pinned host inputs in, outputs back, every step
+    e2e_steps = min(args.steps, 500)
+    q_h = q.cpu().pin_memory()
+    tables_h = tables.cpu().pin_memory()
+    ctx_h = ctx.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    q_d, tables_d, ctx_d = torch.empty_like(q), torch.empty_like(tables), torch.empty_like(ctx)
+    h2d = q_h.numel() * q_h.element_size() + tables_h.numel() * 4 + ctx_h.numel() * 4
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+
+    def e2e_step(i):
+        q_d.copy_(q_h, non_blocking=True)
+        tables_d.copy_(tables_h, non_blocking=True)
+        ctx_d.copy_(ctx_h, non_blocking=True)
+        step(i, q_=q_d, tables_=tables_d, ctx_=ctx_d)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    pk, pk_src = peaks()
+    mean_launch_ms = statistics.mean(per_launch_ms)
+    if case.kind == "gqa":
+        value = kv_bytes * world / (ms_per_step * 1e-3) / 1e9
+        unit = "GB/s"
+        achieved = kv_bytes / (mean_launch_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "peak_source": f"hbm_gbs of {pk_src}",
+                "frac_of_8TBs_spec": achieved / 8000.0}
+        e2e_value = kv_bytes / (e2e_ms * 1e-3) / 1e9
+    else:
+        value = flops * world / (ms_per_step * 1e-3) / 1e12
+        unit = "TFLOP/s"
+        t_bytes = kv_bytes / (pk["hbm_gbs"] * 1e9)
+        t_flops = flops / (pk["bf16_tflops"] * 1e12)
+        achieved_gbs = kv_bytes / (mean_launch_ms * 1e-3) / 1e9
+        achieved_tf = flops / (mean_launch_ms * 1e-3) / 1e12
+        if t_bytes >= t_flops:
+            roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": achieved_gbs / pk["hbm_gbs"], "peak_source": f"hbm_gbs of {pk_src}"}
+        else:
+            roof = {"bound": "tensor", "achieved": achieved_tf, "peak": pk["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": achieved_tf / pk["bf16_tflops"],
+                    "peak_source": f"bf16_tflops of {pk_src}"}
+        roof["tflops"] = achieved_tf
+        roof["frac_of_slower_roof"] = max(t_bytes, t_flops) / (mean_launch_ms * 1e-3)
+        e2e_value = flops / (e2e_ms * 1e-3) / 1e12
+    roof["traffic"] = recorded_traffic(workload, case.kind)
+    roof["algorithmic_bytes_per_launch"] = kv_bytes
+    roof["mean_launch_us"] = mean_launch_ms * 1e3
+    roof["median_launch_us"] = statistics.median(per_launch_ms) * 1e3
+
+    cpu = None if args.no_cpu_baseline else cpu_baseline(workload)
+    line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_step": ms_per_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16" if case.dtype == synth.FP16 else "bf16",
+            "data": "synthetic (seeded N(0,1) values, random block tables, seed = rank)",
+            "config": workload_config(case, copies), "roofline": roof, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "path": "pinned host q/block_tables/context_lens -> device, C-ABI decode, "
+                            "out/lse -> pinned host, every step; caches resident in HBM"},
+            "gpu_launches": args.steps, "clocks": clocks,
+            "plan": {"num_ctas": plan.num_ctas, "max_splits": max(plan.num_splits(b)
+                                                                  for b in range(case.batch))}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=synth.WORKLOADS)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = env_int("RANK", 0)
+    world = env_int("WORLD_SIZE", 1)
+    local_rank = env_int("LOCAL_RANK", 0)
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, args.workload)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_gpu(args, args.workload, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
