@@ -2,6 +2,8 @@
 
 Usage: python -m paged_kv_cache_61_gb300.build   (or call build()).
 The translation units compile in parallel; the result lands next to this file.
+PDA_EXTRA_NVCC_FLAGS (environment) adds flags, e.g. -DPDA_GQA_STAGES=12 to
+change a kernel's tuning constants.
 """
 from __future__ import annotations
 
@@ -30,7 +32,8 @@ def _nvcc() -> str:
 
 def _compile(src: str, verbose: bool) -> str:
     obj = os.path.join(OBJDIR, src + ".o")
-    cmd = [_nvcc(), "-std=c++17", "-O3", "-lineinfo", *ARCH, "-Xcompiler", "-fPIC",
+    extra = os.environ.get("PDA_EXTRA_NVCC_FLAGS", "").split()
+    cmd = [_nvcc(), "-std=c++17", "-O3", "-lineinfo", *ARCH, *extra, "-Xcompiler", "-fPIC",
            "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC,
            "-DPDA_BUILD", "-c", os.path.join(CSRC, src), "-o", obj]
     if src.endswith(".cu"):

@@ -28,9 +28,11 @@
 //    hold (even NaN) cannot reach the output.
 //  * At the end of each (sequence, KV head) piece the warps merge their states
 //    in shared memory; a complete segment is written directly, a split piece
-//    writes (O_s, L_s) to its CTA's slot, and the last piece to arrive (atomic
-//    counter) combines all pieces ("From MHA to MLA", section 4) and resets the
-//    counter.
+//    writes (O_s, L_s) to its CTA's slot. A segment cut into a few pieces is
+//    merged ("From MHA to MLA", section 4) by the last piece to arrive (atomic
+//    counter, reset afterwards); one cut into many pieces (a single long
+//    sequence, MQA) is merged by the split-merge kernel, which the decode grid
+//    releases early through programmatic dependent launch.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -50,9 +52,22 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 // Ring stages: a multiple of the consumer warps, so stage s is only ever read by
 // the warps whose tiles are t = s (mod kConsumerWarps / NHT), each of which takes
 // every fill of that stage in order (the parity waits rely on this).
-constexpr int kStages = 8;
+#ifndef PDA_GQA_STAGES
+#define PDA_GQA_STAGES 8
+#endif
+#ifndef PDA_GQA_CTAS_PER_SM
+#define PDA_GQA_CTAS_PER_SM 2
+#endif
+#ifndef PDA_GQA_L2_PREFETCH
+#define PDA_GQA_L2_PREFETCH 16
+#endif
+constexpr int kStages = PDA_GQA_STAGES;
 constexpr int kBoxBytes = kPage * 128;  // one TMA box: 16 tokens x 64 dims x 16 bit
-constexpr int kCtasPerSm = 2;
+constexpr int kCtasPerSm = PDA_GQA_CTAS_PER_SM;
+// The producer also asks L2 for the page this many tiles ahead of the one it loads
+// into the ring (0 = off): more bytes in flight without more shared memory.
+constexpr int kPrefetchAhead = PDA_GQA_L2_PREFETCH;
+static_assert(kPrefetchAhead >= 0 && kPrefetchAhead <= 32, "prefetch distance within the table window");
 static_assert(kStages % kConsumerWarps == 0, "each stage needs a fixed set of consumer warps");
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -68,6 +83,7 @@ struct GqaParams {
   int64_t num_blocks;
   float scale_log2;
   int64_t total_tiles, tiles_per_cta;
+  int32_t heavy_min;  // split segments with more pieces are merged by the split-merge kernel
   int32_t* err;
   int32_t* counters;
   float* part_lse;
@@ -194,6 +210,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const int lane = threadIdx.x & 31;
   const int64_t g_lo = int64_t(blockIdx.x) * p.tiles_per_cta;
   const int64_t g_hi = min(p.total_tiles, g_lo + p.tiles_per_cta);
+  // Let the split-merge grid that may follow on this stream be scheduled early; it
+  // waits for this grid's completion before it reads anything.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (g_lo >= g_hi) return;
 
   if (threadIdx.x == 0) {
@@ -231,8 +250,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int n = min(32, pt.p1 - base);
         for (int j = 0; j < n; ++j) {
           const int32_t phys = __shfl_sync(kFull, cur, j);
+          int32_t pf_phys = 0;
+          if (kPrefetchAhead > 0)
+            pf_phys = __shfl_sync(kFull, (j + kPrefetchAhead < 32) ? cur : next,
+                                  (j + kPrefetchAhead) & 31);
           int good = 1;
           if (lane == 0) {
+            if (kPrefetchAhead > 0 && base + j + kPrefetchAhead < pt.p1) {
+#pragma unroll
+              for (int db = 0; db < kDB; ++db) {
+                ptx::tma_prefetch_l2_4d(&tm_k, db * 64, pt.kvh, 0, pf_phys);
+                ptx::tma_prefetch_l2_4d(&tm_v, db * 64, pt.kvh, 0, pf_phys);
+              }
+            }
             if (!wait_stage(&empty[stage], phase ^ 1, flags)) {
               good = 0;
             } else {
@@ -469,49 +499,67 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
 
     if (!whole) {
-      // ---- split piece: count arrivals; the last piece combines all of them
-      __threadfence();
-      ptx::named_barrier_sync(1, kConsumerWarps * 32);
+      // ---- split piece. Few pieces: count arrivals and let the last piece merge them
+      // here. Many pieces: the split-merge kernel that follows merges them in parallel.
       const int64_t c0 = pt.seg_start / p.tiles_per_cta;
       const int64_t c1 = (pt.seg_start + pt.np - 1) / p.tiles_per_cta;
       const int pieces = int(c1 - c0 + 1);
-      int32_t* counter = p.counters + int64_t(pt.b) * p.num_kv_heads + pt.kvh;
-      if (tid == 0) {
-        const int prev = aborted ? -1 : atomicAdd(counter, 1);
-        flags[1] = (prev == pieces - 1) ? 1 : 0;
-      }
-      ptx::named_barrier_sync(1, kConsumerWarps * 32);
-      if (flags[1]) {
+      if (pieces <= p.heavy_min) {
         __threadfence();
-        for (int idx = tid; idx < p.group * kChunks; idx += kConsumerWarps * 32) {
-          const int j = idx / kChunks;
-          const int dc = idx - j * kChunks;
-          float mx = -INFINITY;
-          for (int64_t c = c0; c <= c1; ++c) {
-            const int sl = (c == c0 && pt.seg_start > c * p.tiles_per_cta) ? 1 : 0;
-            mx = fmaxf(mx, __ldcg(p.part_lse + (c * 2 + sl) * p.group + j));
-          }
-          float den = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          for (int64_t c = c0; c <= c1; ++c) {
-            const int sl = (c == c0 && pt.seg_start > c * p.tiles_per_cta) ? 1 : 0;
-            const int64_t rowi = (c * 2 + sl) * p.group + j;
-            const float ls = __ldcg(p.part_lse + rowi);
-            if (ls == -INFINITY) continue;
-            const float wgt = ptx::exp2_approx((ls - mx) * kLog2e);
-            den += wgt;
-            const float4 a = __ldcg(reinterpret_cast<const float4*>(p.part_out + rowi * D + dc * 8));
-            const float4 b = __ldcg(reinterpret_cast<const float4*>(p.part_out + rowi * D + dc * 8 + 4));
-            o[0] += wgt * a.x; o[1] += wgt * a.y; o[2] += wgt * a.z; o[3] += wgt * a.w;
-            o[4] += wgt * b.x; o[5] += wgt * b.y; o[6] += wgt * b.z; o[7] += wgt * b.w;
-          }
-          const float inv = 1.f / den;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] *= inv;
-          const int64_t orow = int64_t(pt.b) * p.num_q_heads + int64_t(pt.kvh) * p.group + j;
-          *reinterpret_cast<uint4*>(outg + orow * D + dc * 8) = pack8<T>(o);
-          if (dc == 0 && p.lse != nullptr) p.lse[orow] = mx + logf(den);
+        ptx::named_barrier_sync(1, kConsumerWarps * 32);
+        int32_t* counter = p.counters + int64_t(pt.b) * p.num_kv_heads + pt.kvh;
+        if (tid == 0) {
+          const int prev = aborted ? -1 : atomicAdd(counter, 1);
+          flags[1] = (prev == pieces - 1) ? 1 : 0;
         }
-        if (tid == 0) atomicExch(counter, 0);
+        ptx::named_barrier_sync(1, kConsumerWarps * 32);
+        if (flags[1]) {
+          __threadfence();
+          for (int idx = tid; idx < p.group * kChunks; idx += kConsumerWarps * 32) {
+            const int j = idx / kChunks;
+            const int dc = idx - j * kChunks;
+            // online merge over the pieces, four at a time with independent loads
+            float mx = -INFINITY, den = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int64_t cb = c0; cb <= c1; cb += 4) {
+              float ls[4];
+              float4 va[4], vb[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int64_t c = cb + u;
+                ls[u] = -INFINITY;
+                va[u] = vb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (c <= c1) {
+                  const int sl = (c == c0 && pt.seg_start > c * p.tiles_per_cta) ? 1 : 0;
+                  const int64_t rowi = (c * 2 + sl) * p.group + j;
+                  ls[u] = __ldcg(p.part_lse + rowi);
+                  va[u] = __ldcg(reinterpret_cast<const float4*>(p.part_out + rowi * D + dc * 8));
+                  vb[u] = __ldcg(reinterpret_cast<const float4*>(p.part_out + rowi * D + dc * 8 + 4));
+                }
+              }
+              const float nm = fmaxf(fmaxf(mx, fmaxf(ls[0], ls[1])), fmaxf(ls[2], ls[3]));
+              if (nm == -INFINITY) continue;
+              const float f = ptx::exp2_approx((mx - nm) * kLog2e);
+              den *= f;
+#pragma unroll
+              for (int e = 0; e < 8; ++e) o[e] *= f;
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const float wgt = ptx::exp2_approx((ls[u] - nm) * kLog2e);
+                den += wgt;
+                o[0] += wgt * va[u].x; o[1] += wgt * va[u].y; o[2] += wgt * va[u].z; o[3] += wgt * va[u].w;
+                o[4] += wgt * vb[u].x; o[5] += wgt * vb[u].y; o[6] += wgt * vb[u].z; o[7] += wgt * vb[u].w;
+              }
+              mx = nm;
+            }
+            const float inv = 1.f / den;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] *= inv;
+            const int64_t orow = int64_t(pt.b) * p.num_q_heads + int64_t(pt.kvh) * p.group + j;
+            *reinterpret_cast<uint4*>(outg + orow * D + dc * 8) = pack8<T>(o);
+            if (dc == 0 && p.lse != nullptr) p.lse[orow] = mx + logf(den);
+          }
+          if (tid == 0) atomicExch(counter, 0);
+        }
       }
     }
     // the merge area is rewritten by the next portion
@@ -633,17 +681,22 @@ int launch_gqa_decode(const Plan& plan, const GqaArgs& a, const Workspace& ws, v
   prm.scale_log2 = a.scale * kLog2e;
   prm.total_tiles = plan.total_tiles;
   prm.tiles_per_cta = plan.tiles_per_cta;
+  prm.heavy_min = plan.heavy_min_pieces;
   prm.err = ws.err;
   prm.counters = ws.counters;
   prm.part_lse = ws.part_lse;
   prm.part_out = ws.part_out;
   const int nht = plan.head_subtiles <= 1 ? 1 : (plan.head_subtiles <= 2 ? 2 : 4);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int e;
   if (pr.head_dim_qk == 64)
-    return bf16 ? launch_d<64, __nv_bfloat16>(nht, tk, tv, prm, plan.num_ctas, s)
-                : launch_d<64, __half>(nht, tk, tv, prm, plan.num_ctas, s);
-  return bf16 ? launch_d<128, __nv_bfloat16>(nht, tk, tv, prm, plan.num_ctas, s)
-              : launch_d<128, __half>(nht, tk, tv, prm, plan.num_ctas, s);
+    e = bf16 ? launch_d<64, __nv_bfloat16>(nht, tk, tv, prm, plan.num_ctas, s)
+             : launch_d<64, __half>(nht, tk, tv, prm, plan.num_ctas, s);
+  else
+    e = bf16 ? launch_d<128, __nv_bfloat16>(nht, tk, tv, prm, plan.num_ctas, s)
+             : launch_d<128, __half>(nht, tk, tv, prm, plan.num_ctas, s);
+  if (e != 0) return e;
+  return launch_split_merge(plan, ws, a.out, a.lse, stream);
 }
 
 }  // namespace pda

@@ -19,6 +19,18 @@ namespace pda {
 // A segment covered by several CTAs is a Flash-Decoding split: each piece
 // writes a normalized partial (O_s, L_s) into a per-CTA slot and the last piece
 // to finish merges them.
+// A segment split over more CTAs than the decode kernel merges in-line. Its pieces
+// are merged by the stand-alone split-merge kernel that follows the decode kernel.
+struct HeavySegment {
+  int32_t b;          // sequence
+  int32_t seg;        // KV head (GQA) or head group (MLA)
+  int32_t np;         // pages of the sequence
+  int32_t pad;
+  int64_t seg_start;  // flattened index of the segment's first tile
+};
+constexpr int kMaxHeavySegments = 64;
+constexpr int kMaxCtas = 2048;
+
 struct Plan {
   pda_problem prob{};
   int32_t group = 1;            // query heads per segment (GQA: Hq/Hkv; MLA: Hq / head groups)
@@ -29,6 +41,8 @@ struct Plan {
   int32_t num_ctas = 0;
   std::vector<int32_t> context_lens;  // host copy used for planning
   std::vector<int32_t> splits;        // per sequence: max pieces over its segments
+  int32_t heavy_min_pieces = 4;       // segments with more pieces than this are "heavy"
+  std::vector<HeavySegment> heavy;    // at most kMaxHeavySegments
   // workspace layout (byte offsets)
   size_t ws_err = 0;        // int32 device error word
   size_t ws_counters = 0;   // int32 [B * segs_per_seq]
@@ -73,6 +87,10 @@ struct MlaArgs {
   float* lse;
 };
 int launch_mla_decode(const Plan& plan, const MlaArgs& args, const Workspace& ws, void* stream);
+
+// Merge the pieces of the plan's heavy segments (launched after a decode kernel on the
+// same stream, overlapping its tail through programmatic dependent launch).
+int launch_split_merge(const Plan& plan, const Workspace& ws, void* out, float* lse, void* stream);
 
 int launch_combine(const float* partial_out, const float* partial_lse, int rows, int num_splits,
                    int head_dim_v, void* out, int out_dtype, float* lse, void* stream);

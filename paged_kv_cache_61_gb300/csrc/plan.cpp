@@ -141,11 +141,17 @@ extern "C" PDA_API pda_status pda_plan_create(pda_plan** out, const pda_problem*
       const int64_t max_ctas = int64_t(num_sms) * ctas_per_sm;
       q = std::max(min_tiles_per_cta, pda::cdiv(plan->total_tiles, max_ctas));
     }
+    q = std::max(q, pda::cdiv(plan->total_tiles, pda::kMaxCtas));
     plan->tiles_per_cta = q;
     plan->num_ctas = int32_t(pda::cdiv(plan->total_tiles, q));
   }
 
-  // Splits per sequence: how many CTA ranges cut each of its segments.
+  // Splits per sequence: how many CTA ranges cut each of its segments. A segment cut
+  // into more than heavy_min_pieces pieces is merged by the split-merge kernel; the
+  // threshold keeps that list within kMaxHeavySegments (each heavy segment spans more
+  // than heavy_min_pieces CTAs, and neighbours share at most one CTA).
+  plan->heavy_min_pieces = int32_t(std::max<int64_t>(
+      4, pda::cdiv(plan->num_ctas, pda::kMaxHeavySegments)));
   plan->splits.assign(p.batch, 1);
   int64_t start = 0;
   for (int32_t b = 0; b < p.batch; ++b) {
@@ -153,8 +159,16 @@ extern "C" PDA_API pda_status pda_plan_create(pda_plan** out, const pda_problem*
     int32_t worst = 1;
     for (int32_t s = 0; s < plan->segs_per_seq; ++s) {
       const int64_t s0 = start + s * np, s1 = s0 + np;
-      worst = std::max<int32_t>(worst, int32_t((s1 - 1) / plan->tiles_per_cta -
-                                               s0 / plan->tiles_per_cta + 1));
+      const int32_t pieces =
+          int32_t((s1 - 1) / plan->tiles_per_cta - s0 / plan->tiles_per_cta + 1);
+      worst = std::max(worst, pieces);
+      if (pieces > plan->heavy_min_pieces) {
+        if (plan->heavy.size() >= size_t(pda::kMaxHeavySegments)) {
+          delete plan;
+          return fail(PDA_ERR_UNSUPPORTED, "too many heavily split segments");
+        }
+        plan->heavy.push_back(pda::HeavySegment{b, s, int32_t(np), 0, s0});
+      }
     }
     plan->splits[b] = worst;
     start += np * plan->segs_per_seq;
