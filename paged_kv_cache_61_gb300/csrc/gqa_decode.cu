@@ -59,7 +59,7 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 #define PDA_GQA_CTAS_PER_SM 2
 #endif
 #ifndef PDA_GQA_L2_PREFETCH
-#define PDA_GQA_L2_PREFETCH 16
+#define PDA_GQA_L2_PREFETCH 0
 #endif
 constexpr int kStages = PDA_GQA_STAGES;
 constexpr int kBoxBytes = kPage * 128;  // one TMA box: 16 tokens x 64 dims x 16 bit
