@@ -61,12 +61,13 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // ---------------------------------------------------------------- heavy-segment merge
-// One CTA per (heavy segment, head, 32 output dims). The pieces' LSEs are reduced
-// across the CTA, then 16 piece lanes x 8 float4 columns accumulate the weighted
-// partial outputs with independent loads, so a segment cut into hundreds of
-// pieces is merged by many SMs at once instead of by one.
-constexpr int kMergeThreads = 128;
-constexpr int kPieceLanes = 16;
+// One CTA per (heavy segment, head, 32 output dims): 8 float4 columns x 32 piece
+// lanes. Each thread merges its pieces online (running max, rescaled sum and
+// accumulator) with four pieces' loads in flight at a time; the 32 lanes of a
+// column are then merged through shared memory. A segment cut into hundreds of
+// pieces is thus merged by many SMs at once, in a few L2 round trips.
+constexpr int kMergeThreads = 256;
+constexpr int kPieceLanes = kMergeThreads / 8;
 
 struct MergeParams {
   const float* part_out;
@@ -78,29 +79,15 @@ struct MergeParams {
   HeavySegment seg[kMaxHeavySegments];
 };
 
-__device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) {
-  for (int o = 16; o > 0; o >>= 1) {
-    const float u = __shfl_xor_sync(0xffffffffu, v, o);
-    v = is_max ? fmaxf(v, u) : v + u;
-  }
-  const int warp = threadIdx.x >> 5;
-  if ((threadIdx.x & 31) == 0) red[warp] = v;
-  __syncthreads();
-  float r = red[0];
-  for (int w = 1; w < kMergeThreads / 32; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
-  __syncthreads();
-  return r;
-}
-
 template <typename T>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_heavy_kernel(const __grid_constant__ MergeParams p) {
   // Wait until the decode grid that wrote the pieces has completed (programmatic
   // dependent launch lets this grid be scheduled while that one drains).
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  __shared__ float wts[kMaxCtas];
-  __shared__ float red[kMergeThreads / 32];
-  __shared__ float4 part[kPieceLanes][8];
+  __shared__ float sm_m[kPieceLanes][8];
+  __shared__ float sm_l[kPieceLanes][8];
+  __shared__ float4 sm_o[kPieceLanes][8];
 
   const int chunks = p.dv / 32;
   int w = blockIdx.x;
@@ -111,57 +98,63 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int64_t q = p.tiles_per_cta;
   const int64_t c0 = hs.seg_start / q;
   const int n = int((hs.seg_start + hs.np - 1) / q - c0 + 1);
-  auto row_of = [&](int i) -> int64_t {
-    const int slot = (i == 0 && hs.seg_start > c0 * q) ? 1 : 0;
-    return ((c0 + i) * 2 + slot) * p.group + j;
-  };
-
-  float mx = -INFINITY;
-  for (int i = threadIdx.x; i < n; i += kMergeThreads) {
-    const float ls = __ldcg(p.part_lse + row_of(i));
-    wts[i] = ls;
-    mx = fmaxf(mx, ls);
-  }
-  mx = block_reduce(mx, red, true);
-  float sum = 0.f;
-  for (int i = threadIdx.x; i < n; i += kMergeThreads) {
-    const float ls = wts[i];
-    const float wgt = (ls == -INFINITY) ? 0.f : exp2f((ls - mx) * kLog2e);
-    wts[i] = wgt;
-    sum += wgt;
-  }
-  const float den = block_reduce(sum, red, false);  // also orders the wts[] writes
-
   const int col = threadIdx.x & 7;
   const int pl = threadIdx.x >> 3;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const int64_t dofs = int64_t(dchunk) * 32 + col * 4;
-#pragma unroll 4
-  for (int i = pl; i < n; i += kPieceLanes) {
-    const float wgt = wts[i];
-    const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_out + row_of(i) * p.dv + dofs));
-    acc.x += wgt * o.x;
-    acc.y += wgt * o.y;
-    acc.z += wgt * o.z;
-    acc.w += wgt * o.w;
+
+  float m = -INFINITY, l = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i0 = pl; i0 < n; i0 += 4 * kPieceLanes) {
+    float ls[4];
+    float4 o[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * kPieceLanes;
+      ls[u] = -INFINITY;
+      o[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < n) {
+        const int slot = (i == 0 && hs.seg_start > c0 * q) ? 1 : 0;
+        const int64_t row = ((c0 + i) * 2 + slot) * p.group + j;
+        ls[u] = __ldcg(p.part_lse + row);
+        o[u] = __ldcg(reinterpret_cast<const float4*>(p.part_out + row * p.dv + dofs));
+      }
+    }
+    const float nm = fmaxf(fmaxf(m, fmaxf(ls[0], ls[1])), fmaxf(ls[2], ls[3]));
+    if (nm == -INFINITY) continue;
+    const float f = exp2f((m - nm) * kLog2e);
+    l *= f;
+    acc.x *= f; acc.y *= f; acc.z *= f; acc.w *= f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float wgt = exp2f((ls[u] - nm) * kLog2e);
+      l += wgt;
+      acc.x += wgt * o[u].x; acc.y += wgt * o[u].y; acc.z += wgt * o[u].z; acc.w += wgt * o[u].w;
+    }
+    m = nm;
   }
-  part[pl][col] = acc;
+  sm_m[pl][col] = m;
+  sm_l[pl][col] = l;
+  sm_o[pl][col] = acc;
   __syncthreads();
   if (pl == 0) {
-    float4 r = part[0][col];
-    for (int l = 1; l < kPieceLanes; ++l) {
-      r.x += part[l][col].x;
-      r.y += part[l][col].y;
-      r.z += part[l][col].z;
-      r.w += part[l][col].w;
+    float mx = -INFINITY;
+    for (int r = 0; r < kPieceLanes; ++r) mx = fmaxf(mx, sm_m[r][col]);
+    float den = 0.f;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r = 0; r < kPieceLanes; ++r) {
+      if (sm_m[r][col] == -INFINITY) continue;
+      const float f = exp2f((sm_m[r][col] - mx) * kLog2e);
+      den += f * sm_l[r][col];
+      s.x += f * sm_o[r][col].x; s.y += f * sm_o[r][col].y;
+      s.z += f * sm_o[r][col].z; s.w += f * sm_o[r][col].w;
     }
     const float inv = 1.f / den;
     const int64_t orow = int64_t(hs.b) * p.num_q_heads + int64_t(hs.seg) * p.group + j;
-    T* o = static_cast<T*>(p.out) + orow * p.dv + dofs;
-    o[0] = to_out<T>(r.x * inv);
-    o[1] = to_out<T>(r.y * inv);
-    o[2] = to_out<T>(r.z * inv);
-    o[3] = to_out<T>(r.w * inv);
+    T* out = static_cast<T*>(p.out) + orow * p.dv + dofs;
+    out[0] = to_out<T>(s.x * inv);
+    out[1] = to_out<T>(s.y * inv);
+    out[2] = to_out<T>(s.z * inv);
+    out[3] = to_out<T>(s.w * inv);
     if (dchunk == 0 && col == 0 && p.lse != nullptr) p.lse[orow] = mx + logf(den);
   }
 }

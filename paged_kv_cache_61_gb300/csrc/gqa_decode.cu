@@ -58,16 +58,13 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 #ifndef PDA_GQA_CTAS_PER_SM
 #define PDA_GQA_CTAS_PER_SM 2
 #endif
-#ifndef PDA_GQA_L2_PREFETCH
-#define PDA_GQA_L2_PREFETCH 0
+#ifndef PDA_GQA_TMA_5D
+#define PDA_GQA_TMA_5D 1
 #endif
 constexpr int kStages = PDA_GQA_STAGES;
 constexpr int kBoxBytes = kPage * 128;  // one TMA box: 16 tokens x 64 dims x 16 bit
 constexpr int kCtasPerSm = PDA_GQA_CTAS_PER_SM;
-// The producer also asks L2 for the page this many tiles ahead of the one it loads
-// into the ring (0 = off): more bytes in flight without more shared memory.
-constexpr int kPrefetchAhead = PDA_GQA_L2_PREFETCH;
-static_assert(kPrefetchAhead >= 0 && kPrefetchAhead <= 32, "prefetch distance within the table window");
+
 static_assert(kStages % kConsumerWarps == 0, "each stage needs a fixed set of consumer warps");
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -250,19 +247,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int n = min(32, pt.p1 - base);
         for (int j = 0; j < n; ++j) {
           const int32_t phys = __shfl_sync(kFull, cur, j);
-          int32_t pf_phys = 0;
-          if (kPrefetchAhead > 0)
-            pf_phys = __shfl_sync(kFull, (j + kPrefetchAhead < 32) ? cur : next,
-                                  (j + kPrefetchAhead) & 31);
           int good = 1;
           if (lane == 0) {
-            if (kPrefetchAhead > 0 && base + j + kPrefetchAhead < pt.p1) {
-#pragma unroll
-              for (int db = 0; db < kDB; ++db) {
-                ptx::tma_prefetch_l2_4d(&tm_k, db * 64, pt.kvh, 0, pf_phys);
-                ptx::tma_prefetch_l2_4d(&tm_v, db * 64, pt.kvh, 0, pf_phys);
-              }
-            }
             if (!wait_stage(&empty[stage], phase ^ 1, flags)) {
               good = 0;
             } else {
@@ -270,6 +256,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
               if (phys < 0 || int64_t(phys) >= p.num_blocks) atomicOr(p.err, 1);
               ptx::mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
               uint8_t* st = ring + stage * L::kStageBytes;
+#if PDA_GQA_TMA_5D
+              // one copy per tensor: box (64 d, 16 slots, D/64 d-blocks) of one kvh
+              ptx::tma_load_5d(st, &tm_k, &full[stage], 0, 0, 0, pt.kvh, phys, policy);
+              ptx::tma_load_5d(st + kDB * kBoxBytes, &tm_v, &full[stage], 0, 0, 0, pt.kvh, phys,
+                               policy);
+#else
 #pragma unroll
               for (int db = 0; db < kDB; ++db) {
                 ptx::tma_load_4d(st + db * kBoxBytes, &tm_k, &full[stage], db * 64, pt.kvh, 0,
@@ -277,6 +269,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 ptx::tma_load_4d(st + (kDB + db) * kBoxBytes, &tm_v, &full[stage], db * 64,
                                  pt.kvh, 0, phys, policy);
               }
+#endif
               filled |= 1u << stage;
             }
           }
@@ -589,12 +582,28 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Map over a paged cache [num_blocks, P, Hkv, D] (16-bit): dims (d, kvh, slot, block),
-// box (64, 1, P, 1), 128-byte swizzle.
+// Map over a paged cache [num_blocks, P, Hkv, D] (16-bit), 128-byte swizzle.
+// 5-D form: dims (d mod 64, slot, d / 64, kvh, block) with box (64, P, D/64, 1, 1), so
+// one copy lands a (block, kvh) tile as D/64 swizzled [P][64] sub-tiles.
+// 4-D form: dims (d, kvh, slot, block) with box (64, 1, P, 1), one copy per 64 dims.
 bool encode_cache_map(CUtensorMap* map, const void* base, int64_t num_blocks, int page, int hkv,
                       int d, bool bf16) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
+#if PDA_GQA_TMA_5D
+  {
+    const cuuint64_t dims[5] = {64, cuuint64_t(page), cuuint64_t(d / 64), cuuint64_t(hkv),
+                                cuuint64_t(num_blocks)};
+    const cuuint64_t strides[4] = {cuuint64_t(hkv) * d * 2, 128, cuuint64_t(d) * 2,
+                                   cuuint64_t(page) * hkv * d * 2};
+    const cuuint32_t box[5] = {64, cuuint32_t(page), cuuint32_t(d / 64), 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5,
+              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+#endif
   const cuuint64_t dims[4] = {cuuint64_t(d), cuuint64_t(hkv), cuuint64_t(page),
                               cuuint64_t(num_blocks)};
   const cuuint64_t strides[3] = {cuuint64_t(d) * 2, cuuint64_t(hkv) * d * 2,
