@@ -39,7 +39,8 @@ from paged_kv_cache_61_gb300 import synth, traffic  # noqa: E402
 
 DEFAULT_WORKLOAD = "gqa_b64_ctx1k"
 L2_BYTES = 129 * 2 ** 20
-KERNEL_SOURCES = {"gqa": ["gqa_decode.cu", "ptx.cuh"], "mla": ["mla_decode.cu", "ptx.cuh"]}
+KERNEL_SOURCES = {"gqa": ["gqa_decode.cu", "ptx.cuh", "tile_walk.cuh"],
+                  "mla": ["mla_decode.cu", "ptx.cuh", "tile_walk.cuh"]}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 

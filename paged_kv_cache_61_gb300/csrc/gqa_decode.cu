@@ -41,6 +41,7 @@
 
 #include "pda_internal.h"
 #include "ptx.cuh"
+#include "tile_walk.cuh"
 
 namespace pda {
 
@@ -66,7 +67,7 @@ constexpr int kBoxBytes = kPage * 128;  // one TMA box: 16 tokens x 64 dims x 16
 constexpr int kCtasPerSm = PDA_GQA_CTAS_PER_SM;
 
 static_assert(kStages % kConsumerWarps == 0, "each stage needs a fixed set of consumer warps");
-constexpr unsigned kFull = 0xffffffffu;
+constexpr unsigned kFull = kFullMask;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -98,83 +99,6 @@ struct Layout {
   static constexpr int kBarBytes = 2 * kStages * 8 + 16;
   static constexpr int kSmemBytes = 1024 + kRingBytes + kMergeBytes + kBarBytes;
 };
-
-__device__ __forceinline__ int pages_of(int ctx) { return (ctx + kPage - 1) / kPage; }
-
-// ------------------------------------------------------------------ tile walk
-// The CTA's tiles [g_lo, g_hi) of the flattened list (sequence-major, KV-head
-// next, page last) are visited as "portions": maximal runs inside one segment.
-struct Walker {
-  int b;
-  int np;           // pages of sequence b
-  int64_t start_b;  // flattened index of sequence b's first tile
-  int64_t g;        // next tile to visit
-};
-
-struct Portion {
-  int b, kvh, p0, p1, np;
-  int64_t seg_start;
-};
-
-// Warp-collective: find the sequence whose tiles contain flattened tile g.
-__device__ __forceinline__ void walker_init(Walker& w, const GqaParams& p, int64_t g, int lane) {
-  int64_t base = 0;
-  w.b = p.batch;
-  w.start_b = 0;
-  w.np = 1;
-  w.g = g;
-  for (int b0 = 0; b0 < p.batch; b0 += 32) {
-    const int b = b0 + lane;
-    const int np = b < p.batch ? pages_of(__ldg(p.context_lens + b)) : 0;
-    const int64_t width = int64_t(np) * p.num_kv_heads;
-    int64_t incl = width;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int64_t t = __shfl_up_sync(kFull, incl, o);
-      if (lane >= o) incl += t;
-    }
-    const int64_t excl = incl - width;
-    const unsigned hit = __ballot_sync(kFull, b < p.batch && base + excl <= g && g < base + incl);
-    if (hit) {
-      const int src = __ffs(hit) - 1;
-      w.b = b0 + src;
-      w.start_b = base + __shfl_sync(kFull, excl, src);
-      w.np = __shfl_sync(kFull, np, src);
-      return;
-    }
-    base += __shfl_sync(kFull, incl, 31);
-  }
-}
-
-__device__ __forceinline__ Portion walker_next(Walker& w, const GqaParams& p, int64_t g_hi) {
-  const int64_t off = w.g - w.start_b;
-  const int kvh = int(off / w.np);
-  const int p0 = int(off - int64_t(kvh) * w.np);
-  const int p1 = int(min(int64_t(w.np), int64_t(p0) + (g_hi - w.g)));
-  Portion pt{w.b, kvh, p0, p1, w.np, w.start_b + int64_t(kvh) * w.np};
-  w.g += p1 - p0;
-  if (p1 == w.np && kvh + 1 == p.num_kv_heads) {
-    w.start_b += int64_t(p.num_kv_heads) * w.np;
-    ++w.b;
-    if (w.b < p.batch && w.g < g_hi) w.np = pages_of(__ldg(p.context_lens + w.b));
-  }
-  return pt;
-}
-
-// Wait for a ring stage; gives up on timeout or when another warp aborted.
-__device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = ptx::globaltimer();
-  while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (ptx::globaltimer() - t0 > ptx::kWaitLimitNs) return false;
-  }
-}
-
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
 
 template <typename T>
 __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
@@ -223,8 +147,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   __syncthreads();
 
+  const WalkSpec spec{p.context_lens, p.batch, p.num_kv_heads, kPage};
   Walker walk;
-  walker_init(walk, p, g_lo, lane);
+  walker_init(walk, spec, g_lo, lane);
 
   if (warp == kConsumerWarps) {
     // ============================== producer warp ==============================
@@ -238,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint32_t filled = 0;  // bit s: stage s was filled at least once
     bool ok = true;
     while (ok && walk.g < g_hi) {
-      const Portion pt = walker_next(walk, p, g_hi);
+      const Portion pt = walker_next(walk, spec, g_hi);
       const int32_t* row = p.block_tables + int64_t(pt.b) * p.max_blocks;
       int32_t next = (pt.p0 + lane < pt.p1) ? __ldg(row + pt.p0 + lane) : 0;
       for (int base = pt.p0; ok && base < pt.p1; base += 32) {
@@ -249,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           const int32_t phys = __shfl_sync(kFull, cur, j);
           int good = 1;
           if (lane == 0) {
-            if (!wait_stage(&empty[stage], phase ^ 1, flags)) {
+            if (!wait_phase(&empty[stage], phase ^ 1, flags)) {
               good = 0;
             } else {
               // An id outside the pool is flagged; TMA fills such a tile with zeros.
@@ -258,16 +183,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
               uint8_t* st = ring + stage * L::kStageBytes;
 #if PDA_GQA_TMA_5D
               // one copy per tensor: box (64 d, 16 slots, D/64 d-blocks) of one kvh
-              ptx::tma_load_5d(st, &tm_k, &full[stage], 0, 0, 0, pt.kvh, phys, policy);
-              ptx::tma_load_5d(st + kDB * kBoxBytes, &tm_v, &full[stage], 0, 0, 0, pt.kvh, phys,
+              ptx::tma_load_5d(st, &tm_k, &full[stage], 0, 0, 0, pt.seg, phys, policy);
+              ptx::tma_load_5d(st + kDB * kBoxBytes, &tm_v, &full[stage], 0, 0, 0, pt.seg, phys,
                                policy);
 #else
 #pragma unroll
               for (int db = 0; db < kDB; ++db) {
-                ptx::tma_load_4d(st + db * kBoxBytes, &tm_k, &full[stage], db * 64, pt.kvh, 0,
+                ptx::tma_load_4d(st + db * kBoxBytes, &tm_k, &full[stage], db * 64, pt.seg, 0,
                                  phys, policy);
                 ptx::tma_load_4d(st + (kDB + db) * kBoxBytes, &tm_v, &full[stage], db * 64,
-                                 pt.kvh, 0, phys, policy);
+                                 pt.seg, 0, phys, policy);
               }
 #endif
               filled |= 1u << stage;
@@ -319,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   bool aborted = false;
   int64_t k = 0;  // CTA-local index of the current portion's first tile
   while (walk.g < g_hi) {
-    const Portion pt = walker_next(walk, p, g_hi);
+    const Portion pt = walker_next(walk, spec, g_hi);
     const int ctx = __ldg(p.context_lens + pt.b);
     const int npg = pt.p1 - pt.p0;
 
@@ -329,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     {
       const bool hv = jq < p.group;
       const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-          qg + (int64_t(pt.b) * p.num_q_heads + int64_t(pt.kvh) * p.group + (hv ? jq : 0)) * D);
+          qg + (int64_t(pt.b) * p.num_q_heads + int64_t(pt.seg) * p.group + (hv ? jq : 0)) * D);
 #pragma unroll
       for (int ks = 0; ks < kKS; ++ks) {
         qf[ks][0] = hv ? __ldg(qrow + (ks * 16 + cq) / 2) : 0u;
@@ -348,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const int64_t t = k + i;
       const int stage = int(t % kStages);
       const uint32_t par = uint32_t(t / kStages) & 1u;
-      if (!aborted && !wait_stage(&full[stage], par, flags)) {
+      if (!aborted && !wait_phase(&full[stage], par, flags)) {
         aborted = true;
         if (lane == 0) {
           flags[0] = 1;
@@ -451,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
     // ---- merge the warps of each head subtile; write final rows or this CTA's split slot
     const bool whole = (pt.p0 == 0 && pt.p1 == pt.np);
-    const int slot = (pt.seg_start <= g_lo) ? 0 : 1;
+    const int slot = piece_slot(pt.seg_start, g_lo);
     const int64_t slot_row = (int64_t(blockIdx.x) * 2 + slot) * p.group;
     constexpr int kChunks = D / 8;
     for (int idx = tid; idx < p.group * kChunks; idx += kConsumerWarps * 32) {
@@ -480,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       for (int e = 0; e < 8; ++e) o[e] *= inv;
       const float lse_nat = (mx + log2f(lsum)) * kLn2;
       if (whole) {
-        const int64_t orow = int64_t(pt.b) * p.num_q_heads + int64_t(pt.kvh) * p.group + j;
+        const int64_t orow = int64_t(pt.b) * p.num_q_heads + int64_t(pt.seg) * p.group + j;
         *reinterpret_cast<uint4*>(outg + orow * D + dc * 8) = pack8<T>(o);
         if (dc == 0 && p.lse != nullptr) p.lse[orow] = lse_nat;
       } else {
@@ -500,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (pieces <= p.heavy_min) {
         __threadfence();
         ptx::named_barrier_sync(1, kConsumerWarps * 32);
-        int32_t* counter = p.counters + int64_t(pt.b) * p.num_kv_heads + pt.kvh;
+        int32_t* counter = p.counters + int64_t(pt.b) * p.num_kv_heads + pt.seg;
         if (tid == 0) {
           const int prev = aborted ? -1 : atomicAdd(counter, 1);
           flags[1] = (prev == pieces - 1) ? 1 : 0;
@@ -547,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const float inv = 1.f / den;
 #pragma unroll
             for (int e = 0; e < 8; ++e) o[e] *= inv;
-            const int64_t orow = int64_t(pt.b) * p.num_q_heads + int64_t(pt.kvh) * p.group + j;
+            const int64_t orow = int64_t(pt.b) * p.num_q_heads + int64_t(pt.seg) * p.group + j;
             *reinterpret_cast<uint4*>(outg + orow * D + dc * 8) = pack8<T>(o);
             if (dc == 0 && p.lse != nullptr) p.lse[orow] = mx + logf(den);
           }

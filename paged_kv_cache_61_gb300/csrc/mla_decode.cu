@@ -1,21 +1,711 @@
-// Absorbed-MLA paged decode for sm_103a (tcgen05 / TMEM). Not built yet: every
-// MLA problem is reported as unsupported.
+// Absorbed-MLA paged decode for sm_103a on the 5th-generation tensor cores.
+//
+// What it computes ("From MHA to MLA", section 6; FlashMLA-ETAP README, "Usage"
+// and "Supported configurations"): every query head attends to one shared record
+// per cached token of 576 values (512 latent + 64 rope). The score of head h and
+// token j is scale * (<q_h[:512], c_j> + <q_h[512:], k_j^R>) = scale * <q_h, rec_j>;
+// the value is the latent c_j = rec_j[:512]. Output [B, Hq, 512] and fp32 LSE.
+//
+// How (GB300 design; the FlashMLA-ETAP page describes a Hopper WGMMA kernel with
+// the transposed pipeline, whose idea of putting keys on the MMA's M axis is kept):
+//  * One CTA per range of (sequence, head group, page) tiles, the same equal-work
+//    split as the GQA kernel; a head group is N = min(Hq, 64) heads, so TMEM holds
+//    the N score columns plus 4 x N columns of the transposed output.
+//  * Warp 0 streams pages with one TMA copy each (a 64-token x 576 page lands as
+//    nine 128-byte-swizzled [64][64] sub-tiles) into a two-stage ring, and loads
+//    the head group's q once per piece.
+//  * Warp 1 issues tcgen05.mma from one thread:
+//      S^T[64 tokens x N]  = K[64 x 576] * q^T        (M=64, K-major A and B)
+//      O^T[512 x N]       += V^T[512 x 64] * P^T       (4 x M=128, MN-major A and B)
+//    V^T is read in place from the same page sub-tiles (MN-major descriptor), so
+//    each latent byte is read from HBM once.
+//  * Warps 2-5 read S^T from TMEM (tcgen05.ld), run the online softmax down each
+//    head column and write P^T (bf16/fp16) over the page's rope sub-tile, which
+//    the score MMA no longer needs. The running maximum is kept lazily: an exact
+//    column maximum is taken on a piece's first page and whenever some score
+//    exceeds the maximum in use by more than 2^8; only then is O^T rescaled in
+//    TMEM. The result is the same softmax (the common factor cancels in O/l).
+//  * At the end of a piece the same warps normalise O^T and write the output, or
+//    write a split piece that is merged like the GQA splits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
+#include <mutex>
+
 #include "pda_internal.h"
+#include "ptx.cuh"
+#include "tile_walk.cuh"
 
 namespace pda {
 
-bool mla_supported(const pda_problem&, std::string* why) {
-  *why = "MLA decode is not available in this build";
+namespace {
+
+constexpr int kPage = 64;
+constexpr int kDqk = 576;
+constexpr int kDv = 512;
+constexpr int kSubTiles = kDqk / 64;          // nine 64-dim sub-tiles per record
+constexpr int kSubBytes = kPage * 128;        // [64 tokens][64 dims] x 16 bit
+constexpr int kPageBytes = kSubTiles * kSubBytes;
+constexpr int kRopeSub = kSubTiles - 1;       // sub-tile reused for P^T
+constexpr int kStages = 2;
+constexpr int kThreads = 192;                 // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.f;           // lazy-max slack (log2 units)
+
+struct MlaParams {
+  const void* q;
+  void* out;
+  float* lse;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int32_t batch, num_q_heads, groups, max_blocks;
+  int64_t num_blocks;
+  float scale_log2;
+  int64_t total_tiles, tiles_per_cta;
+  int32_t heavy_min;
+  int32_t* err;
+  int32_t* counters;
+  float* part_lse;
+  float* part_out;
+};
+
+template <int N>
+struct MlaLayout {
+  static constexpr int kQBytes = kSubTiles * N * 128;  // q as nine K-major [N][64] sub-tiles
+  static constexpr int kKV = 0;
+  static constexpr int kQ = kKV + kStages * kPageBytes;
+  static constexpr int kRed = kQ + kQBytes;            // [64 heads][4 warps] floats
+  static constexpr int kMused = kRed + 64 * 4 * 4;     // running maximum per head (log2 units)
+  static constexpr int kAlpha = kMused + 64 * 4;       // rescale factor per head
+  static constexpr int kLtot = kAlpha + 64 * 4;        // softmax denominator per head
+  static constexpr int kBar = kLtot + 64 * 4;
+  static constexpr int kBarCount = 20;
+  static constexpr int kSmem = 1024 + kBar + kBarCount * 8 + 64;
+  // TMEM columns: S^T double-buffered at [0, 2N), O^T d-tile mt at 2N + mt*N
+  static constexpr int kTmemCols = (6 * N <= 128) ? 128 : (6 * N <= 256 ? 256 : 512);
+  static constexpr int kColS = 0;
+  static constexpr int kColO = 2 * N;
+  static_assert(kQBytes % 1024 == 0, "q sub-tiles stay 1024-byte aligned");
+};
+
+__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                             int32_t* err) {
+  if (wait_phase(bar, parity, abort)) return true;
+  *abort = 1;
+  atomicOr(err, 2);
   return false;
 }
 
-int mla_ctas_per_sm(const pda_problem&) { return 1; }
-int mla_heads_per_cta(const pda_problem& p) { return p.num_q_heads; }
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
 
-int launch_mla_decode(const Plan&, const MlaArgs&, const Workspace&, void*) {
-  return cudaErrorNotSupported;
+template <int N, typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_kv, const MlaParams p) {
+  using L = MlaLayout<N>;
+  constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  uint8_t* kv = base + L::kKV;
+  uint8_t* qs = base + L::kQ;
+  float* red = reinterpret_cast<float*>(base + L::kRed);
+  float* mused = reinterpret_cast<float*>(base + L::kMused);
+  float* alpha_s = reinterpret_cast<float*>(base + L::kAlpha);
+  float* ltot = reinterpret_cast<float*>(base + L::kLtot);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::kBar);
+  uint64_t* kv_full = bars + 0;   // [2]
+  uint64_t* kv_empty = bars + 2;  // [2]
+  uint64_t* q_full = bars + 4;
+  uint64_t* q_empty = bars + 5;
+  // Barriers that complete once per page come in pairs indexed by page parity, so a
+  // waiter is never two phases behind (the S^T buffer and the P^T sub-tile alternate too).
+  uint64_t* s_full = bars + 6;    // [2] S^T buffer written
+  uint64_t* s_free = bars + 8;    // [2] S^T buffer read, P^T written
+  uint64_t* p_full = bars + 10;   // [2]
+  uint64_t* pv_done = bars + 12;  // [2] PV of a page completed
+  volatile int* flags = reinterpret_cast<volatile int*>(bars + 14);  // [0] abort [1] last [2..5] votes (3 slots)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t g_lo = int64_t(blockIdx.x) * p.tiles_per_cta;
+  const int64_t g_hi = min(p.total_tiles, g_lo + p.tiles_per_cta);
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (g_lo >= g_hi) return;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&kv_full[s], 1);
+      ptx::mbar_init(&kv_empty[s], 1);
+    }
+    ptx::mbar_init(q_full, 1);
+    ptx::mbar_init(q_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&s_full[b], 1);
+      ptx::mbar_init(&s_free[b], 4);
+      ptx::mbar_init(&p_full[b], 4);
+      ptx::mbar_init(&pv_done[b], 1);
+    }
+    for (int i = 0; i < 6; ++i) flags[i] = 0;
+    ptx::fence_mbarrier_init();
+  }
+  if (warp == 1) ptx::tmem_alloc(tmem_slot, L::kTmemCols);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const WalkSpec spec{p.context_lens, p.batch, p.groups, kPage};
+  Walker walk;
+  walker_init(walk, spec, g_lo, lane);
+
+  if (warp == 0) {
+    // ============================== TMA producer ==============================
+    if (lane == 0) {
+      ptx::prefetch_tensormap(&tm_q);
+      ptx::prefetch_tensormap(&tm_kv);
+    }
+    const uint64_t pol_stream = ptx::policy_evict_first();
+    int t = 0, u = 0;
+    bool ok = true;
+    while (ok && walk.g < g_hi) {
+      const Portion pt = walker_next(walk, spec, g_hi);
+      if (lane == 0) {
+        if (u > 0) ok = bounded_wait(q_empty, (u - 1) & 1, flags, p.err);
+        if (ok) {
+          ptx::mbar_arrive_expect_tx(q_full, L::kQBytes);
+          ptx::tma_load_3d(qs, &tm_q, q_full, 0, pt.b * p.num_q_heads + pt.seg * N, 0,
+                           pol_stream);
+        }
+      }
+      ok = __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
+      const int32_t* row = p.block_tables + int64_t(pt.b) * p.max_blocks;
+      for (int base_pg = pt.p0; ok && base_pg < pt.p1; base_pg += 32) {
+        const int32_t ids = (base_pg + lane < pt.p1) ? __ldg(row + base_pg + lane) : 0;
+        const int n = min(32, pt.p1 - base_pg);
+        for (int j = 0; j < n; ++j, ++t) {
+          const int32_t phys = __shfl_sync(kFullMask, ids, j);
+          int good = 1;
+          if (lane == 0) {
+            const int s = t & 1;
+            if (!bounded_wait(&kv_empty[s], ((t >> 1) & 1) ^ 1, flags, p.err)) {
+              good = 0;
+            } else {
+              if (phys < 0 || int64_t(phys) >= p.num_blocks) atomicOr(p.err, 1);
+              ptx::mbar_arrive_expect_tx(&kv_full[s], kPageBytes);
+              ptx::tma_load_4d(kv + s * kPageBytes, &tm_kv, &kv_full[s], 0, 0, 0, phys,
+                               pol_stream);
+            }
+          }
+          ok = __shfl_sync(kFullMask, good, 0) != 0;
+          if (!ok) break;
+        }
+      }
+      ++u;
+    }
+    // Leave no copy in flight: the last fill of each stage and of q (bounded).
+    if (lane == 0) {
+      for (int k = 1; k <= 2 && t - k >= 0; ++k) {
+        const int tt = t - k;
+        const uint64_t t0 = ptx::globaltimer();
+        while (!ptx::mbar_try_wait(&kv_full[tt & 1], (tt >> 1) & 1) &&
+               ptx::globaltimer() - t0 < ptx::kWaitLimitNs) {
+        }
+      }
+      if (u > 0) {
+        const uint64_t t0 = ptx::globaltimer();
+        while (!ptx::mbar_try_wait(q_full, (u - 1) & 1) &&
+               ptx::globaltimer() - t0 < ptx::kWaitLimitNs) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ============================== MMA issuer ==============================
+    constexpr uint32_t kIdQK = ptx::umma_idesc_f16(64, N, 0, 0, kBf16);
+    constexpr uint32_t kIdPV = ptx::umma_idesc_f16(128, N, 1, 1, kBf16);
+    const uint32_t kv_s = ptx::smem_addr(kv);
+    const uint32_t q_s = ptx::smem_addr(qs);
+    int t = 0, u = 0;
+    int pending = -1;
+    bool pending_first = false;
+    bool ok = true;
+    auto issue_pv = [&](int tp, bool first) {
+      if (!ok || !bounded_wait(&p_full[tp & 1], (tp >> 1) & 1, flags, p.err)) {
+        ok = false;
+        return;
+      }
+      ptx::tc_fence_after();
+      const uint32_t st = kv_s + (tp & 1) * kPageBytes;
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t a = ptx::umma_desc_sw128(st + 2 * mt * kSubBytes + ks * 2048, kSubBytes, 1024);
+          const uint64_t b = ptx::umma_desc_sw128(st + kRopeSub * kSubBytes + ks * 2048, kSubBytes, 1024);
+          ptx::umma_f16(tmem + L::kColO + mt * N, a, b, kIdPV, !(first && ks == 0));
+        }
+      }
+      ptx::umma_commit(&kv_empty[tp & 1]);
+      ptx::umma_commit(&pv_done[tp & 1]);
+    };
+    while (walk.g < g_hi) {
+      const Portion pt = walker_next(walk, spec, g_hi);
+      const int npg = pt.p1 - pt.p0;
+      if (lane == 0) {
+        if (ok && !bounded_wait(q_full, u & 1, flags, p.err)) ok = false;
+        for (int i = 0; i < npg; ++i, ++t) {
+          const int s = t & 1;
+          if (ok && !bounded_wait(&kv_full[s], (t >> 1) & 1, flags, p.err)) ok = false;
+          // S^T buffer s was last read by the softmax of page t-2
+          if (ok && t > 1 && !bounded_wait(&s_free[s], ((t >> 1) - 1) & 1, flags, p.err)) ok = false;
+          if (ok) {
+            ptx::tc_fence_after();
+            const uint32_t st = kv_s + s * kPageBytes;
+#pragma unroll
+            for (int kb = 0; kb < kSubTiles; ++kb) {
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t a = ptx::umma_desc_sw128(st + kb * kSubBytes + ks * 32, 16, 1024);
+                const uint64_t b = ptx::umma_desc_sw128(q_s + kb * (N * 128) + ks * 32, 16, 1024);
+                ptx::umma_f16(tmem + L::kColS + s * N, a, b, kIdQK, (kb | ks) != 0);
+              }
+            }
+            if (i == npg - 1) ptx::umma_commit(q_empty);
+            ptx::umma_commit(&s_full[s]);
+          }
+          if (pending >= 0) issue_pv(pending, pending_first);
+          pending = t;
+          pending_first = (i == 0);
+        }
+      }
+      t = __shfl_sync(kFullMask, t, 0);
+      ++u;
+    }
+    if (lane == 0 && pending >= 0) issue_pv(pending, pending_first);
+    // Wait (bounded) for the last MMAs before TMEM is released.
+    if (lane == 0 && pending >= 0) {
+      const uint64_t t0 = ptx::globaltimer();
+      while (!ptx::mbar_try_wait(&pv_done[pending & 1], (pending >> 1) & 1) &&
+             ptx::globaltimer() - t0 < ptx::kWaitLimitNs) {
+      }
+    }
+    __syncwarp();
+  } else {
+    // ============================== softmax / epilogue warps ==============================
+    const int sw = warp - 2;               // 0..3
+    const int sp = warp & 3;               // TMEM sub-partition of this warp
+    const bool active = lane < 16;         // M=64 scores: rows in lanes 0..15 of each sub-partition
+    const int row = 16 * sp + lane;        // token within the page (active lanes)
+    const int ctid = threadIdx.x - 64;     // 0..127
+    const uint32_t t_lane = tmem + (uint32_t(32 * sp) << 16);
+    T* outg = static_cast<T*>(p.out);
+    float l_reg[N];
+    bool aborted = false;
+    int t = 0;
+
+    // 16 scaled scores of this thread's token (or -inf) from TMEM columns [c, c+16)
+    auto load_scores = [&](int c, bool valid, float (&x)[16]) {
+      if (!aborted) {
+        ptx::tmem_ld16(t_lane + L::kColS + (t & 1) * N + c, x);
+        ptx::tmem_ld_wait();
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e) x[e] = valid ? x[e] * p.scale_log2 : -INFINITY;
+    };
+    // exact per-head maximum over the page's 64 tokens -> red[h*4 + warp]
+    auto column_max = [&](bool valid) {
+#pragma unroll
+      for (int c = 0; c < N; c += 16) {
+        float x[16];
+        load_scores(c, valid, x);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float v = x[e];
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, o));
+          if (lane == ((c + e) & 31)) red[(c + e) * 4 + sw] = v;
+        }
+      }
+      ptx::named_barrier_sync(1, 128);
+    };
+
+    while (walk.g < g_hi) {
+      const Portion pt = walker_next(walk, spec, g_hi);
+      const int npg = pt.p1 - pt.p0;
+      const int ctx = __ldg(p.context_lens + pt.b);
+#pragma unroll
+      for (int h = 0; h < N; ++h) l_reg[h] = 0.f;
+
+      for (int i = 0; i < npg; ++i, ++t) {
+        if (!aborted && !bounded_wait(&s_full[t & 1], (t >> 1) & 1, flags, p.err)) aborted = true;
+        aborted = __any_sync(kFullMask, aborted);  // keep .sync.aligned TMEM accesses warp-uniform
+        ptx::tc_fence_after();
+        const int token = (pt.p0 + i) * kPage + row;
+        const bool valid = active && token < ctx && !aborted;
+        if (i == 0) {
+          // first page of the piece: the running maximum starts at the exact column maximum
+          column_max(valid);
+          if (ctid < N) {
+            const float4 r = *reinterpret_cast<const float4*>(red + ctid * 4);
+            mused[ctid] = fmaxf(fmaxf(r.x, r.y), fmaxf(r.z, r.w));
+          }
+          ptx::named_barrier_sync(1, 128);
+        } else {
+          // lazy maximum: only if a score exceeds the maximum in use by 2^8 is it raised
+          bool need = false;
+#pragma unroll
+          for (int c = 0; c < N; c += 16) {
+            float x[16];
+            load_scores(c, valid, x);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) need |= x[e] > mused[c + e] + kRescaleLog2;
+          }
+          const bool wneed = __any_sync(kFullMask, need);
+          if (lane == 0) flags[2 + sw] = wneed ? 1 : 0;
+          ptx::named_barrier_sync(1, 128);
+          const bool cneed = (flags[2] | flags[3] | flags[4] | flags[5]) != 0;
+          ptx::named_barrier_sync(1, 128);
+          if (cneed) {
+            column_max(valid);
+            if (ctid < N) {
+              const float4 r = *reinterpret_cast<const float4*>(red + ctid * 4);
+              const float mo = mused[ctid];
+              const float mn = fmaxf(mo, fmaxf(fmaxf(r.x, r.y), fmaxf(r.z, r.w)));
+              alpha_s[ctid] = ptx::exp2_approx(mo - mn);
+              mused[ctid] = mn;
+            }
+            ptx::named_barrier_sync(1, 128);
+#pragma unroll
+            for (int h = 0; h < N; ++h) l_reg[h] *= alpha_s[h];
+            // O^T holds the pages up to t-1: wait for their PV, then rescale it in TMEM
+            if (!aborted && !bounded_wait(&pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, flags, p.err))
+              aborted = true;
+            aborted = __any_sync(kFullMask, aborted);
+            ptx::tc_fence_after();
+            if (!aborted) {
+#pragma unroll
+              for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+                for (int c = 0; c < N; c += 16) {
+                  float v[16];
+                  const uint32_t a = t_lane + L::kColO + mt * N + c;
+                  ptx::tmem_ld16(a, v);
+                  ptx::tmem_ld_wait();
+#pragma unroll
+                  for (int e = 0; e < 16; ++e) v[e] *= alpha_s[c + e];
+                  ptx::tmem_st16(a, v);
+                }
+              }
+              ptx::tmem_st_wait();
+            }
+          }
+        }
+        // P^T row `row` (heads contiguous) over the page's rope sub-tile
+        uint8_t* pbuf = kv + (t & 1) * kPageBytes + kRopeSub * kSubBytes;
+#pragma unroll
+        for (int c = 0; c < N; c += 16) {
+          float x[16];
+          load_scores(c, valid, x);
+          float pv[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            pv[e] = ptx::exp2_approx(x[e] - mused[c + e]);
+            l_reg[c + e] += pv[e];
+          }
+          if (active) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const int chunk = c / 8 + half;
+              uint4 w;
+              w.x = ptx::Mma<T>::pack(pv[8 * half + 0], pv[8 * half + 1]);
+              w.y = ptx::Mma<T>::pack(pv[8 * half + 2], pv[8 * half + 3]);
+              w.z = ptx::Mma<T>::pack(pv[8 * half + 4], pv[8 * half + 5]);
+              w.w = ptx::Mma<T>::pack(pv[8 * half + 6], pv[8 * half + 7]);
+              *reinterpret_cast<uint4*>(pbuf + row * 128 + ((chunk ^ (row & 7)) << 4)) = w;
+            }
+          }
+        }
+        // Slots past ctx in the last page: their P is 0, but 0 * (whatever the slot holds,
+        // NaN included) must not reach O, so their V rows are cleared before the PV MMA
+        // (the score MMA has already consumed the page).
+        if (active && token >= ctx) {
+          uint8_t* stg = kv + (t & 1) * kPageBytes;
+#pragma unroll
+          for (int sub = 0; sub < kDv / 64; ++sub) {
+            uint4* r = reinterpret_cast<uint4*>(stg + sub * kSubBytes + row * 128);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) r[c] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        ptx::tc_fence_before();
+        ptx::fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive(&s_free[t & 1]);   // S^T buffer has been read
+          ptx::mbar_arrive(&p_full[t & 1]);   // P^T is in shared memory
+        }
+      }
+
+      // ---- end of the piece: softmax denominators, then O = O^T / l
+#pragma unroll
+      for (int h = 0; h < N; ++h) {
+        float v = l_reg[h];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) v += __shfl_xor_sync(kFullMask, v, o);
+        if (lane == (h & 31)) red[h * 4 + sw] = v;
+      }
+      ptx::named_barrier_sync(1, 128);
+      if (ctid < N) {
+        const float4 r = *reinterpret_cast<const float4*>(red + ctid * 4);
+        ltot[ctid] = (r.x + r.y) + (r.z + r.w);
+      }
+      ptx::named_barrier_sync(1, 128);
+      if (!aborted && !bounded_wait(&pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, flags, p.err))
+        aborted = true;
+      aborted = __any_sync(kFullMask, aborted);
+      ptx::tc_fence_after();
+
+      const bool whole = (pt.p0 == 0 && pt.p1 == pt.np);
+      const int slot = piece_slot(pt.seg_start, g_lo);
+      const int64_t head0 = int64_t(pt.b) * p.num_q_heads + int64_t(pt.seg) * N;
+      const int64_t slot_row = (int64_t(blockIdx.x) * 2 + slot) * N;
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        const int d = mt * 128 + 32 * sp + lane;
+#pragma unroll
+        for (int c = 0; c < N; c += 16) {
+          float v[16];
+          if (!aborted) {
+            ptx::tmem_ld16(t_lane + L::kColO + mt * N + c, v);
+            ptx::tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = 0.f;
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int h = c + e;
+            const float o = v[e] / ltot[h];
+            if (whole)
+              outg[(head0 + h) * kDv + d] = from_f32<T>(o);
+            else
+              __stcg(p.part_out + (slot_row + h) * kDv + d, o);
+          }
+        }
+      }
+      if (ctid < N) {
+        const float lse_nat = (mused[ctid] + log2f(ltot[ctid])) * kLn2;
+        if (whole) {
+          if (p.lse != nullptr) p.lse[head0 + ctid] = lse_nat;
+        } else {
+          __stcg(p.part_lse + slot_row + ctid, lse_nat);
+        }
+      }
+      ptx::tc_fence_before();
+
+      if (!whole) {
+        // few pieces: the last to arrive merges them here; many: the split-merge kernel
+        const int64_t c0 = pt.seg_start / p.tiles_per_cta;
+        const int64_t c1 = (pt.seg_start + pt.np - 1) / p.tiles_per_cta;
+        const int pieces = int(c1 - c0 + 1);
+        if (pieces <= p.heavy_min) {
+          __threadfence();
+          ptx::named_barrier_sync(1, 128);
+          int32_t* counter = p.counters + int64_t(pt.b) * p.groups + pt.seg;
+          if (ctid == 0) {
+            const int prev = aborted ? -1 : atomicAdd(counter, 1);
+            flags[1] = (prev == pieces - 1) ? 1 : 0;
+          }
+          ptx::named_barrier_sync(1, 128);
+          if (flags[1]) {
+            __threadfence();
+            for (int idx = ctid; idx < N * (kDv / 4); idx += 128) {
+              const int j = idx / (kDv / 4);
+              const int dq = idx - j * (kDv / 4);
+              float mx = -INFINITY;
+              for (int64_t c = c0; c <= c1; ++c) {
+                const int sl = (c == c0 && pt.seg_start > c * p.tiles_per_cta) ? 1 : 0;
+                mx = fmaxf(mx, __ldcg(p.part_lse + (c * 2 + sl) * N + j));
+              }
+              float den = 0.f;
+              float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int64_t c = c0; c <= c1; ++c) {
+                const int sl = (c == c0 && pt.seg_start > c * p.tiles_per_cta) ? 1 : 0;
+                const int64_t rowi = (c * 2 + sl) * N + j;
+                const float wgt = ptx::exp2_approx((__ldcg(p.part_lse + rowi) - mx) * kLog2e);
+                const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_out + rowi * kDv) + dq);
+                den += wgt;
+                acc.x += wgt * o.x; acc.y += wgt * o.y; acc.z += wgt * o.z; acc.w += wgt * o.w;
+              }
+              const float inv = 1.f / den;
+              T* o = outg + (head0 + j) * kDv + dq * 4;
+              o[0] = from_f32<T>(acc.x * inv);
+              o[1] = from_f32<T>(acc.y * inv);
+              o[2] = from_f32<T>(acc.z * inv);
+              o[3] = from_f32<T>(acc.w * inv);
+              if (dq == 0 && p.lse != nullptr) p.lse[head0 + j] = mx + logf(den);
+            }
+            if (ctid == 0) atomicExch(counter, 0);
+          }
+        }
+      }
+      ptx::named_barrier_sync(1, 128);
+    }
+  }
+
+  // ---- teardown: everyone done with TMEM before it is released
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn mla_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// q [rows, 576]: dims (d mod 64, row, d / 64), box (64, N, 9) -> nine [N][64] sub-tiles.
+// kv [blocks, 64, 576]: dims (d mod 64, slot, d / 64, block), box (64, 64, 9, 1) ->
+// nine [64][64] sub-tiles per page. Both with 128-byte swizzle.
+bool encode_mla_maps(CUtensorMap* tq, CUtensorMap* tkv, const void* q, int64_t rows, int n,
+                     const void* kv, int64_t num_blocks, bool bf16) {
+  EncodeTiledFn fn = mla_encode_fn();
+  if (fn == nullptr) return false;
+  const CUtensorMapDataType dt =
+      bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const cuuint64_t qdims[3] = {64, cuuint64_t(rows), kSubTiles};
+  const cuuint64_t qstr[2] = {kDqk * 2, 128};
+  const cuuint32_t qbox[3] = {64, cuuint32_t(n), kSubTiles};
+  const cuuint32_t e3[3] = {1, 1, 1};
+  if (fn(tq, dt, 3, const_cast<void*>(q), qdims, qstr, qbox, e3, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  const cuuint64_t kdims[4] = {64, kPage, kSubTiles, cuuint64_t(num_blocks)};
+  const cuuint64_t kstr[3] = {kDqk * 2, 128, cuuint64_t(kPage) * kDqk * 2};
+  const cuuint32_t kbox[4] = {64, kPage, kSubTiles, 1};
+  const cuuint32_t e4[4] = {1, 1, 1, 1};
+  return fn(tkv, dt, 4, const_cast<void*>(kv), kdims, kstr, kbox, e4,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int N, typename T>
+int launch_mla_n(const CUtensorMap& tq, const CUtensorMap& tkv, const MlaParams& prm, int grid,
+                 cudaStream_t stream) {
+  auto kern = mla_decode_kernel<N, T>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    MlaLayout<N>::kSmem);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  kern<<<grid, kThreads, MlaLayout<N>::kSmem, stream>>>(tq, tkv, prm);
+  return cudaGetLastError();
+}
+
+template <typename T>
+int launch_mla_t(int n, const CUtensorMap& tq, const CUtensorMap& tkv, const MlaParams& prm,
+                 int grid, cudaStream_t s) {
+  switch (n) {
+    case 16: return launch_mla_n<16, T>(tq, tkv, prm, grid, s);
+    case 32: return launch_mla_n<32, T>(tq, tkv, prm, grid, s);
+    default: return launch_mla_n<64, T>(tq, tkv, prm, grid, s);
+  }
+}
+
+}  // namespace
+
+int mla_heads_per_cta(const pda_problem& p) { return p.num_q_heads <= 64 ? p.num_q_heads : 64; }
+int mla_ctas_per_sm(const pda_problem&) { return 1; }
+
+bool mla_supported(const pda_problem& p, std::string* why) {
+  if (p.head_dim_qk != kDqk || p.head_dim_v != kDv) {
+    *why = "MLA decode supports head_dim_qk 576 and head_dim_v 512";
+    return false;
+  }
+  if (p.page_size != kPage) {
+    *why = "MLA decode supports page_size 64";
+    return false;
+  }
+  if (p.num_kv_heads != 1) {
+    *why = "MLA decode has one shared latent head (num_kv_heads must be 1)";
+    return false;
+  }
+  const int n = mla_heads_per_cta(p);
+  if (!(n == 16 || n == 32 || n == 64) || p.num_q_heads % n != 0) {
+    *why = "MLA decode supports num_q_heads 16, 32 or a multiple of 64";
+    return false;
+  }
+  if (p.num_blocks > INT32_MAX) {
+    *why = "num_blocks must fit in int32 (block-table entries are int32)";
+    return false;
+  }
+  return true;
+}
+
+int launch_mla_decode(const Plan& plan, const MlaArgs& a, const Workspace& ws, void* stream) {
+  const pda_problem& pr = plan.prob;
+  const bool bf16 = pr.dtype == PDA_BF16;
+  const int n = plan.group;
+  CUtensorMap tq, tkv;
+  if (!encode_mla_maps(&tq, &tkv, a.q, int64_t(pr.batch) * pr.num_q_heads, n, a.kv_cache,
+                       pr.num_blocks, bf16))
+    return -1;
+  MlaParams prm{};
+  prm.q = a.q;
+  prm.out = a.out;
+  prm.lse = a.lse;
+  prm.block_tables = a.block_tables;
+  prm.context_lens = a.context_lens;
+  prm.batch = pr.batch;
+  prm.num_q_heads = pr.num_q_heads;
+  prm.groups = plan.segs_per_seq;
+  prm.max_blocks = pr.max_blocks_per_seq;
+  prm.num_blocks = pr.num_blocks;
+  prm.scale_log2 = a.scale * kLog2e;
+  prm.total_tiles = plan.total_tiles;
+  prm.tiles_per_cta = plan.tiles_per_cta;
+  prm.heavy_min = plan.heavy_min_pieces;
+  prm.err = ws.err;
+  prm.counters = ws.counters;
+  prm.part_lse = ws.part_lse;
+  prm.part_out = ws.part_out;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int e = bf16 ? launch_mla_t<__nv_bfloat16>(n, tq, tkv, prm, plan.num_ctas, s)
+                     : launch_mla_t<__half>(n, tq, tkv, prm, plan.num_ctas, s);
+  if (e != 0) return e;
+  return launch_split_merge(plan, ws, a.out, a.lse, stream);
 }
 
 }  // namespace pda

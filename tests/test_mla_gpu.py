@@ -1,0 +1,129 @@
+"""Absorbed-MLA paged decode on the GPU (tcgen05 kernel, through the C ABI) vs the float64 oracle.
+
+Tolerances: out max-abs <= 1e-2 (bf16) / 2e-3 (fp16), fp32 LSE within 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import TOL_LSE, TOL_OUT, DeviceCase, compare, device_bits
+from paged_kv_cache_61_gb300 import pda, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    pda.lib()
+
+
+def _oracle(case, rows=None):
+    return oracle.mla_decode(case.q, case.kv_cache, case.block_tables, case.context_lens,
+                             case.scale, case.page_size, case.dtype, rows=rows)
+
+
+def _case(hq, ctx, dtype=synth.BF16, seed=5):
+    return synth.make_mla_case(batch=len(ctx), num_q_heads=hq, dtype=dtype, context_lens=ctx,
+                               seed=seed)
+
+
+def _assert_close(case, dc, rows=None):
+    out, lse = dc.run()
+    torch.cuda.synchronize()
+    ref_out, ref_lse = _oracle(case, rows)
+    eo, el = compare(case, out, lse, ref_out, ref_lse, rows)
+    assert eo <= TOL_OUT[case.dtype], f"out max-abs error {eo}"
+    assert el <= TOL_LSE, f"lse max-abs error {el}"
+    assert pda.read_device_error(dc.ws) == 0
+    return out, lse
+
+
+@pytest.mark.parametrize("hq", [16, 32, 64, 128])
+@pytest.mark.parametrize("force", [0, 1, 3, 17])
+def test_small_cases(hq, force):
+    case = _case(hq, [1, 63, 64, 65, 130, 700])
+    _assert_close(case, DeviceCase(case, force_num_ctas=force))
+
+
+def test_fp16():
+    case = _case(16, [200, 64, 1], dtype=synth.FP16)
+    _assert_close(case, DeviceCase(case))
+
+
+def test_many_pages_with_rising_scores():
+    # later pages carry larger rope scores, so the running maximum has to be raised
+    # (and the accumulated output rescaled) several times within one piece
+    case = _case(64, [2000, 900])
+    kv = synth.bits_to_float32(case.kv_cache, case.dtype)
+    for b, c in enumerate(case.context_lens):
+        npg = (int(c) + 63) // 64
+        for pg in range(npg):
+            blk = int(case.block_tables[b, pg])
+            kv[blk, :, 512:] *= 1.0 + 2.5 * pg / npg
+    case.kv_cache = synth.float32_to_bits(kv, case.dtype)
+    for force in (0, 1):
+        _assert_close(case, DeviceCase(case, force_num_ctas=force))
+
+
+def test_rope_needle_is_bit_exact():
+    ctx = 300
+    case = _case(16, [ctx] * 6, seed=9)
+    one = synth.float32_to_bits(np.float32(1.0), case.dtype)
+    sixteen = synth.float32_to_bits(np.float32(16.0), case.dtype)
+    case.q[..., :512] = 0
+    case.q[..., 512:] = one
+    case.kv_cache[..., 512:] = 0
+    targets = [0, 63, 64, 150, 255, 299]
+    for b, t in enumerate(targets):
+        blk = int(case.block_tables[b, t // 64])
+        case.kv_cache[blk, t % 64, 512:] = sixteen
+    for force in (0, 1, 5):
+        dc = DeviceCase(case, force_num_ctas=force)
+        out, _ = dc.run()
+        torch.cuda.synchronize()
+        got = device_bits(out)
+        for b, t in enumerate(targets):
+            blk = int(case.block_tables[b, t // 64])
+            for h in range(16):
+                assert np.array_equal(got[b, h], case.kv_cache[blk, t % 64, :512]), (force, b, h)
+
+
+def test_ctx1_returns_latent_of_token0():
+    case = _case(128, [1, 1])
+    dc = DeviceCase(case)
+    out, _ = _assert_close(case, dc)
+    got = device_bits(out)
+    for b in range(2):
+        blk = int(case.block_tables[b, 0])
+        for h in range(128):
+            assert np.array_equal(got[b, h], case.kv_cache[blk, 0, :512])
+
+
+def test_poisoned_stale_slots_and_table_entries():
+    case = _case(32, [70, 129, 5])
+    out0, lse0 = DeviceCase(case).run()
+    torch.cuda.synchronize()
+    kv, tab = case.kv_cache.copy(), case.block_tables.copy()
+    for b, c in enumerate(case.context_lens):
+        npg = (int(c) + 63) // 64
+        last, fill = int(tab[b, npg - 1]), int(c) - (npg - 1) * 64
+        kv[last, fill:] = 0x7FC0
+        tab[b, npg:] = -99
+    bad = synth.DecodeCase(**{**case.__dict__})
+    bad.kv_cache, bad.block_tables = kv, tab
+    dc = DeviceCase(bad)
+    out1, lse1 = dc.run()
+    torch.cuda.synchronize()
+    assert torch.equal(out0.view(torch.int16), out1.view(torch.int16))
+    assert torch.equal(lse0, lse1)
+    assert pda.read_device_error(dc.ws) == 0
+
+
+@pytest.mark.parametrize("name", ["mla_b16_ctx64k_h16", "mla_b16_ctx64k_h128"])
+def test_full_size_workload_sampled_rows(name):
+    case = synth.workload(name)
+    hq = case.num_q_heads
+    rows = [(b, h) for b in (0, 7, 15) for h in sorted({0, 1, hq // 2, hq - 1})]
+    _assert_close(case, DeviceCase(case), rows=rows)
