@@ -52,16 +52,20 @@ def test_fp16():
     _assert_close(case, DeviceCase(case))
 
 
-def test_many_pages_with_rising_scores():
-    # later pages carry larger rope scores, so the running maximum has to be raised
-    # (and the accumulated output rescaled) several times within one piece
+def test_score_jumps_force_rescales():
+    # q's rope half is all ones and the rope keys of pages >= 3 and >= 10 get a constant
+    # added, so the scores jump twice by ~8.7 in log2 units: the running maximum must be
+    # raised and the accumulated output rescaled within one piece. After each jump many
+    # tokens share the weight, so the check stays inside the bf16 tolerance.
     case = _case(64, [2000, 900])
+    case.q[..., 512:] = synth.float32_to_bits(np.float32(1.0), case.dtype)
     kv = synth.bits_to_float32(case.kv_cache, case.dtype)
+    step = 6.0 * np.sqrt(192.0) / 64.0          # +6 on the natural-log score per jump
     for b, c in enumerate(case.context_lens):
         npg = (int(c) + 63) // 64
         for pg in range(npg):
             blk = int(case.block_tables[b, pg])
-            kv[blk, :, 512:] *= 1.0 + 2.5 * pg / npg
+            kv[blk, :, 512:] += step * ((pg >= 3) + (pg >= 10))
     case.kv_cache = synth.float32_to_bits(kv, case.dtype)
     for force in (0, 1):
         _assert_close(case, DeviceCase(case, force_num_ctas=force))
