@@ -230,44 +230,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ============================== MMA issuer ==============================
+    // One thread polls for whichever MMA group is ready and issues it: the scores of
+    // the next page (its data, q and an S^T buffer are ready) or the PV of the oldest
+    // page whose P^T is written. PV never waits behind the next page's load, so the
+    // stage it frees is refilled as early as possible.
     constexpr uint32_t kIdQK = ptx::umma_idesc_f16(64, N, 0, 0, kBf16);
     constexpr uint32_t kIdPV = ptx::umma_idesc_f16(128, N, 1, 1, kBf16);
     const uint32_t kv_s = ptx::smem_addr(kv);
     const uint32_t q_s = ptx::smem_addr(qs);
-    int t = 0, u = 0;
-    int pending = -1;
-    bool pending_first = false;
-    bool ok = true;
-    auto issue_pv = [&](int tp, bool first) {
-      if (!ok || !bounded_wait(&p_full[tp & 1], (tp >> 1) & 1, flags, p.err)) {
-        ok = false;
-        return;
-      }
-      ptx::tc_fence_after();
-      const uint32_t st = kv_s + (tp & 1) * kPageBytes;
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t a = ptx::umma_desc_sw128(st + 2 * mt * kSubBytes + ks * 2048, kSubBytes, 1024);
-          const uint64_t b = ptx::umma_desc_sw128(st + kRopeSub * kSubBytes + ks * 2048, kSubBytes, 1024);
-          ptx::umma_f16(tmem + L::kColO + mt * N, a, b, kIdPV, !(first && ks == 0));
+    int t_qk = 0, t_pv = 0;   // next page to score / to apply
+    if (lane == 0) {
+      int u = 0, i = 0, npg = 0;
+      bool have = false, need_q = false, qk_done = false;
+      uint32_t first_bits = 0;   // bit (t & 31): page t is the first of its piece
+      uint64_t last_progress = ptx::globaltimer();
+      while (true) {
+        bool progress = false;
+        if (!qk_done && (!have || i == npg)) {
+          if (walk.g < g_hi) {
+            const Portion pt = walker_next(walk, spec, g_hi);
+            npg = pt.p1 - pt.p0;
+            i = 0;
+            have = true;
+            need_q = true;
+          } else {
+            qk_done = true;
+          }
         }
-      }
-      ptx::umma_commit(&kv_empty[tp & 1]);
-      ptx::umma_commit(&pv_done[tp & 1]);
-    };
-    while (walk.g < g_hi) {
-      const Portion pt = walker_next(walk, spec, g_hi);
-      const int npg = pt.p1 - pt.p0;
-      if (lane == 0) {
-        if (ok && !bounded_wait(q_full, u & 1, flags, p.err)) ok = false;
-        for (int i = 0; i < npg; ++i, ++t) {
-          const int s = t & 1;
-          if (ok && !bounded_wait(&kv_full[s], (t >> 1) & 1, flags, p.err)) ok = false;
-          // S^T buffer s was last read by the softmax of page t-2
-          if (ok && t > 1 && !bounded_wait(&s_free[s], ((t >> 1) - 1) & 1, flags, p.err)) ok = false;
-          if (ok) {
+        if (!qk_done && i < npg) {
+          const int s = t_qk & 1;
+          const bool ready = (!need_q || ptx::mbar_try_wait(q_full, u & 1)) &&
+                             ptx::mbar_try_wait(&kv_full[s], (t_qk >> 1) & 1) &&
+                             (t_qk < 2 || ptx::mbar_try_wait(&s_free[s], ((t_qk >> 1) - 1) & 1));
+          if (ready) {
+            need_q = false;
             ptx::tc_fence_after();
             const uint32_t st = kv_s + s * kPageBytes;
 #pragma unroll
@@ -279,23 +275,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::umma_f16(tmem + L::kColS + s * N, a, b, kIdQK, (kb | ks) != 0);
               }
             }
-            if (i == npg - 1) ptx::umma_commit(q_empty);
+            if (i == npg - 1) {
+              ptx::umma_commit(q_empty);
+              ++u;
+            }
             ptx::umma_commit(&s_full[s]);
+            first_bits = (first_bits & ~(1u << (t_qk & 31))) | (uint32_t(i == 0) << (t_qk & 31));
+            ++t_qk;
+            ++i;
+            progress = true;
           }
-          if (pending >= 0) issue_pv(pending, pending_first);
-          pending = t;
-          pending_first = (i == 0);
+        }
+        if (t_pv < t_qk && ptx::mbar_try_wait(&p_full[t_pv & 1], (t_pv >> 1) & 1)) {
+          ptx::tc_fence_after();
+          const bool first = (first_bits >> (t_pv & 31)) & 1u;
+          const uint32_t st = kv_s + (t_pv & 1) * kPageBytes;
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t a =
+                  ptx::umma_desc_sw128(st + 2 * mt * kSubBytes + ks * 2048, kSubBytes, 1024);
+              const uint64_t b =
+                  ptx::umma_desc_sw128(st + kRopeSub * kSubBytes + ks * 2048, kSubBytes, 1024);
+              ptx::umma_f16(tmem + L::kColO + mt * N, a, b, kIdPV, !(first && ks == 0));
+            }
+          }
+          ptx::umma_commit(&kv_empty[t_pv & 1]);
+          ptx::umma_commit(&pv_done[t_pv & 1]);
+          ++t_pv;
+          progress = true;
+        }
+        if (qk_done && t_pv == t_qk) break;
+        if (progress) {
+          last_progress = ptx::globaltimer();
+        } else if (flags[0] || ptx::globaltimer() - last_progress > ptx::kWaitLimitNs) {
+          flags[0] = 1;
+          atomicOr(p.err, 2);
+          break;
         }
       }
-      t = __shfl_sync(kFullMask, t, 0);
-      ++u;
-    }
-    if (lane == 0 && pending >= 0) issue_pv(pending, pending_first);
-    // Wait (bounded) for the last MMAs before TMEM is released.
-    if (lane == 0 && pending >= 0) {
-      const uint64_t t0 = ptx::globaltimer();
-      while (!ptx::mbar_try_wait(&pv_done[pending & 1], (pending >> 1) & 1) &&
-             ptx::globaltimer() - t0 < ptx::kWaitLimitNs) {
+      // Wait (bounded) for the last MMAs before TMEM is released.
+      if (t_pv > 0) {
+        const int tl = t_pv - 1;
+        const uint64_t t0 = ptx::globaltimer();
+        while (!ptx::mbar_try_wait(&pv_done[tl & 1], (tl >> 1) & 1) &&
+               ptx::globaltimer() - t0 < ptx::kWaitLimitNs) {
+        }
       }
     }
     __syncwarp();
