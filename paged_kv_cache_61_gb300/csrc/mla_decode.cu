@@ -53,10 +53,6 @@ constexpr int kThreads = 192;                 // warp 0 TMA, warp 1 MMA, warps 2
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.f;           // lazy-max slack (log2 units)
-#ifndef PDA_MLA_PREFETCH_PAGES
-#define PDA_MLA_PREFETCH_PAGES 2
-#endif
-constexpr int kPrefetchPages = PDA_MLA_PREFETCH_PAGES;  // L2 prefetch distance (pages)
 
 struct MlaParams {
   const void* q;
@@ -198,14 +194,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = min(32, pt.p1 - base_pg);
         for (int j = 0; j < n; ++j, ++t) {
           const int32_t phys = __shfl_sync(kFullMask, ids, j);
-          const int32_t ahead = __shfl_sync(kFullMask, ids, (j + kPrefetchPages) & 31);
           int good = 1;
           if (lane == 0) {
             const int s = t & 1;
-            // Ask L2 for the page kPrefetchPages ahead, so refilling a stage (which must
-            // wait for the PV that frees it) finds its data close by.
-            if (kPrefetchPages > 0 && j + kPrefetchPages < n)
-              ptx::tma_prefetch_l2_4d(&tm_kv, 0, 0, 0, ahead);
             if (!bounded_wait(&kv_empty[s], ((t >> 1) & 1) ^ 1, flags, p.err)) {
               good = 0;
             } else {
@@ -251,12 +242,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int u = 0, i = 0, npg = 0;
       bool have = false, need_q = false, qk_done = false;
-      int kb_next = 0;           // next 64-dim block of the page being scored (0 = not started)
       uint32_t first_bits = 0;   // bit (t & 31): page t is the first of its piece
       uint64_t last_progress = ptx::globaltimer();
       while (true) {
         bool progress = false;
-        // PV first: it frees a ring stage; one PV group may slip between score blocks
+        if (!qk_done && (!have || i == npg)) {
+          if (walk.g < g_hi) {
+            const Portion pt = walker_next(walk, spec, g_hi);
+            npg = pt.p1 - pt.p0;
+            i = 0;
+            have = true;
+            need_q = true;
+          } else {
+            qk_done = true;
+          }
+        }
+        if (!qk_done && i < npg) {
+          const int s = t_qk & 1;
+          const bool ready = (!need_q || ptx::mbar_try_wait(q_full, u & 1)) &&
+                             ptx::mbar_try_wait(&kv_full[s], (t_qk >> 1) & 1) &&
+                             (t_qk < 2 || ptx::mbar_try_wait(&s_free[s], ((t_qk >> 1) - 1) & 1));
+          if (ready) {
+            need_q = false;
+            ptx::tc_fence_after();
+            const uint32_t st = kv_s + s * kPageBytes;
+#pragma unroll
+            for (int kb = 0; kb < kSubTiles; ++kb) {
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t a = ptx::umma_desc_sw128(st + kb * kSubBytes + ks * 32, 16, 1024);
+                const uint64_t b = ptx::umma_desc_sw128(q_s + kb * (N * 128) + ks * 32, 16, 1024);
+                ptx::umma_f16(tmem + L::kColS + s * N, a, b, kIdQK, (kb | ks) != 0);
+              }
+            }
+            if (i == npg - 1) {
+              ptx::umma_commit(q_empty);
+              ++u;
+            }
+            ptx::umma_commit(&s_full[s]);
+            first_bits = (first_bits & ~(1u << (t_qk & 31))) | (uint32_t(i == 0) << (t_qk & 31));
+            ++t_qk;
+            ++i;
+            progress = true;
+          }
+        }
         if (t_pv < t_qk && ptx::mbar_try_wait(&p_full[t_pv & 1], (t_pv >> 1) & 1)) {
           ptx::tc_fence_after();
           const bool first = (first_bits >> (t_pv & 31)) & 1u;
@@ -277,52 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++t_pv;
           progress = true;
         }
-        if (!qk_done && kb_next == 0 && (!have || i == npg)) {
-          if (walk.g < g_hi) {
-            const Portion pt = walker_next(walk, spec, g_hi);
-            npg = pt.p1 - pt.p0;
-            i = 0;
-            have = true;
-            need_q = true;
-          } else {
-            qk_done = true;
-          }
-        }
-        if (!qk_done && i < npg) {
-          const int s = t_qk & 1;
-          const bool ready =
-              kb_next > 0 ||
-              ((!need_q || ptx::mbar_try_wait(q_full, u & 1)) &&
-               ptx::mbar_try_wait(&kv_full[s], (t_qk >> 1) & 1) &&
-               (t_qk < 2 || ptx::mbar_try_wait(&s_free[s], ((t_qk >> 1) - 1) & 1)));
-          if (ready) {
-            if (kb_next == 0) {
-              need_q = false;
-              ptx::tc_fence_after();
-            }
-            const uint32_t st = kv_s + s * kPageBytes;
-            const int kb = kb_next;
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              const uint64_t a = ptx::umma_desc_sw128(st + kb * kSubBytes + ks * 32, 16, 1024);
-              const uint64_t b = ptx::umma_desc_sw128(q_s + kb * (N * 128) + ks * 32, 16, 1024);
-              ptx::umma_f16(tmem + L::kColS + s * N, a, b, kIdQK, (kb | ks) != 0);
-            }
-            progress = true;
-            if (++kb_next == kSubTiles) {
-              kb_next = 0;
-              if (i == npg - 1) {
-                ptx::umma_commit(q_empty);
-                ++u;
-              }
-              ptx::umma_commit(&s_full[s]);
-              first_bits = (first_bits & ~(1u << (t_qk & 31))) | (uint32_t(i == 0) << (t_qk & 31));
-              ++t_qk;
-              ++i;
-            }
-          }
-        }
-        if (qk_done && kb_next == 0 && t_pv == t_qk) break;
+        if (qk_done && t_pv == t_qk) break;
         if (progress) {
           last_progress = ptx::globaltimer();
         } else if (flags[0] || ptx::globaltimer() - last_progress > ptx::kWaitLimitNs) {
@@ -354,25 +338,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool aborted = false;
     int t = 0;
 
-    // all N scaled scores of this thread's token (or -inf): N/16 TMEM loads, one wait
-    auto load_scores = [&](bool valid, float (&x)[N]) {
+    // 16 scaled scores of this thread's token (or -inf) from TMEM columns [c, c+16)
+    auto load_scores = [&](int c, bool valid, float (&x)[16]) {
       if (!aborted) {
-#pragma unroll
-        for (int c = 0; c < N; c += 16)
-          ptx::tmem_ld16(t_lane + L::kColS + (t & 1) * N + c, *reinterpret_cast<float(*)[16]>(x + c));
+        ptx::tmem_ld16(t_lane + L::kColS + (t & 1) * N + c, x);
         ptx::tmem_ld_wait();
       }
 #pragma unroll
-      for (int h = 0; h < N; ++h) x[h] = valid ? x[h] * p.scale_log2 : -INFINITY;
+      for (int e = 0; e < 16; ++e) x[e] = valid ? x[e] * p.scale_log2 : -INFINITY;
     };
     // exact per-head maximum over the page's 64 tokens -> red[h*4 + warp]
-    auto column_max = [&](const float (&x)[N]) {
+    auto column_max = [&](bool valid) {
 #pragma unroll
-      for (int h = 0; h < N; ++h) {
-        float v = x[h];
+      for (int c = 0; c < N; c += 16) {
+        float x[16];
+        load_scores(c, valid, x);
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, o));
-        if (lane == (h & 31)) red[h * 4 + sw] = v;
+        for (int e = 0; e < 16; ++e) {
+          float v = x[e];
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, o));
+          if (lane == ((c + e) & 31)) red[(c + e) * 4 + sw] = v;
+        }
       }
       ptx::named_barrier_sync(1, 128);
     };
@@ -390,11 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         const int token = (pt.p0 + i) * kPage + row;
         const bool valid = active && token < ctx && !aborted;
-        float x[N];
-        load_scores(valid, x);
         if (i == 0) {
           // first page of the piece: the running maximum starts at the exact column maximum
-          column_max(x);
+          column_max(valid);
           if (ctid < N) {
             const float4 r = *reinterpret_cast<const float4*>(red + ctid * 4);
             mused[ctid] = fmaxf(fmaxf(r.x, r.y), fmaxf(r.z, r.w));
@@ -404,10 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           // lazy maximum: only if a score exceeds the maximum in use by 2^8 is it raised
           bool need = false;
 #pragma unroll
-          for (int c = 0; c < N; c += 4) {
-            const float4 m4 = *reinterpret_cast<const float4*>(mused + c);
-            need |= (x[c] > m4.x + kRescaleLog2) | (x[c + 1] > m4.y + kRescaleLog2) |
-                    (x[c + 2] > m4.z + kRescaleLog2) | (x[c + 3] > m4.w + kRescaleLog2);
+          for (int c = 0; c < N; c += 16) {
+            float x[16];
+            load_scores(c, valid, x);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) need |= x[e] > mused[c + e] + kRescaleLog2;
           }
           const bool wneed = __any_sync(kFullMask, need);
           if (lane == 0) flags[2 + sw] = wneed ? 1 : 0;
@@ -415,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool cneed = (flags[2] | flags[3] | flags[4] | flags[5]) != 0;
           ptx::named_barrier_sync(1, 128);
           if (cneed) {
-            column_max(x);
+            column_max(valid);
             if (ctid < N) {
               const float4 r = *reinterpret_cast<const float4*>(red + ctid * 4);
               const float mo = mused[ctid];
@@ -452,23 +438,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P^T row `row` (heads contiguous) over the page's rope sub-tile
         uint8_t* pbuf = kv + (t & 1) * kPageBytes + kRopeSub * kSubBytes;
 #pragma unroll
-        for (int c = 0; c < N; c += 8) {
-          const float4 ma = *reinterpret_cast<const float4*>(mused + c);
-          const float4 mb = *reinterpret_cast<const float4*>(mused + c + 4);
-          const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
-          float pv[8];
+        for (int c = 0; c < N; c += 16) {
+          float x[16];
+          load_scores(c, valid, x);
+          float pv[16];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            pv[e] = ptx::exp2_approx(x[c + e] - mm[e]);
+          for (int e = 0; e < 16; ++e) {
+            pv[e] = ptx::exp2_approx(x[e] - mused[c + e]);
             l_reg[c + e] += pv[e];
           }
           if (active) {
-            uint4 w;
-            w.x = ptx::Mma<T>::pack(pv[0], pv[1]);
-            w.y = ptx::Mma<T>::pack(pv[2], pv[3]);
-            w.z = ptx::Mma<T>::pack(pv[4], pv[5]);
-            w.w = ptx::Mma<T>::pack(pv[6], pv[7]);
-            *reinterpret_cast<uint4*>(pbuf + row * 128 + (((c / 8) ^ (row & 7)) << 4)) = w;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const int chunk = c / 8 + half;
+              uint4 w;
+              w.x = ptx::Mma<T>::pack(pv[8 * half + 0], pv[8 * half + 1]);
+              w.y = ptx::Mma<T>::pack(pv[8 * half + 2], pv[8 * half + 3]);
+              w.z = ptx::Mma<T>::pack(pv[8 * half + 4], pv[8 * half + 5]);
+              w.w = ptx::Mma<T>::pack(pv[8 * half + 6], pv[8 * half + 7]);
+              *reinterpret_cast<uint4*>(pbuf + row * 128 + ((chunk ^ (row & 7)) << 4)) = w;
+            }
           }
         }
         // Slots past ctx in the last page: their P is 0, but 0 * (whatever the slot holds,
