@@ -180,6 +180,39 @@ PDA_API pda_status pda_combine_splits(const float* partial_out, const float* par
                               int32_t num_splits, int32_t head_dim_v, void* out,
                               int32_t out_dtype, float* lse, pda_stream_t stream);
 
+/*
+ * GQA / MQA / MHA paged decode without a caller-provided workspace.
+ *
+ * The sources this library follows have no counterpart to this call: it exists
+ * for callers that cannot allocate device memory when they decode, for example
+ * code running inside another framework's memory pool, a plug-in that is only
+ * handed input and output buffers, or a host that must not call cudaMalloc
+ * after start-up. It computes exactly what paged_decode_attn computes, with the
+ * same arguments minus `workspace`.
+ *
+ * Its split pieces, merge counters and error word live instead in one
+ * library-owned device array of PDA_NO_ALLOC_WORKSPACE_BYTES (16 MiB) that every
+ * GPU which loads this library keeps until the process exits. The call
+ * allocates nothing and calls no allocating routine:
+ *  - the first call on a device looks up that device's address of the array
+ *    (once per device, with that device current); make that first call before
+ *    any stream capture;
+ *  - each call clears the array's counters and error word on `stream` before
+ *    its kernel runs;
+ *  - every call shares the one array, so calls that can overlap on the GPU
+ *    (different streams, or several host threads) race and give wrong results;
+ *    issue them on one stream, or serialize them;
+ *  - a plan whose workspace exceeds the array (pda_plan_workspace_bytes(plan) >
+ *    PDA_NO_ALLOC_WORKSPACE_BYTES) is rejected with PDA_ERR_WORKSPACE.
+ * Device-side errors (the word pda_read_device_error reads) are not reported.
+ */
+#define PDA_NO_ALLOC_WORKSPACE_BYTES (16u << 20)
+PDA_API pda_status paged_decode_attn_no_alloc(const void* q, const void* k_cache,
+                                              const void* v_cache, const int32_t* block_tables,
+                                              const int32_t* context_lens, float scale, void* out,
+                                              float* lse, const pda_plan* plan,
+                                              pda_stream_t stream);
+
 /* Static name of a status code. */
 PDA_API const char* pda_status_string(pda_status status);
 

@@ -49,6 +49,7 @@ def _declare(lib):
         "paged_decode_attn": (I32, [P, P, P, P, P, F32, P, P, P, P, P]),
         "mla_decode": (I32, [P, P, P, P, F32, P, P, P, P, P]),
         "pda_combine_splits": (I32, [P, P, I32, I32, I32, P, I32, P, P]),
+        "paged_decode_attn_no_alloc": (I32, [P, P, P, P, P, F32, P, P, P, P]),
         "pda_status_string": (ctypes.c_char_p, [I32]),
         "pda_last_error": (ctypes.c_char_p, []),
     }
@@ -161,6 +162,15 @@ def paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, scale: fl
                                    _ptr(context_lens), float(scale), _ptr(out), _ptr(lse),
                                    plan.handle, _ptr(workspace), _stream(stream)),
            "paged_decode_attn")
+
+
+def paged_decode_attn_no_alloc(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                               out, lse, plan: Plan, stream=None):
+    """paged_decode_attn without a workspace (library-owned scratch; see include/pda.h)."""
+    _check(lib().paged_decode_attn_no_alloc(_ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                            _ptr(block_tables), _ptr(context_lens), float(scale),
+                                            _ptr(out), _ptr(lse), plan.handle, _stream(stream)),
+           "paged_decode_attn_no_alloc")
 
 
 def mla_decode(q, kv_cache, block_tables, context_lens, scale: float, out, lse, plan: Plan,
