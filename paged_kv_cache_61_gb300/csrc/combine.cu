@@ -6,6 +6,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include "pda_internal.h"
@@ -61,13 +62,13 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // ---------------------------------------------------------------- heavy-segment merge
-// One CTA per (heavy segment, head, 32 output dims): 8 float4 columns x 32 piece
-// lanes. Each thread merges its pieces online (running max, rescaled sum and
-// accumulator) with four pieces' loads in flight at a time; the 32 lanes of a
-// column are then merged through shared memory. A segment cut into hundreds of
-// pieces is thus merged by many SMs at once, in a few L2 round trips.
+// One CTA per (heavy segment, head, COLS float4 output columns) with 256 / COLS
+// piece lanes. Each thread merges its pieces online (running max, rescaled sum and
+// accumulator) with four pieces' loads in flight; the piece lanes of a column are
+// then merged through shared memory. The launcher picks COLS from the piece count:
+// wide CTAs for a few pieces of long rows (MLA), narrow ones with many piece lanes
+// when a segment was cut into hundreds of pieces (one long MQA sequence).
 constexpr int kMergeThreads = 256;
-constexpr int kPieceLanes = kMergeThreads / 8;
 
 struct MergeParams {
   const float* part_out;
@@ -79,17 +80,18 @@ struct MergeParams {
   HeavySegment seg[kMaxHeavySegments];
 };
 
-template <typename T>
+template <typename T, int COLS>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_heavy_kernel(const __grid_constant__ MergeParams p) {
+  constexpr int kLanes = kMergeThreads / COLS;
   // Wait until the decode grid that wrote the pieces has completed (programmatic
   // dependent launch lets this grid be scheduled while that one drains).
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  __shared__ float sm_m[kPieceLanes][8];
-  __shared__ float sm_l[kPieceLanes][8];
-  __shared__ float4 sm_o[kPieceLanes][8];
+  __shared__ float sm_m[kLanes][COLS];
+  __shared__ float sm_l[kLanes][COLS];
+  __shared__ float4 sm_o[kLanes][COLS];
 
-  const int chunks = p.dv / 32;
+  const int chunks = p.dv / (4 * COLS);
   int w = blockIdx.x;
   const int dchunk = w % chunks;
   w /= chunks;
@@ -98,18 +100,18 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int64_t q = p.tiles_per_cta;
   const int64_t c0 = hs.seg_start / q;
   const int n = int((hs.seg_start + hs.np - 1) / q - c0 + 1);
-  const int col = threadIdx.x & 7;
-  const int pl = threadIdx.x >> 3;
-  const int64_t dofs = int64_t(dchunk) * 32 + col * 4;
+  const int col = threadIdx.x % COLS;
+  const int pl = threadIdx.x / COLS;
+  const int64_t dofs = (int64_t(dchunk) * COLS + col) * 4;
 
   float m = -INFINITY, l = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i0 = pl; i0 < n; i0 += 4 * kPieceLanes) {
+  for (int i0 = pl; i0 < n; i0 += 4 * kLanes) {
     float ls[4];
     float4 o[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u * kPieceLanes;
+      const int i = i0 + u * kLanes;
       ls[u] = -INFINITY;
       o[u] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (i < n) {
@@ -138,10 +140,10 @@ __global__ void __launch_bounds__(kMergeThreads)
   __syncthreads();
   if (pl == 0) {
     float mx = -INFINITY;
-    for (int r = 0; r < kPieceLanes; ++r) mx = fmaxf(mx, sm_m[r][col]);
+    for (int r = 0; r < kLanes; ++r) mx = fmaxf(mx, sm_m[r][col]);
     float den = 0.f;
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int r = 0; r < kPieceLanes; ++r) {
+    for (int r = 0; r < kLanes; ++r) {
       if (sm_m[r][col] == -INFINITY) continue;
       const float f = exp2f((sm_m[r][col] - mx) * kLog2e);
       den += f * sm_l[r][col];
@@ -156,6 +158,17 @@ __global__ void __launch_bounds__(kMergeThreads)
     out[2] = to_out<T>(s.z * inv);
     out[3] = to_out<T>(s.w * inv);
     if (dchunk == 0 && col == 0 && p.lse != nullptr) p.lse[orow] = mx + logf(den);
+  }
+}
+
+template <typename T>
+cudaError_t launch_merge_t(int cols, const cudaLaunchConfig_t& base, const MergeParams& prm) {
+  cudaLaunchConfig_t cfg = base;
+  cfg.gridDim = dim3(unsigned(prm.count * prm.group * (prm.dv / (4 * cols))));
+  switch (cols) {
+    case 8: return cudaLaunchKernelEx(&cfg, merge_heavy_kernel<T, 8>, prm);
+    case 32: return cudaLaunchKernelEx(&cfg, merge_heavy_kernel<T, 32>, prm);
+    default: return cudaLaunchKernelEx(&cfg, merge_heavy_kernel<T, 128>, prm);
   }
 }
 
@@ -174,9 +187,19 @@ int launch_split_merge(const Plan& plan, const Workspace& ws, void* out, float* 
   prm.dv = plan.prob.head_dim_v;
   prm.num_q_heads = plan.prob.num_q_heads;
   prm.count = int32_t(plan.heavy.size());
-  for (size_t i = 0; i < plan.heavy.size(); ++i) prm.seg[i] = plan.heavy[i];
+  int max_pieces = 0;
+  for (size_t i = 0; i < plan.heavy.size(); ++i) {
+    prm.seg[i] = plan.heavy[i];
+    const HeavySegment& h = plan.heavy[i];
+    const int64_t pieces =
+        (h.seg_start + h.np - 1) / plan.tiles_per_cta - h.seg_start / plan.tiles_per_cta + 1;
+    max_pieces = std::max(max_pieces, int(pieces));
+  }
+  // float4 columns per CTA: wide rows with few pieces, narrow rows with many
+  int cols = max_pieces >= 64 ? 8 : (max_pieces >= 16 ? 32 : 128);
+  cols = std::min(cols, prm.dv / 4);
+  if (cols != 8 && cols != 32 && cols != 128) cols = 8;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(unsigned(prm.count * prm.group * (prm.dv / 32)));
   cfg.blockDim = dim3(kMergeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = static_cast<cudaStream_t>(stream);
@@ -185,12 +208,8 @@ int launch_split_merge(const Plan& plan, const Workspace& ws, void* out, float* 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e;
-  if (plan.prob.dtype == PDA_BF16)
-    e = cudaLaunchKernelEx(&cfg, merge_heavy_kernel<__nv_bfloat16>, prm);
-  else
-    e = cudaLaunchKernelEx(&cfg, merge_heavy_kernel<__half>, prm);
-  return e;
+  return plan.prob.dtype == PDA_BF16 ? launch_merge_t<__nv_bfloat16>(cols, cfg, prm)
+                                     : launch_merge_t<__half>(cols, cfg, prm);
 }
 
 int launch_combine(const float* partial_out, const float* partial_lse, int rows, int num_splits,

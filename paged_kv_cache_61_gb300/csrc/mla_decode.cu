@@ -49,7 +49,14 @@ constexpr int kSubBytes = kPage * 128;        // [64 tokens][64 dims] x 16 bit
 constexpr int kPageBytes = kSubTiles * kSubBytes;
 constexpr int kRopeSub = kSubTiles - 1;       // sub-tile reused for P^T
 constexpr int kStages = 2;
-constexpr int kThreads = 192;                 // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+// Warp 0 TMA, warp 1 MMA, then the softmax warps: 4 (one per TMEM sub-partition) for
+// N = 16 heads, 8 for N >= 32 (two per sub-partition, each owning half the head columns).
+template <int N>
+struct SoftmaxWarps {
+  static constexpr int kWarps = N >= 32 ? 8 : 4;
+  static constexpr int kThreads = 64 + 32 * kWarps;
+  static constexpr int kCols = N / (kWarps / 4);   // head columns per softmax thread
+};
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.f;           // lazy-max slack (log2 units)
@@ -81,7 +88,7 @@ struct MlaLayout {
   static constexpr int kAlpha = kMused + 64 * 4;       // rescale factor per head
   static constexpr int kLtot = kAlpha + 64 * 4;        // softmax denominator per head
   static constexpr int kBar = kLtot + 64 * 4;
-  static constexpr int kBarCount = 20;
+  static constexpr int kBarCount = 24;
   static constexpr int kSmem = 1024 + kBar + kBarCount * 8 + 64;
   // TMEM columns: S^T double-buffered at [0, 2N), O^T d-tile mt at 2N + mt*N
   static constexpr int kTmemCols = (6 * N <= 128) ? 128 : (6 * N <= 256 ? 256 : 512);
@@ -108,7 +115,7 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
 }
 
 template <int N, typename T>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_kv, const MlaParams p) {
   using L = MlaLayout<N>;
@@ -132,8 +139,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_free = bars + 8;    // [2] S^T buffer read, P^T written
   uint64_t* p_full = bars + 10;   // [2]
   uint64_t* pv_done = bars + 12;  // [2] PV of a page completed
-  volatile int* flags = reinterpret_cast<volatile int*>(bars + 14);  // [0] abort [1] last [2..5] votes (3 slots)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
+  // [0] abort, [1] last piece, [2..9] softmax-warp votes (5 slots)
+  volatile int* flags = reinterpret_cast<volatile int*>(bars + 14);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -151,11 +159,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(q_empty, 1);
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&s_full[b], 1);
-      ptx::mbar_init(&s_free[b], 4);
-      ptx::mbar_init(&p_full[b], 4);
+      ptx::mbar_init(&s_free[b], SoftmaxWarps<N>::kWarps);
+      ptx::mbar_init(&p_full[b], SoftmaxWarps<N>::kWarps);
       ptx::mbar_init(&pv_done[b], 1);
     }
-    for (int i = 0; i < 6; ++i) flags[i] = 0;
+    for (int i = 0; i < 10; ++i) flags[i] = 0;
     ptx::fence_mbarrier_init();
   }
   if (warp == 1) ptx::tmem_alloc(tmem_slot, L::kTmemCols);
@@ -327,41 +335,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ============================== softmax / epilogue warps ==============================
-    const int sw = warp - 2;               // 0..3
+    constexpr int kSW = SoftmaxWarps<N>::kWarps;
+    constexpr int NC = SoftmaxWarps<N>::kCols;   // head columns this thread owns
+    constexpr int kST = 32 * kSW;                // softmax threads
+    const int sw = warp - 2;               // 0 .. kSW-1
     const int sp = warp & 3;               // TMEM sub-partition of this warp
+    const int cb = (sw / 4) * NC;          // first head column of this warp
     const bool active = lane < 16;         // M=64 scores: rows in lanes 0..15 of each sub-partition
     const int row = 16 * sp + lane;        // token within the page (active lanes)
-    const int ctid = threadIdx.x - 64;     // 0..127
+    const int ctid = threadIdx.x - 64;     // 0 .. kST-1
     const uint32_t t_lane = tmem + (uint32_t(32 * sp) << 16);
     T* outg = static_cast<T*>(p.out);
-    float l_reg[N];
+    float l_reg[NC];
     bool aborted = false;
     int t = 0;
 
-    // 16 scaled scores of this thread's token (or -inf) from TMEM columns [c, c+16)
-    auto load_scores = [&](int c, bool valid, float (&x)[16]) {
+    // this thread's NC scaled scores (or -inf): NC/16 TMEM loads behind one wait
+    auto load_scores = [&](bool valid, float (&x)[NC]) {
       if (!aborted) {
-        ptx::tmem_ld16(t_lane + L::kColS + (t & 1) * N + c, x);
+#pragma unroll
+        for (int c = 0; c < NC; c += 16)
+          ptx::tmem_ld16(t_lane + L::kColS + (t & 1) * N + cb + c,
+                         *reinterpret_cast<float(*)[16]>(x + c));
         ptx::tmem_ld_wait();
       }
 #pragma unroll
-      for (int e = 0; e < 16; ++e) x[e] = valid ? x[e] * p.scale_log2 : -INFINITY;
+      for (int h = 0; h < NC; ++h) x[h] = valid ? x[h] * p.scale_log2 : -INFINITY;
     };
-    // exact per-head maximum over the page's 64 tokens -> red[h*4 + warp]
-    auto column_max = [&](bool valid) {
+    // exact per-head maximum over the page's 64 tokens -> red[h*4 + sub-partition]
+    auto column_max = [&](const float (&x)[NC]) {
 #pragma unroll
-      for (int c = 0; c < N; c += 16) {
-        float x[16];
-        load_scores(c, valid, x);
+      for (int h = 0; h < NC; ++h) {
+        float v = x[h];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float v = x[e];
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, o));
-          if (lane == ((c + e) & 31)) red[(c + e) * 4 + sw] = v;
-        }
+        for (int o = 1; o < 32; o <<= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, o));
+        if (lane == (h & 31)) red[(cb + h) * 4 + sp] = v;
       }
-      ptx::named_barrier_sync(1, 128);
+      ptx::named_barrier_sync(1, kST);
     };
 
     while (walk.g < g_hi) {
@@ -369,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int npg = pt.p1 - pt.p0;
       const int ctx = __ldg(p.context_lens + pt.b);
 #pragma unroll
-      for (int h = 0; h < N; ++h) l_reg[h] = 0.f;
+      for (int h = 0; h < NC; ++h) l_reg[h] = 0.f;
 
       for (int i = 0; i < npg; ++i, ++t) {
         if (!aborted && !bounded_wait(&s_full[t & 1], (t >> 1) & 1, flags, p.err)) aborted = true;
@@ -377,31 +387,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         const int token = (pt.p0 + i) * kPage + row;
         const bool valid = active && token < ctx && !aborted;
+        float x[NC];
+        load_scores(valid, x);
         if (i == 0) {
           // first page of the piece: the running maximum starts at the exact column maximum
-          column_max(valid);
+          column_max(x);
           if (ctid < N) {
             const float4 r = *reinterpret_cast<const float4*>(red + ctid * 4);
             mused[ctid] = fmaxf(fmaxf(r.x, r.y), fmaxf(r.z, r.w));
           }
-          ptx::named_barrier_sync(1, 128);
+          ptx::named_barrier_sync(1, kST);
         } else {
           // lazy maximum: only if a score exceeds the maximum in use by 2^8 is it raised
           bool need = false;
 #pragma unroll
-          for (int c = 0; c < N; c += 16) {
-            float x[16];
-            load_scores(c, valid, x);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) need |= x[e] > mused[c + e] + kRescaleLog2;
+          for (int c = 0; c < NC; c += 4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(mused + cb + c);
+            need |= (x[c] > m4.x + kRescaleLog2) | (x[c + 1] > m4.y + kRescaleLog2) |
+                    (x[c + 2] > m4.z + kRescaleLog2) | (x[c + 3] > m4.w + kRescaleLog2);
           }
           const bool wneed = __any_sync(kFullMask, need);
           if (lane == 0) flags[2 + sw] = wneed ? 1 : 0;
-          ptx::named_barrier_sync(1, 128);
-          const bool cneed = (flags[2] | flags[3] | flags[4] | flags[5]) != 0;
-          ptx::named_barrier_sync(1, 128);
-          if (cneed) {
-            column_max(valid);
+          ptx::named_barrier_sync(1, kST);
+          int any = 0;
+#pragma unroll
+          for (int k = 0; k < kSW; ++k) any |= flags[2 + k];
+          ptx::named_barrier_sync(1, kST);
+          if (any) {
+            column_max(x);
             if (ctid < N) {
               const float4 r = *reinterpret_cast<const float4*>(red + ctid * 4);
               const float mo = mused[ctid];
@@ -409,9 +422,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               alpha_s[ctid] = ptx::exp2_approx(mo - mn);
               mused[ctid] = mn;
             }
-            ptx::named_barrier_sync(1, 128);
+            ptx::named_barrier_sync(1, kST);
 #pragma unroll
-            for (int h = 0; h < N; ++h) l_reg[h] *= alpha_s[h];
+            for (int h = 0; h < NC; ++h) l_reg[h] *= alpha_s[cb + h];
             // O^T holds the pages up to t-1: wait for their PV, then rescale it in TMEM
             if (!aborted && !bounded_wait(&pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, flags, p.err))
               aborted = true;
@@ -421,13 +434,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
-                for (int c = 0; c < N; c += 16) {
+                for (int c = 0; c < NC; c += 16) {
                   float v[16];
-                  const uint32_t a = t_lane + L::kColO + mt * N + c;
+                  const uint32_t a = t_lane + L::kColO + mt * N + cb + c;
                   ptx::tmem_ld16(a, v);
                   ptx::tmem_ld_wait();
 #pragma unroll
-                  for (int e = 0; e < 16; ++e) v[e] *= alpha_s[c + e];
+                  for (int e = 0; e < 16; ++e) v[e] *= alpha_s[cb + c + e];
                   ptx::tmem_st16(a, v);
                 }
               }
@@ -438,35 +451,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P^T row `row` (heads contiguous) over the page's rope sub-tile
         uint8_t* pbuf = kv + (t & 1) * kPageBytes + kRopeSub * kSubBytes;
 #pragma unroll
-        for (int c = 0; c < N; c += 16) {
-          float x[16];
-          load_scores(c, valid, x);
-          float pv[16];
+        for (int c = 0; c < NC; c += 8) {
+          const float4 ma = *reinterpret_cast<const float4*>(mused + cb + c);
+          const float4 mb = *reinterpret_cast<const float4*>(mused + cb + c + 4);
+          const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+          float pv[8];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            pv[e] = ptx::exp2_approx(x[e] - mused[c + e]);
+          for (int e = 0; e < 8; ++e) {
+            pv[e] = ptx::exp2_approx(x[c + e] - mm[e]);
             l_reg[c + e] += pv[e];
           }
           if (active) {
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              const int chunk = c / 8 + half;
-              uint4 w;
-              w.x = ptx::Mma<T>::pack(pv[8 * half + 0], pv[8 * half + 1]);
-              w.y = ptx::Mma<T>::pack(pv[8 * half + 2], pv[8 * half + 3]);
-              w.z = ptx::Mma<T>::pack(pv[8 * half + 4], pv[8 * half + 5]);
-              w.w = ptx::Mma<T>::pack(pv[8 * half + 6], pv[8 * half + 7]);
-              *reinterpret_cast<uint4*>(pbuf + row * 128 + ((chunk ^ (row & 7)) << 4)) = w;
-            }
+            uint4 w;
+            w.x = ptx::Mma<T>::pack(pv[0], pv[1]);
+            w.y = ptx::Mma<T>::pack(pv[2], pv[3]);
+            w.z = ptx::Mma<T>::pack(pv[4], pv[5]);
+            w.w = ptx::Mma<T>::pack(pv[6], pv[7]);
+            const int chunk = (cb + c) / 8;
+            *reinterpret_cast<uint4*>(pbuf + row * 128 + ((chunk ^ (row & 7)) << 4)) = w;
           }
         }
         // Slots past ctx in the last page: their P is 0, but 0 * (whatever the slot holds,
         // NaN included) must not reach O, so their V rows are cleared before the PV MMA
-        // (the score MMA has already consumed the page).
+        // (the score MMA has already consumed the page). The warps of a sub-partition
+        // split the eight latent sub-tiles.
         if (active && token >= ctx) {
           uint8_t* stg = kv + (t & 1) * kPageBytes;
+          constexpr int kSubPerWarp = (kDv / 64) / (kSW / 4);
 #pragma unroll
-          for (int sub = 0; sub < kDv / 64; ++sub) {
+          for (int k = 0; k < kSubPerWarp; ++k) {
+            const int sub = (sw / 4) * kSubPerWarp + k;
             uint4* r = reinterpret_cast<uint4*>(stg + sub * kSubBytes + row * 128);
 #pragma unroll
             for (int c = 0; c < 8; ++c) r[c] = make_uint4(0u, 0u, 0u, 0u);
@@ -483,18 +497,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---- end of the piece: softmax denominators, then O = O^T / l
 #pragma unroll
-      for (int h = 0; h < N; ++h) {
+      for (int h = 0; h < NC; ++h) {
         float v = l_reg[h];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) v += __shfl_xor_sync(kFullMask, v, o);
-        if (lane == (h & 31)) red[h * 4 + sw] = v;
+        if (lane == (h & 31)) red[(cb + h) * 4 + sp] = v;
       }
-      ptx::named_barrier_sync(1, 128);
+      ptx::named_barrier_sync(1, kST);
       if (ctid < N) {
         const float4 r = *reinterpret_cast<const float4*>(red + ctid * 4);
         ltot[ctid] = (r.x + r.y) + (r.z + r.w);
       }
-      ptx::named_barrier_sync(1, 128);
+      ptx::named_barrier_sync(1, kST);
       if (!aborted && !bounded_wait(&pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, flags, p.err))
         aborted = true;
       aborted = __any_sync(kFullMask, aborted);
@@ -508,10 +522,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int mt = 0; mt < 4; ++mt) {
         const int d = mt * 128 + 32 * sp + lane;
 #pragma unroll
-        for (int c = 0; c < N; c += 16) {
+        for (int c = 0; c < NC; c += 16) {
           float v[16];
           if (!aborted) {
-            ptx::tmem_ld16(t_lane + L::kColO + mt * N + c, v);
+            ptx::tmem_ld16(t_lane + L::kColO + mt * N + cb + c, v);
             ptx::tmem_ld_wait();
           } else {
 #pragma unroll
@@ -519,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const int h = c + e;
+            const int h = cb + c + e;
             const float o = v[e] / ltot[h];
             if (whole)
               outg[(head0 + h) * kDv + d] = from_f32<T>(o);
@@ -545,16 +559,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pieces = int(c1 - c0 + 1);
         if (pieces <= p.heavy_min) {
           __threadfence();
-          ptx::named_barrier_sync(1, 128);
+          ptx::named_barrier_sync(1, kST);
           int32_t* counter = p.counters + int64_t(pt.b) * p.groups + pt.seg;
           if (ctid == 0) {
             const int prev = aborted ? -1 : atomicAdd(counter, 1);
             flags[1] = (prev == pieces - 1) ? 1 : 0;
           }
-          ptx::named_barrier_sync(1, 128);
+          ptx::named_barrier_sync(1, kST);
           if (flags[1]) {
             __threadfence();
-            for (int idx = ctid; idx < N * (kDv / 4); idx += 128) {
+            for (int idx = ctid; idx < N * (kDv / 4); idx += kST) {
               const int j = idx / (kDv / 4);
               const int dq = idx - j * (kDv / 4);
               float mx = -INFINITY;
@@ -584,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      ptx::named_barrier_sync(1, 128);
+      ptx::named_barrier_sync(1, kST);
     }
   }
 
@@ -656,7 +670,7 @@ int launch_mla_n(const CUtensorMap& tq, const CUtensorMap& tkv, const MlaParams&
                                     MlaLayout<N>::kSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  kern<<<grid, kThreads, MlaLayout<N>::kSmem, stream>>>(tq, tkv, prm);
+  kern<<<grid, SoftmaxWarps<N>::kThreads, MlaLayout<N>::kSmem, stream>>>(tq, tkv, prm);
   return cudaGetLastError();
 }
 
