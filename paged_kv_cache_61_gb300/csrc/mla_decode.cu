@@ -60,6 +60,10 @@ struct SoftmaxWarps {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.f;           // lazy-max slack (log2 units)
+#ifndef PDA_MLA_PREFETCH_PAGES
+#define PDA_MLA_PREFETCH_PAGES 0
+#endif
+constexpr int kPrefetchPages = PDA_MLA_PREFETCH_PAGES;  // L2 prefetch distance in pages
 
 struct MlaParams {
   const void* q;
@@ -202,9 +206,13 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
         const int n = min(32, pt.p1 - base_pg);
         for (int j = 0; j < n; ++j, ++t) {
           const int32_t phys = __shfl_sync(kFullMask, ids, j);
+          const int32_t ahead = __shfl_sync(kFullMask, ids, (j + kPrefetchPages) & 31);
           int good = 1;
           if (lane == 0) {
             const int s = t & 1;
+            // Optionally ask L2 for the page kPrefetchPages ahead (0 = off).
+            if (kPrefetchPages > 0 && j + kPrefetchPages < n)
+              ptx::tma_prefetch_l2_4d(&tm_kv, 0, 0, 0, ahead);
             if (!bounded_wait(&kv_empty[s], ((t >> 1) & 1) ^ 1, flags, p.err)) {
               good = 0;
             } else {
