@@ -256,6 +256,8 @@ def run_gpu(args, workload, rank, world, local_rank):
     from paged_kv_cache_61_gb300 import pda
 
     torch.cuda.set_device(local_rank)
+    # everything on one non-default stream (CUDA graphs cannot capture the legacy stream)
+    torch.cuda.set_stream(torch.cuda.Stream())
     dist = None
     if world > 1:
         import torch.distributed as dist
