@@ -243,6 +243,21 @@ METRIC = "paged decode attn achieved HBM GB/s (% of GB300 peak), μs/step; MLA T
 
 
 # ---------------------------------------------------------------- GPU arm
+def reduce_step_time(ms_per_step: float, dist, device) -> float:
+    """Max over ranks of the time per step (weak scaling: the slowest rank sets it)."""
+    if dist is None:
+        return ms_per_step
+    import torch
+    t = torch.tensor([ms_per_step], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step: float, world: int, ms_per_step: float) -> float:
+    """Units (bytes or FLOPs) all ranks process per second, every rank doing one step."""
+    return units_per_rank_step * world / (ms_per_step * 1e-3)
+
+
 def _has_merge(plan, case):
     """Whether a decode call on this plan also launches the split-merge kernel."""
     return plan.num_ctas > 0 and max(plan.num_splits(b) for b in range(case.batch)) > max(
@@ -345,10 +360,7 @@ def run_gpu(args, workload, rank, world, local_rank):
         sampler.mark_stop()
     total_ms = t_all0.elapsed_time(t_all1)
     ms_per_step = total_ms / args.steps
-    if dist is not None:
-        t = torch.tensor([ms_per_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
+    ms_per_step = reduce_step_time(ms_per_step, dist, "cuda")
     clocks = sampler.stop() if sampler else None
     if rank != 0:
         return
@@ -391,7 +403,7 @@ def run_gpu(args, workload, rank, world, local_rank):
     # segments (then the figure covers both, which understates the decode kernel alone).
     mean_launch_ms = ms_per_step
     if case.kind == "gqa":
-        value = kv_bytes * world / (ms_per_step * 1e-3) / 1e9
+        value = whole_job_rate(kv_bytes, world, ms_per_step) / 1e9
         unit = "GB/s"
         achieved = kv_bytes / (mean_launch_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
@@ -399,7 +411,7 @@ def run_gpu(args, workload, rank, world, local_rank):
                 "frac_of_8TBs_spec": achieved / 8000.0}
         e2e_value = kv_bytes / (e2e_ms * 1e-3) / 1e9
     else:
-        value = flops * world / (ms_per_step * 1e-3) / 1e12
+        value = whole_job_rate(flops, world, ms_per_step) / 1e12
         unit = "TFLOP/s"
         t_bytes = kv_bytes / (pk["hbm_gbs"] * 1e9)
         t_flops = flops / (pk["bf16_tflops"] * 1e12)
