@@ -1,0 +1,100 @@
+"""The oracle's pins catch plausible mistakes: each mutation planted in the oracle here
+(on the CPU, for the duration of one test) must make at least one pin fail."""
+import numpy as np
+import pytest
+
+import oracle
+import oracle.decode as od
+import test_oracle_pins as pins
+from paged_kv_cache_61_gb300 import synth
+
+PIN_CALLS = [
+    pins.test_worked_example_ctx37_mapping,
+    pins.test_worked_example_gather_reads_only_three_entries,
+    pins.test_unused_entries_and_stale_slots_never_matter,
+    pins.test_block_permutation_invariance,
+    pins.test_ctx1_gives_first_value_row,
+    pins.test_equal_keys_give_mean_value_and_log_length,
+    pins.test_constant_values_give_that_value,
+    pins.test_needle_selects_one_token,
+    pins.test_gqa_equals_mha_with_repeated_kv_heads,
+    lambda: pins.test_matches_torch_float64_softmax(synth.FP16),
+    pins.test_tiny_workload_matches_torch_float64,
+    pins.test_split_combine_equals_whole,
+    pins.test_combine_weights_by_split_mass_and_skips_empty,
+    pins.test_mla_equals_generic_with_one_kv_head,
+    pins.test_mla_rope_only_needle_returns_latent_of_target,
+]
+
+
+def _attend_log2(q_rows, keys, values, scale):
+    s = float(scale) * (np.asarray(q_rows, float) @ np.asarray(keys, float).T)
+    m = s.max(axis=1)
+    e = np.exp(s - m[:, None])
+    z = e.sum(axis=1)
+    return (e @ np.asarray(values, float)) / z[:, None], m + np.log2(z)
+
+
+def _attend_no_scale(q_rows, keys, values, scale):
+    return od.__dict__["_orig_attend"](q_rows, keys, values, 1.0)
+
+
+def _attend_keys_as_values(q_rows, keys, values, scale):
+    return od.__dict__["_orig_attend"](q_rows, keys, keys[:, : np.asarray(values).shape[1]], scale)
+
+
+def _token_locations_next_entry(row, ctx, page):
+    phys, slots = od.__dict__["_orig_token_locations"](row, ctx, page)
+    shifted = [int(row[j // page + 1]) if j // page + 1 < len(row) else int(row[j // page])
+               for j in range(int(ctx))]
+    return np.asarray(shifted, dtype=np.int64), slots
+
+
+def _token_locations_bad_slot(row, ctx, page):
+    phys, _ = od.__dict__["_orig_token_locations"](row, ctx, page)
+    return phys, np.asarray([j % (page - 1) for j in range(int(ctx))], dtype=np.int64)
+
+
+def _kv_head_interleaved(h, hq, hkv):
+    return h % hkv
+
+
+def _combine_plain_mean(po, pl):
+    po, pl = np.asarray(po, float), np.asarray(pl, float)
+    keep = np.isfinite(pl)
+    return po[keep].mean(axis=0), pl[keep].max()
+
+
+def _mla_drops_rope(q, kv, tables, ctx, scale, page, dtype, head_dim_v=512, rows=None):
+    q2 = q.copy()
+    q2[..., head_dim_v:] = 0
+    return od.__dict__["_orig_mla"](q2, kv, tables, ctx, scale, page, dtype, head_dim_v, rows)
+
+
+MUTATIONS = {
+    "lse in log2": ("attend", _attend_log2),
+    "scale dropped": ("attend", _attend_no_scale),
+    "keys used as values": ("attend", _attend_keys_as_values),
+    "next table entry read": ("token_locations", _token_locations_next_entry),
+    "wrong slot within the page": ("token_locations", _token_locations_bad_slot),
+    "interleaved head grouping": ("kv_head_of", _kv_head_interleaved),
+    "splits averaged without weights": ("combine_splits", _combine_plain_mean),
+    "MLA rope dims ignored": ("mla_decode", _mla_drops_rope),
+}
+
+
+@pytest.mark.parametrize("name", list(MUTATIONS))
+def test_mutation_is_caught_by_a_pin(name, monkeypatch):
+    func, repl = MUTATIONS[name]
+    monkeypatch.setitem(od.__dict__, "_orig_attend", od.attend)
+    monkeypatch.setitem(od.__dict__, "_orig_token_locations", od.token_locations)
+    monkeypatch.setitem(od.__dict__, "_orig_mla", od.mla_decode)
+    monkeypatch.setattr(od, func, repl)
+    monkeypatch.setattr(oracle, func, repl)
+    caught = []
+    for call in PIN_CALLS:
+        try:
+            call()
+        except (AssertionError, IndexError, ValueError):
+            caught.append(getattr(call, "__name__", "lambda"))
+    assert caught, f"no pin fails when the oracle has the mistake: {name}"
