@@ -40,7 +40,8 @@ from paged_kv_cache_61_gb300 import synth, traffic  # noqa: E402
 DEFAULT_WORKLOAD = "gqa_b64_ctx1k"
 L2_BYTES = 129 * 2 ** 20
 KERNEL_SOURCES = {"gqa": ["gqa_decode.cu", "ptx.cuh", "tile_walk.cuh"],
-                  "mla": ["mla_decode.cu", "ptx.cuh", "tile_walk.cuh"]}
+                  "mla": ["mla_decode.cu", "ptx.cuh", "tile_walk.cuh"],
+                  "mla_pair": ["mla_pair.cu", "ptx.cuh", "ptx_cluster.cuh", "tile_walk.cuh"]}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -67,6 +68,13 @@ def kernel_hash(kind: str) -> str:
         with open(os.path.join(ROOT, "paged_kv_cache_61_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def kernel_kind(case) -> str:
+    """Which decode kernel a case runs on (MLA head groups of 128 use the two-CTA kernel)."""
+    if case.kind == "gqa":
+        return "gqa"
+    return "mla_pair" if case.num_q_heads % 128 == 0 else "mla"
 
 
 def recorded_traffic(workload: str, kind: str):
@@ -427,7 +435,7 @@ def run_gpu(args, workload, rank, world, local_rank):
         roof["tflops"] = achieved_tf
         roof["frac_of_slower_roof"] = max(t_bytes, t_flops) / (mean_launch_ms * 1e-3)
         e2e_value = flops / (e2e_ms * 1e-3) / 1e12
-    roof["traffic"] = recorded_traffic(workload, case.kind)
+    roof["traffic"] = recorded_traffic(workload, kernel_kind(case))
     roof["algorithmic_bytes_per_launch"] = kv_bytes
     roof["mean_launch_us"] = mean_launch_ms * 1e3
     roof["scope"] = ("decode kernel + split-merge kernel per step" if launches_per_step > 1

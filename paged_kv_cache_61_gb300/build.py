@@ -19,7 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpda.so")
-SOURCES = ["plan.cpp", "api.cpp", "gqa_decode.cu", "combine.cu", "mla_decode.cu", "no_alloc.cu"]
+SOURCES = ["plan.cpp", "api.cpp", "gqa_decode.cu", "combine.cu", "mla_decode.cu", "mla_pair.cu",
+           "no_alloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -694,7 +694,10 @@ int launch_mla_t(int n, const CUtensorMap& tq, const CUtensorMap& tkv, const Mla
 
 }  // namespace
 
-int mla_heads_per_cta(const pda_problem& p) { return p.num_q_heads <= 64 ? p.num_q_heads : 64; }
+int mla_heads_per_cta(const pda_problem& p) {
+  if (mla_uses_pairs(p)) return 128;   // one 128-head group per CTA pair
+  return p.num_q_heads <= 64 ? p.num_q_heads : 64;
+}
 int mla_ctas_per_sm(const pda_problem&) { return 1; }
 
 bool mla_supported(const pda_problem& p, std::string* why) {
@@ -711,7 +714,7 @@ bool mla_supported(const pda_problem& p, std::string* why) {
     return false;
   }
   const int n = mla_heads_per_cta(p);
-  if (!(n == 16 || n == 32 || n == 64) || p.num_q_heads % n != 0) {
+  if (!(n == 16 || n == 32 || n == 64 || n == 128) || p.num_q_heads % n != 0) {
     *why = "MLA decode supports num_q_heads 16, 32 or a multiple of 64";
     return false;
   }
@@ -723,6 +726,7 @@ bool mla_supported(const pda_problem& p, std::string* why) {
 }
 
 int launch_mla_decode(const Plan& plan, const MlaArgs& a, const Workspace& ws, void* stream) {
+  if (plan.cluster == 2) return launch_mla_pair(plan, a, ws, stream);
   const pda_problem& pr = plan.prob;
   const bool bf16 = pr.dtype == PDA_BF16;
   const int n = plan.group;

@@ -36,16 +36,17 @@ struct Plan {
   int32_t group = 1;            // query heads per segment (GQA: Hq/Hkv; MLA: Hq / head groups)
   int32_t segs_per_seq = 1;     // segments per sequence (GQA: Hkv; MLA: head groups)
   int32_t head_subtiles = 1;    // GQA: 8-head MMA column tiles per segment
+  int32_t cluster = 1;          // CTAs per work unit (2: the MLA kernel for 128-head groups)
   int64_t total_tiles = 0;
   int64_t tiles_per_cta = 0;
-  int32_t num_ctas = 0;
+  int32_t num_ctas = 0;         // work units (CTA pairs when cluster == 2)
   std::vector<int32_t> context_lens;  // host copy used for planning
   std::vector<int32_t> splits;        // per sequence: max pieces over its segments
   int32_t heavy_min_pieces = 4;       // segments with more pieces than this are "heavy"
   std::vector<HeavySegment> heavy;    // at most kMaxHeavySegments
   // workspace layout (byte offsets)
   size_t ws_err = 0;        // int32 device error word
-  size_t ws_counters = 0;   // int32 [B * segs_per_seq]
+  size_t ws_counters = 0;   // int32 [B * segs_per_seq * cluster]
   size_t ws_part_lse = 0;   // float [num_ctas * 2 * group]
   size_t ws_part_out = 0;   // float [num_ctas * 2 * group * head_dim_v]
   size_t ws_bytes = 0;
@@ -103,6 +104,11 @@ bool mla_supported(const pda_problem& p, std::string* why);
 int gqa_ctas_per_sm(const pda_problem& p);
 int mla_ctas_per_sm(const pda_problem& p);
 int mla_heads_per_cta(const pda_problem& p);
+
+// MLA with head groups of 128: one group per two-CTA cluster (mla_pair.cu).
+bool mla_uses_pairs(const pda_problem& p);
+int mla_pair_units(int num_sms);   // co-resident CTA pairs (falls back to num_sms / 2)
+int launch_mla_pair(const Plan& plan, const MlaArgs& args, const Workspace& ws, void* stream);
 
 }  // namespace pda
 

@@ -125,6 +125,7 @@ extern "C" PDA_API pda_status pda_plan_create(pda_plan** out, const pda_problem*
     plan->group = pda::mla_heads_per_cta(p);
     plan->segs_per_seq = p.num_q_heads / plan->group;
     plan->head_subtiles = 1;
+    plan->cluster = pda::mla_uses_pairs(p) ? 2 : 1;
     ctas_per_sm = pda::mla_ctas_per_sm(p);
     min_tiles_per_cta = 2;
   }
@@ -138,7 +139,8 @@ extern "C" PDA_API pda_status pda_plan_create(pda_plan** out, const pda_problem*
     if (p.force_num_ctas > 0) {
       q = pda::cdiv(plan->total_tiles, p.force_num_ctas);
     } else {
-      const int64_t max_ctas = int64_t(num_sms) * ctas_per_sm;
+      const int64_t max_ctas = plan->cluster == 2 ? int64_t(pda::mla_pair_units(num_sms))
+                                                  : int64_t(num_sms) * ctas_per_sm;
       q = std::max(min_tiles_per_cta, pda::cdiv(plan->total_tiles, max_ctas));
     }
     q = std::max(q, pda::cdiv(plan->total_tiles, pda::kMaxCtas));
@@ -178,7 +180,8 @@ extern "C" PDA_API pda_status pda_plan_create(pda_plan** out, const pda_problem*
   plan->ws_err = off;
   off += 256;
   plan->ws_counters = off;
-  off = pda::round_up(off + sizeof(int32_t) * size_t(p.batch) * plan->segs_per_seq, 256);
+  off = pda::round_up(
+      off + sizeof(int32_t) * size_t(p.batch) * plan->segs_per_seq * plan->cluster, 256);
   plan->ws_part_lse = off;
   off = pda::round_up(off + sizeof(float) * size_t(plan->num_ctas) * 2 * plan->group, 256);
   plan->ws_part_out = off;

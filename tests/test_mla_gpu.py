@@ -47,17 +47,28 @@ def test_small_cases(hq, force):
     _assert_close(case, DeviceCase(case, force_num_ctas=force))
 
 
-def test_fp16():
-    case = _case(16, [200, 64, 1], dtype=synth.FP16)
+@pytest.mark.parametrize("hq", [16, 128])
+def test_fp16(hq):
+    case = _case(hq, [200, 64, 1], dtype=synth.FP16)
     _assert_close(case, DeviceCase(case))
 
 
-def test_score_jumps_force_rescales():
+@pytest.mark.parametrize("hq", [128, 256])
+@pytest.mark.parametrize("force", [0, 2, 5])
+def test_head_groups_of_128_ragged_batch(hq, force):
+    # head groups of 128 run on CTA pairs: ragged last pages, a one-token sequence and
+    # sequences split over several pairs (merged in-kernel and by the merge kernel)
+    case = _case(hq, [1, 65, 127, 128, 129, 1000, 3000], seed=11)
+    _assert_close(case, DeviceCase(case, force_num_ctas=force))
+
+
+@pytest.mark.parametrize("hq", [64, 128])
+def test_score_jumps_force_rescales(hq):
     # q's rope half is all ones and the rope keys of pages >= 3 and >= 10 get a constant
     # added, so the scores jump twice by ~8.7 in log2 units: the running maximum must be
     # raised and the accumulated output rescaled within one piece. After each jump many
     # tokens share the weight, so the check stays inside the bf16 tolerance.
-    case = _case(64, [2000, 900])
+    case = _case(hq, [2000, 900])
     case.q[..., 512:] = synth.float32_to_bits(np.float32(1.0), case.dtype)
     kv = synth.bits_to_float32(case.kv_cache, case.dtype)
     step = 6.0 * np.sqrt(192.0) / 64.0          # +6 on the natural-log score per jump
@@ -71,9 +82,10 @@ def test_score_jumps_force_rescales():
         _assert_close(case, DeviceCase(case, force_num_ctas=force))
 
 
-def test_rope_needle_is_bit_exact():
+@pytest.mark.parametrize("hq", [16, 128])
+def test_rope_needle_is_bit_exact(hq):
     ctx = 300
-    case = _case(16, [ctx] * 6, seed=9)
+    case = _case(hq, [ctx] * 6, seed=9)
     one = synth.float32_to_bits(np.float32(1.0), case.dtype)
     sixteen = synth.float32_to_bits(np.float32(16.0), case.dtype)
     case.q[..., :512] = 0
@@ -90,7 +102,7 @@ def test_rope_needle_is_bit_exact():
         got = device_bits(out)
         for b, t in enumerate(targets):
             blk = int(case.block_tables[b, t // 64])
-            for h in range(16):
+            for h in range(hq):
                 assert np.array_equal(got[b, h], case.kv_cache[blk, t % 64, :512]), (force, b, h)
 
 
@@ -105,8 +117,9 @@ def test_ctx1_returns_latent_of_token0():
             assert np.array_equal(got[b, h], case.kv_cache[blk, 0, :512])
 
 
-def test_poisoned_stale_slots_and_table_entries():
-    case = _case(32, [70, 129, 5])
+@pytest.mark.parametrize("hq", [32, 128])
+def test_poisoned_stale_slots_and_table_entries(hq):
+    case = _case(hq, [70, 129, 5])
     out0, lse0 = DeviceCase(case).run()
     torch.cuda.synchronize()
     kv, tab = case.kv_cache.copy(), case.block_tables.copy()
