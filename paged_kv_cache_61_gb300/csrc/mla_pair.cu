@@ -16,17 +16,21 @@
 //  * Scores with the heads on the MMA's M axis: S_r[128 x 64 tokens] = q_r * K_r^T
 //    (M=128, N=64, K=288: 18 tcgen05.mma). On this part an MMA's issue cost is set by
 //    N (a floor of ~46 cycles up to N=64), so 128 heads on M cost what 64 would.
-//  * The two partial score tiles are swapped through distributed shared memory: each
-//    CTA stages its tile in its own shared memory and one bulk copy per warp moves it
-//    into the peer's buffer, counted on the peer's mbarrier. Both CTAs then hold
-//    S = S_0 + S_1 bit for bit (fp32 addition commutes) and run the same online softmax,
-//    one thread per head with the running maximum and sums in registers, so they take
-//    the same rescaling decisions without exchanging them.
-//  * P (16-bit) is written to tensor memory and is the A operand of the PV MMA:
-//    O_r[128 x 256] += P[128 x 64] * V_r[64 x 256] (M=128, N=256, 4 MMAs), V_r read in
-//    place from the page's latent sub-tiles. CTA r owns output dims [256r, 256r+256).
-//  * Split pieces and their merge follow the other decode kernels; each CTA writes and
-//    merges its half of the output dims.
+//  * CTA r owns the softmax of heads [64r, 64r+64) ("owner" warps; the other two
+//    softmax-group warps "relay" the peer's heads). Per page, the relays send the
+//    partial scores of the peer's heads (16 KB fp32) into the peer's shared memory; the
+//    owners add the peer's partial for their heads, run the online softmax (one thread
+//    per head) and send their P rows (8 KB, 16-bit) and rescale factors back. The
+//    transfers between the two SMs (bulk copies and st.async counted on the receiver's
+//    mbarriers) run about 40 GB/s each way with ~0.4 us latency, so the exchange is
+//    double-buffered and kept small.
+//  * P[128 x 64] in shared memory is the A operand of the PV MMA:
+//    O_r[128 x 256] += P * V_r[64 x 256] (M=128, N=256, 4 MMAs), V_r read in place
+//    from the page's latent sub-tiles. CTA r owns output dims [256r, 256r+256); the
+//    owners rescale their heads' rows of O_r, the relays the peer's heads' rows.
+//  * At the end of a piece the owners send (m, l, lq) of their heads to the peer, and
+//    both CTAs normalise and write their output half. Split pieces and their merge
+//    follow the other decode kernels; each CTA merges its half of the output dims.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -46,6 +50,7 @@ constexpr int kPage = 64;
 constexpr int kDqk = 576;
 constexpr int kDv = 512;
 constexpr int kHeads = 128;                 // query heads per pair
+constexpr int kOwnHeads = kHeads / 2;       // heads whose softmax a CTA runs
 constexpr int kHalfDv = kDv / 2;            // output / latent dims per CTA
 constexpr int kLatSubs = kHalfDv / 64;      // 128-byte-swizzled 64-dim sub-tiles per CTA
 constexpr int kRopeHalf = 32;               // rope dims per CTA (64-byte swizzle)
@@ -53,11 +58,22 @@ constexpr int kStages = 4;
 constexpr int kLatSubBytes = kPage * 128;                          // [64 tokens][64 dims]
 constexpr int kRopeBytes = kPage * kRopeHalf * 2;                  // [64 tokens][32 dims]
 constexpr int kStageBytes = kLatSubs * kLatSubBytes + kRopeBytes;  // 36 KB
-constexpr int kXBytes = kHeads * kPage * 4;                        // one fp32 score tile
-constexpr int kSoftmaxWarps = 4;                                   // one thread per head
-constexpr int kThreads = 64 + 32 * kSoftmaxWarps;
+constexpr int kXsBytes = kOwnHeads * kPage * 4;                    // 64 heads' fp32 scores
+constexpr int kPRowsBytes = kOwnHeads * kPage * 2;                 // 64 heads' P rows, 16-bit
+constexpr int kPMsgBytes = kPRowsBytes + kOwnHeads * 4;            // P rows + factors
+constexpr int kFinBytes = kOwnHeads * 16;                          // (m, l, lq, -) per head
+// Softmax group: two warps per tensor-memory sub-partition. On the owner sub-partitions
+// they split each page's tokens; on the relay sub-partitions one sends scores and the
+// other receives P rows and factors.
+constexpr int kGroupWarps = 8;
+constexpr int kHalfTok = kPage / 2;
+constexpr int kQWarps = 6;     // warps that load q (all but the two receivers)
+constexpr int kPWarps = 6;     // warps that arrive on p_full (owners and receivers)
+constexpr int kSWarps = 6;     // warps that read S (owners and senders)
+constexpr int kMergeThreads = 32 * 6;   // owners and receivers: the end-of-piece work
+constexpr int kThreads = 64 + 32 * kGroupWarps;
 constexpr int kTmemCols = 512;
-// tensor-memory columns (32-bit): q_r as 16-bit pairs, S, P as 16-bit pairs, O_r
+// tensor-memory columns (32-bit): q_r as 16-bit pairs, P as 16-bit pairs, S, O_r
 constexpr int kColQ = 0;     // 144 columns: latent dims in [0, 128), rope dims in [128, 144)
 constexpr int kColP = 160;   // 32 columns
 constexpr int kColS = 192;   // 64 columns
@@ -68,12 +84,17 @@ constexpr float kRescaleLog2 = 8.f;   // lazy-max slack (log2 units)
 
 struct Layout {
   static constexpr int kKV = 0;
-  static constexpr int kX = kKV + kStages * kStageBytes;   // the peer's partial scores land here
-  static constexpr int kStg = kX + kXBytes;                 // this CTA's, on their way out
-  static constexpr int kBar = kStg + kXBytes;
-  static constexpr int kBarCount = 24;
-  static constexpr int kSmem = 1024 + kBar + kBarCount * 8 + 64;
-  static_assert(kStageBytes % 1024 == 0 && kX % 1024 == 0, "swizzled tiles stay 1024-byte aligned");
+  static constexpr int kXs = kKV + kStages * kStageBytes;   // [2] the peer's partials, own heads
+  static constexpr int kSstg = kXs + 2 * kXsBytes;          // own partials of the peer's heads
+  static constexpr int kPout = kSstg + kXsBytes;             // the owners' P rows, outgoing
+  static constexpr int kPin = kPout + kPRowsBytes;           // [2] the peer's P rows
+  static constexpr int kAlpha = kPin + 2 * kPRowsBytes;      // [2][64] the peer's factors
+  static constexpr int kFin = kAlpha + 2 * kOwnHeads * 4;    // [64] the peer's (m, l, lq)
+  static constexpr int kRed = kFin + kFinBytes;              // owner halves: maxima, sums
+  static constexpr int kBar = kRed + 1024;
+  static constexpr int kBarCount = 32;
+  static constexpr int kSmem = 1024 + kBar + kBarCount * 8;
+  static_assert(kStageBytes % 1024 == 0 && kXs % 1024 == 0, "swizzled tiles stay 1024-byte aligned");
   static_assert(kSmem <= 227 * 1024, "fits one SM's shared memory");
 };
 
@@ -143,25 +164,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // the same offset in both CTAs of the pair (same kernel, same static layout)
   uint8_t* base = align1024(smem_raw);
   uint8_t* kv = base + Layout::kKV;
-  uint8_t* xbuf = base + Layout::kX;
-  uint8_t* stg_out = base + Layout::kStg;
+  uint8_t* xs = base + Layout::kXs;
+  uint8_t* sstg = base + Layout::kSstg;
+  uint8_t* pout = base + Layout::kPout;
+  uint8_t* pin = base + Layout::kPin;
+  float* alpha_in = reinterpret_cast<float*>(base + Layout::kAlpha);
+  float4* fin_in = reinterpret_cast<float4*>(base + Layout::kFin);
+  float* red = reinterpret_cast<float*>(base + Layout::kRed);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + Layout::kBar);
   uint64_t* kv_full = bars + 0;    // [4]
   uint64_t* kv_empty = bars + 4;   // [4]
-  uint64_t* q_full = bars + 8;     // q of the next piece is in tensor memory
+  uint64_t* q_full = bars + 8;     // q of the current piece is in tensor memory
   uint64_t* s_full = bars + 9;     // S written by the score MMA
-  uint64_t* s_free = bars + 10;    // S read by the softmax warps
-  uint64_t* p_full = bars + 11;    // P written
-  uint64_t* pv_done = bars + 12;   // PV of a page completed
-  uint64_t* x_full = bars + 13;    // the peer's partial scores are in xbuf
-  uint64_t* x_free = bars + 14;    // the peer has read this CTA's partial scores
+  uint64_t* s_free = bars + 10;    // S read by the four softmax-group warps
+  uint64_t* p_full = bars + 11;    // [2] P complete in tensor memory, O rows rescaled
+  uint64_t* pv_done = bars + 13;   // [2] PV of a page completed
+  uint64_t* xs_full = bars + 15;   // [2] the peer's partial scores of this CTA's heads
+  uint64_t* xs_free = bars + 17;   // [2] the peer's owners have read what this CTA sent
+  uint64_t* pr_full = bars + 19;   // [2] the peer's P rows and factors have landed
+  uint64_t* pr_free = bars + 21;   // [2] the peer's receivers have read this CTA's P rows
+  uint64_t* fin_full = bars + 23;  // the peer's (m, l, lq) of a piece have landed
+  uint64_t* fin_free = bars + 24;  // the peer's relays have read this CTA's (m, l, lq)
   // [0] abort, [1] last piece to arrive
-  volatile int* flags = reinterpret_cast<volatile int*>(bars + 16);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
+  volatile int* flags = reinterpret_cast<volatile int*>(bars + 26);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 30);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
+  const uint32_t peer = rank ^ 1;
   const int64_t pair = blockIdx.x >> 1;
   const int64_t g_lo = pair * p.tiles_per_cta;
   const int64_t g_hi = min(p.total_tiles, g_lo + p.tiles_per_cta);
@@ -174,17 +205,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&kv_full[s], 1);
       ptx::mbar_init(&kv_empty[s], 1);
     }
-    ptx::mbar_init(q_full, kSoftmaxWarps);
+    ptx::mbar_init(q_full, kQWarps);
     ptx::mbar_init(s_full, 1);
-    ptx::mbar_init(s_free, kSoftmaxWarps);
-    ptx::mbar_init(p_full, kSoftmaxWarps);
-    ptx::mbar_init(pv_done, 1);
-    ptx::mbar_init(x_full, 1);
-    ptx::mbar_init(x_free, kSoftmaxWarps);
+    ptx::mbar_init(s_free, kSWarps);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&p_full[b], kPWarps);
+      ptx::mbar_init(&pv_done[b], 1);
+      ptx::mbar_init(&xs_full[b], 1);
+      ptx::mbar_init(&xs_free[b], 4);   // the peer's four owner warps
+      ptx::mbar_init(&pr_full[b], 1);
+      ptx::mbar_init(&pr_free[b], 2);   // the peer's two receiver warps
+    }
+    ptx::mbar_init(fin_full, 1);
+    ptx::mbar_init(fin_free, 2);        // the peer's two receiver warps
     for (int i = 0; i < 8; ++i) flags[i] = 0;
     ptx::fence_mbarrier_init();
-    // the first page's partial scores from the peer (its copies may land first)
-    ptx::mbar_arrive_expect_tx(x_full, kXBytes);
+    // what the peer sends for the first two pages and the first piece (it may land first)
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_arrive_expect_tx(&xs_full[b], kXsBytes);
+      ptx::mbar_arrive_expect_tx(&pr_full[b], kPMsgBytes);
+    }
+    ptx::mbar_arrive_expect_tx(fin_full, kFinBytes);
   }
   if (warp == 1) ptx::tmem_alloc(tmem_slot, kTmemCols);
   ptx::tc_fence_before();
@@ -195,7 +236,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const WalkSpec spec{p.context_lens, p.batch, p.groups, kPage};
   Walker walk;
   walker_init(walk, spec, g_lo, lane);
-
   if (warp == 0) {
     // ============================== TMA producer ==============================
     if (lane == 0) {
@@ -252,7 +292,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ============================== MMA issuer ==============================
     // One thread issues whichever MMA group is ready: the scores of the next page
     // (its stage, q and the S columns are ready) or the PV of the oldest page whose P
-    // is in tensor memory.
+    // tile is complete.
     constexpr uint32_t kIdQK = ptx::umma_idesc_f16(128, 64, 0, 0, kBf16);
     constexpr uint32_t kIdPV = ptx::umma_idesc_f16(128, 256, 0, 1, kBf16);
     const uint32_t kv_s = ptx::smem_addr(kv);
@@ -310,18 +350,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             progress = true;
           }
         }
-        if (t_pv < t_qk && ptx::mbar_try_wait(p_full, t_pv & 1)) {
+        if (t_pv < t_qk && ptx::mbar_try_wait(&p_full[t_pv & 1], (t_pv >> 1) & 1)) {
           ptx::tc_fence_after();
           const bool first = (first_bits >> (t_pv & 31)) & 1u;
           const uint32_t stg = kv_s + st_pv * kStageBytes;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            // V_r: 16 tokens x 256 dims, dims contiguous in four 64-dim sub-tiles
+            // P: 128 heads x 16 tokens in tensor memory; V_r: 16 tokens x 256 dims (dims
+            // contiguous in four 64-dim sub-tiles)
             const uint64_t b = ptx::umma_desc_sw128(stg + ks * 2048, kLatSubBytes, 1024);
             ptx::umma_f16_ts(tmem + kColO, tmem + kColP + ks * 8, b, kIdPV, !(first && ks == 0));
           }
           ptx::umma_commit(&kv_empty[st_pv]);
-          ptx::umma_commit(pv_done);
+          ptx::umma_commit(&pv_done[t_pv & 1]);
           ++t_pv;
           if (++st_pv == kStages) st_pv = 0;
           progress = true;
@@ -333,40 +374,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           flags[0] = 1;
           atomicOr(p.err, 2);
           break;
+        } else {
+          __nanosleep(32);   // leave issue slots to the softmax warps on this sub-partition
         }
       }
       // Wait (bounded) for the last MMAs before tensor memory is released.
       if (t_pv > 0) {
+        const int tl = t_pv - 1;
         const uint64_t t0 = ptx::globaltimer();
-        while (!ptx::mbar_try_wait(pv_done, (t_pv - 1) & 1) &&
+        while (!ptx::mbar_try_wait(&pv_done[tl & 1], (tl >> 1) & 1) &&
                ptx::globaltimer() - t0 < ptx::kWaitLimitNs) {
         }
       }
     }
     __syncwarp();
   } else {
-    // ============================== softmax / epilogue warps ==============================
-    const int sp = warp & 3;                 // TMEM sub-partition of this warp
-    const int h = 32 * sp + lane;            // head of the group = TMEM lane
-    const int ctid = threadIdx.x - 64;       // 0 .. 127
+    // ============================== softmax group: owners and relays ==============================
+    const int sp = warp & 3;                   // TMEM sub-partition of this warp
+    const int pos = (warp - 2) >> 2;           // 0 or 1: which of the sub-partition's two warps
+    const bool owner = (sp >> 1) == int(rank); // heads [64 rank, 64 rank + 64) are this CTA's
+    const bool sender = !owner && pos == 0;
+    const bool receiver = !owner && pos == 1;
+    const int h = 32 * sp + lane;              // head of the group = TMEM lane
+    const int r = h & (kOwnHeads - 1);         // row of the head among its owner's 64
+    const int gw = sp & 1;                     // sub-partition within its role
     const uint32_t t_lane = tmem + (uint32_t(32 * sp) << 16);
-    const uint32_t sw = uint32_t(h & 7);     // 16-byte chunk swizzle of the score rows
-    const uint32_t row_off = uint32_t(h) * (kPage * 4);
-    const uint32_t x_own = ptx::smem_addr(xbuf) + row_off;
-    const uint32_t s_own = ptx::smem_addr(stg_out) + row_off;
-    const uint32_t blk = uint32_t(32 * sp) * (kPage * 4);   // this warp's 32 rows
-    const uint32_t x_peer_blk = ptx::mapa_shared(ptx::smem_addr(xbuf) + blk, rank ^ 1);
-    const uint32_t xfull_peer = ptx::mapa_shared(ptx::smem_addr(x_full), rank ^ 1);
-    const uint32_t xfree_peer = ptx::mapa_shared(ptx::smem_addr(x_free), rank ^ 1);
+    const uint32_t swz = uint32_t(h & 7);
+    const uint32_t row_off = uint32_t(r) * (kPage * 4);          // score rows: 256 B
+    const uint32_t wblk_off = uint32_t(32 * gw) * (kPage * 4);   // a sub-partition's 32 rows
+    const uint32_t xs_s = ptx::smem_addr(xs);
+    const uint32_t prow_off = uint32_t(r) * (kPage * 2);         // P rows: 128 B
+    const uint32_t pair_bar = 2 + sp;          // named barrier of a sub-partition's two warps
+    const bool owner_lead = owner && gw == 0 && pos == 0 && lane == 0;
+    const bool recv_lead = receiver && gw == 0 && lane == 0;
     const T* qg = static_cast<const T*>(p.q);
     T* outg = static_cast<T*>(p.out);
     bool aborted = false;
-    float sown[kPage];   // this CTA's partial scores of the page being exchanged
 
-    // q_r of this head for the piece into tensor memory: latent dims [256r, 256r+256)
-    // in columns [0, 128), rope dims [512+32r, 512+32r+32) in [128, 144).
-    auto load_q = [&](const Portion& pq) {
+    auto remote = [&](const void* local) __attribute__((always_inline)) -> uint32_t {
+      return ptx::mapa_shared(ptx::smem_addr(local), peer);
+    };
+    // q_r rows of this warp's heads into tensor memory (latent dims in columns [0, 128),
+    // rope dims in [128, 144)); the two owner warps of a sub-partition split the chunks
+    auto load_q = [&](const Portion& pq) __attribute__((always_inline)) {
       const T* qrow = qg + (int64_t(pq.b) * p.num_q_heads + int64_t(pq.seg) * kHeads + h) * kDqk;
+      const int c_lo = owner ? (pos == 0 ? 0 : 5) : 0;
+      const int c_hi = owner ? (pos == 0 ? 5 : 9) : 9;
 #pragma unroll
       for (int c0 = 0; c0 < 9; c0 += 3) {
         uint4 v[12];
@@ -374,13 +427,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 3; ++k) {
           const int c = c0 + k;
           const T* src = c < 8 ? qrow + int(rank) * kHalfDv + 32 * c : qrow + kDv + int(rank) * kRopeHalf;
+          if (c >= c_lo && c < c_hi) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) v[4 * k + e] = __ldg(reinterpret_cast<const uint4*>(src) + e);
+            for (int e = 0; e < 4; ++e) v[4 * k + e] = __ldg(reinterpret_cast<const uint4*>(src) + e);
+          }
         }
-        if (!aborted) {
 #pragma unroll
-          for (int k = 0; k < 3; ++k)
-            ptx::tmem_st16(t_lane + kColQ + 16 * (c0 + k), *reinterpret_cast<float(*)[16]>(v + 4 * k));
+        for (int k = 0; k < 3; ++k) {
+          const int c = c0 + k;
+          if (!aborted && c >= c_lo && c < c_hi)
+            ptx::tmem_st16(t_lane + kColQ + 16 * c, *reinterpret_cast<float(*)[16]>(v + 4 * k));
         }
       }
       ptx::tmem_st_wait();
@@ -388,203 +444,73 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(q_full);
     };
-
-    // Own partial scores of page tt from TMEM into the staging rows, then one bulk
-    // copy per warp into the peer's buffer once the peer has read the previous page's.
-    auto fetch_send = [&](int tt) {
+    // NC partial scores of page tt from column col0 of S; releases the S columns
+    auto read_s = [&](int tt, int col0, auto& v) __attribute__((always_inline)) {
+      constexpr int NC = sizeof(v) / sizeof(float);
       if (!aborted && !bounded_wait(s_full, tt & 1, flags, p.err)) aborted = true;
       aborted = __any_sync(kFullMask, aborted);
       ptx::tc_fence_after();
       if (!aborted) {
 #pragma unroll
-        for (int c = 0; c < kPage; c += 16)
-          ptx::tmem_ld16(t_lane + kColS + c, *reinterpret_cast<float(*)[16]>(sown + c));
+        for (int c = 0; c < NC; c += 16)
+          ptx::tmem_ld16(t_lane + kColS + col0 + c, *reinterpret_cast<float(*)[16]>(&v[c]));
         ptx::tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int j = 0; j < NC; ++j) v[j] = 0.f;
       }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(s_free);
-      if (!aborted && !bounded_wait_cluster(x_free, (tt & 1) ^ 1, flags, p.err)) aborted = true;
-      if (lane == 0) ptx::bulk_wait_read_all();   // the staging rows are free again
-      __syncwarp();
-#pragma unroll
-      for (int j = 0; j < kPage / 4; ++j)
-        ptx::st_shared_v4(s_own + ((uint32_t(j) ^ sw) << 4), sown[4 * j], sown[4 * j + 1],
-                          sown[4 * j + 2], sown[4 * j + 3]);
-      ptx::fence_proxy_async_shared();
-      __syncwarp();
-      if (lane == 0 && !aborted) {
-        ptx::bulk_copy_to_peer(x_peer_blk, ptx::smem_addr(stg_out) + blk, 32 * kPage * 4, xfull_peer);
-        ptx::bulk_commit();
-      }
     };
-
-    int t = 0;           // page index within this CTA's range
-    // running maximum (log2 units), the sum of the fp32 weights (for the LSE) and the sum
-    // of the 16-bit weights the PV MMA multiplies V by (O is normalised by this one, so
-    // the output is a convex combination of V rows whatever the rounding of P)
-    float m = 0.f, l = 0.f, lq = 0.f;
-    Portion cur = walker_next(walk, spec, g_hi);
-    load_q(cur);
-    fetch_send(0);
-    while (true) {
-      const bool have_next = walk.g < g_hi;
-      Portion nxt = cur;
-      if (have_next) nxt = walker_next(walk, spec, g_hi);
-      const int npg = cur.p1 - cur.p0;
-      const int ctx = __ldg(p.context_lens + cur.b);
-
-      for (int i = 0; i < npg; ++i, ++t) {
-        // ---- the peer's partial scores of page t: S = S_own + S_peer
-        float s[kPage];
-        if (!aborted && !bounded_wait_cluster(x_full, t & 1, flags, p.err)) aborted = true;
-        if (ctid == 0 && !aborted) ptx::mbar_arrive_expect_tx(x_full, kXBytes);  // next page
-#pragma unroll
-        for (int j = 0; j < kPage / 4; ++j) {
-          const float4 v = aborted ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                   : ptx::ld_shared_v4(x_own + ((uint32_t(j) ^ sw) << 4));
-          s[4 * j] = sown[4 * j] + v.x;
-          s[4 * j + 1] = sown[4 * j + 1] + v.y;
-          s[4 * j + 2] = sown[4 * j + 2] + v.z;
-          s[4 * j + 3] = sown[4 * j + 3] + v.w;
-        }
-        __syncwarp();
-        if (lane == 0 && !aborted) ptx::mbar_arrive_remote(xfree_peer);
-
-        // ---- send the next page's partial scores before this page's softmax when its
-        // scores are ready (same piece), so the exchange overlaps the exponentials
-        const bool last = (i + 1 == npg);
-        const bool more = !last || have_next;
-        bool sent = false;
-        if (!last) {
-          int rdy = (lane == 0) ? int(ptx::mbar_try_wait(s_full, (t + 1) & 1)) : 0;
-          if (__shfl_sync(kFullMask, rdy, 0)) {
-            fetch_send(t + 1);
-            sent = true;
-          }
-        }
-
-        // ---- online softmax of page t (one head per thread)
-        const int nvalid = min(kPage, ctx - (cur.p0 + i) * kPage);
-        if (nvalid < kPage) {
-#pragma unroll
-          for (int j = 0; j < kPage; ++j)
-            if (j >= nvalid) s[j] = -INFINITY;
-        }
-        float smax = s[0];
-#pragma unroll
-        for (int j = 1; j < kPage; ++j) smax = fmaxf(smax, s[j]);
-        const float mx = smax * p.scale_log2;
-        float alpha = 1.f;
-        bool rescale = false;
-        if (i == 0) {
-          m = mx;
-          l = 0.f;
-          lq = 0.f;
-        } else {
-          // lazy maximum: raised only when a score exceeds the one in use by 2^8
-          const bool need = mx > m + kRescaleLog2;
-          rescale = __any_sync(kFullMask, need);
-          if (need) {
-            alpha = ptx::exp2_approx(m - mx);
-            l *= alpha;
-            lq *= alpha;
-            m = mx;
-          }
-        }
-        float pk[kPage / 2];   // P as 16-bit pairs (bit patterns)
-        float lsum = 0.f, lqsum = 0.f;
-#pragma unroll
-        for (int j = 0; j < kPage / 2; ++j) {
-          const float p0 = ptx::exp2_approx(fmaf(s[2 * j], p.scale_log2, -m));
-          const float p1 = ptx::exp2_approx(fmaf(s[2 * j + 1], p.scale_log2, -m));
-          const uint32_t w = pack2<T>(p0, p1);
-          lsum += p0 + p1;
-          lqsum += sum2<T>(w);
-          pk[j] = __uint_as_float(w);
-        }
-        l += lsum;
-        lq += lqsum;
-        // P and O were last used by the PV of page t-1
-        if (t >= 1 && !aborted && !bounded_wait(pv_done, (t - 1) & 1, flags, p.err)) aborted = true;
-        aborted = __any_sync(kFullMask, aborted);
-        ptx::tc_fence_after();
-        if (!aborted) {
-          if (rescale) {
-            // O holds the piece's pages up to t-1: rescale this head's row
-#pragma unroll 4
-            for (int c = 0; c < kHalfDv; c += 16) {
-              float v[16];
-              ptx::tmem_ld16(t_lane + kColO + c, v);
-              ptx::tmem_ld_wait();
-#pragma unroll
-              for (int e = 0; e < 16; ++e) v[e] *= alpha;
-              ptx::tmem_st16(t_lane + kColO + c, v);
-            }
-          }
-          ptx::tmem_st16(t_lane + kColP, *reinterpret_cast<float(*)[16]>(pk));
-          ptx::tmem_st16(t_lane + kColP + 16, *reinterpret_cast<float(*)[16]>(pk + 16));
-          ptx::tmem_st_wait();
-        }
-        // Slots past ctx: P is 0 there, but 0 * (whatever the slot holds, NaN included)
-        // must not reach O, so their V rows are cleared before the PV MMA (the score MMA
-        // has consumed the page). Thread ctid clears token ctid % 64 in two sub-tiles.
-        if (nvalid < kPage) {
-          const int r = ctid & (kPage - 1);
-          if (r >= nvalid) {
-            uint8_t* stg = kv + (t % kStages) * kStageBytes;
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              uint4* dst =
-                  reinterpret_cast<uint4*>(stg + ((ctid >> 6) * 2 + k) * kLatSubBytes + r * 128);
-#pragma unroll
-              for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
-            }
-          }
-          ptx::fence_proxy_async_shared();
-        }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(p_full);
-
-        if (more && !sent) {
-          if (last) load_q(nxt);   // the score MMA of page t (the piece's last) is done
-          fetch_send(t + 1);
-        }
-      }
-
-      // ---- end of the piece: O_r / lq for this head
-      const int tl = t - 1;
-      if (!aborted && !bounded_wait(pv_done, tl & 1, flags, p.err)) aborted = true;
+    // rescale columns [c0, c0 + n) of this head's row of O_r once the PV of page tt-1 is done
+    auto rescale_row = [&](int tt, float alpha, int c0, int n) __attribute__((always_inline)) {
+      if (!aborted && !bounded_wait(&pv_done[(tt - 1) & 1], ((tt - 1) >> 1) & 1, flags, p.err))
+        aborted = true;
       aborted = __any_sync(kFullMask, aborted);
       ptx::tc_fence_after();
-
-      const bool whole = (cur.p0 == 0 && cur.p1 == cur.np);
-      const int slot = piece_slot(cur.seg_start, g_lo);
-      const int64_t head_row = int64_t(cur.b) * p.num_q_heads + int64_t(cur.seg) * kHeads + h;
-      const int64_t slot_row = (pair * 2 + slot) * kHeads + h;
-      const float inv = 1.f / lq;
-#pragma unroll 4
-      for (int c = 0; c < kHalfDv; c += 16) {
-        float v[16];
-        if (!aborted) {
+      if (!aborted) {
+#pragma unroll 1
+        for (int c = c0; c < c0 + n; c += 16) {
+          float v[16];
           ptx::tmem_ld16(t_lane + kColO + c, v);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] *= alpha;
+          ptx::tmem_st16(t_lane + kColO + c, v);
+        }
+        ptx::tmem_st_wait();
+      }
+    };
+    // normalise columns [c0, c0 + n) of this head's row of O_r by 1/lq and write them out
+    auto write_out = [&](const Portion& pc, float lq_tot, float lse_nat, int c0, int n,
+                         bool write_lse) __attribute__((always_inline)) {
+      const bool whole = (pc.p0 == 0 && pc.p1 == pc.np);
+      const int slot = piece_slot(pc.seg_start, g_lo);
+      const int64_t head_row = int64_t(pc.b) * p.num_q_heads + int64_t(pc.seg) * kHeads + h;
+      const int64_t slot_row = (pair * 2 + slot) * kHeads + h;
+      const float inv = 1.f / lq_tot;
+#pragma unroll 2
+      for (int c = c0; c < c0 + n; c += 16) {
+        float o16[16];
+        if (!aborted) {
+          ptx::tmem_ld16(t_lane + kColO + c, o16);
           ptx::tmem_ld_wait();
         } else {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] = 0.f;
+          for (int e = 0; e < 16; ++e) o16[e] = 0.f;
         }
         const int d = int(rank) * kHalfDv + c;
         if (whole) {
           uint4 w0, w1;
-          w0.x = pack2<T>(v[0] * inv, v[1] * inv);
-          w0.y = pack2<T>(v[2] * inv, v[3] * inv);
-          w0.z = pack2<T>(v[4] * inv, v[5] * inv);
-          w0.w = pack2<T>(v[6] * inv, v[7] * inv);
-          w1.x = pack2<T>(v[8] * inv, v[9] * inv);
-          w1.y = pack2<T>(v[10] * inv, v[11] * inv);
-          w1.z = pack2<T>(v[12] * inv, v[13] * inv);
-          w1.w = pack2<T>(v[14] * inv, v[15] * inv);
+          w0.x = pack2<T>(o16[0] * inv, o16[1] * inv);
+          w0.y = pack2<T>(o16[2] * inv, o16[3] * inv);
+          w0.z = pack2<T>(o16[4] * inv, o16[5] * inv);
+          w0.w = pack2<T>(o16[6] * inv, o16[7] * inv);
+          w1.x = pack2<T>(o16[8] * inv, o16[9] * inv);
+          w1.y = pack2<T>(o16[10] * inv, o16[11] * inv);
+          w1.z = pack2<T>(o16[12] * inv, o16[13] * inv);
+          w1.w = pack2<T>(o16[14] * inv, o16[15] * inv);
           uint4* o = reinterpret_cast<uint4*>(outg + head_row * kDv + d);
           o[0] = w0;
           o[1] = w1;
@@ -592,50 +518,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           float4* o = reinterpret_cast<float4*>(p.part_out + slot_row * kDv + d);
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            __stcg(o + e, make_float4(v[4 * e] * inv, v[4 * e + 1] * inv, v[4 * e + 2] * inv,
-                                      v[4 * e + 3] * inv));
+            __stcg(o + e, make_float4(o16[4 * e] * inv, o16[4 * e + 1] * inv, o16[4 * e + 2] * inv,
+                                      o16[4 * e + 3] * inv));
         }
       }
-      const float lse_nat = (m + log2f(l)) * kLn2;
-      if (whole) {
-        if (rank == 0 && p.lse != nullptr) p.lse[head_row] = lse_nat;
-      } else {
-        // both CTAs of the pair store this same value, so each half's merge finds it
-        // once its own counter says every piece has arrived
-        __stcg(p.part_lse + slot_row, lse_nat);
+      if (write_lse) {
+        if (whole) {
+          if (owner && p.lse != nullptr) p.lse[head_row] = lse_nat;
+        } else {
+          // each CTA stores the LSE of all 128 heads (its owners' values and the peer's,
+          // received at the end of the piece), so each half's merge finds them once its own
+          // counter says every piece has arrived
+          __stcg(p.part_lse + slot_row, lse_nat);
+        }
       }
-      ptx::tc_fence_before();
-
+    };
+    // the merge of a split segment's pieces by the last to arrive (this CTA's output half),
+    // or nothing when the segment is whole or heavily split (the merge kernel's work);
+    // run by the owners and receivers (kMergeThreads, dense index mtid), never the senders
+    auto merge_tail = [&](const Portion& pc) __attribute__((always_inline)) {
+      const bool whole = (pc.p0 == 0 && pc.p1 == pc.np);
+      const int mtid = (owner ? gw * 2 + pos : 4 + gw) * 32 + lane;
       if (!whole) {
-        // few pieces: the last to arrive merges its output half here; many: the
-        // split-merge kernel that follows
-        const int64_t c0 = cur.seg_start / p.tiles_per_cta;
-        const int64_t c1 = (cur.seg_start + cur.np - 1) / p.tiles_per_cta;
+        const int64_t c0 = pc.seg_start / p.tiles_per_cta;
+        const int64_t c1 = (pc.seg_start + pc.np - 1) / p.tiles_per_cta;
         const int pieces = int(c1 - c0 + 1);
         if (pieces <= p.heavy_min) {
           __threadfence();
-          ptx::named_barrier_sync(1, 32 * kSoftmaxWarps);
-          int32_t* counter = p.counters + (int64_t(cur.b) * p.groups + cur.seg) * 2 + rank;
-          if (ctid == 0) {
+          ptx::named_barrier_sync(1, kMergeThreads);
+          int32_t* counter = p.counters + (int64_t(pc.b) * p.groups + pc.seg) * 2 + rank;
+          if (mtid == 0) {
             const int prev = aborted ? -1 : atomicAdd(counter, 1);
             flags[1] = (prev == pieces - 1) ? 1 : 0;
           }
-          ptx::named_barrier_sync(1, 32 * kSoftmaxWarps);
+          ptx::named_barrier_sync(1, kMergeThreads);
           if (flags[1]) {
             __threadfence();
-            const int64_t head0 = int64_t(cur.b) * p.num_q_heads + int64_t(cur.seg) * kHeads;
-            for (int idx = ctid; idx < kHeads * (kHalfDv / 4); idx += 32 * kSoftmaxWarps) {
+            const int64_t head0 = int64_t(pc.b) * p.num_q_heads + int64_t(pc.seg) * kHeads;
+            for (int idx = mtid; idx < kHeads * (kHalfDv / 4); idx += kMergeThreads) {
               const int j = idx / (kHalfDv / 4);
               const int dq = idx - j * (kHalfDv / 4);
               float mxl = -INFINITY;
               for (int64_t c = c0; c <= c1; ++c) {
-                const int sl = (c == c0 && cur.seg_start > c * p.tiles_per_cta) ? 1 : 0;
+                const int sl = (c == c0 && pc.seg_start > c * p.tiles_per_cta) ? 1 : 0;
                 mxl = fmaxf(mxl, __ldcg(p.part_lse + (c * 2 + sl) * kHeads + j));
               }
               float den = 0.f;
               float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
               for (int64_t c = c0; c <= c1; ++c) {
-                const int sl = (c == c0 && cur.seg_start > c * p.tiles_per_cta) ? 1 : 0;
+                const int sl = (c == c0 && pc.seg_start > c * p.tiles_per_cta) ? 1 : 0;
                 const int64_t rowi = (c * 2 + sl) * kHeads + j;
                 const float wgt = ptx::exp2_approx((__ldcg(p.part_lse + rowi) - mxl) * kLog2e);
                 const float4 o = __ldcg(reinterpret_cast<const float4*>(
@@ -653,15 +584,279 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               *reinterpret_cast<uint2*>(outg + (head0 + j) * kDv + int(rank) * kHalfDv + dq * 4) = w;
               if (rank == 0 && dq == 0 && p.lse != nullptr) p.lse[head0 + j] = mxl + logf(den);
             }
-            if (ctid == 0) atomicExch(counter, 0);
+            if (mtid == 0) atomicExch(counter, 0);
           }
         }
       }
-      ptx::named_barrier_sync(1, 32 * kSoftmaxWarps);
-      if (!have_next) break;
-      cur = nxt;
+      ptx::named_barrier_sync(1, kMergeThreads);
+    };
+
+    int t = 0;           // page index within this CTA's range
+    int u = 0;           // piece index within this CTA's range
+    Portion cur = walker_next(walk, spec, g_hi);
+    if (!receiver) load_q(cur);
+
+    if (sender) {
+      // ---- sender: this CTA's partial scores of the peer's heads, as soon as they exist
+      while (true) {
+        const int npg = cur.p1 - cur.p0;
+        for (int i = 0; i < npg; ++i, ++t) {
+          const int b2 = t & 1;
+          const uint32_t par2 = uint32_t(t >> 1) & 1;
+          float v[kPage];
+          read_s(t, 0, v);
+          if (lane == 0) ptx::bulk_wait_read_all();   // the staging rows were copied out
+          __syncwarp();
+          const uint32_t srow = ptx::smem_addr(sstg) + row_off;
+#pragma unroll
+          for (int j = 0; j < kPage / 4; ++j)
+            ptx::st_shared_v4(srow + ((uint32_t(j) ^ swz) << 4), v[4 * j], v[4 * j + 1],
+                              v[4 * j + 2], v[4 * j + 3]);
+          ptx::fence_proxy_async_shared();
+          __syncwarp();
+          int ok = 1;
+          if (lane == 0 && !aborted) {
+            if (bounded_wait_cluster(&xs_free[b2], par2 ^ 1, flags, p.err)) {
+              ptx::bulk_copy_to_peer(remote(xs + b2 * kXsBytes + wblk_off),
+                                     ptx::smem_addr(sstg) + wblk_off, 32 * kPage * 4,
+                                     remote(&xs_full[b2]));
+              ptx::bulk_commit();
+            } else {
+              ok = 0;
+            }
+          }
+          if (!__shfl_sync(kFullMask, ok, 0)) aborted = true;
+        }
+        if (walk.g >= g_hi) break;
+        cur = walker_next(walk, spec, g_hi);
+        load_q(cur);   // this piece's last score MMA is done (read_s saw it)
+      }
+      if (lane == 0) ptx::bulk_wait_all();
+    } else if (receiver) {
+      // ---- receiver: the peer's P rows and factors for its heads; rescale their rows of O_r
+      while (true) {
+        const int npg = cur.p1 - cur.p0;
+        for (int i = 0; i < npg; ++i, ++t) {
+          const int b2 = t & 1;
+          const uint32_t par2 = uint32_t(t >> 1) & 1;
+          if (!aborted && !bounded_wait_cluster(&pr_full[b2], par2, flags, p.err)) aborted = true;
+          const float alpha = aborted ? 1.f : alpha_in[b2 * kOwnHeads + r];
+          uint32_t pr[kPage / 2];   // the peer's P row of this head
+          const uint32_t pin_row = ptx::smem_addr(pin) + b2 * kPRowsBytes + prow_off;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (!aborted) {
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(pr[4 * j]), "=r"(pr[4 * j + 1]), "=r"(pr[4 * j + 2]), "=r"(pr[4 * j + 3])
+                           : "r"(pin_row + ((uint32_t(j) ^ swz) << 4))
+                           : "memory");
+            } else {
+              pr[4 * j] = pr[4 * j + 1] = pr[4 * j + 2] = pr[4 * j + 3] = 0u;
+            }
+          }
+          __syncwarp();
+          if (lane == 0 && !aborted) ptx::mbar_arrive_remote(remote(&pr_free[b2]));
+          if (recv_lead && !aborted) ptx::mbar_arrive_expect_tx(&pr_full[b2], kPMsgBytes);  // page t+2
+          // P and O were last used by the PV of page t-1
+          if (t >= 1 && !aborted &&
+              !bounded_wait(&pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, flags, p.err))
+            aborted = true;
+          if (__any_sync(kFullMask, alpha != 1.f)) rescale_row(t, alpha, 0, kHalfDv);
+          aborted = __any_sync(kFullMask, aborted);
+          ptx::tc_fence_after();
+          if (!aborted) {
+            ptx::tmem_st16(t_lane + kColP, *reinterpret_cast<float(*)[16]>(pr));
+            ptx::tmem_st16(t_lane + kColP + 16, *reinterpret_cast<float(*)[16]>(pr + 16));
+            ptx::tmem_st_wait();
+          }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&p_full[b2]);
+        }
+        // end of the piece: the owner's (m, l, lq) of this head, then the output
+        if (!aborted && !bounded_wait_cluster(fin_full, u & 1, flags, p.err)) aborted = true;
+        const float4 f = aborted ? make_float4(0.f, 1.f, 1.f, 0.f) : fin_in[r];
+        __syncwarp();
+        if (lane == 0 && !aborted) ptx::mbar_arrive_remote(remote(fin_free));
+        if (recv_lead && !aborted) ptx::mbar_arrive_expect_tx(fin_full, kFinBytes);  // next piece
+        const int tl = t - 1;
+        if (!aborted && !bounded_wait(&pv_done[tl & 1], (tl >> 1) & 1, flags, p.err)) aborted = true;
+        aborted = __any_sync(kFullMask, aborted);
+        ptx::tc_fence_after();
+        write_out(cur, f.z, (f.x + log2f(f.y)) * kLn2, 0, kHalfDv, true);
+        ptx::tc_fence_before();
+        merge_tail(cur);
+        ++u;
+        if (walk.g >= g_hi) break;
+        cur = walker_next(walk, spec, g_hi);
+      }
+    } else {
+      // ---- owner (token half `pos`): S = S_own + S_peer, online softmax, P row half out
+      // [2 halves][64 rows] half maxima of the page in hand; at the end of a piece the same
+      // words hold [2 halves][2 sums][64 rows] (the pair barriers order the reuse)
+      float* hmx = red;
+      float* hsm = red;
+      const int o = (gw * 2 + pos) * 32 + lane;   // 0 .. 127 over the owner warps
+      // running maximum (log2 units), this half's sums of the fp32 weights (for the LSE)
+      // and of the 16-bit weights the PV MMA multiplies V by (O is normalised by the
+      // latter, so the output is a convex combination of V rows whatever the rounding of P)
+      float m = 0.f, l = 0.f, lq = 0.f;
+      while (true) {
+        const int npg = cur.p1 - cur.p0;
+        const int ctx = __ldg(p.context_lens + cur.b);
+        for (int i = 0; i < npg; ++i, ++t) {
+          const int b2 = t & 1;
+          const uint32_t par2 = uint32_t(t >> 1) & 1;
+          const int nvalid = min(kPage, ctx - (cur.p0 + i) * kPage);
+          float v[kHalfTok];
+          read_s(t, kHalfTok * pos, v);
+          if (!aborted && !bounded_wait_cluster(&xs_full[b2], par2, flags, p.err)) aborted = true;
+          if (owner_lead && !aborted) ptx::mbar_arrive_expect_tx(&xs_full[b2], kXsBytes);  // page t+2
+          const uint32_t xr = xs_s + b2 * kXsBytes + row_off;
+#pragma unroll
+          for (int j = 0; j < kHalfTok / 4; ++j) {
+            const float4 x = aborted ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                     : ptx::ld_shared_v4(xr + ((uint32_t(8 * pos + j) ^ swz) << 4));
+            v[4 * j] += x.x;
+            v[4 * j + 1] += x.y;
+            v[4 * j + 2] += x.z;
+            v[4 * j + 3] += x.w;
+          }
+          __syncwarp();
+          if (lane == 0 && !aborted) ptx::mbar_arrive_remote(remote(&xs_free[b2]));
+          const int nv = nvalid - kHalfTok * pos;   // valid tokens of this half
+          if (nv < kHalfTok) {
+#pragma unroll
+            for (int j = 0; j < kHalfTok; ++j)
+              if (j >= nv) v[j] = -INFINITY;
+          }
+          float smax = v[0];
+#pragma unroll
+          for (int j = 1; j < kHalfTok; ++j) smax = fmaxf(smax, v[j]);
+          // the head's maximum over both halves (the two warps agree on every decision)
+          hmx[pos * kOwnHeads + r] = smax;
+          ptx::named_barrier_sync(pair_bar, 64);
+          const float mx = fmaxf(hmx[r], hmx[kOwnHeads + r]) * p.scale_log2;
+          float alpha = 1.f;
+          bool need = false;
+          if (i == 0) {
+            m = mx;
+            l = 0.f;
+            lq = 0.f;
+          } else if (mx > m + kRescaleLog2) {
+            // lazy maximum: raised only when a score exceeds the one in use by 2^8
+            need = true;
+            alpha = ptx::exp2_approx(m - mx);
+            l *= alpha;
+            lq *= alpha;
+            m = mx;
+          }
+          uint32_t pk[kHalfTok / 2];   // P as 16-bit pairs
+          float lsum = 0.f, lqsum = 0.f;
+#pragma unroll
+          for (int j = 0; j < kHalfTok / 2; ++j) {
+            const float p0 = ptx::exp2_approx(fmaf(v[2 * j], p.scale_log2, -m));
+            const float p1 = ptx::exp2_approx(fmaf(v[2 * j + 1], p.scale_log2, -m));
+            pk[j] = pack2<T>(p0, p1);
+            lsum += p0 + p1;
+            lqsum += sum2<T>(pk[j]);
+          }
+          l += lsum;
+          lq += lqsum;
+          // P and O were last used by the PV of page t-1
+          if (t >= 1 && !aborted &&
+              !bounded_wait(&pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, flags, p.err))
+            aborted = true;
+          if (__any_sync(kFullMask, need)) rescale_row(t, alpha, (kHalfDv / 2) * pos, kHalfDv / 2);
+          aborted = __any_sync(kFullMask, aborted);
+          ptx::tc_fence_after();
+          if (!aborted) {
+            ptx::tmem_st16(t_lane + kColP + 16 * pos, *reinterpret_cast<float(*)[16]>(pk));
+            ptx::tmem_st_wait();
+          }
+          // the same P row half to the outgoing rows (their previous copy has been read)
+          if (pos == 0 && lane == 0) ptx::bulk_wait_read_all();
+          ptx::named_barrier_sync(pair_bar, 64);
+          const uint32_t prow = ptx::smem_addr(pout) + prow_off;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             prow + ((uint32_t(4 * pos + j) ^ swz) << 4)),
+                         "r"(pk[4 * j]), "r"(pk[4 * j + 1]), "r"(pk[4 * j + 2]), "r"(pk[4 * j + 3])
+                         : "memory");
+          }
+          // Slots past ctx: P is 0 there, but 0 * (whatever the slot holds, NaN included)
+          // must not reach O, so their V rows are cleared before the PV MMA (the score MMA
+          // has consumed the page). Owner thread o clears token o % 64 in two sub-tiles.
+          if (nvalid < kPage && (o & (kPage - 1)) >= nvalid) {
+            uint8_t* stg = kv + (t % kStages) * kStageBytes + (o & (kPage - 1)) * 128;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              uint4* dst = reinterpret_cast<uint4*>(stg + ((o >> 6) * 2 + k) * kLatSubBytes);
+#pragma unroll
+              for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+          ptx::fence_proxy_async_shared();
+          ptx::named_barrier_sync(pair_bar, 64);
+          // to the peer, once its receivers have read page t-2's: the factors and the P rows
+          if (pos == 0) {
+            int ok = 1;
+            if (lane == 0 && !aborted &&
+                !bounded_wait_cluster(&pr_free[b2], par2 ^ 1, flags, p.err))
+              ok = 0;
+            if (!__shfl_sync(kFullMask, ok, 0)) aborted = true;
+            const uint32_t pr_peer = remote(&pr_full[b2]);
+            if (!aborted)
+              ptx::st_async_b32(remote(alpha_in + b2 * kOwnHeads + r), __float_as_uint(alpha), pr_peer);
+            __syncwarp();
+            if (lane == 0 && !aborted) {
+              const uint32_t blk = uint32_t(32 * gw) * (kPage * 2);
+              ptx::bulk_copy_to_peer(remote(pin + b2 * kPRowsBytes + blk), ptx::smem_addr(pout) + blk,
+                                     32 * kPage * 2, pr_peer);
+              ptx::bulk_commit();
+            }
+          }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&p_full[b2]);
+        }
+        // ---- the next piece's q once this piece's last score MMA is done (read_s saw it)
+        const bool have_next = walk.g < g_hi;
+        Portion nxt = cur;
+        if (have_next) {
+          nxt = walker_next(walk, spec, g_hi);
+          load_q(nxt);
+        }
+        // ---- end of the piece: both halves' sums, (m, l, lq) to the peer, then O_r / lq
+        hsm[(pos * 2) * kOwnHeads + r] = l;
+        hsm[(pos * 2 + 1) * kOwnHeads + r] = lq;
+        ptx::named_barrier_sync(pair_bar, 64);
+        const float l_tot = hsm[r] + hsm[2 * kOwnHeads + r];
+        const float lq_tot = hsm[kOwnHeads + r] + hsm[3 * kOwnHeads + r];
+        ptx::named_barrier_sync(pair_bar, 64);
+        if (pos == 0) {
+          int ok = 1;
+          if (lane == 0 && !aborted && !bounded_wait_cluster(fin_free, (u & 1) ^ 1, flags, p.err))
+            ok = 0;
+          if (!__shfl_sync(kFullMask, ok, 0)) aborted = true;
+          if (!aborted)
+            ptx::st_async_v4(remote(fin_in + r), __float_as_uint(m), __float_as_uint(l_tot),
+                             __float_as_uint(lq_tot), 0u, remote(fin_full));
+        }
+        const int tl = t - 1;
+        if (!aborted && !bounded_wait(&pv_done[tl & 1], (tl >> 1) & 1, flags, p.err)) aborted = true;
+        aborted = __any_sync(kFullMask, aborted);
+        ptx::tc_fence_after();
+        write_out(cur, lq_tot, (m + log2f(l_tot)) * kLn2, (kHalfDv / 2) * pos, kHalfDv / 2, pos == 0);
+        ptx::tc_fence_before();
+        merge_tail(cur);
+        ++u;
+        if (!have_next) break;
+        cur = nxt;
+      }
+      if (lane == 0) ptx::bulk_wait_all();   // the last copies into the peer have landed
     }
-    if (lane == 0) ptx::bulk_wait_all();   // the last copy into the peer has landed
   }
 
   // ---- teardown: no access to this CTA's shared memory from the peer after the

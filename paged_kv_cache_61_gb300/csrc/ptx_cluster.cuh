@@ -125,6 +125,23 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Arrive once on the mbarrier at shared-memory offset `bar` of every CTA in `cta_mask`
+// when all tcgen05 operations issued so far by this thread complete.
+__device__ __forceinline__ void umma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// 4 bytes into a peer CTA's shared memory, counted on the peer's mbarrier (cluster addresses).
+__device__ __forceinline__ void st_async_b32(uint32_t raddr, uint32_t v, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(raddr),
+               "r"(v), "r"(rbar)
+               : "memory");
+}
+
 // 2-D tiled load global -> shared; completion is signalled on `bar` as transaction bytes.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int32_t c0, int32_t c1, uint64_t cache_policy) {
