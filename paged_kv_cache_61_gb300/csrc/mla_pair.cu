@@ -54,12 +54,13 @@ constexpr int kOwnHeads = kHeads / 2;       // heads whose softmax a CTA runs
 constexpr int kHalfDv = kDv / 2;            // output / latent dims per CTA
 constexpr int kLatSubs = kHalfDv / 64;      // 128-byte-swizzled 64-dim sub-tiles per CTA
 constexpr int kRopeHalf = 32;               // rope dims per CTA (64-byte swizzle)
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kLatSubBytes = kPage * 128;                          // [64 tokens][64 dims]
 constexpr int kRopeBytes = kPage * kRopeHalf * 2;                  // [64 tokens][32 dims]
 constexpr int kStageBytes = kLatSubs * kLatSubBytes + kRopeBytes;  // 36 KB
 constexpr int kXsBytes = kOwnHeads * kPage * 4;                    // 64 heads' fp32 scores
-constexpr int kPRowsBytes = kOwnHeads * kPage * 2;                 // 64 heads' P rows, 16-bit
+constexpr int kPBytes = kHeads * kPage * 2;                        // P tile, 16-bit
+constexpr int kPRowsBytes = kOwnHeads * kPage * 2;                 // 64 heads' P rows
 constexpr int kPMsgBytes = kPRowsBytes + kOwnHeads * 4;            // P rows + factors
 constexpr int kFinBytes = kOwnHeads * 16;                          // (m, l, lq, -) per head
 // Softmax group: two warps per tensor-memory sub-partition. On the owner sub-partitions
@@ -73,9 +74,8 @@ constexpr int kSWarps = 6;     // warps that read S (owners and senders)
 constexpr int kMergeThreads = 32 * 6;   // owners and receivers: the end-of-piece work
 constexpr int kThreads = 64 + 32 * kGroupWarps;
 constexpr int kTmemCols = 512;
-// tensor-memory columns (32-bit): q_r as 16-bit pairs, P as 16-bit pairs, S, O_r
+// tensor-memory columns (32-bit): q_r as 16-bit pairs, S, O_r
 constexpr int kColQ = 0;     // 144 columns: latent dims in [0, 128), rope dims in [128, 144)
-constexpr int kColP = 160;   // 32 columns
 constexpr int kColS = 192;   // 64 columns
 constexpr int kColO = 256;   // 256 columns
 constexpr float kLog2e = 1.4426950408889634f;
@@ -86,15 +86,15 @@ struct Layout {
   static constexpr int kKV = 0;
   static constexpr int kXs = kKV + kStages * kStageBytes;   // [2] the peer's partials, own heads
   static constexpr int kSstg = kXs + 2 * kXsBytes;          // own partials of the peer's heads
-  static constexpr int kPout = kSstg + kXsBytes;             // the owners' P rows, outgoing
-  static constexpr int kPin = kPout + kPRowsBytes;           // [2] the peer's P rows
-  static constexpr int kAlpha = kPin + 2 * kPRowsBytes;      // [2][64] the peer's factors
+  static constexpr int kP = kSstg + kXsBytes;                // [2] P tiles (both CTAs' rows)
+  static constexpr int kAlpha = kP + 2 * kPBytes;            // [2][64] the peer's factors
   static constexpr int kFin = kAlpha + 2 * kOwnHeads * 4;    // [64] the peer's (m, l, lq)
   static constexpr int kRed = kFin + kFinBytes;              // owner halves: maxima, sums
   static constexpr int kBar = kRed + 1024;
   static constexpr int kBarCount = 32;
   static constexpr int kSmem = 1024 + kBar + kBarCount * 8;
-  static_assert(kStageBytes % 1024 == 0 && kXs % 1024 == 0, "swizzled tiles stay 1024-byte aligned");
+  static_assert(kStageBytes % 1024 == 0 && kXs % 1024 == 0 && kP % 1024 == 0,
+                "swizzled tiles stay 1024-byte aligned");
   static_assert(kSmem <= 227 * 1024, "fits one SM's shared memory");
 };
 
@@ -166,23 +166,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* kv = base + Layout::kKV;
   uint8_t* xs = base + Layout::kXs;
   uint8_t* sstg = base + Layout::kSstg;
-  uint8_t* pout = base + Layout::kPout;
-  uint8_t* pin = base + Layout::kPin;
+  uint8_t* pbuf = base + Layout::kP;
   float* alpha_in = reinterpret_cast<float*>(base + Layout::kAlpha);
   float4* fin_in = reinterpret_cast<float4*>(base + Layout::kFin);
   float* red = reinterpret_cast<float*>(base + Layout::kRed);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + Layout::kBar);
-  uint64_t* kv_full = bars + 0;    // [4]
-  uint64_t* kv_empty = bars + 4;   // [4]
+  uint64_t* kv_full = bars + 0;    // [3] (4 slots kept)
+  uint64_t* kv_empty = bars + 4;   // [3]
   uint64_t* q_full = bars + 8;     // q of the current piece is in tensor memory
   uint64_t* s_full = bars + 9;     // S written by the score MMA
   uint64_t* s_free = bars + 10;    // S read by the four softmax-group warps
-  uint64_t* p_full = bars + 11;    // [2] P complete in tensor memory, O rows rescaled
+  uint64_t* p_full = bars + 11;    // [2] P tile complete, O rows rescaled
   uint64_t* pv_done = bars + 13;   // [2] PV of a page completed
   uint64_t* xs_full = bars + 15;   // [2] the peer's partial scores of this CTA's heads
   uint64_t* xs_free = bars + 17;   // [2] the peer's owners have read what this CTA sent
   uint64_t* pr_full = bars + 19;   // [2] the peer's P rows and factors have landed
-  uint64_t* pr_free = bars + 21;   // [2] the peer's receivers have read this CTA's P rows
+  uint64_t* pr_free = bars + 21;   // [2] the peer's PV of the page two back completed
   uint64_t* fin_full = bars + 23;  // the peer's (m, l, lq) of a piece have landed
   uint64_t* fin_free = bars + 24;  // the peer's relays have read this CTA's (m, l, lq)
   // [0] abort, [1] last piece to arrive
@@ -214,7 +213,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&xs_full[b], 1);
       ptx::mbar_init(&xs_free[b], 4);   // the peer's four owner warps
       ptx::mbar_init(&pr_full[b], 1);
-      ptx::mbar_init(&pr_free[b], 2);   // the peer's two receiver warps
+      ptx::mbar_init(&pr_free[b], 1);   // the peer's MMA commit
     }
     ptx::mbar_init(fin_full, 1);
     ptx::mbar_init(fin_free, 2);        // the peer's two receiver warps
@@ -296,6 +295,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     constexpr uint32_t kIdQK = ptx::umma_idesc_f16(128, 64, 0, 0, kBf16);
     constexpr uint32_t kIdPV = ptx::umma_idesc_f16(128, 256, 0, 1, kBf16);
     const uint32_t kv_s = ptx::smem_addr(kv);
+    const uint32_t p_s = ptx::smem_addr(pbuf);
     if (lane == 0) {
       int u = 0, i = 0, npg = 0;
       int t_qk = 0, t_pv = 0, st_qk = 0, st_pv = 0;
@@ -354,15 +354,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ptx::tc_fence_after();
           const bool first = (first_bits >> (t_pv & 31)) & 1u;
           const uint32_t stg = kv_s + st_pv * kStageBytes;
+          const uint32_t pt = p_s + (t_pv & 1) * kPBytes;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            // P: 128 heads x 16 tokens in tensor memory; V_r: 16 tokens x 256 dims (dims
-            // contiguous in four 64-dim sub-tiles)
+            // P: 128 heads x 16 tokens (K-major, 128-byte swizzle); V_r: 16 tokens x 256
+            // dims (dims contiguous in four 64-dim sub-tiles)
+            const uint64_t a = ptx::umma_desc_sw128(pt + ks * 32, 16, 1024);
             const uint64_t b = ptx::umma_desc_sw128(stg + ks * 2048, kLatSubBytes, 1024);
-            ptx::umma_f16_ts(tmem + kColO, tmem + kColP + ks * 8, b, kIdPV, !(first && ks == 0));
+            ptx::umma_f16(tmem + kColO, a, b, kIdPV, !(first && ks == 0));
           }
           ptx::umma_commit(&kv_empty[st_pv]);
           ptx::umma_commit(&pv_done[t_pv & 1]);
+          // the peer may now write its P rows of the page two ahead into this CTA's tile
+          ptx::umma_commit_multicast(&pr_free[t_pv & 1], uint16_t(1u << peer));
           ++t_pv;
           if (++st_pv == kStages) st_pv = 0;
           progress = true;
@@ -403,7 +407,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t row_off = uint32_t(r) * (kPage * 4);          // score rows: 256 B
     const uint32_t wblk_off = uint32_t(32 * gw) * (kPage * 4);   // a sub-partition's 32 rows
     const uint32_t xs_s = ptx::smem_addr(xs);
-    const uint32_t prow_off = uint32_t(r) * (kPage * 2);         // P rows: 128 B
+    const uint32_t p_s = ptx::smem_addr(pbuf);
     const uint32_t pair_bar = 2 + sp;          // named barrier of a sub-partition's two warps
     const bool owner_lead = owner && gw == 0 && pos == 0 && lane == 0;
     const bool recv_lead = receiver && gw == 0 && lane == 0;
@@ -641,34 +645,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t par2 = uint32_t(t >> 1) & 1;
           if (!aborted && !bounded_wait_cluster(&pr_full[b2], par2, flags, p.err)) aborted = true;
           const float alpha = aborted ? 1.f : alpha_in[b2 * kOwnHeads + r];
-          uint32_t pr[kPage / 2];   // the peer's P row of this head
-          const uint32_t pin_row = ptx::smem_addr(pin) + b2 * kPRowsBytes + prow_off;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (!aborted) {
-              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                           : "=r"(pr[4 * j]), "=r"(pr[4 * j + 1]), "=r"(pr[4 * j + 2]), "=r"(pr[4 * j + 3])
-                           : "r"(pin_row + ((uint32_t(j) ^ swz) << 4))
-                           : "memory");
-            } else {
-              pr[4 * j] = pr[4 * j + 1] = pr[4 * j + 2] = pr[4 * j + 3] = 0u;
-            }
-          }
           __syncwarp();
-          if (lane == 0 && !aborted) ptx::mbar_arrive_remote(remote(&pr_free[b2]));
           if (recv_lead && !aborted) ptx::mbar_arrive_expect_tx(&pr_full[b2], kPMsgBytes);  // page t+2
-          // P and O were last used by the PV of page t-1
-          if (t >= 1 && !aborted &&
-              !bounded_wait(&pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, flags, p.err))
-            aborted = true;
+          // the peer's P rows of page t are in this CTA's tile; rescale those heads' O rows
           if (__any_sync(kFullMask, alpha != 1.f)) rescale_row(t, alpha, 0, kHalfDv);
-          aborted = __any_sync(kFullMask, aborted);
-          ptx::tc_fence_after();
-          if (!aborted) {
-            ptx::tmem_st16(t_lane + kColP, *reinterpret_cast<float(*)[16]>(pr));
-            ptx::tmem_st16(t_lane + kColP + 16, *reinterpret_cast<float(*)[16]>(pr + 16));
-            ptx::tmem_st_wait();
-          }
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&p_full[b2]);
@@ -677,7 +657,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!aborted && !bounded_wait_cluster(fin_full, u & 1, flags, p.err)) aborted = true;
         const float4 f = aborted ? make_float4(0.f, 1.f, 1.f, 0.f) : fin_in[r];
         __syncwarp();
-        if (lane == 0 && !aborted) ptx::mbar_arrive_remote(remote(fin_free));
+        if (lane == 0 && !aborted) ptx::mbar_arrive_remote_relaxed(remote(fin_free));
         if (recv_lead && !aborted) ptx::mbar_arrive_expect_tx(fin_full, kFinBytes);  // next piece
         const int tl = t - 1;
         if (!aborted && !bounded_wait(&pv_done[tl & 1], (tl >> 1) & 1, flags, p.err)) aborted = true;
@@ -723,7 +703,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             v[4 * j + 3] += x.w;
           }
           __syncwarp();
-          if (lane == 0 && !aborted) ptx::mbar_arrive_remote(remote(&xs_free[b2]));
+          if (lane == 0 && !aborted) ptx::mbar_arrive_remote_relaxed(remote(&xs_free[b2]));
           const int nv = nvalid - kHalfTok * pos;   // valid tokens of this half
           if (nv < kHalfTok) {
 #pragma unroll
@@ -763,21 +743,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           l += lsum;
           lq += lqsum;
-          // P and O were last used by the PV of page t-1
-          if (t >= 1 && !aborted &&
-              !bounded_wait(&pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, flags, p.err))
-            aborted = true;
           if (__any_sync(kFullMask, need)) rescale_row(t, alpha, (kHalfDv / 2) * pos, kHalfDv / 2);
-          aborted = __any_sync(kFullMask, aborted);
-          ptx::tc_fence_after();
-          if (!aborted) {
-            ptx::tmem_st16(t_lane + kColP + 16 * pos, *reinterpret_cast<float(*)[16]>(pk));
-            ptx::tmem_st_wait();
-          }
-          // the same P row half to the outgoing rows (their previous copy has been read)
+          // this CTA's P tile of page t was last read by the PV of page t-2, and its owner
+          // rows by the copy to the peer (issued by warp pos 0 of each sub-partition)
+          if (t >= 2 && !aborted &&
+              !bounded_wait(&pv_done[b2], ((t >> 1) - 1) & 1, flags, p.err))
+            aborted = true;
           if (pos == 0 && lane == 0) ptx::bulk_wait_read_all();
           ptx::named_barrier_sync(pair_bar, 64);
-          const uint32_t prow = ptx::smem_addr(pout) + prow_off;
+          const uint32_t prow = p_s + b2 * kPBytes + uint32_t(h) * 128;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
@@ -799,7 +773,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           ptx::fence_proxy_async_shared();
           ptx::named_barrier_sync(pair_bar, 64);
-          // to the peer, once its receivers have read page t-2's: the factors and the P rows
+          // to the peer, once its PV of page t-2 is done: the factors and this sub-partition's
+          // P rows (32 heads x 128 B)
           if (pos == 0) {
             int ok = 1;
             if (lane == 0 && !aborted &&
@@ -811,9 +786,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               ptx::st_async_b32(remote(alpha_in + b2 * kOwnHeads + r), __float_as_uint(alpha), pr_peer);
             __syncwarp();
             if (lane == 0 && !aborted) {
-              const uint32_t blk = uint32_t(32 * gw) * (kPage * 2);
-              ptx::bulk_copy_to_peer(remote(pin + b2 * kPRowsBytes + blk), ptx::smem_addr(pout) + blk,
-                                     32 * kPage * 2, pr_peer);
+              const uint32_t blk = b2 * kPBytes + uint32_t(32 * sp) * 128;
+              ptx::bulk_copy_to_peer(remote(pbuf + blk), p_s + blk, 32 * 128, pr_peer);
               ptx::bulk_commit();
             }
           }

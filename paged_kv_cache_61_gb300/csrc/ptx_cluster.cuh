@@ -50,6 +50,15 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t rbar) {
                : "memory");
 }
 
+// Arrive on an mbarrier of a peer CTA with no ordering of this thread's earlier memory
+// accesses: for signalling that a buffer the peer writes has been read (the loads have
+// returned their values before the arrive is issued), without waiting for this thread's
+// own outstanding stores to the peer.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t rbar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar)
+               : "memory");
+}
+
 // Like mbar_try_wait, acquiring at cluster scope (for phases completed by a peer CTA).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t done;
