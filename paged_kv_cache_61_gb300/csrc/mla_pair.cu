@@ -16,14 +16,15 @@
 //  * Scores with the heads on the MMA's M axis: S_r[128 x 64 tokens] = q_r * K_r^T
 //    (M=128, N=64, K=288: 18 tcgen05.mma). On this part an MMA's issue cost is set by
 //    N (a floor of ~46 cycles up to N=64), so 128 heads on M cost what 64 would.
-//  * CTA r owns the softmax of heads [64r, 64r+64) ("owner" warps; the other two
-//    softmax-group warps "relay" the peer's heads). Per page, the relays send the
-//    partial scores of the peer's heads (16 KB fp32) into the peer's shared memory; the
-//    owners add the peer's partial for their heads, run the online softmax (one thread
-//    per head) and send their P rows (8 KB, 16-bit) and rescale factors back. The
-//    transfers between the two SMs (bulk copies and st.async counted on the receiver's
-//    mbarriers) run about 40 GB/s each way with ~0.4 us latency, so the exchange is
-//    double-buffered and kept small.
+//  * CTA r owns the softmax of heads [64r, 64r+64), kept on tensor-memory lanes 64..127
+//    (the peer's heads on lanes 0..63). Four "owner" warps (two per sub-partition,
+//    splitting each page's tokens) add the peer's partial scores for their heads, run the
+//    online softmax and send their P rows (8 KB, 16-bit) and rescale factors back; two
+//    "relay" warps send the partial scores of the peer's heads (16 KB fp32 per page) as
+//    soon as they exist and take in the peer's P rows and factors. The transfers between
+//    the two SMs (bulk copies and st.async counted on the receiver's mbarriers) run about
+//    40 GB/s each way with ~0.4 us latency, so they are double-buffered, and the owners
+//    read their scores one page ahead so that the exchange overlaps a page of work.
 //  * P[128 x 64] in shared memory is the A operand of the PV MMA:
 //    O_r[128 x 256] += P * V_r[64 x 256] (M=128, N=256, 4 MMAs), V_r read in place
 //    from the page's latent sub-tiles. CTA r owns output dims [256r, 256r+256); the
@@ -54,24 +55,26 @@ constexpr int kOwnHeads = kHeads / 2;       // heads whose softmax a CTA runs
 constexpr int kHalfDv = kDv / 2;            // output / latent dims per CTA
 constexpr int kLatSubs = kHalfDv / 64;      // 128-byte-swizzled 64-dim sub-tiles per CTA
 constexpr int kRopeHalf = 32;               // rope dims per CTA (64-byte swizzle)
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kLatSubBytes = kPage * 128;                          // [64 tokens][64 dims]
 constexpr int kRopeBytes = kPage * kRopeHalf * 2;                  // [64 tokens][32 dims]
 constexpr int kStageBytes = kLatSubs * kLatSubBytes + kRopeBytes;  // 36 KB
-constexpr int kXsBytes = kOwnHeads * kPage * 4;                    // 64 heads' fp32 scores
+// 64 heads' fp32 scores of one page, laid out [token half][64 heads][32 tokens] so that
+// each owner warp's half and each sender's half-block are contiguous
+constexpr int kXsBytes = kOwnHeads * kPage * 4;
+constexpr int kXsHalfBytes = kXsBytes / 2;
 constexpr int kPBytes = kHeads * kPage * 2;                        // P tile, 16-bit
 constexpr int kPRowsBytes = kOwnHeads * kPage * 2;                 // 64 heads' P rows
 constexpr int kPMsgBytes = kPRowsBytes + kOwnHeads * 4;            // P rows + factors
 constexpr int kFinBytes = kOwnHeads * 16;                          // (m, l, lq, -) per head
-// Softmax group: two warps per tensor-memory sub-partition. On the owner sub-partitions
-// they split each page's tokens; on the relay sub-partitions one sends scores and the
-// other receives P rows and factors.
-constexpr int kGroupWarps = 8;
+// Softmax group: two owner warps on each of the two sub-partitions that hold this CTA's
+// heads (they split each page's tokens) and one relay warp on each of the other two.
+constexpr int kGroupWarps = 6;
 constexpr int kHalfTok = kPage / 2;
-constexpr int kQWarps = 6;     // warps that load q (all but the two receivers)
-constexpr int kPWarps = 6;     // warps that arrive on p_full (owners and receivers)
-constexpr int kSWarps = 6;     // warps that read S (owners and senders)
-constexpr int kMergeThreads = 32 * 6;   // owners and receivers: the end-of-piece work
+constexpr int kQWarps = kGroupWarps;     // warps that load q rows
+constexpr int kPWarps = kGroupWarps;     // warps that arrive on p_full
+constexpr int kSWarps = kGroupWarps;     // warps that read S
+constexpr int kMergeThreads = 32 * kGroupWarps;   // the end-of-piece work
 constexpr int kThreads = 64 + 32 * kGroupWarps;
 constexpr int kTmemCols = 512;
 // tensor-memory columns (32-bit): q_r as 16-bit pairs, S, O_r
@@ -85,8 +88,8 @@ constexpr float kRescaleLog2 = 8.f;   // lazy-max slack (log2 units)
 struct Layout {
   static constexpr int kKV = 0;
   static constexpr int kXs = kKV + kStages * kStageBytes;   // [2] the peer's partials, own heads
-  static constexpr int kSstg = kXs + 2 * kXsBytes;          // own partials of the peer's heads
-  static constexpr int kP = kSstg + kXsBytes;                // [2] P tiles (both CTAs' rows)
+  static constexpr int kSstg = kXs + 2 * kXsBytes;          // [2 senders] 32 heads x 32 tokens
+  static constexpr int kP = kSstg + kXsHalfBytes;            // [2] P tiles (both CTAs' rows)
   static constexpr int kAlpha = kP + 2 * kPBytes;            // [2][64] the peer's factors
   static constexpr int kFin = kAlpha + 2 * kOwnHeads * 4;    // [64] the peer's (m, l, lq)
   static constexpr int kRed = kFin + kFinBytes;              // owner halves: maxima, sums
@@ -216,7 +219,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&pr_free[b], 1);   // the peer's MMA commit
     }
     ptx::mbar_init(fin_full, 1);
-    ptx::mbar_init(fin_free, 2);        // the peer's two receiver warps
+    ptx::mbar_init(fin_free, 2);        // the peer's two relay warps
     for (int i = 0; i < 8; ++i) flags[i] = 0;
     ptx::fence_mbarrier_init();
     // what the peer sends for the first two pages and the first piece (it may land first)
@@ -394,23 +397,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ============================== softmax group: owners and relays ==============================
+    // Tensor-memory lane L of CTA r holds head (L + 64 (1 - r)) mod 128: each CTA's own
+    // heads sit on lanes 64..127 (sub-partitions 2 and 3, which have two warps each: the
+    // owners), the peer's on lanes 0..63 (one relay warp on each of sub-partitions 0, 1).
     const int sp = warp & 3;                   // TMEM sub-partition of this warp
-    const int pos = (warp - 2) >> 2;           // 0 or 1: which of the sub-partition's two warps
-    const bool owner = (sp >> 1) == int(rank); // heads [64 rank, 64 rank + 64) are this CTA's
-    const bool sender = !owner && pos == 0;
-    const bool receiver = !owner && pos == 1;
-    const int h = 32 * sp + lane;              // head of the group = TMEM lane
-    const int r = h & (kOwnHeads - 1);         // row of the head among its owner's 64
+    const int pos = (warp - 2) >> 2;           // owners: which of the sub-partition's two warps
+    const bool owner = sp >= 2;
+    const int lrow = 32 * sp + lane;           // TMEM lane = row of S, P and O_r
+    const int h = (lrow + kOwnHeads * (1 - int(rank))) & (kHeads - 1);   // head of this lane
+    const int r = lrow & (kOwnHeads - 1);      // row of the head among its owner's 64
     const int gw = sp & 1;                     // sub-partition within its role
     const uint32_t t_lane = tmem + (uint32_t(32 * sp) << 16);
-    const uint32_t swz = uint32_t(h & 7);
-    const uint32_t row_off = uint32_t(r) * (kPage * 4);          // score rows: 256 B
-    const uint32_t wblk_off = uint32_t(32 * gw) * (kPage * 4);   // a sub-partition's 32 rows
+    const uint32_t swz = uint32_t(lrow & 7);
+    const uint32_t row_off = uint32_t(r) * (kHalfTok * 4);       // half score rows: 128 B
+    const uint32_t wblk_off = uint32_t(32 * gw) * (kHalfTok * 4);  // a sub-partition's 32 rows
     const uint32_t xs_s = ptx::smem_addr(xs);
     const uint32_t p_s = ptx::smem_addr(pbuf);
     const uint32_t pair_bar = 2 + sp;          // named barrier of a sub-partition's two warps
     const bool owner_lead = owner && gw == 0 && pos == 0 && lane == 0;
-    const bool recv_lead = receiver && gw == 0 && lane == 0;
+    const bool relay_lead = !owner && gw == 0 && lane == 0;
     const T* qg = static_cast<const T*>(p.q);
     T* outg = static_cast<T*>(p.out);
     bool aborted = false;
@@ -539,7 +544,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     };
     // the merge of a split segment's pieces by the last to arrive (this CTA's output half),
     // or nothing when the segment is whole or heavily split (the merge kernel's work);
-    // run by the owners and receivers (kMergeThreads, dense index mtid), never the senders
+    // run by all softmax-group warps (kMergeThreads, dense index mtid)
     auto merge_tail = [&](const Portion& pc) __attribute__((always_inline)) {
       const bool whole = (pc.p0 == 0 && pc.p1 == pc.np);
       const int mtid = (owner ? gw * 2 + pos : 4 + gw) * 32 + lane;
@@ -598,78 +603,113 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int t = 0;           // page index within this CTA's range
     int u = 0;           // piece index within this CTA's range
     Portion cur = walker_next(walk, spec, g_hi);
-    if (!receiver) load_q(cur);
+    load_q(cur);
 
-    if (sender) {
-      // ---- sender: this CTA's partial scores of the peer's heads, as soon as they exist
-      while (true) {
-        const int npg = cur.p1 - cur.p0;
-        for (int i = 0; i < npg; ++i, ++t) {
-          const int b2 = t & 1;
-          const uint32_t par2 = uint32_t(t >> 1) & 1;
-          float v[kPage];
-          read_s(t, 0, v);
-          if (lane == 0) ptx::bulk_wait_read_all();   // the staging rows were copied out
-          __syncwarp();
-          const uint32_t srow = ptx::smem_addr(sstg) + row_off;
-#pragma unroll
-          for (int j = 0; j < kPage / 4; ++j)
-            ptx::st_shared_v4(srow + ((uint32_t(j) ^ swz) << 4), v[4 * j], v[4 * j + 1],
-                              v[4 * j + 2], v[4 * j + 3]);
-          ptx::fence_proxy_async_shared();
-          __syncwarp();
-          int ok = 1;
-          if (lane == 0 && !aborted) {
-            if (bounded_wait_cluster(&xs_free[b2], par2 ^ 1, flags, p.err)) {
-              ptx::bulk_copy_to_peer(remote(xs + b2 * kXsBytes + wblk_off),
-                                     ptx::smem_addr(sstg) + wblk_off, 32 * kPage * 4,
-                                     remote(&xs_full[b2]));
-              ptx::bulk_commit();
-            } else {
-              ok = 0;
-            }
-          }
-          if (!__shfl_sync(kFullMask, ok, 0)) aborted = true;
-        }
-        if (walk.g >= g_hi) break;
-        cur = walker_next(walk, spec, g_hi);
-        load_q(cur);   // this piece's last score MMA is done (read_s saw it)
-      }
-      if (lane == 0) ptx::bulk_wait_all();
-    } else if (receiver) {
-      // ---- receiver: the peer's P rows and factors for its heads; rescale their rows of O_r
-      while (true) {
-        const int npg = cur.p1 - cur.p0;
-        for (int i = 0; i < npg; ++i, ++t) {
-          const int b2 = t & 1;
-          const uint32_t par2 = uint32_t(t >> 1) & 1;
-          if (!aborted && !bounded_wait_cluster(&pr_full[b2], par2, flags, p.err)) aborted = true;
-          const float alpha = aborted ? 1.f : alpha_in[b2 * kOwnHeads + r];
-          __syncwarp();
-          if (recv_lead && !aborted) ptx::mbar_arrive_expect_tx(&pr_full[b2], kPMsgBytes);  // page t+2
-          // the peer's P rows of page t are in this CTA's tile; rescale those heads' O rows
-          if (__any_sync(kFullMask, alpha != 1.f)) rescale_row(t, alpha, 0, kHalfDv);
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&p_full[b2]);
-        }
-        // end of the piece: the owner's (m, l, lq) of this head, then the output
-        if (!aborted && !bounded_wait_cluster(fin_full, u & 1, flags, p.err)) aborted = true;
-        const float4 f = aborted ? make_float4(0.f, 1.f, 1.f, 0.f) : fin_in[r];
-        __syncwarp();
-        if (lane == 0 && !aborted) ptx::mbar_arrive_remote_relaxed(remote(fin_free));
-        if (recv_lead && !aborted) ptx::mbar_arrive_expect_tx(fin_full, kFinBytes);  // next piece
-        const int tl = t - 1;
-        if (!aborted && !bounded_wait(&pv_done[tl & 1], (tl >> 1) & 1, flags, p.err)) aborted = true;
+    if (!owner) {
+      // ---- relay: this CTA's partial scores of the peer's heads go out as soon as they
+      // exist, and the peer's P rows and factors for those heads come in; one warp polls
+      // both. After an abort every step counts as ready, so the relay still reaches each
+      // piece's end (and its named barrier with the owners) exactly once.
+      const int total = int(g_hi - g_lo);
+      int ts = 0;                        // next page to send
+      int s_rem = cur.p1 - cur.p0;       // pages of the send cursor's piece still to send
+      Walker swalk = walk;               // send cursor, positioned after `cur`
+      int i = 0;                         // receive cursor: page within `cur`
+      const uint32_t sblk = ptx::smem_addr(sstg) + uint32_t(gw) * (32 * kHalfTok * 4);
+      const uint32_t srow = sblk + uint32_t(lane) * (kHalfTok * 4);
+      uint64_t last = ptx::globaltimer();
+      while (t < total) {
+        if (flags[0]) aborted = true;
         aborted = __any_sync(kFullMask, aborted);
-        ptx::tc_fence_after();
-        write_out(cur, f.z, (f.x + log2f(f.y)) * kLn2, 0, kHalfDv, true);
-        ptx::tc_fence_before();
-        merge_tail(cur);
-        ++u;
-        if (walk.g >= g_hi) break;
-        cur = walker_next(walk, spec, g_hi);
+        bool progress = false;
+        if (ts < total) {
+          if (s_rem == 0) {
+            // the previous piece's scores were all sent, so its last score MMA is done
+            const Portion np = walker_next(swalk, spec, g_hi);
+            s_rem = np.p1 - np.p0;
+            load_q(np);
+          }
+          const int rdy = (lane == 0) ? int(aborted || ptx::mbar_try_wait(s_full, ts & 1)) : 0;
+          if (__shfl_sync(kFullMask, rdy, 0)) {
+            const int b2 = ts & 1;
+            const uint32_t par2 = uint32_t(ts >> 1) & 1;
+            float v[kPage];
+            read_s(ts, 0, v);
+            // the peer's owners have read page ts-2 from the buffer this page goes to
+            int ok = 1;
+            if (lane == 0 && !aborted &&
+                !bounded_wait_cluster(&xs_free[b2], par2 ^ 1, flags, p.err))
+              ok = 0;
+            if (!__shfl_sync(kFullMask, ok, 0)) aborted = true;
+            // two half-rows through this warp's 4 KB staging block, one copy each
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              if (lane == 0) ptx::bulk_wait_read_all();   // the staging block was copied out
+              __syncwarp();
+#pragma unroll
+              for (int j = 0; j < kHalfTok / 4; ++j)
+                ptx::st_shared_v4(srow + ((uint32_t(j) ^ swz) << 4), v[32 * hf + 4 * j],
+                                  v[32 * hf + 4 * j + 1], v[32 * hf + 4 * j + 2],
+                                  v[32 * hf + 4 * j + 3]);
+              ptx::fence_proxy_async_shared();
+              __syncwarp();
+              if (lane == 0 && !aborted) {
+                ptx::bulk_copy_to_peer(remote(xs + b2 * kXsBytes + hf * kXsHalfBytes + wblk_off),
+                                       sblk, 32 * kHalfTok * 4, remote(&xs_full[b2]));
+                ptx::bulk_commit();
+              }
+            }
+            ++ts;
+            --s_rem;
+            progress = true;
+          }
+        }
+        if (t < ts) {
+          const int b2 = t & 1;
+          const uint32_t par2 = uint32_t(t >> 1) & 1;
+          const int rdy =
+              (lane == 0) ? int(aborted || ptx::mbar_try_wait_cluster(&pr_full[b2], par2)) : 0;
+          if (__shfl_sync(kFullMask, rdy, 0)) {
+            // the peer's P rows of page t are in this CTA's tile: rescale those heads' O rows
+            const float alpha = aborted ? 1.f : alpha_in[b2 * kOwnHeads + r];
+            __syncwarp();
+            if (relay_lead && !aborted) ptx::mbar_arrive_expect_tx(&pr_full[b2], kPMsgBytes);  // page t+2
+            if (__any_sync(kFullMask, alpha != 1.f)) rescale_row(t, alpha, 0, kHalfDv);
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&p_full[b2]);
+            if (++i == cur.p1 - cur.p0) {
+              // end of the piece: the owner's (m, l, lq) of this head, then the output
+              if (!aborted && !bounded_wait_cluster(fin_full, u & 1, flags, p.err)) aborted = true;
+              const float4 f = aborted ? make_float4(0.f, 1.f, 1.f, 0.f) : fin_in[r];
+              __syncwarp();
+              if (lane == 0 && !aborted) ptx::mbar_arrive_remote_relaxed(remote(fin_free));
+              if (relay_lead && !aborted) ptx::mbar_arrive_expect_tx(fin_full, kFinBytes);  // next piece
+              if (!aborted && !bounded_wait(&pv_done[b2], par2, flags, p.err)) aborted = true;
+              aborted = __any_sync(kFullMask, aborted);
+              ptx::tc_fence_after();
+              write_out(cur, f.z, (f.x + log2f(f.y)) * kLn2, 0, kHalfDv, true);
+              ptx::tc_fence_before();
+              merge_tail(cur);
+              ++u;
+              i = 0;
+              if (walk.g < g_hi) cur = walker_next(walk, spec, g_hi);
+            }
+            ++t;
+            progress = true;
+          }
+        }
+        if (progress) {
+          last = ptx::globaltimer();
+        } else if (ptx::globaltimer() - last > ptx::kWaitLimitNs) {
+          if (lane == 0) {
+            flags[0] = 1;
+            atomicOr(p.err, 2);
+          }
+          aborted = true;
+        }
       }
+      if (lane == 0) ptx::bulk_wait_all();   // the last copies into the peer have landed
     } else {
       // ---- owner (token half `pos`): S = S_own + S_peer, online softmax, P row half out
       // [2 halves][64 rows] half maxima of the page in hand; at the end of a piece the same
@@ -681,6 +721,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // and of the 16-bit weights the PV MMA multiplies V by (O is normalised by the
       // latter, so the output is a convex combination of V rows whatever the rounding of P)
       float m = 0.f, l = 0.f, lq = 0.f;
+      // Scores are read one page ahead: reading S(t+1) at the top of page t frees the S
+      // columns, so the score MMA runs two pages ahead of this loop and the peer's partial
+      // scores of page t have a whole page of work to arrive in.
+      const int total = int(g_hi - g_lo);
+      float vn[kHalfTok];      // own partial scores of the page read ahead
+      int tr = 0;              // next page to read
+      int r_rem = cur.p1 - cur.p0;   // pages of the read cursor's piece still to read
+      Walker rwalk = walk;     // positioned after `cur`
+      Portion q_next = cur;    // a piece whose q is to be loaded at the end of this page
+      bool q_pending = false;
+      auto read_next = [&]() __attribute__((always_inline)) {
+        read_s(tr, kHalfTok * pos, vn);
+        ++tr;
+        if (--r_rem == 0 && rwalk.g < g_hi) {
+          // the piece's last score MMA is done: q of the next piece, loaded once this
+          // page's registers are free (and before the next read needs it)
+          q_next = walker_next(rwalk, spec, g_hi);
+          r_rem = q_next.p1 - q_next.p0;
+          q_pending = true;
+        }
+      };
+      read_next();
+      if (q_pending) {
+        load_q(q_next);
+        q_pending = false;
+      }
       while (true) {
         const int npg = cur.p1 - cur.p0;
         const int ctx = __ldg(p.context_lens + cur.b);
@@ -689,14 +755,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t par2 = uint32_t(t >> 1) & 1;
           const int nvalid = min(kPage, ctx - (cur.p0 + i) * kPage);
           float v[kHalfTok];
-          read_s(t, kHalfTok * pos, v);
+#pragma unroll
+          for (int j = 0; j < kHalfTok; ++j) v[j] = vn[j];
+          if (tr < total) read_next();
           if (!aborted && !bounded_wait_cluster(&xs_full[b2], par2, flags, p.err)) aborted = true;
           if (owner_lead && !aborted) ptx::mbar_arrive_expect_tx(&xs_full[b2], kXsBytes);  // page t+2
-          const uint32_t xr = xs_s + b2 * kXsBytes + row_off;
+          const uint32_t xr = xs_s + b2 * kXsBytes + pos * kXsHalfBytes + row_off;
 #pragma unroll
           for (int j = 0; j < kHalfTok / 4; ++j) {
             const float4 x = aborted ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                     : ptx::ld_shared_v4(xr + ((uint32_t(8 * pos + j) ^ swz) << 4));
+                                     : ptx::ld_shared_v4(xr + ((uint32_t(j) ^ swz) << 4));
             v[4 * j] += x.x;
             v[4 * j + 1] += x.y;
             v[4 * j + 2] += x.z;
@@ -751,7 +819,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             aborted = true;
           if (pos == 0 && lane == 0) ptx::bulk_wait_read_all();
           ptx::named_barrier_sync(pair_bar, 64);
-          const uint32_t prow = p_s + b2 * kPBytes + uint32_t(h) * 128;
+          const uint32_t prow = p_s + b2 * kPBytes + uint32_t(lrow) * 128;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
@@ -786,22 +854,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               ptx::st_async_b32(remote(alpha_in + b2 * kOwnHeads + r), __float_as_uint(alpha), pr_peer);
             __syncwarp();
             if (lane == 0 && !aborted) {
-              const uint32_t blk = b2 * kPBytes + uint32_t(32 * sp) * 128;
-              ptx::bulk_copy_to_peer(remote(pbuf + blk), p_s + blk, 32 * 128, pr_peer);
+              // this CTA's lanes 64..127 are the peer's lanes 0..63 (the same heads)
+              const uint32_t src = b2 * kPBytes + uint32_t(32 * sp) * 128;
+              const uint32_t dst = b2 * kPBytes + uint32_t(32 * gw) * 128;
+              ptx::bulk_copy_to_peer(remote(pbuf + dst), p_s + src, 32 * 128, pr_peer);
               ptx::bulk_commit();
             }
           }
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&p_full[b2]);
+          if (q_pending) {
+            load_q(q_next);
+            q_pending = false;
+          }
         }
-        // ---- the next piece's q once this piece's last score MMA is done (read_s saw it)
+        // ---- the next piece (its q was loaded by the read-ahead)
         const bool have_next = walk.g < g_hi;
         Portion nxt = cur;
-        if (have_next) {
-          nxt = walker_next(walk, spec, g_hi);
-          load_q(nxt);
-        }
+        if (have_next) nxt = walker_next(walk, spec, g_hi);
         // ---- end of the piece: both halves' sums, (m, l, lq) to the peer, then O_r / lq
         hsm[(pos * 2) * kOwnHeads + r] = l;
         hsm[(pos * 2 + 1) * kOwnHeads + r] = lq;
