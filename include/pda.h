@@ -124,7 +124,8 @@ PDA_API pda_status pda_workspace_init(const pda_plan* plan, void* workspace, pda
  * Read and clear the device error word of a workspace (synchronizes `stream`).
  * *code = 0: no error; bit 0: a block-table entry of a read page was outside
  * [0, num_blocks) (that page was read as zeros); bit 1: a pipeline wait timed
- * out and the kernel abandoned its work.
+ * out and the kernel abandoned its work; bit 2: the MLA kernel for head groups of
+ * 128 found its shared memory not 1024-byte aligned and did no work.
  */
 PDA_API pda_status pda_read_device_error(void* workspace, pda_stream_t stream, int32_t* code);
 

@@ -88,14 +88,16 @@ constexpr float kRescaleLog2 = 8.f;   // lazy-max slack (log2 units)
 struct Layout {
   static constexpr int kKV = 0;
   static constexpr int kXs = kKV + kStages * kStageBytes;   // [2] the peer's partials, own heads
-  static constexpr int kSstg = kXs + 2 * kXsBytes;          // [2 senders] 32 heads x 32 tokens
-  static constexpr int kP = kSstg + kXsHalfBytes;            // [2] P tiles (both CTAs' rows)
+  static constexpr int kSstg = kXs + 2 * kXsBytes;          // [2 relays] 32 heads x 64 tokens
+  static constexpr int kP = kSstg + kXsBytes;                // [2] P tiles (both CTAs' rows)
   static constexpr int kAlpha = kP + 2 * kPBytes;            // [2][64] the peer's factors
   static constexpr int kFin = kAlpha + 2 * kOwnHeads * 4;    // [64] the peer's (m, l, lq)
   static constexpr int kRed = kFin + kFinBytes;              // owner halves: maxima, sums
   static constexpr int kBar = kRed + 1024;
   static constexpr int kBarCount = 32;
-  static constexpr int kSmem = 1024 + kBar + kBarCount * 8;
+  // The dynamic shared memory must start on a 1024-byte boundary (checked at run time):
+  // the layout leaves no room to align it by hand.
+  static constexpr int kSmem = kBar + kBarCount * 8;
   static_assert(kStageBytes % 1024 == 0 && kXs % 1024 == 0 && kP % 1024 == 0,
                 "swizzled tiles stay 1024-byte aligned");
   static_assert(kSmem <= 227 * 1024, "fits one SM's shared memory");
@@ -163,9 +165,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_pair_kernel(const __grid_constant__ CUtensorMap tm_kv_lat,
                     const __grid_constant__ CUtensorMap tm_kv_rope, const PairParams p) {
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-  extern __shared__ uint8_t smem_raw[];
-  // the same offset in both CTAs of the pair (same kernel, same static layout)
-  uint8_t* base = align1024(smem_raw);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // Swizzled tiles need 1024-byte alignment and the layout has no slack to align by hand.
+  // Both CTAs of a pair see the same address, so both leave here together if it is not.
+  if ((ptx::smem_addr(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicOr(p.err, 4);
+    return;
+  }
+  uint8_t* base = smem_raw;
   uint8_t* kv = base + Layout::kKV;
   uint8_t* xs = base + Layout::kXs;
   uint8_t* sstg = base + Layout::kSstg;
@@ -381,8 +388,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           flags[0] = 1;
           atomicOr(p.err, 2);
           break;
-        } else {
-          __nanosleep(32);   // leave issue slots to the softmax warps on this sub-partition
         }
       }
       // Wait (bounded) for the last MMAs before tensor memory is released.
@@ -615,7 +620,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int s_rem = cur.p1 - cur.p0;       // pages of the send cursor's piece still to send
       Walker swalk = walk;               // send cursor, positioned after `cur`
       int i = 0;                         // receive cursor: page within `cur`
-      const uint32_t sblk = ptx::smem_addr(sstg) + uint32_t(gw) * (32 * kHalfTok * 4);
+      // this warp's 8 KB staging block: [token half][32 rows][32 fp32]
+      const uint32_t sblk = ptx::smem_addr(sstg) + uint32_t(gw) * (32 * kPage * 4);
       const uint32_t srow = sblk + uint32_t(lane) * (kHalfTok * 4);
       uint64_t last = ptx::globaltimer();
       while (t < total) {
@@ -641,23 +647,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 !bounded_wait_cluster(&xs_free[b2], par2 ^ 1, flags, p.err))
               ok = 0;
             if (!__shfl_sync(kFullMask, ok, 0)) aborted = true;
-            // two half-rows through this warp's 4 KB staging block, one copy each
+            // both half-rows through this warp's staging block (its previous page's copies
+            // have long been read), then one copy per half
+            if (lane == 0) ptx::bulk_wait_read_all();
+            __syncwarp();
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-              if (lane == 0) ptx::bulk_wait_read_all();   // the staging block was copied out
-              __syncwarp();
+            for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
               for (int j = 0; j < kHalfTok / 4; ++j)
-                ptx::st_shared_v4(srow + ((uint32_t(j) ^ swz) << 4), v[32 * hf + 4 * j],
-                                  v[32 * hf + 4 * j + 1], v[32 * hf + 4 * j + 2],
-                                  v[32 * hf + 4 * j + 3]);
-              ptx::fence_proxy_async_shared();
-              __syncwarp();
-              if (lane == 0 && !aborted) {
+                ptx::st_shared_v4(srow + hf * (32 * kHalfTok * 4) + ((uint32_t(j) ^ swz) << 4),
+                                  v[32 * hf + 4 * j], v[32 * hf + 4 * j + 1],
+                                  v[32 * hf + 4 * j + 2], v[32 * hf + 4 * j + 3]);
+            ptx::fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0 && !aborted) {
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf)
                 ptx::bulk_copy_to_peer(remote(xs + b2 * kXsBytes + hf * kXsHalfBytes + wblk_off),
-                                       sblk, 32 * kHalfTok * 4, remote(&xs_full[b2]));
-                ptx::bulk_commit();
-              }
+                                       sblk + hf * (32 * kHalfTok * 4), 32 * kHalfTok * 4,
+                                       remote(&xs_full[b2]));
+              ptx::bulk_commit();
             }
             ++ts;
             --s_rem;
