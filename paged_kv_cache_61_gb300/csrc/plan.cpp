@@ -120,7 +120,10 @@ extern "C" PDA_API pda_status pda_plan_create(pda_plan** out, const pda_problem*
     plan->segs_per_seq = p.num_kv_heads;
     plan->head_subtiles = (plan->group + 7) / 8;
     ctas_per_sm = pda::gqa_ctas_per_sm(p);
-    min_tiles_per_cta = 4;
+    // A split piece writes a 4·G·D-byte fp32 partial and reads 64·D bytes per tile: at
+    // least G/4 + 1 tiles keep the partial under a quarter of what the piece reads (for a
+    // 32-head MQA group on a 32K sequence this is also the fastest count in a sweep).
+    min_tiles_per_cta = std::max<int64_t>(4, plan->group / 4 + 1);
   } else {
     plan->group = pda::mla_heads_per_cta(p);
     plan->segs_per_seq = p.num_q_heads / plan->group;
