@@ -71,10 +71,12 @@ def kernel_hash(kind: str) -> str:
 
 
 def kernel_kind(case) -> str:
-    """Which decode kernel a case runs on (MLA head groups of 128 use the two-CTA kernel)."""
+    """Which decode kernel a case runs on (576-wide MLA records with head groups of 128 use
+    the two-CTA kernel; every other MLA shape the single-CTA one)."""
     if case.kind == "gqa":
         return "gqa"
-    return "mla_pair" if case.num_q_heads % 128 == 0 else "mla"
+    pair = case.head_dim_qk == 576 and case.num_q_heads % 128 == 0
+    return "mla_pair" if pair else "mla"
 
 
 def recorded_traffic(workload: str, kind: str):
@@ -197,7 +199,8 @@ def oracle_sample(case, budget_s: float):
                                                case.head_dim_qk, 2)
         else:
             oracle.mla_decode(case.q, case.kv_cache, case.block_tables, case.context_lens,
-                              case.scale, case.page_size, case.dtype, rows=rows)
+                              case.scale, case.page_size, case.dtype,
+                              head_dim_v=case.head_dim_v, rows=rows)
             done_bytes += traffic.mla_kv_bytes([case.context_lens[b]], case.head_dim_qk, 2)
         b = (b + 1) % case.batch
         if time.perf_counter() - t0 >= budget_s:
@@ -215,7 +218,14 @@ def cpu_baseline(workload: str, budget_s: float = 10.0):
     if r.returncode != 0:
         return {"value": None, "error": r.stderr.strip().splitlines()[-1:]}
     done, secs, nseq = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": done / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+    case = synth.workload(workload)
+    gbs = done / secs / 1e9
+    if case.kind == "gqa":
+        value, unit = gbs, "GB/s"
+    else:                                   # MLA lines are in TFLOP/s: same FLOPs per KV byte
+        kv, flops = accounting(case)
+        value, unit = gbs * (flops / kv) / 1e3, "TFLOP/s"
+    return {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
             "sample": f"float64 numpy oracle, one thread, {max(nseq, 1)} whole sequences "
                       f"(all heads) of {workload} in {secs:.1f} s"}
 

@@ -16,7 +16,7 @@
  * GQA" (kzhou003.github.io gpu-kernel-drills), sections ③-⑤ (grid over
  * (batch, KV head), page loop, masking of the partial last page); FlashMLA-ETAP
  * README, sections "Usage" and "Supported configurations" (per-step scheduling
- * metadata, 576/512 latent layout, page size 64, fp32 lse).
+ * metadata, 576/512 and 320/256 latent layouts, page size 64, fp32 lse).
  *
  * Conventions for every call:
  *  - The caller owns every buffer and the stream. Device pointers are CUDA
@@ -70,8 +70,8 @@ typedef struct pda_problem {
   int32_t batch;              /* B >= 0 sequences (B == 0: every call is a no-op) */
   int32_t num_q_heads;        /* Hq */
   int32_t num_kv_heads;       /* Hkv, Hq % Hkv == 0 ("H_q must be divisible by H_kv"); MLA: 1 */
-  int32_t head_dim_qk;        /* GQA: 64 or 128; MLA: 576 (512 latent + 64 rope) */
-  int32_t head_dim_v;         /* GQA: == head_dim_qk; MLA: 512 (V = first 512 dims of the record) */
+  int32_t head_dim_qk;        /* GQA: 64 or 128; MLA: 576 (512 latent + 64 rope) or 320 (256 + 64) */
+  int32_t head_dim_v;         /* GQA: == head_dim_qk; MLA: head_dim_qk - 64 (V = the latent dims) */
   int32_t page_size;          /* tokens per physical block P; GQA: 16; MLA: 64 */
   int32_t max_blocks_per_seq; /* columns of block_tables */
   int64_t num_blocks;         /* physical blocks in the cache pool */
@@ -152,15 +152,17 @@ PDA_API pda_status paged_decode_attn(const void* q, const void* k_cache, const v
                              void* workspace, pda_stream_t stream);
 
 /*
- * Absorbed MLA decode ("From MHA to MLA", section 6; FlashMLA-ETAP "Usage"):
- * every query head attends to one shared record per token of
- * head_dim_qk = 576 values (512 latent then 64 rope). Scores use all 576,
- * values are the first 512.
- *   q             device [B, Hq, 576] dtype (absorbed content query then rope query)
- *   kv_cache      device [num_blocks, 64, 576] dtype (one KV head)
+ * Absorbed MLA decode ("From MHA to MLA", section 6; FlashMLA-ETAP "Usage" and
+ * "Supported configurations"): every query head attends to one shared record
+ * per token of Dqk = head_dim_qk values, Dv = head_dim_v latent then 64 rope,
+ * with (Dqk, Dv) = (576, 512) (kv_lora_rank 512) or (320, 256) (kv_lora_rank
+ * 256). Scores use all Dqk values, values are the first Dv.
+ *   q             device [B, Hq, Dqk] dtype (absorbed content query then rope query)
+ *   kv_cache      device [num_blocks, 64, Dqk] dtype (one KV head)
  *   block_tables, context_lens, scale, plan (kind PDA_KIND_MLA), workspace: as above
- *   out           device [B, Hq, 512] dtype
+ *   out           device [B, Hq, Dv] dtype
  *   lse           device [B, Hq] float32 or NULL
+ * Hq: 16, 32 or a multiple of 64.
  */
 PDA_API pda_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_tables,
                       const int32_t* context_lens, float scale, void* out, float* lse,

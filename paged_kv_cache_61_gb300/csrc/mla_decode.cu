@@ -2,21 +2,22 @@
 //
 // What it computes ("From MHA to MLA", section 6; FlashMLA-ETAP README, "Usage"
 // and "Supported configurations"): every query head attends to one shared record
-// per cached token of 576 values (512 latent + 64 rope). The score of head h and
-// token j is scale * (<q_h[:512], c_j> + <q_h[512:], k_j^R>) = scale * <q_h, rec_j>;
-// the value is the latent c_j = rec_j[:512]. Output [B, Hq, 512] and fp32 LSE.
+// per cached token of Dqk values, Dv latent then 64 rope: (576, 512) for kv_lora_rank
+// 512, (320, 256) for kv_lora_rank 256. The score of head h and token j is
+// scale * (<q_h[:Dv], c_j> + <q_h[Dv:], k_j^R>) = scale * <q_h, rec_j>; the value is
+// the latent c_j = rec_j[:Dv]. Output [B, Hq, Dv] and fp32 LSE.
 //
 // How (GB300 design; the FlashMLA-ETAP page describes a Hopper WGMMA kernel with
 // the transposed pipeline, whose idea of putting keys on the MMA's M axis is kept):
 //  * One CTA per range of (sequence, head group, page) tiles, the same equal-work
 //    split as the GQA kernel; a head group is N = min(Hq, 64) heads, so TMEM holds
-//    the N score columns plus 4 x N columns of the transposed output.
-//  * Warp 0 streams pages with one TMA copy each (a 64-token x 576 page lands as
-//    nine 128-byte-swizzled [64][64] sub-tiles) into a two-stage ring, and loads
-//    the head group's q once per piece.
+//    the N score columns plus Dv / 128 x N columns of the transposed output.
+//  * Warp 0 streams pages with one TMA copy each (a 64-token x Dqk page lands as
+//    Dqk / 64 128-byte-swizzled [64][64] sub-tiles) into a two-stage ring, and
+//    loads the head group's q once per piece.
 //  * Warp 1 issues tcgen05.mma from one thread:
-//      S^T[64 tokens x N]  = K[64 x 576] * q^T        (M=64, K-major A and B)
-//      O^T[512 x N]       += V^T[512 x 64] * P^T       (4 x M=128, MN-major A and B)
+//      S^T[64 tokens x N]  = K[64 x Dqk] * q^T        (M=64, K-major A and B)
+//      O^T[Dv x N]        += V^T[Dv x 64] * P^T        (Dv / 128 x M=128, MN-major A and B)
 //    V^T is read in place from the same page sub-tiles (MN-major descriptor), so
 //    each latent byte is read from HBM once.
 //  * Warps 2-5 read S^T from TMEM (tcgen05.ld), run the online softmax down each
@@ -42,13 +43,20 @@ namespace pda {
 namespace {
 
 constexpr int kPage = 64;
-constexpr int kDqk = 576;
-constexpr int kDv = 512;
-constexpr int kSubTiles = kDqk / 64;          // nine 64-dim sub-tiles per record
 constexpr int kSubBytes = kPage * 128;        // [64 tokens][64 dims] x 16 bit
-constexpr int kPageBytes = kSubTiles * kSubBytes;
-constexpr int kRopeSub = kSubTiles - 1;       // sub-tile reused for P^T
 constexpr int kStages = 2;
+// A cached record of DQK 16-bit values: DQK - 64 latent dims (the value) then 64 rope
+// dims. FlashMLA-ETAP "Supported configurations": (576, 512) for kv_lora_rank 512 and
+// (320, 256) for kv_lora_rank 256.
+template <int DQK>
+struct Rec {
+  static constexpr int kDv = DQK - 64;
+  static constexpr int kSubTiles = DQK / 64;          // 64-dim sub-tiles per record
+  static constexpr int kPageBytes = kSubTiles * kSubBytes;
+  static constexpr int kRopeSub = kSubTiles - 1;      // sub-tile reused for P^T
+  static constexpr int kMTiles = kDv / 128;           // 128-dim O^T tiles of the PV MMA
+  static_assert(DQK % 64 == 0 && (DQK - 64) % 128 == 0, "latent width a multiple of 128");
+};
 // Warp 0 TMA, warp 1 MMA, then the softmax warps: 4 (one per TMEM sub-partition) for
 // N = 16 heads, 8 for N >= 32 (two per sub-partition, each owning half the head columns).
 template <int N>
@@ -60,10 +68,6 @@ struct SoftmaxWarps {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.f;           // lazy-max slack (log2 units)
-#ifndef PDA_MLA_PREFETCH_PAGES
-#define PDA_MLA_PREFETCH_PAGES 0
-#endif
-constexpr int kPrefetchPages = PDA_MLA_PREFETCH_PAGES;  // L2 prefetch distance in pages
 
 struct MlaParams {
   const void* q;
@@ -82,11 +86,12 @@ struct MlaParams {
   float* part_out;
 };
 
-template <int N>
+template <int N, int DQK>
 struct MlaLayout {
-  static constexpr int kQBytes = kSubTiles * N * 128;  // q as nine K-major [N][64] sub-tiles
+  using R = Rec<DQK>;
+  static constexpr int kQBytes = R::kSubTiles * N * 128;  // q as K-major [N][64] sub-tiles
   static constexpr int kKV = 0;
-  static constexpr int kQ = kKV + kStages * kPageBytes;
+  static constexpr int kQ = kKV + kStages * R::kPageBytes;
   static constexpr int kRed = kQ + kQBytes;            // [64 heads][4 warps] floats
   static constexpr int kMused = kRed + 64 * 4 * 4;     // running maximum per head (log2 units)
   static constexpr int kAlpha = kMused + 64 * 4;       // rescale factor per head
@@ -95,7 +100,8 @@ struct MlaLayout {
   static constexpr int kBarCount = 24;
   static constexpr int kSmem = 1024 + kBar + kBarCount * 8 + 64;
   // TMEM columns: S^T double-buffered at [0, 2N), O^T d-tile mt at 2N + mt*N
-  static constexpr int kTmemCols = (6 * N <= 128) ? 128 : (6 * N <= 256 ? 256 : 512);
+  static constexpr int kCols = (2 + R::kMTiles) * N;
+  static constexpr int kTmemCols = kCols <= 128 ? 128 : (kCols <= 256 ? 256 : 512);
   static constexpr int kColS = 0;
   static constexpr int kColO = 2 * N;
   static_assert(kQBytes % 1024 == 0, "q sub-tiles stay 1024-byte aligned");
@@ -118,11 +124,16 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
   return __float2bfloat16_rn(x);
 }
 
-template <int N, typename T>
+template <int N, int DQK, typename T>
 __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_kv, const MlaParams p) {
-  using L = MlaLayout<N>;
+  using L = MlaLayout<N, DQK>;
+  using R = Rec<DQK>;
+  constexpr int kDv = R::kDv;
+  constexpr int kSubTiles = R::kSubTiles;
+  constexpr int kPageBytes = R::kPageBytes;
+  constexpr int kRopeSub = R::kRopeSub;
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
@@ -206,13 +217,9 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
         const int n = min(32, pt.p1 - base_pg);
         for (int j = 0; j < n; ++j, ++t) {
           const int32_t phys = __shfl_sync(kFullMask, ids, j);
-          const int32_t ahead = __shfl_sync(kFullMask, ids, (j + kPrefetchPages) & 31);
           int good = 1;
           if (lane == 0) {
             const int s = t & 1;
-            // Optionally ask L2 for the page kPrefetchPages ahead (0 = off).
-            if (kPrefetchPages > 0 && j + kPrefetchPages < n)
-              ptx::tma_prefetch_l2_4d(&tm_kv, 0, 0, 0, ahead);
             if (!bounded_wait(&kv_empty[s], ((t >> 1) & 1) ^ 1, flags, p.err)) {
               good = 0;
             } else {
@@ -307,7 +314,7 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
           const bool first = (first_bits >> (t_pv & 31)) & 1u;
           const uint32_t st = kv_s + (t_pv & 1) * kPageBytes;
 #pragma unroll
-          for (int mt = 0; mt < 4; ++mt) {
+          for (int mt = 0; mt < R::kMTiles; ++mt) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
               const uint64_t a =
@@ -440,7 +447,7 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
             ptx::tc_fence_after();
             if (!aborted) {
 #pragma unroll
-              for (int mt = 0; mt < 4; ++mt) {
+              for (int mt = 0; mt < R::kMTiles; ++mt) {
 #pragma unroll
                 for (int c = 0; c < NC; c += 16) {
                   float v[16];
@@ -482,7 +489,7 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
         // Slots past ctx in the last page: their P is 0, but 0 * (whatever the slot holds,
         // NaN included) must not reach O, so their V rows are cleared before the PV MMA
         // (the score MMA has already consumed the page). The warps of a sub-partition
-        // split the eight latent sub-tiles.
+        // split the latent sub-tiles.
         if (active && token >= ctx) {
           uint8_t* stg = kv + (t & 1) * kPageBytes;
           constexpr int kSubPerWarp = (kDv / 64) / (kSW / 4);
@@ -527,7 +534,7 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
       const int64_t head0 = int64_t(pt.b) * p.num_q_heads + int64_t(pt.seg) * N;
       const int64_t slot_row = (int64_t(blockIdx.x) * 2 + slot) * N;
 #pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
+      for (int mt = 0; mt < R::kMTiles; ++mt) {
         const int d = mt * 128 + 32 * sp + lane;
 #pragma unroll
         for (int c = 0; c < NC; c += 16) {
@@ -641,15 +648,18 @@ EncodeTiledFn mla_encode_fn() {
   return fn;
 }
 
-// q [rows, 576]: dims (d mod 64, row, d / 64), box (64, N, 9) -> nine [N][64] sub-tiles.
-// kv [blocks, 64, 576]: dims (d mod 64, slot, d / 64, block), box (64, 64, 9, 1) ->
-// nine [64][64] sub-tiles per page. Both with 128-byte swizzle.
+// With S = dqk / 64 sub-tiles per record (9 for 576, 5 for 320):
+// q [rows, dqk]: dims (d mod 64, row, d / 64), box (64, N, S) -> S [N][64] sub-tiles.
+// kv [blocks, 64, dqk]: dims (d mod 64, slot, d / 64, block), box (64, 64, S, 1) ->
+// S [64][64] sub-tiles per page. Both with 128-byte swizzle.
 bool encode_mla_maps(CUtensorMap* tq, CUtensorMap* tkv, const void* q, int64_t rows, int n,
-                     const void* kv, int64_t num_blocks, bool bf16) {
+                     const void* kv, int64_t num_blocks, bool bf16, int dqk) {
   EncodeTiledFn fn = mla_encode_fn();
   if (fn == nullptr) return false;
   const CUtensorMapDataType dt =
       bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const cuuint32_t kSubTiles = cuuint32_t(dqk / 64);
+  const cuuint64_t kDqk = cuuint64_t(dqk);
   const cuuint64_t qdims[3] = {64, cuuint64_t(rows), kSubTiles};
   const cuuint64_t qstr[2] = {kDqk * 2, 128};
   const cuuint32_t qbox[3] = {64, cuuint32_t(n), kSubTiles};
@@ -667,29 +677,36 @@ bool encode_mla_maps(CUtensorMap* tq, CUtensorMap* tkv, const void* q, int64_t r
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int N, typename T>
+template <int N, int DQK, typename T>
 int launch_mla_n(const CUtensorMap& tq, const CUtensorMap& tkv, const MlaParams& prm, int grid,
                  cudaStream_t stream) {
-  auto kern = mla_decode_kernel<N, T>;
+  auto kern = mla_decode_kernel<N, DQK, T>;
+  using L = MlaLayout<N, DQK>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    MlaLayout<N>::kSmem);
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  kern<<<grid, SoftmaxWarps<N>::kThreads, MlaLayout<N>::kSmem, stream>>>(tq, tkv, prm);
+  kern<<<grid, SoftmaxWarps<N>::kThreads, L::kSmem, stream>>>(tq, tkv, prm);
   return cudaGetLastError();
 }
 
-template <typename T>
+template <int DQK, typename T>
 int launch_mla_t(int n, const CUtensorMap& tq, const CUtensorMap& tkv, const MlaParams& prm,
                  int grid, cudaStream_t s) {
   switch (n) {
-    case 16: return launch_mla_n<16, T>(tq, tkv, prm, grid, s);
-    case 32: return launch_mla_n<32, T>(tq, tkv, prm, grid, s);
-    default: return launch_mla_n<64, T>(tq, tkv, prm, grid, s);
+    case 16: return launch_mla_n<16, DQK, T>(tq, tkv, prm, grid, s);
+    case 32: return launch_mla_n<32, DQK, T>(tq, tkv, prm, grid, s);
+    default: return launch_mla_n<64, DQK, T>(tq, tkv, prm, grid, s);
   }
+}
+
+template <typename T>
+int launch_mla_dt(int dqk, int n, const CUtensorMap& tq, const CUtensorMap& tkv,
+                  const MlaParams& prm, int grid, cudaStream_t s) {
+  return dqk == 320 ? launch_mla_t<320, T>(n, tq, tkv, prm, grid, s)
+                    : launch_mla_t<576, T>(n, tq, tkv, prm, grid, s);
 }
 
 }  // namespace
@@ -701,8 +718,9 @@ int mla_heads_per_cta(const pda_problem& p) {
 int mla_ctas_per_sm(const pda_problem&) { return 1; }
 
 bool mla_supported(const pda_problem& p, std::string* why) {
-  if (p.head_dim_qk != kDqk || p.head_dim_v != kDv) {
-    *why = "MLA decode supports head_dim_qk 576 and head_dim_v 512";
+  if (!((p.head_dim_qk == 576 && p.head_dim_v == 512) ||
+        (p.head_dim_qk == 320 && p.head_dim_v == 256))) {
+    *why = "MLA decode supports (head_dim_qk, head_dim_v) = (576, 512) or (320, 256)";
     return false;
   }
   if (p.page_size != kPage) {
@@ -732,7 +750,7 @@ int launch_mla_decode(const Plan& plan, const MlaArgs& a, const Workspace& ws, v
   const int n = plan.group;
   CUtensorMap tq, tkv;
   if (!encode_mla_maps(&tq, &tkv, a.q, int64_t(pr.batch) * pr.num_q_heads, n, a.kv_cache,
-                       pr.num_blocks, bf16))
+                       pr.num_blocks, bf16, pr.head_dim_qk))
     return -1;
   MlaParams prm{};
   prm.q = a.q;
@@ -754,8 +772,9 @@ int launch_mla_decode(const Plan& plan, const MlaArgs& a, const Workspace& ws, v
   prm.part_lse = ws.part_lse;
   prm.part_out = ws.part_out;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int e = bf16 ? launch_mla_t<__nv_bfloat16>(n, tq, tkv, prm, plan.num_ctas, s)
-                     : launch_mla_t<__half>(n, tq, tkv, prm, plan.num_ctas, s);
+  const int dqk = pr.head_dim_qk;
+  const int e = bf16 ? launch_mla_dt<__nv_bfloat16>(dqk, n, tq, tkv, prm, plan.num_ctas, s)
+                     : launch_mla_dt<__half>(dqk, n, tq, tkv, prm, plan.num_ctas, s);
   if (e != 0) return e;
   return launch_split_merge(plan, ws, a.out, a.lse, stream);
 }

@@ -991,7 +991,9 @@ cudaError_t pair_kernel_attributes() {
 
 }  // namespace
 
-bool mla_uses_pairs(const pda_problem& p) { return p.num_q_heads % kHeads == 0; }
+bool mla_uses_pairs(const pda_problem& p) {
+  return p.head_dim_qk == kDqk && p.num_q_heads % kHeads == 0;
+}
 
 int mla_pair_units(int num_sms) {
   int clusters = 0;

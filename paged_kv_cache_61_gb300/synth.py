@@ -19,7 +19,8 @@ Recipe (every workload):
 
 Workload names follow the five decode workloads this library is measured on:
 ``gqa_tiny``, ``gqa_b64_ctx1k``, ``gqa_b1_ctx32k`` (``_mqa`` for one KV head),
-``gqa_varlen_b128`` and ``mla_b16_ctx64k_h16`` / ``_h128``.
+``gqa_varlen_b128`` and ``mla_b16_ctx64k_h16`` / ``_h128``; ``mla_r256_b16_ctx64k_h16`` /
+``_h128`` are the same MLA shapes with the kv_lora_rank 256 record (256 latent + 64 rope).
 """
 from __future__ import annotations
 
@@ -77,8 +78,8 @@ class DecodeCase:
       k_cache      [num_blocks, page_size, Hkv, D]
       v_cache      [num_blocks, page_size, Hkv, D]
     MLA (``kind == "mla"``):
-      q            [B, Hq, 576]   (512 absorbed-content dims then 64 rope dims)
-      kv_cache     [num_blocks, page_size, 576]  (K = all 576 dims, V = the first 512)
+      q            [B, Hq, Dqk]   (Dv absorbed-content dims then 64 rope dims; Dqk 576 or 320)
+      kv_cache     [num_blocks, page_size, Dqk]  (K = all Dqk dims, V = the first Dv = Dqk - 64)
     Both:
       block_tables [B, max_blocks_per_seq] int32
       context_lens [B] int32
@@ -232,12 +233,15 @@ def workload(name: str, seed: int = 0) -> DecodeCase:
         return make_gqa_case(batch=128, num_q_heads=64, num_kv_heads=8, head_dim=128, dtype=BF16,
                              ctx_dist="loguniform", ctx_low=16, ctx_high=32768,
                              max_blocks_per_seq=2048, table_layout="pool", seed=seed, name=name)
-    if name in ("mla_b16_ctx64k_h16", "mla_b16_ctx64k_h128"):
+    if name in ("mla_b16_ctx64k_h16", "mla_b16_ctx64k_h128",
+                "mla_r256_b16_ctx64k_h16", "mla_r256_b16_ctx64k_h128"):
         hq = 16 if name.endswith("h16") else 128
+        latent = 256 if "_r256_" in name else 512
         return make_mla_case(batch=16, num_q_heads=hq, dtype=BF16, context_lens=[65536] * 16,
-                             seed=seed, name=name)
+                             latent_dim=latent, seed=seed, name=name)
     raise KeyError(name)
 
 
 WORKLOADS = ("gqa_tiny", "gqa_b64_ctx1k", "gqa_b1_ctx32k", "gqa_b1_ctx32k_mqa",
-             "gqa_varlen_b128", "mla_b16_ctx64k_h16", "mla_b16_ctx64k_h128")
+             "gqa_varlen_b128", "mla_b16_ctx64k_h16", "mla_b16_ctx64k_h128",
+             "mla_r256_b16_ctx64k_h16", "mla_r256_b16_ctx64k_h128")

@@ -1,5 +1,8 @@
 """Absorbed-MLA paged decode on the GPU (tcgen05 kernel, through the C ABI) vs the float64 oracle.
 
+Two record widths: kv_lora_rank 512 (576 = 512 latent + 64 rope, V = first 512) and
+kv_lora_rank 256 (320 = 256 latent + 64 rope, V = first 256).
+
 Tolerances: out max-abs <= 1e-2 (bf16) / 2e-3 (fp16), fp32 LSE within 1e-3.
 """
 import numpy as np
@@ -21,12 +24,13 @@ def _gpu():
 
 def _oracle(case, rows=None):
     return oracle.mla_decode(case.q, case.kv_cache, case.block_tables, case.context_lens,
-                             case.scale, case.page_size, case.dtype, rows=rows)
+                             case.scale, case.page_size, case.dtype, head_dim_v=case.head_dim_v,
+                             rows=rows)
 
 
-def _case(hq, ctx, dtype=synth.BF16, seed=5):
+def _case(hq, ctx, dtype=synth.BF16, seed=5, latent=512):
     return synth.make_mla_case(batch=len(ctx), num_q_heads=hq, dtype=dtype, context_lens=ctx,
-                               seed=seed)
+                               latent_dim=latent, seed=seed)
 
 
 def _assert_close(case, dc, rows=None):
@@ -40,17 +44,28 @@ def _assert_close(case, dc, rows=None):
     return out, lse
 
 
+@pytest.mark.parametrize("latent", [512, 256])
 @pytest.mark.parametrize("hq", [16, 32, 64, 128])
 @pytest.mark.parametrize("force", [0, 1, 3, 17])
-def test_small_cases(hq, force):
-    case = _case(hq, [1, 63, 64, 65, 130, 700])
+def test_small_cases(hq, force, latent):
+    case = _case(hq, [1, 63, 64, 65, 130, 700], latent=latent)
     _assert_close(case, DeviceCase(case, force_num_ctas=force))
 
 
+@pytest.mark.parametrize("latent", [512, 256])
 @pytest.mark.parametrize("hq", [16, 128])
-def test_fp16(hq):
-    case = _case(hq, [200, 64, 1], dtype=synth.FP16)
+def test_fp16(hq, latent):
+    case = _case(hq, [200, 64, 1], dtype=synth.FP16, latent=latent)
     _assert_close(case, DeviceCase(case))
+
+
+@pytest.mark.parametrize("hq", [128, 192])
+@pytest.mark.parametrize("force", [0, 2, 5])
+def test_rank256_several_head_groups_ragged_batch(hq, force):
+    # the 320-wide record runs 64-head groups on single CTAs: several groups per
+    # sequence, ragged last pages, a one-token sequence, split sequences
+    case = _case(hq, [1, 65, 127, 128, 129, 1000, 3000], seed=11, latent=256)
+    _assert_close(case, DeviceCase(case, force_num_ctas=force))
 
 
 @pytest.mark.parametrize("hq", [128, 256])
@@ -62,39 +77,41 @@ def test_head_groups_of_128_ragged_batch(hq, force):
     _assert_close(case, DeviceCase(case, force_num_ctas=force))
 
 
+@pytest.mark.parametrize("latent", [512, 256])
 @pytest.mark.parametrize("hq", [64, 128])
-def test_score_jumps_force_rescales(hq):
+def test_score_jumps_force_rescales(hq, latent):
     # q's rope half is all ones and the rope keys of pages >= 3 and >= 10 get a constant
     # added, so the scores jump twice by ~8.7 in log2 units: the running maximum must be
     # raised and the accumulated output rescaled within one piece. After each jump many
     # tokens share the weight, so the check stays inside the bf16 tolerance.
-    case = _case(hq, [2000, 900])
-    case.q[..., 512:] = synth.float32_to_bits(np.float32(1.0), case.dtype)
+    case = _case(hq, [2000, 900], latent=latent)
+    case.q[..., latent:] = synth.float32_to_bits(np.float32(1.0), case.dtype)
     kv = synth.bits_to_float32(case.kv_cache, case.dtype)
     step = 6.0 * np.sqrt(192.0) / 64.0          # +6 on the natural-log score per jump
     for b, c in enumerate(case.context_lens):
         npg = (int(c) + 63) // 64
         for pg in range(npg):
             blk = int(case.block_tables[b, pg])
-            kv[blk, :, 512:] += step * ((pg >= 3) + (pg >= 10))
+            kv[blk, :, latent:] += step * ((pg >= 3) + (pg >= 10))
     case.kv_cache = synth.float32_to_bits(kv, case.dtype)
     for force in (0, 1):
         _assert_close(case, DeviceCase(case, force_num_ctas=force))
 
 
+@pytest.mark.parametrize("latent", [512, 256])
 @pytest.mark.parametrize("hq", [16, 128])
-def test_rope_needle_is_bit_exact(hq):
+def test_rope_needle_is_bit_exact(hq, latent):
     ctx = 300
-    case = _case(hq, [ctx] * 6, seed=9)
+    case = _case(hq, [ctx] * 6, seed=9, latent=latent)
     one = synth.float32_to_bits(np.float32(1.0), case.dtype)
     sixteen = synth.float32_to_bits(np.float32(16.0), case.dtype)
-    case.q[..., :512] = 0
-    case.q[..., 512:] = one
-    case.kv_cache[..., 512:] = 0
+    case.q[..., :latent] = 0
+    case.q[..., latent:] = one
+    case.kv_cache[..., latent:] = 0
     targets = [0, 63, 64, 150, 255, 299]
     for b, t in enumerate(targets):
         blk = int(case.block_tables[b, t // 64])
-        case.kv_cache[blk, t % 64, 512:] = sixteen
+        case.kv_cache[blk, t % 64, latent:] = sixteen
     for force in (0, 1, 5):
         dc = DeviceCase(case, force_num_ctas=force)
         out, _ = dc.run()
@@ -103,7 +120,7 @@ def test_rope_needle_is_bit_exact(hq):
         for b, t in enumerate(targets):
             blk = int(case.block_tables[b, t // 64])
             for h in range(hq):
-                assert np.array_equal(got[b, h], case.kv_cache[blk, t % 64, :512]), (force, b, h)
+                assert np.array_equal(got[b, h], case.kv_cache[blk, t % 64, :latent]), (force, b, h)
 
 
 def test_ctx1_returns_latent_of_token0():
@@ -138,7 +155,8 @@ def test_poisoned_stale_slots_and_table_entries(hq):
     assert pda.read_device_error(dc.ws) == 0
 
 
-@pytest.mark.parametrize("name", ["mla_b16_ctx64k_h16", "mla_b16_ctx64k_h128"])
+@pytest.mark.parametrize("name", ["mla_b16_ctx64k_h16", "mla_b16_ctx64k_h128",
+                                  "mla_r256_b16_ctx64k_h16", "mla_r256_b16_ctx64k_h128"])
 def test_full_size_workload_sampled_rows(name):
     case = synth.workload(name)
     hq = case.num_q_heads

@@ -298,37 +298,43 @@ def test_combine_weights_by_split_mass_and_skips_empty():
 
 
 # ---------------------------------------------------------------- MLA
-def _small_mla(hq=16, ctx=(70, 1, 129), seed=4):
+def _small_mla(hq=16, ctx=(70, 1, 129), seed=4, latent=512):
     return synth.make_mla_case(batch=len(ctx), num_q_heads=hq, dtype=synth.BF16,
-                               context_lens=list(ctx), seed=seed)
+                               context_lens=list(ctx), latent_dim=latent, seed=seed)
 
 
-def test_mla_equals_generic_with_one_kv_head():
-    case = _small_mla()
+def test_mla_equals_generic_with_one_kv_head(latent=512):
+    case = _small_mla(latent=latent)
     out, lse = oracle.mla_decode(case.q, case.kv_cache, case.block_tables, case.context_lens,
-                                 case.scale, case.page_size, case.dtype)
+                                 case.scale, case.page_size, case.dtype, head_dim_v=latent)
     k = case.kv_cache[:, :, None, :]
-    v = case.kv_cache[:, :, None, :512]
+    v = case.kv_cache[:, :, None, :latent]
     out2, lse2 = oracle.paged_decode(case.q, k, v, case.block_tables, case.context_lens,
                                      case.scale, case.page_size, case.dtype)
     np.testing.assert_allclose(out, out2, rtol=0, atol=1e-12)
     np.testing.assert_allclose(lse, lse2, rtol=0, atol=1e-12)
 
 
-def test_mla_rope_only_needle_returns_latent_of_target():
-    case = _small_mla(hq=4, ctx=(100,))
+def test_mla_rope_only_needle_returns_latent_of_target(latent=512):
+    case = _small_mla(hq=4, ctx=(100,), latent=latent)
     kv = case.kv_cache.copy()
     q = case.q.copy()
-    q[..., :512] = 0                                   # no content score at all
-    q[..., 512:] = synth.float32_to_bits(np.float32(1.0), case.dtype)
-    kv[..., 512:] = 0
+    q[..., :latent] = 0                                   # no content score at all
+    q[..., latent:] = synth.float32_to_bits(np.float32(1.0), case.dtype)
+    kv[..., latent:] = 0
     target = 77
     blk = int(case.block_tables[0, target // 64])
-    kv[blk, target % 64, 512:] = synth.float32_to_bits(np.float32(16.0), case.dtype)
+    kv[blk, target % 64, latent:] = synth.float32_to_bits(np.float32(16.0), case.dtype)
     out, lse = oracle.mla_decode(q, kv, case.block_tables, case.context_lens, case.scale,
-                                 case.page_size, case.dtype)
-    want = oracle.widen(kv[blk, target % 64, :512], case.dtype)
+                                 case.page_size, case.dtype, head_dim_v=latent)
+    want = oracle.widen(kv[blk, target % 64, :latent], case.dtype)
     for h in range(4):
         np.testing.assert_allclose(out[0, h], want, rtol=0, atol=1e-30)
         assert lse[0, h] == pytest.approx(case.scale * 16 * 64, abs=1e-9)
-    assert out.shape[-1] == 512
+    assert out.shape[-1] == latent
+
+
+def test_rank256_record_pins():
+    """The same two pins on the kv_lora_rank 256 record (256 latent + 64 rope)."""
+    test_mla_equals_generic_with_one_kv_head(latent=256)
+    test_mla_rope_only_needle_returns_latent_of_target(latent=256)
