@@ -44,7 +44,6 @@ namespace {
 
 constexpr int kPage = 64;
 constexpr int kSubBytes = kPage * 128;        // [64 tokens][64 dims] x 16 bit
-constexpr int kStages = 2;
 // A cached record of DQK 16-bit values: DQK - 64 latent dims (the value) then 64 rope
 // dims. FlashMLA-ETAP "Supported configurations": (576, 512) for kv_lora_rank 512 and
 // (320, 256) for kv_lora_rank 256.
@@ -55,6 +54,9 @@ struct Rec {
   static constexpr int kPageBytes = kSubTiles * kSubBytes;
   static constexpr int kRopeSub = kSubTiles - 1;      // sub-tile reused for P^T
   static constexpr int kMTiles = kDv / 128;           // 128-dim O^T tiles of the PV MMA
+  // Page ring stages: two 72 KB pages of the 576 record (with q for 64 heads, most of
+  // shared memory), four 40 KB pages of the 320 record.
+  static constexpr int kStages = DQK == 576 ? 2 : 4;
   static_assert(DQK % 64 == 0 && (DQK - 64) % 128 == 0, "latent width a multiple of 128");
 };
 // Warp 0 TMA, warp 1 MMA, then the softmax warps: 4 (one per TMEM sub-partition) for
@@ -91,14 +93,15 @@ struct MlaLayout {
   using R = Rec<DQK>;
   static constexpr int kQBytes = R::kSubTiles * N * 128;  // q as K-major [N][64] sub-tiles
   static constexpr int kKV = 0;
-  static constexpr int kQ = kKV + kStages * R::kPageBytes;
+  static constexpr int kQ = kKV + R::kStages * R::kPageBytes;
   static constexpr int kRed = kQ + kQBytes;            // [64 heads][4 warps] floats
   static constexpr int kMused = kRed + 64 * 4 * 4;     // running maximum per head (log2 units)
   static constexpr int kAlpha = kMused + 64 * 4;       // rescale factor per head
   static constexpr int kLtot = kAlpha + 64 * 4;        // softmax denominator per head
   static constexpr int kBar = kLtot + 64 * 4;
-  static constexpr int kBarCount = 24;
+  static constexpr int kBarCount = 2 * R::kStages + 20;
   static constexpr int kSmem = 1024 + kBar + kBarCount * 8 + 64;
+  static_assert(kSmem <= 232448, "fits the 227 KB of dynamic shared memory per block");
   // TMEM columns: S^T double-buffered at [0, 2N), O^T d-tile mt at 2N + mt*N
   static constexpr int kCols = (2 + R::kMTiles) * N;
   static constexpr int kTmemCols = kCols <= 128 ? 128 : (kCols <= 256 ? 256 : 512);
@@ -134,6 +137,7 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
   constexpr int kSubTiles = R::kSubTiles;
   constexpr int kPageBytes = R::kPageBytes;
   constexpr int kRopeSub = R::kRopeSub;
+  constexpr int KS = R::kStages;
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
@@ -144,19 +148,20 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
   float* alpha_s = reinterpret_cast<float*>(base + L::kAlpha);
   float* ltot = reinterpret_cast<float*>(base + L::kLtot);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::kBar);
-  uint64_t* kv_full = bars + 0;   // [2]
-  uint64_t* kv_empty = bars + 2;  // [2]
-  uint64_t* q_full = bars + 4;
-  uint64_t* q_empty = bars + 5;
+  // Page t sits in ring stage t % KS (its P^T in that stage's rope sub-tile).
+  uint64_t* kv_full = bars + 0;        // [KS]
+  uint64_t* kv_empty = bars + KS;      // [KS]
+  uint64_t* q_full = bars + 2 * KS;
+  uint64_t* q_empty = bars + 2 * KS + 1;
   // Barriers that complete once per page come in pairs indexed by page parity, so a
-  // waiter is never two phases behind (the S^T buffer and the P^T sub-tile alternate too).
-  uint64_t* s_full = bars + 6;    // [2] S^T buffer written
-  uint64_t* s_free = bars + 8;    // [2] S^T buffer read, P^T written
-  uint64_t* p_full = bars + 10;   // [2]
-  uint64_t* pv_done = bars + 12;  // [2] PV of a page completed
+  // waiter is never two phases behind (the S^T buffer alternates too).
+  uint64_t* s_full = bars + 2 * KS + 2;    // [2] S^T buffer written
+  uint64_t* s_free = bars + 2 * KS + 4;    // [2] S^T buffer read, P^T written
+  uint64_t* p_full = bars + 2 * KS + 6;    // [2]
+  uint64_t* pv_done = bars + 2 * KS + 8;   // [2] PV of a page completed
   // [0] abort, [1] last piece, [2..9] softmax-warp votes (5 slots)
-  volatile int* flags = reinterpret_cast<volatile int*>(bars + 14);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
+  volatile int* flags = reinterpret_cast<volatile int*>(bars + 2 * KS + 10);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * KS + 16);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -166,7 +171,7 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
   if (g_lo >= g_hi) return;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < KS; ++s) {
       ptx::mbar_init(&kv_full[s], 1);
       ptx::mbar_init(&kv_empty[s], 1);
     }
@@ -219,8 +224,8 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
           const int32_t phys = __shfl_sync(kFullMask, ids, j);
           int good = 1;
           if (lane == 0) {
-            const int s = t & 1;
-            if (!bounded_wait(&kv_empty[s], ((t >> 1) & 1) ^ 1, flags, p.err)) {
+            const int s = t % KS;
+            if (!bounded_wait(&kv_empty[s], ((t / KS) & 1) ^ 1, flags, p.err)) {
               good = 0;
             } else {
               if (phys < 0 || int64_t(phys) >= p.num_blocks) atomicOr(p.err, 1);
@@ -237,10 +242,10 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
     }
     // Leave no copy in flight: the last fill of each stage and of q (bounded).
     if (lane == 0) {
-      for (int k = 1; k <= 2 && t - k >= 0; ++k) {
+      for (int k = 1; k <= KS && t - k >= 0; ++k) {
         const int tt = t - k;
         const uint64_t t0 = ptx::globaltimer();
-        while (!ptx::mbar_try_wait(&kv_full[tt & 1], (tt >> 1) & 1) &&
+        while (!ptx::mbar_try_wait(&kv_full[tt % KS], (tt / KS) & 1) &&
                ptx::globaltimer() - t0 < ptx::kWaitLimitNs) {
         }
       }
@@ -281,14 +286,15 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
           }
         }
         if (!qk_done && i < npg) {
-          const int s = t_qk & 1;
+          const int s = t_qk & 1;          // S^T buffer
+          const int kst = t_qk % KS;       // ring stage
           const bool ready = (!need_q || ptx::mbar_try_wait(q_full, u & 1)) &&
-                             ptx::mbar_try_wait(&kv_full[s], (t_qk >> 1) & 1) &&
+                             ptx::mbar_try_wait(&kv_full[kst], (t_qk / KS) & 1) &&
                              (t_qk < 2 || ptx::mbar_try_wait(&s_free[s], ((t_qk >> 1) - 1) & 1));
           if (ready) {
             need_q = false;
             ptx::tc_fence_after();
-            const uint32_t st = kv_s + s * kPageBytes;
+            const uint32_t st = kv_s + kst * kPageBytes;
 #pragma unroll
             for (int kb = 0; kb < kSubTiles; ++kb) {
 #pragma unroll
@@ -312,7 +318,7 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
         if (t_pv < t_qk && ptx::mbar_try_wait(&p_full[t_pv & 1], (t_pv >> 1) & 1)) {
           ptx::tc_fence_after();
           const bool first = (first_bits >> (t_pv & 31)) & 1u;
-          const uint32_t st = kv_s + (t_pv & 1) * kPageBytes;
+          const uint32_t st = kv_s + (t_pv % KS) * kPageBytes;
 #pragma unroll
           for (int mt = 0; mt < R::kMTiles; ++mt) {
 #pragma unroll
@@ -324,7 +330,7 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
               ptx::umma_f16(tmem + L::kColO + mt * N, a, b, kIdPV, !(first && ks == 0));
             }
           }
-          ptx::umma_commit(&kv_empty[t_pv & 1]);
+          ptx::umma_commit(&kv_empty[t_pv % KS]);
           ptx::umma_commit(&pv_done[t_pv & 1]);
           ++t_pv;
           progress = true;
@@ -464,7 +470,7 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
           }
         }
         // P^T row `row` (heads contiguous) over the page's rope sub-tile
-        uint8_t* pbuf = kv + (t & 1) * kPageBytes + kRopeSub * kSubBytes;
+        uint8_t* pbuf = kv + (t % KS) * kPageBytes + kRopeSub * kSubBytes;
 #pragma unroll
         for (int c = 0; c < NC; c += 8) {
           const float4 ma = *reinterpret_cast<const float4*>(mused + cb + c);
@@ -491,7 +497,7 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
         // (the score MMA has already consumed the page). The warps of a sub-partition
         // split the latent sub-tiles.
         if (active && token >= ctx) {
-          uint8_t* stg = kv + (t & 1) * kPageBytes;
+          uint8_t* stg = kv + (t % KS) * kPageBytes;
           constexpr int kSubPerWarp = (kDv / 64) / (kSW / 4);
 #pragma unroll
           for (int k = 0; k < kSubPerWarp; ++k) {
