@@ -32,6 +32,15 @@ Sources (web pages this library follows):
 
 Inputs are the 16-bit bit patterns produced by the shared input generator; the
 oracle widens them exactly to float64 itself.
+
+fp8 caches ("Attention Kernel Variants: MQA, GQA, and MLA" (vanos001.github.io),
+the KV-cache arithmetic table's fp8 MLA row and pitfall 5: an fp8 cache stores
+one byte per cached value and kernels dequantize its tiles before the attention
+arithmetic). The pages fix no format details beyond "fp8", so the oracle reads
+each byte as an E4M3 code (the OCP 8-bit floating-point format: 1 sign bit, 4
+exponent bits with bias 7, 3 mantissa bits, no infinities, S.1111.111 = NaN) and
+multiplies it by one per-tensor scale: K_j = e4m3(code) * k_scale, V_j likewise
+with v_scale (MLA: one kv_scale for the record).
 """
 from __future__ import annotations
 
@@ -52,6 +61,37 @@ def widen(bits: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == BF16:
         return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
     raise ValueError(dtype)
+
+
+FP8_E4M3 = "e4m3"
+
+
+def decode_e4m3(codes: np.ndarray) -> np.ndarray:
+    """E4M3 byte codes -> float64, exactly, from the format's definition.
+
+    sign s = bit 7, exponent field e = bits 6..3, mantissa field m = bits 2..0:
+      e == 15 and m == 7 -> NaN (the format has no infinities)
+      e == 0             -> (-1)^s * 2^(1 - 7) * (m / 8)      (subnormal, zero)
+      otherwise          -> (-1)^s * 2^(e - 7) * (1 + m / 8)
+    """
+    codes = np.asarray(codes, dtype=np.uint8)
+    sign = np.where((codes >> 7) & 1, -1.0, 1.0)
+    e = ((codes >> 3) & 0xF).astype(np.int64)
+    m = (codes & 0x7).astype(np.float64)
+    normal = sign * np.ldexp(1.0 + m / 8.0, e - 7)
+    subnormal = sign * np.ldexp(m / 8.0, 1 - 7)
+    out = np.where(e == 0, subnormal, normal)
+    return np.where((e == 15) & (m == 7), np.nan, out)
+
+
+def dequantize(stored: np.ndarray, dtype: str, kv_format: str = None, scale: float = 1.0):
+    """Cached values as float64: 16-bit patterns widened (kv_format None), or E4M3 codes
+    decoded and multiplied by the per-tensor scale (kv_format "e4m3")."""
+    if kv_format is None:
+        return widen(stored, dtype)
+    if kv_format == FP8_E4M3:
+        return decode_e4m3(stored) * float(scale)
+    raise ValueError(kv_format)
 
 
 # --------------------------------------------------------------------------------------
@@ -116,10 +156,11 @@ def kv_head_of(h: int, num_q_heads: int, num_kv_heads: int) -> int:
 
 
 def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale, page_size, dtype,
-                 rows=None):
+                 rows=None, kv_format=None, k_scale=1.0, v_scale=1.0):
     """Oracle for GQA/MQA/MHA decode over a paged cache.
 
-    q [B, Hq, D] (16-bit bits), k_cache/v_cache [NB, P, Hkv, D] (bits),
+    q [B, Hq, D] (16-bit bits), k_cache/v_cache [NB, P, Hkv, D] (bits; E4M3 codes when
+    kv_format is "e4m3", dequantized with k_scale / v_scale),
     block_tables [B, max_blocks] int32, context_lens [B] int32 (>= 1).
     rows: optional list of (b, h) pairs to evaluate (others left NaN).
     Returns out [B, Hq, Dv] float64 and lse [B, Hq] float64.
@@ -140,8 +181,10 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale, page_si
                 continue
             heads_by_kv.setdefault(kv_head_of(h, Hq, Hkv), []).append(h)
         for kvh, heads in heads_by_kv.items():
-            keys = widen(gather_tokens(k_cache[:, :, kvh, :], block_tables[b], ctx, page_size), dtype)
-            vals = widen(gather_tokens(v_cache[:, :, kvh, :], block_tables[b], ctx, page_size), dtype)
+            keys = dequantize(gather_tokens(k_cache[:, :, kvh, :], block_tables[b], ctx, page_size),
+                              dtype, kv_format, k_scale)
+            vals = dequantize(gather_tokens(v_cache[:, :, kvh, :], block_tables[b], ctx, page_size),
+                              dtype, kv_format, v_scale)
             o, l = attend(widen(q[b, heads, :], dtype), keys, vals, scale)
             out[b, heads] = o
             lse[b, heads] = l
@@ -152,10 +195,11 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale, page_si
 # absorbed MLA decode ("From MHA to MLA", section 6; FlashMLA-ETAP "Supported configurations")
 # --------------------------------------------------------------------------------------
 def mla_decode(q, kv_cache, block_tables, context_lens, scale, page_size, dtype,
-               head_dim_v=512, rows=None):
+               head_dim_v=512, rows=None, kv_format=None, kv_scale=1.0):
     """Oracle for absorbed-MLA decode: every query head attends to one shared latent record.
 
-    q [B, Hq, Dqk] (content dims then rope dims), kv_cache [NB, P, Dqk] (bits).
+    q [B, Hq, Dqk] (content dims then rope dims), kv_cache [NB, P, Dqk] (bits; E4M3 codes
+    when kv_format is "e4m3", dequantized with kv_scale).
     Score = scale * (content dot + rope dot) = scale * <q, kv[:Dqk]>; value = kv[:head_dim_v].
     """
     B, Hq, Dqk = q.shape
@@ -169,7 +213,8 @@ def mla_decode(q, kv_cache, block_tables, context_lens, scale, page_size, dtype,
         heads = [h for h in range(Hq) if wanted is None or (b, h) in wanted]
         if not heads:
             continue
-        record = widen(gather_tokens(kv_cache, block_tables[b], ctx, page_size), dtype)  # [L, Dqk]
+        record = dequantize(gather_tokens(kv_cache, block_tables[b], ctx, page_size), dtype,
+                            kv_format, kv_scale)                                     # [L, Dqk]
         qb = widen(q[b, heads, :], dtype)
         content = float(scale) * (qb[:, :head_dim_v] @ record[:, :head_dim_v].T)
         rope = float(scale) * (qb[:, head_dim_v:] @ record[:, head_dim_v:Dqk].T)

@@ -15,7 +15,11 @@ Recipe (every workload):
     patterns (``uint16``);
   * block tables are random permutations of the physical block pool; table
     entries past a sequence's last page are filled with ``UNUSED_ENTRY`` (an
-    out-of-range id) unless the workload says otherwise.
+    out-of-range id) unless the workload says otherwise;
+  * fp8 caches (``kv_format="e4m3"``): the same N(0, 1) float32 draws, divided by
+    one per-tensor scale amax|x| / 448 (448 = the largest E4M3 value) and cast
+    to E4M3 by PyTorch's float8_e4m3fn conversion; the arrays hold the codes
+    (``uint8``) and the case carries the scales. q stays 16-bit.
 
 Workload names follow the five decode workloads this library is measured on:
 ``gqa_tiny``, ``gqa_b64_ctx1k``, ``gqa_b1_ctx32k`` (``_mqa`` for one KV head),
@@ -32,6 +36,8 @@ import numpy as np
 
 FP16 = "fp16"
 BF16 = "bf16"
+FP8_E4M3 = "e4m3"          # cache format: one E4M3 byte per value, one scale per tensor
+E4M3_MAX = 448.0
 UNUSED_ENTRY = -1          # block-table filler past the last page of a sequence
 _CHUNK = 1 << 22           # values drawn per call; fixed so results never depend on the caller
 
@@ -57,6 +63,35 @@ def normal_16bit(rng: np.random.Generator, shape, dtype: str) -> np.ndarray:
     return out.reshape(shape)
 
 
+def normal_e4m3(rng: np.random.Generator, shape):
+    """N(0,1) float32 draws stored as E4M3 codes with one per-tensor scale.
+
+    Returns (codes uint8 of ``shape``, scale) with scale = amax|x| / 448, so the
+    largest draw maps to the largest finite code. The cast is PyTorch's.
+    """
+    import torch
+    n = int(np.prod(shape, dtype=np.int64))
+    x = np.empty(n, dtype=np.float32)
+    for start in range(0, n, _CHUNK):
+        stop = min(n, start + _CHUNK)
+        x[start:stop] = rng.standard_normal(stop - start, dtype=np.float32)
+    amax = float(np.abs(x).max()) if n else 1.0
+    scale = np.float32(amax / E4M3_MAX if amax > 0 else 1.0)
+    codes = np.empty(n, dtype=np.uint8)
+    for start in range(0, n, _CHUNK):
+        stop = min(n, start + _CHUNK)
+        y = np.clip(x[start:stop] / scale, -E4M3_MAX, E4M3_MAX)
+        codes[start:stop] = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    return codes.reshape(shape), float(scale)
+
+
+def float32_to_e4m3(x: np.ndarray) -> np.ndarray:
+    """E4M3 codes of float32 values (PyTorch's float8_e4m3fn cast; for structured inputs)."""
+    import torch
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    return torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
 def bits_to_float32(bits: np.ndarray, dtype: str) -> np.ndarray:
     """Exact widening of 16-bit patterns to float32 (for building structured inputs)."""
     if dtype == FP16:
@@ -71,7 +106,9 @@ def float32_to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
 
 @dataclasses.dataclass
 class DecodeCase:
-    """One decode-attention problem in host memory (16-bit values stored as uint16 bits).
+    """One decode-attention problem in host memory (16-bit values stored as uint16 bits;
+    with ``kv_format == "e4m3"`` the caches hold uint8 E4M3 codes, dequantized as
+    code * k_scale (K, or the MLA record) and code * v_scale (V)).
 
     GQA (``kind == "gqa"``):
       q            [B, Hq, D]
@@ -101,6 +138,9 @@ class DecodeCase:
     k_cache: Optional[np.ndarray] = None
     v_cache: Optional[np.ndarray] = None
     kv_cache: Optional[np.ndarray] = None
+    kv_format: Optional[str] = None
+    k_scale: float = 1.0
+    v_scale: float = 1.0
 
     @property
     def max_blocks_per_seq(self) -> int:
@@ -132,7 +172,8 @@ def make_gqa_case(*, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: 
                   dtype: str, page_size: int = 16, context_lens=None, ctx_low: int = 1,
                   ctx_high: int = 256, ctx_dist: str = "fixed", num_blocks: Optional[int] = None,
                   max_blocks_per_seq: Optional[int] = None, scale: Optional[float] = None,
-                  seed: int = 0, name: str = "gqa", table_layout: str = "pool") -> DecodeCase:
+                  seed: int = 0, name: str = "gqa", table_layout: str = "pool",
+                  kv_format: Optional[str] = None) -> DecodeCase:
     """Build a GQA/MQA/MHA decode problem.
 
     ctx_dist: "fixed" (``context_lens`` given), "uniform" (integers in
@@ -172,20 +213,30 @@ def make_gqa_case(*, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: 
     else:
         raise ValueError(table_layout)
     q = normal_16bit(r_q, (batch, num_q_heads, head_dim), dtype)
-    k = normal_16bit(r_k, (num_blocks, page_size, num_kv_heads, head_dim), dtype)
-    v = normal_16bit(r_v, (num_blocks, page_size, num_kv_heads, head_dim), dtype)
+    cache_shape = (num_blocks, page_size, num_kv_heads, head_dim)
+    k_scale = v_scale = 1.0
+    if kv_format is None:
+        k = normal_16bit(r_k, cache_shape, dtype)
+        v = normal_16bit(r_v, cache_shape, dtype)
+    elif kv_format == FP8_E4M3:
+        k, k_scale = normal_e4m3(r_k, cache_shape)
+        v, v_scale = normal_e4m3(r_v, cache_shape)
+    else:
+        raise ValueError(kv_format)
     if scale is None:
         scale = 1.0 / math.sqrt(head_dim)
     return DecodeCase(name=name, kind="gqa", dtype=dtype, batch=batch, num_q_heads=num_q_heads,
                       num_kv_heads=num_kv_heads, head_dim_qk=head_dim, head_dim_v=head_dim,
                       page_size=page_size, num_blocks=int(num_blocks), scale=float(scale),
-                      context_lens=ctx, block_tables=tables, q=q, k_cache=k, v_cache=v)
+                      context_lens=ctx, block_tables=tables, q=q, k_cache=k, v_cache=v,
+                      kv_format=kv_format, k_scale=k_scale, v_scale=v_scale)
 
 
 def make_mla_case(*, batch: int, num_q_heads: int, dtype: str = BF16, page_size: int = 64,
                   context_lens=None, ctx_low: int = 1, ctx_high: int = 4096, ctx_dist: str = "fixed",
                   latent_dim: int = 512, rope_dim: int = 64, num_blocks: Optional[int] = None,
-                  scale: Optional[float] = None, seed: int = 0, name: str = "mla") -> DecodeCase:
+                  scale: Optional[float] = None, seed: int = 0, name: str = "mla",
+                  kv_format: Optional[str] = None) -> DecodeCase:
     """Build an absorbed-MLA decode problem: one shared (latent_dim + rope_dim)-wide KV head."""
     r_ctx, r_tab, r_q, r_k, _ = _streams(seed)
     if ctx_dist == "fixed":
@@ -203,45 +254,65 @@ def make_mla_case(*, batch: int, num_q_heads: int, dtype: str = BF16, page_size:
     tables = _tables_from_pool(pool, pages, max_blocks, None)
     width = latent_dim + rope_dim
     q = normal_16bit(r_q, (batch, num_q_heads, width), dtype)
-    kv = normal_16bit(r_k, (num_blocks, page_size, width), dtype)
+    kv_scale = 1.0
+    if kv_format is None:
+        kv = normal_16bit(r_k, (num_blocks, page_size, width), dtype)
+    elif kv_format == FP8_E4M3:
+        kv, kv_scale = normal_e4m3(r_k, (num_blocks, page_size, width))
+    else:
+        raise ValueError(kv_format)
     if scale is None:
         scale = 1.0 / math.sqrt(192.0)
     return DecodeCase(name=name, kind="mla", dtype=dtype, batch=batch, num_q_heads=num_q_heads,
                       num_kv_heads=1, head_dim_qk=width, head_dim_v=latent_dim,
                       page_size=page_size, num_blocks=int(num_blocks), scale=float(scale),
-                      context_lens=ctx, block_tables=tables, q=q, kv_cache=kv)
+                      context_lens=ctx, block_tables=tables, q=q, kv_cache=kv,
+                      kv_format=kv_format, k_scale=kv_scale, v_scale=kv_scale)
 
 
 # The five decode workloads (seed 0 everywhere).
 def workload(name: str, seed: int = 0) -> DecodeCase:
+    """The named workload; a ``_fp8`` suffix gives the same workload with E4M3 caches."""
+    fmt = None
+    base = name
+    if name.endswith("_fp8"):
+        fmt, base = FP8_E4M3, name[: -len("_fp8")]
+    case = _workload16(base, seed, fmt)
+    case.name = name
+    return case
+
+
+def _workload16(name: str, seed: int, kv_format: Optional[str]) -> DecodeCase:
     if name == "gqa_tiny":
         # B=4, Hq=8, Hkv=2, D=64, fp16, PAGE=16, ctx ~ U{1..256}, tables = one permutation of 64 blocks.
         return make_gqa_case(batch=4, num_q_heads=8, num_kv_heads=2, head_dim=64, dtype=FP16,
                              ctx_dist="uniform", ctx_low=1, ctx_high=256, num_blocks=64,
                              max_blocks_per_seq=16, table_layout="permutation",
-                             scale=1.0 / 8.0, seed=seed, name=name)
+                             scale=1.0 / 8.0, seed=seed, name=name, kv_format=kv_format)
     if name == "gqa_b64_ctx1k":
         return make_gqa_case(batch=64, num_q_heads=32, num_kv_heads=8, head_dim=128, dtype=FP16,
                              context_lens=[1024] * 64, table_layout="permutation",
-                             seed=seed, name=name)
+                             seed=seed, name=name, kv_format=kv_format)
     if name in ("gqa_b1_ctx32k", "gqa_b1_ctx32k_mqa"):
         hkv = 1 if name.endswith("mqa") else 8
         return make_gqa_case(batch=1, num_q_heads=32, num_kv_heads=hkv, head_dim=128, dtype=BF16,
                              context_lens=[32768], table_layout="permutation", seed=seed,
-                             name=name)
+                             name=name, kv_format=kv_format)
     if name == "gqa_varlen_b128":
         return make_gqa_case(batch=128, num_q_heads=64, num_kv_heads=8, head_dim=128, dtype=BF16,
                              ctx_dist="loguniform", ctx_low=16, ctx_high=32768,
-                             max_blocks_per_seq=2048, table_layout="pool", seed=seed, name=name)
+                             max_blocks_per_seq=2048, table_layout="pool", seed=seed, name=name, kv_format=kv_format)
     if name in ("mla_b16_ctx64k_h16", "mla_b16_ctx64k_h128",
-                "mla_r256_b16_ctx64k_h16", "mla_r256_b16_ctx64k_h128"):
+                "mla_r256_b16_ctx64k_h16", "mla_r256_b16_ctx64k_h128",
+             "gqa_b64_ctx1k_fp8", "gqa_b1_ctx32k_fp8"):
         hq = 16 if name.endswith("h16") else 128
         latent = 256 if "_r256_" in name else 512
         return make_mla_case(batch=16, num_q_heads=hq, dtype=BF16, context_lens=[65536] * 16,
-                             latent_dim=latent, seed=seed, name=name)
+                             latent_dim=latent, seed=seed, name=name, kv_format=kv_format)
     raise KeyError(name)
 
 
 WORKLOADS = ("gqa_tiny", "gqa_b64_ctx1k", "gqa_b1_ctx32k", "gqa_b1_ctx32k_mqa",
              "gqa_varlen_b128", "mla_b16_ctx64k_h16", "mla_b16_ctx64k_h128",
-             "mla_r256_b16_ctx64k_h16", "mla_r256_b16_ctx64k_h128")
+             "mla_r256_b16_ctx64k_h16", "mla_r256_b16_ctx64k_h128",
+             "gqa_b64_ctx1k_fp8", "gqa_b1_ctx32k_fp8")

@@ -24,6 +24,13 @@ PIN_CALLS = [
     pins.test_combine_weights_by_split_mass_and_skips_empty,
     pins.test_mla_equals_generic_with_one_kv_head,
     pins.test_mla_rope_only_needle_returns_latent_of_target,
+    pins.test_e4m3_closed_forms,
+    pins.test_e4m3_order_and_sign_symmetry,
+    pins.test_e4m3_matches_torch_float8_for_every_code,
+    lambda: pins.test_fp8_cache_matches_torch_float64_softmax(synth.BF16),
+    pins.test_fp8_scales_enter_as_score_and_value_factors,
+    pins.test_fp8_needle_returns_scaled_value_code,
+    pins.test_fp8_mla_equals_generic_with_one_kv_head,
 ]
 
 
@@ -65,10 +72,34 @@ def _combine_plain_mean(po, pl):
     return po[keep].mean(axis=0), pl[keep].max()
 
 
-def _mla_drops_rope(q, kv, tables, ctx, scale, page, dtype, head_dim_v=512, rows=None):
+def _mla_drops_rope(q, kv, tables, ctx, scale, page, dtype, head_dim_v=512, rows=None, **kw):
     q2 = q.copy()
     q2[..., head_dim_v:] = 0
-    return od.__dict__["_orig_mla"](q2, kv, tables, ctx, scale, page, dtype, head_dim_v, rows)
+    return od.__dict__["_orig_mla"](q2, kv, tables, ctx, scale, page, dtype, head_dim_v, rows,
+                                    **kw)
+
+
+def _e4m3_bias8(codes):
+    return od.__dict__["_orig_e4m3"](codes) / 2.0
+
+
+def _e4m3_no_subnormals(codes):
+    codes = np.asarray(codes, dtype=np.uint8)
+    out = od.__dict__["_orig_e4m3"](codes)
+    e = (codes >> 3) & 0xF
+    m = (codes & 7).astype(np.float64)
+    sign = np.where(codes & 0x80, -1.0, 1.0)
+    return np.where((e == 0) & (m > 0), sign * np.ldexp(1.0 + m / 8.0, -7), out)
+
+
+def _dequantize_no_scale(stored, dtype, kv_format=None, scale=1.0):
+    return od.__dict__["_orig_dequantize"](stored, dtype, kv_format, 1.0)
+
+
+def _paged_decode_swapped_scales(q, k, v, tables, ctx, scale, page, dtype, rows=None,
+                                 kv_format=None, k_scale=1.0, v_scale=1.0):
+    return od.__dict__["_orig_paged"](q, k, v, tables, ctx, scale, page, dtype, rows, kv_format,
+                                      v_scale, k_scale)
 
 
 MUTATIONS = {
@@ -80,6 +111,10 @@ MUTATIONS = {
     "interleaved head grouping": ("kv_head_of", _kv_head_interleaved),
     "splits averaged without weights": ("combine_splits", _combine_plain_mean),
     "MLA rope dims ignored": ("mla_decode", _mla_drops_rope),
+    "E4M3 exponent bias 8": ("decode_e4m3", _e4m3_bias8),
+    "E4M3 subnormals read as normals": ("decode_e4m3", _e4m3_no_subnormals),
+    "fp8 scales ignored": ("dequantize", _dequantize_no_scale),
+    "k_scale and v_scale swapped": ("paged_decode", _paged_decode_swapped_scales),
 }
 
 
@@ -89,6 +124,9 @@ def test_mutation_is_caught_by_a_pin(name, monkeypatch):
     monkeypatch.setitem(od.__dict__, "_orig_attend", od.attend)
     monkeypatch.setitem(od.__dict__, "_orig_token_locations", od.token_locations)
     monkeypatch.setitem(od.__dict__, "_orig_mla", od.mla_decode)
+    monkeypatch.setitem(od.__dict__, "_orig_e4m3", od.decode_e4m3)
+    monkeypatch.setitem(od.__dict__, "_orig_dequantize", od.dequantize)
+    monkeypatch.setitem(od.__dict__, "_orig_paged", od.paged_decode)
     monkeypatch.setattr(od, func, repl)
     monkeypatch.setattr(oracle, func, repl)
     caught = []

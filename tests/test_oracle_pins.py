@@ -26,6 +26,8 @@ def _small_case(dtype=synth.FP16, seed=3, batch=3, hq=8, hkv=2, d=64, ctx=(37, 1
 
 
 def _run(case, **kw):
+    if case.kv_format is not None:
+        kw = dict(kv_format=case.kv_format, k_scale=case.k_scale, v_scale=case.v_scale, **kw)
     return oracle.paged_decode(case.q, case.k_cache, case.v_cache, case.block_tables,
                                case.context_lens, case.scale, case.page_size, case.dtype, **kw)
 
@@ -227,8 +229,12 @@ def _torch_reference(case):
     lse = torch.empty(case.batch, case.num_q_heads, dtype=torch.float64)
     tdt = torch.float16 if case.dtype == synth.FP16 else torch.bfloat16
     q = torch.from_numpy(case.q.view(np.int16)).view(tdt).double()
-    k = torch.from_numpy(case.k_cache.view(np.int16)).view(tdt).double()
-    v = torch.from_numpy(case.v_cache.view(np.int16)).view(tdt).double()
+    if case.kv_format == synth.FP8_E4M3:      # torch's own float8 decoding, then the scales
+        k = torch.from_numpy(case.k_cache).view(torch.float8_e4m3fn).double() * case.k_scale
+        v = torch.from_numpy(case.v_cache).view(torch.float8_e4m3fn).double() * case.v_scale
+    else:
+        k = torch.from_numpy(case.k_cache.view(np.int16)).view(tdt).double()
+        v = torch.from_numpy(case.v_cache.view(np.int16)).view(tdt).double()
     kf = k.reshape(-1, case.num_kv_heads, case.head_dim_qk)
     vf = v.reshape(-1, case.num_kv_heads, case.head_dim_v)
     for b in range(case.batch):
@@ -338,3 +344,100 @@ def test_rank256_record_pins():
     """The same two pins on the kv_lora_rank 256 record (256 latent + 64 rope)."""
     test_mla_equals_generic_with_one_kv_head(latent=256)
     test_mla_rope_only_needle_returns_latent_of_target(latent=256)
+
+
+# ---------------------------------------------------------------- fp8 (E4M3) caches
+def test_e4m3_closed_forms():
+    """Values fixed by the E4M3 definition (bias 7, 3 mantissa bits, no infinities)."""
+    want = {0x00: 0.0, 0x38: 1.0, 0x40: 2.0, 0x3C: 1.5, 0x30: 0.5, 0x7E: 448.0, 0x77: 240.0,
+            0x08: 2.0 ** -6, 0x07: 7 * 2.0 ** -9, 0x01: 2.0 ** -9, 0x58: 16.0, 0xB8: -1.0,
+            0xFE: -448.0, 0x81: -(2.0 ** -9)}
+    got = oracle.decode_e4m3(np.array(list(want), dtype=np.uint8))
+    np.testing.assert_array_equal(got, np.array(list(want.values())))
+    assert math.copysign(1.0, oracle.decode_e4m3(np.array([0x80], np.uint8))[0]) == -1.0
+    assert np.isnan(oracle.decode_e4m3(np.array([0x7F, 0xFF], np.uint8))).all()
+
+
+def test_e4m3_order_and_sign_symmetry():
+    pos = oracle.decode_e4m3(np.arange(0x00, 0x7F, dtype=np.uint8))
+    assert np.all(np.diff(pos) > 0)                       # codes 0x00..0x7E increase strictly
+    neg = oracle.decode_e4m3(np.arange(0x80, 0xFF, dtype=np.uint8))
+    np.testing.assert_array_equal(neg, -pos)
+    # adjacent normal values differ by 2^(e-7)/8: a spacing that doubles every 8 codes
+    steps = np.diff(oracle.decode_e4m3(np.arange(0x08, 0x7F, dtype=np.uint8)))
+    for i, st in enumerate(steps):
+        assert st == 2.0 ** (((0x08 + i) >> 3) - 10)
+
+
+def test_e4m3_matches_torch_float8_for_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.decode_e4m3(codes)
+    lib = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(lib))
+    np.testing.assert_array_equal(ours[~np.isnan(ours)], lib[~np.isnan(lib)])
+
+
+def _fp8_case(seed=3, ctx=(37, 1, 50), hq=8, hkv=2, d=64, dtype=synth.BF16):
+    return synth.make_gqa_case(batch=len(ctx), num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                               dtype=dtype, context_lens=list(ctx), table_layout="permutation",
+                               num_blocks=24, max_blocks_per_seq=5, seed=seed,
+                               kv_format=synth.FP8_E4M3)
+
+
+@pytest.mark.parametrize("dtype", [synth.FP16, synth.BF16])
+def test_fp8_cache_matches_torch_float64_softmax(dtype):
+    case = _fp8_case(dtype=dtype, ctx=(37, 1, 80))
+    assert case.k_scale != 1.0 and case.v_scale != 1.0 and case.k_scale != case.v_scale
+    out, lse = _run(case)
+    ref_out, ref_lse = _torch_reference(case)
+    np.testing.assert_allclose(out, ref_out, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, rtol=0, atol=1e-12)
+
+
+def test_fp8_scales_enter_as_score_and_value_factors():
+    """k_scale multiplies every logit like the softmax scale does; v_scale multiplies the
+    output and leaves the LSE alone."""
+    case = _fp8_case(ctx=(37, 16, 50))
+    out, lse = _run(case)
+    kw = dict(kv_format=case.kv_format)
+    args = (case.q, case.k_cache, case.v_cache, case.block_tables, case.context_lens)
+    o2, l2 = oracle.paged_decode(*args, case.scale * 4.0, case.page_size, case.dtype,
+                                 k_scale=case.k_scale / 4.0, v_scale=case.v_scale, **kw)
+    np.testing.assert_allclose(o2, out, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l2, lse, rtol=0, atol=1e-12)
+    o3, l3 = oracle.paged_decode(*args, case.scale, case.page_size, case.dtype,
+                                 k_scale=case.k_scale, v_scale=case.v_scale * 3.0, **kw)
+    np.testing.assert_allclose(o3, 3.0 * out, rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(l3, lse)
+
+
+def test_fp8_needle_returns_scaled_value_code():
+    case = _fp8_case(ctx=(37, 20, 50))
+    case.q[:] = synth.float32_to_bits(np.float32(1.0), case.dtype)
+    case.k_scale, case.v_scale = 1.0, 0.25
+    for target in (0, 15, 16, 36):
+        k = np.zeros_like(case.k_cache)
+        blk = int(case.block_tables[0, target // 16])
+        k[blk, target % 16] = 0x58                     # 16.0
+        case.k_cache = k
+        out, lse = _run(case)
+        for h in range(case.num_q_heads):
+            codes = case.v_cache[blk, target % 16, h // case.group]
+            np.testing.assert_array_equal(out[0, h], 0.25 * oracle.decode_e4m3(codes))
+            assert lse[0, h] == pytest.approx(case.scale * 16 * case.head_dim_qk, abs=1e-9)
+
+
+def test_fp8_mla_equals_generic_with_one_kv_head():
+    case = synth.make_mla_case(batch=2, num_q_heads=4, dtype=synth.BF16, context_lens=[70, 129],
+                               seed=4, kv_format=synth.FP8_E4M3)
+    out, lse = oracle.mla_decode(case.q, case.kv_cache, case.block_tables, case.context_lens,
+                                 case.scale, case.page_size, case.dtype, kv_format=case.kv_format,
+                                 kv_scale=case.k_scale)
+    k = case.kv_cache[:, :, None, :]
+    v = case.kv_cache[:, :, None, :512]
+    out2, lse2 = oracle.paged_decode(case.q, k, v, case.block_tables, case.context_lens,
+                                     case.scale, case.page_size, case.dtype,
+                                     kv_format=case.kv_format, k_scale=case.k_scale,
+                                     v_scale=case.k_scale)
+    np.testing.assert_allclose(out, out2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse2, rtol=0, atol=1e-12)

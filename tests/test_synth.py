@@ -36,3 +36,19 @@ def test_pool_tables_cover_each_block_once():
     for b, n in enumerate(pages):
         assert (c.block_tables[b, n:] == synth.UNUSED_ENTRY).all()
     assert ((c.context_lens >= 16) & (c.context_lens <= 2000)).all()
+
+
+def test_e4m3_caches_are_seeded_and_use_the_full_code_range():
+    a = synth.workload("gqa_tiny_fp8")
+    b = synth.workload("gqa_tiny_fp8")
+    assert a.kv_format == synth.FP8_E4M3 and a.k_cache.dtype == np.uint8
+    np.testing.assert_array_equal(a.k_cache, b.k_cache)
+    assert a.k_scale == b.k_scale and a.v_scale == b.v_scale
+    # the largest draw maps to the largest finite code (0x7E / 0xFE); no NaN code appears
+    for codes in (a.k_cache, a.v_cache):
+        mags = codes & 0x7F
+        assert mags.max() == 0x7E and not np.any(mags == 0x7F)
+    # q, the tables and the context lengths are those of the 16-bit workload
+    c = synth.workload("gqa_tiny")
+    np.testing.assert_array_equal(a.q, c.q)
+    np.testing.assert_array_equal(a.block_tables, c.block_tables)
