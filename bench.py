@@ -160,10 +160,11 @@ class ClockSampler:
 def accounting(case):
     """Algorithmic bytes and FLOPs of one step (K+V of the attended tokens; 2 FLOP per MAC)."""
     ctx = case.context_lens.tolist()
+    elem = 1 if case.kv_format == synth.FP8_E4M3 else 2     # bytes per cached value
     if case.kind == "gqa":
-        kv = traffic.gqa_kv_bytes(ctx, case.num_kv_heads, case.head_dim_qk, 2)
+        kv = traffic.gqa_kv_bytes(ctx, case.num_kv_heads, case.head_dim_qk, elem)
     else:
-        kv = traffic.mla_kv_bytes(ctx, case.head_dim_qk, 2)
+        kv = traffic.mla_kv_bytes(ctx, case.head_dim_qk, elem)
     flops = traffic.decode_flops(ctx, case.num_q_heads, case.head_dim_qk, case.head_dim_v)
     return kv, flops
 
@@ -173,6 +174,8 @@ def workload_config(case, rotation_copies):
            "num_q_heads": case.num_q_heads, "num_kv_heads": case.num_kv_heads,
            "head_dim_qk": case.head_dim_qk, "head_dim_v": case.head_dim_v,
            "page_size": case.page_size, "dtype": case.dtype,
+           "kv_cache": ("fp8 e4m3, per-tensor scales" if case.kv_format == synth.FP8_E4M3
+                        else case.dtype),
            "context_lens": ("all " + str(int(case.context_lens[0]))
                             if (case.context_lens == case.context_lens[0]).all()
                             else f"varlen sum {int(case.context_lens.sum())}"),
@@ -191,17 +194,20 @@ def oracle_sample(case, budget_s: float):
     b = 0
     while True:
         rows = [(b, h) for h in range(case.num_q_heads)]
+        elem = 1 if case.kv_format == synth.FP8_E4M3 else 2
         if case.kind == "gqa":
             oracle.paged_decode(case.q, case.k_cache, case.v_cache, case.block_tables,
                                 case.context_lens, case.scale, case.page_size, case.dtype,
-                                rows=rows)
+                                rows=rows, kv_format=case.kv_format, k_scale=case.k_scale,
+                                v_scale=case.v_scale)
             done_bytes += traffic.gqa_kv_bytes([case.context_lens[b]], case.num_kv_heads,
-                                               case.head_dim_qk, 2)
+                                               case.head_dim_qk, elem)
         else:
             oracle.mla_decode(case.q, case.kv_cache, case.block_tables, case.context_lens,
                               case.scale, case.page_size, case.dtype,
-                              head_dim_v=case.head_dim_v, rows=rows)
-            done_bytes += traffic.mla_kv_bytes([case.context_lens[b]], case.head_dim_qk, 2)
+                              head_dim_v=case.head_dim_v, rows=rows, kv_format=case.kv_format,
+                              kv_scale=case.k_scale)
+            done_bytes += traffic.mla_kv_bytes([case.context_lens[b]], case.head_dim_qk, elem)
         b = (b + 1) % case.batch
         if time.perf_counter() - t0 >= budget_s:
             return done_bytes, time.perf_counter() - t0, b
@@ -301,13 +307,18 @@ def run_gpu(args, workload, rank, world, local_rank):
     def dev16(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(tdt)
 
+    fp8 = case.kv_format == synth.FP8_E4M3
+
+    def dev_cache(arr):
+        return torch.from_numpy(np.ascontiguousarray(arr)).cuda() if fp8 else dev16(arr)
+
     copies = max(1, min(64, math.ceil(4 * L2_BYTES / kv_bytes)))
     q = dev16(case.q)
     if case.kind == "gqa":
-        k0, v0 = dev16(case.k_cache), dev16(case.v_cache)
+        k0, v0 = dev_cache(case.k_cache), dev_cache(case.v_cache)
         caches = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(copies - 1)]
     else:
-        kv0 = dev16(case.kv_cache)
+        kv0 = dev_cache(case.kv_cache)
         caches = [(kv0, None)] + [(kv0.clone(), None) for _ in range(copies - 1)]
     tables = torch.from_numpy(case.block_tables).cuda()
     ctx = torch.from_numpy(case.context_lens).cuda()
@@ -319,14 +330,18 @@ def run_gpu(args, workload, rank, world, local_rank):
                     num_kv_heads=case.num_kv_heads, head_dim_qk=case.head_dim_qk,
                     head_dim_v=case.head_dim_v, page_size=case.page_size,
                     max_blocks_per_seq=case.max_blocks_per_seq, num_blocks=case.num_blocks,
-                    context_lens=case.context_lens.tolist())
+                    context_lens=case.context_lens.tolist(),
+                    kv_format=pda.PDA_KV_FP8_E4M3 if fp8 else pda.PDA_KV_SAME_AS_Q)
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     pda.workspace_init(plan, ws, stream)
 
     def step(i, q_=q, out_=out, lse_=lse, tables_=tables, ctx_=ctx):
         kc, vc = caches[i % copies]
-        if case.kind == "gqa":
+        if case.kind == "gqa" and fp8:
+            pda.paged_decode_attn_fp8(q_, kc, vc, case.k_scale, case.v_scale, tables_, ctx_,
+                                      case.scale, out_, lse_, plan, ws, stream)
+        elif case.kind == "gqa":
             pda.paged_decode_attn(q_, kc, vc, tables_, ctx_, case.scale, out_, lse_, plan, ws,
                                   stream)
         else:

@@ -63,6 +63,16 @@ typedef enum pda_status {
 typedef enum pda_dtype { PDA_FP16 = 0, PDA_BF16 = 1 } pda_dtype;
 typedef enum pda_kind { PDA_KIND_GQA = 0, PDA_KIND_MLA = 1 } pda_kind;
 
+/* Storage format of the caches ("Attention Kernel Variants: MQA, GQA, and MLA",
+ * KV-cache arithmetic table, fp8 row, and pitfall 5: an fp8 cache stores one byte
+ * per value and the kernel dequantizes its tiles before the attention arithmetic).
+ *   PDA_KV_SAME_AS_Q: the caches hold values of the problem's dtype.
+ *   PDA_KV_FP8_E4M3:  the caches hold one E4M3 byte per value (OCP 8-bit format:
+ *                     bias 7, 3 mantissa bits, no infinities, S.1111.111 = NaN);
+ *                     value = e4m3(code) * scale, one scale per tensor, passed to
+ *                     the *_fp8 decode calls. q, out and lse keep their types. */
+typedef enum pda_kv_format { PDA_KV_SAME_AS_Q = 0, PDA_KV_FP8_E4M3 = 1 } pda_kv_format;
+
 /* Shape of one decode problem. The plan keeps a copy. */
 typedef struct pda_problem {
   int32_t kind;               /* pda_kind */
@@ -77,6 +87,7 @@ typedef struct pda_problem {
   int64_t num_blocks;         /* physical blocks in the cache pool */
   int32_t num_sms;            /* SMs to plan for; 0 = query the current device */
   int32_t force_num_ctas;     /* 0 = automatic; > 0 = split the work over exactly this many CTAs */
+  int32_t kv_format;          /* pda_kv_format of the caches (0 = same type as q) */
 } pda_problem;
 
 typedef struct pda_plan pda_plan;  /* opaque, owned by the library */
@@ -150,6 +161,20 @@ PDA_API pda_status paged_decode_attn(const void* q, const void* k_cache, const v
                              const int32_t* block_tables, const int32_t* context_lens,
                              float scale, void* out, float* lse, const pda_plan* plan,
                              void* workspace, pda_stream_t stream);
+
+/*
+ * paged_decode_attn over fp8 caches (plan created with kv_format PDA_KV_FP8_E4M3).
+ *   k_cache, v_cache  device [num_blocks, P, Hkv, D] uint8 E4M3 codes, 16-byte aligned
+ *   k_scale, v_scale  per-tensor dequantization scales (finite): K_j = e4m3(k) * k_scale,
+ *                     V_j = e4m3(v) * v_scale
+ * Every other argument, and the result, as for paged_decode_attn (q, out in the plan's
+ * 16-bit dtype). A stale slot or an unused block may hold any code, NaN included.
+ */
+PDA_API pda_status paged_decode_attn_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                         float k_scale, float v_scale,
+                                         const int32_t* block_tables, const int32_t* context_lens,
+                                         float scale, void* out, float* lse, const pda_plan* plan,
+                                         void* workspace, pda_stream_t stream);
 
 /*
  * Absorbed MLA decode ("From MHA to MLA", section 6; FlashMLA-ETAP "Usage" and

@@ -66,26 +66,58 @@ extern "C" PDA_API pda_status pda_read_device_error(void* workspace, pda_stream_
   return PDA_OK;
 }
 
-extern "C" PDA_API pda_status paged_decode_attn(const void* q, const void* k_cache, const void* v_cache,
-                                        const int32_t* block_tables, const int32_t* context_lens,
-                                        float scale, void* out, float* lse, const pda_plan* plan,
-                                        void* workspace, pda_stream_t stream) {
-  pda::clear_error();
+namespace {
+
+pda_status gqa_call(const void* q, const void* k_cache, const void* v_cache, float k_scale,
+                    float v_scale, const int32_t* block_tables, const int32_t* context_lens,
+                    float scale, void* out, float* lse, const pda_plan* plan, void* workspace,
+                    pda_stream_t stream) {
   pda_status st = check_common(plan, PDA_KIND_GQA, q, block_tables, context_lens, scale, out,
                                workspace);
   if (st != PDA_OK || plan->prob.batch == 0) return st;
+  if (!std::isfinite(k_scale) || !std::isfinite(v_scale))
+    return fail(PDA_ERR_INVALID_ARG, "k_scale and v_scale must be finite");
   if (k_cache == nullptr || v_cache == nullptr)
     return fail(PDA_ERR_INVALID_ARG, "k_cache and v_cache must be non-NULL");
   if (!aligned(k_cache, 16) || !aligned(v_cache, 16))
     return fail(PDA_ERR_INVALID_ARG, "k_cache and v_cache must start on a 16-byte boundary");
   if (lse != nullptr && !aligned(lse, 4))
     return fail(PDA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
-  pda::GqaArgs args{q, k_cache, v_cache, block_tables, context_lens, scale, out, lse};
+  pda::GqaArgs args{q, k_cache, v_cache, block_tables, context_lens, scale, out, lse,
+                    k_scale, v_scale};
   const int e = pda::launch_gqa_decode(*plan, args, pda::workspace_views(*plan, workspace),
                                        stream);
   if (e == -1) return fail(PDA_ERR_INVALID_ARG, "could not build the TMA descriptor of a cache");
   if (e != 0) return cuda_fail(e, "GQA decode launch");
   return PDA_OK;
+}
+
+}  // namespace
+
+extern "C" PDA_API pda_status paged_decode_attn(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* block_tables, const int32_t* context_lens,
+                                        float scale, void* out, float* lse, const pda_plan* plan,
+                                        void* workspace, pda_stream_t stream) {
+  pda::clear_error();
+  if (plan != nullptr && plan->prob.kv_format != PDA_KV_SAME_AS_Q)
+    return fail(PDA_ERR_INVALID_ARG,
+                "the plan's caches are fp8: call paged_decode_attn_fp8 with their scales");
+  return gqa_call(q, k_cache, v_cache, 1.f, 1.f, block_tables, context_lens, scale, out, lse, plan,
+                  workspace, stream);
+}
+
+extern "C" PDA_API pda_status paged_decode_attn_fp8(const void* q, const void* k_cache,
+                                                    const void* v_cache, float k_scale,
+                                                    float v_scale, const int32_t* block_tables,
+                                                    const int32_t* context_lens, float scale,
+                                                    void* out, float* lse, const pda_plan* plan,
+                                                    void* workspace, pda_stream_t stream) {
+  pda::clear_error();
+  if (plan != nullptr && plan->prob.kv_format != PDA_KV_FP8_E4M3)
+    return fail(PDA_ERR_INVALID_ARG,
+                "the plan's caches are not fp8 (kv_format PDA_KV_FP8_E4M3): call paged_decode_attn");
+  return gqa_call(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale, out,
+                  lse, plan, workspace, stream);
 }
 
 extern "C" PDA_API pda_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_tables,

@@ -49,7 +49,10 @@ namespace {
 
 constexpr int kPage = 16;
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+// Two producer warps take the ring fills alternately: one warp's per-fill chain (barrier
+// wait, expect-tx, tensor-copy issue) took longer than the consumers needed per fill.
+constexpr int kProducerWarps = 2;
+constexpr int kThreads = (kConsumerWarps + kProducerWarps) * 32;
 // Ring stages: a multiple of the consumer warps, so stage s is only ever read by
 // the warps whose tiles are t = s (mod kConsumerWarps / NHT), each of which takes
 // every fill of that stage in order (the parity waits rely on this).
@@ -59,14 +62,13 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 #ifndef PDA_GQA_CTAS_PER_SM
 #define PDA_GQA_CTAS_PER_SM 2
 #endif
-#ifndef PDA_GQA_TMA_5D
-#define PDA_GQA_TMA_5D 1
+#ifndef PDA_GQA_STAGES_F8
+#define PDA_GQA_STAGES_F8 8
 #endif
-constexpr int kStages = PDA_GQA_STAGES;
+constexpr int kStages16 = PDA_GQA_STAGES;     // ring stages for 16-bit caches
+constexpr int kStagesF8 = PDA_GQA_STAGES_F8;  // ring stages for fp8 caches
 constexpr int kBoxBytes = kPage * 128;  // one TMA box: 16 tokens x 64 dims x 16 bit
 constexpr int kCtasPerSm = PDA_GQA_CTAS_PER_SM;
-
-static_assert(kStages % kConsumerWarps == 0, "each stage needs a fixed set of consumer warps");
 constexpr unsigned kFull = kFullMask;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -79,7 +81,8 @@ struct GqaParams {
   const int32_t* context_lens;
   int32_t batch, num_q_heads, num_kv_heads, group, max_blocks;
   int64_t num_blocks;
-  float scale_log2;
+  float scale_log2;     // softmax scale (times k_scale for fp8 caches) times log2(e)
+  float v_scale;        // fp8 caches: V dequantization scale (1 for 16-bit caches)
   int64_t total_tiles, tiles_per_cta;
   int32_t heavy_min;  // split segments with more pieces are merged by the split-merge kernel
   int32_t* err;
@@ -88,17 +91,35 @@ struct GqaParams {
   float* part_out;
 };
 
-template <int D>
+// F8: E4M3 caches. A (page, kvh) tile of one tensor is then 16 rows of D bytes (one
+// TMA box, 128-byte swizzle for D = 128, 64-byte for D = 64), half the bytes of the
+// 16-bit tile, and a ring stage holds two consecutive pages ([K A][V A][K B][V B]), so
+// a stage carries as many bytes as a 16-bit one and the per-stage costs (producer
+// issue, barrier waits, the softmax reductions) are paid once per two pages.
+template <int D, bool F8>
 struct Layout {
   static constexpr int kDBlocks = D / 64;
-  static constexpr int kStageBytes = 2 * kDBlocks * kBoxBytes;
+  static constexpr int kPPT = F8 ? 2 : 1;                  // pages per ring fill
+  static constexpr int kStages = F8 ? kStagesF8 : kStages16;
+  static constexpr int kTileBytes = F8 ? kPage * D : kDBlocks * kBoxBytes;  // page, tensor
+  static constexpr int kStageBytes = 2 * kPPT * kTileBytes;
   static constexpr int kMergeStride = D + 4;  // floats per head row; +4 spreads banks
   static constexpr int kMergeWarpFloats = 8 * kMergeStride + 16;
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kMergeBytes = kConsumerWarps * kMergeWarpFloats * 4;
   static constexpr int kBarBytes = 2 * kStages * 8 + 16;
   static constexpr int kSmemBytes = 1024 + kRingBytes + kMergeBytes + kBarBytes;
+  static_assert(kStages % kConsumerWarps == 0, "each stage needs a fixed set of consumer warps");
 };
+
+// Byte offset of 16-byte chunk `ch` of row `r` in a swizzled fp8 tile of 16 rows of D
+// bytes: the TMA 128-byte swizzle XORs address bits 4-6 with bits 7-9, the 64-byte
+// swizzle bits 4-5 with bits 7-8 (the ring stages are 1024-byte aligned).
+template <int D>
+__device__ __forceinline__ uint32_t f8_tile_offset(int r, int ch) {
+  if constexpr (D == 128) return uint32_t(r * 128 + ((ch ^ (r & 7)) << 4));
+  else return uint32_t(r * 64 + ((ch ^ ((r >> 1) & 3)) << 4));
+}
 
 template <typename T>
 __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
@@ -111,12 +132,13 @@ __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int D, typename T, int NHT>
+template <int D, typename T, int NHT, bool F8>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const GqaParams p) {
-  using L = Layout<D>;
-  constexpr int kDB = L::kDBlocks;
+  using L = Layout<D, F8>;
+  constexpr int kStages = L::kStages;
+  constexpr int kPPT = L::kPPT;
   constexpr int kWP = kConsumerWarps / NHT;  // consumer warps sharing one head subtile
   constexpr int kKS = D / 16;                // k-steps of S^T and m-tiles of O^T
 
@@ -151,8 +173,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   Walker walk;
   walker_init(walk, spec, g_lo, lane);
 
-  if (warp == kConsumerWarps) {
-    // ============================== producer warp ==============================
+  if (warp >= kConsumerWarps) {
+    // ============================== producer warps ==============================
+    // Both walk every fill of the CTA's range; producer pw issues the fills f with
+    // f = pw (mod kProducerWarps) and skips the others.
+    const int pw = warp - kConsumerWarps;
     if (lane == 0) {
       ptx::prefetch_tensormap(&tm_k);
       ptx::prefetch_tensormap(&tm_v);
@@ -160,7 +185,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const uint64_t policy = ptx::policy_evict_first();
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t filled = 0;  // bit s: stage s was filled at least once
+    uint32_t filled = 0;  // bit s: stage s was filled (by this warp) at least once
+    int fill = 0;         // CTA-local fill index
     bool ok = true;
     while (ok && walk.g < g_hi) {
       const Portion pt = walker_next(walk, spec, g_hi);
@@ -170,36 +196,49 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int32_t cur = next;
         if (base + 32 < pt.p1) next = (base + 32 + lane < pt.p1) ? __ldg(row + base + 32 + lane) : 0;
         const int n = min(32, pt.p1 - base);
-        for (int j = 0; j < n; ++j) {
+        // a fill takes kPPT consecutive pages; a batch starts kPPT-aligned within the
+        // portion (32 is a multiple of kPPT), so a fill never spans two batches
+        for (int j = 0; j < n; j += kPPT, ++fill) {
+          if (fill % kProducerWarps != pw) {
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1;
+            }
+            continue;
+          }
           const int32_t phys = __shfl_sync(kFull, cur, j);
+          const int32_t phys2 = __shfl_sync(kFull, cur, min(j + 1, 31));
+          const bool two = kPPT == 2 && j + 1 < n;
           int good = 1;
           if (lane == 0) {
             if (!wait_phase(&empty[stage], phase ^ 1, flags)) {
               good = 0;
             } else {
               // An id outside the pool is flagged; TMA fills such a tile with zeros.
-              if (phys < 0 || int64_t(phys) >= p.num_blocks) atomicOr(p.err, 1);
-              ptx::mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
-              uint8_t* st = ring + stage * L::kStageBytes;
-#if PDA_GQA_TMA_5D
-              // one copy per tensor: box (64 d, 16 slots, D/64 d-blocks) of one kvh
-              ptx::tma_load_5d(st, &tm_k, &full[stage], 0, 0, 0, pt.seg, phys, policy);
-              ptx::tma_load_5d(st + kDB * kBoxBytes, &tm_v, &full[stage], 0, 0, 0, pt.seg, phys,
-                               policy);
-#else
-#pragma unroll
-              for (int db = 0; db < kDB; ++db) {
-                ptx::tma_load_4d(st + db * kBoxBytes, &tm_k, &full[stage], db * 64, pt.seg, 0,
-                                 phys, policy);
-                ptx::tma_load_4d(st + (kDB + db) * kBoxBytes, &tm_v, &full[stage], db * 64,
-                                 pt.seg, 0, phys, policy);
-              }
-#endif
-              filled |= 1u << stage;
+              if (phys < 0 || int64_t(phys) >= p.num_blocks ||
+                  (two && (phys2 < 0 || int64_t(phys2) >= p.num_blocks)))
+                atomicOr(p.err, 1);
+              ptx::mbar_arrive_expect_tx(&full[stage],
+                                         two ? L::kStageBytes : 2 * L::kTileBytes);
             }
           }
           ok = __shfl_sync(kFull, good, 0) != 0;
           if (!ok) break;
+          // The fill's copies are issued by several lanes at once (one copy per lane; a
+          // single thread issuing them one after another was the producer's bottleneck):
+          // lane c copies tensor c & 1 (K, V) of page c >> 1 into [K A][V A][K B][V B].
+          // fp8: box (D bytes, 1 kvh, 16 slots, 1 block); 16-bit: box (64 d, 16 slots,
+          // D/64 d-blocks, 1 kvh, 1 block), landing as D/64 swizzled [16][64] sub-tiles.
+          if (lane < (two ? 4 : 2)) {
+            const CUtensorMap* map = (lane & 1) ? &tm_v : &tm_k;
+            uint8_t* dst = ring + stage * L::kStageBytes + lane * L::kTileBytes;
+            const int32_t ph = (lane >> 1) ? phys2 : phys;
+            if constexpr (F8)
+              ptx::tma_load_4d(dst, map, &full[stage], 0, pt.seg, 0, ph, policy);
+            else
+              ptx::tma_load_5d(dst, map, &full[stage], 0, 0, 0, pt.seg, ph, policy);
+          }
+          filled |= 1u << stage;
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
@@ -249,6 +288,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int npg = pt.p1 - pt.p0;
 
     // Q^T as the B operand (k = head dim, n = head): lane holds head hsub*8 + lane/4.
+    // fp8 caches: the K fragment of a lane holds 4 consecutive dims of a token (one
+    // 32-bit shared-memory word) as its k indices {cq, cq+1, cq+8, cq+9}; the dot
+    // product does not depend on the order of k, so q takes the same assignment:
+    // dims 16ks + 2cq, +1 as k = cq, cq+1 and dims 16ks + 2cq + 2, +3 as k = cq+8, cq+9.
     const int jq = hsub * 8 + r0;
     uint32_t qf[kKS][2];
     {
@@ -257,8 +300,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           qg + (int64_t(pt.b) * p.num_q_heads + int64_t(pt.seg) * p.group + (hv ? jq : 0)) * D);
 #pragma unroll
       for (int ks = 0; ks < kKS; ++ks) {
-        qf[ks][0] = hv ? __ldg(qrow + (ks * 16 + cq) / 2) : 0u;
-        qf[ks][1] = hv ? __ldg(qrow + (ks * 16 + 8 + cq) / 2) : 0u;
+        if constexpr (F8) {
+          qf[ks][0] = hv ? __ldg(qrow + (ks * 16 + 2 * cq) / 2) : 0u;
+          qf[ks][1] = hv ? __ldg(qrow + (ks * 16 + 2 * cq + 2) / 2) : 0u;
+        } else {
+          qf[ks][0] = hv ? __ldg(qrow + (ks * 16 + cq) / 2) : 0u;
+          qf[ks][1] = hv ? __ldg(qrow + (ks * 16 + 8 + cq) / 2) : 0u;
+        }
       }
     }
 
@@ -267,9 +315,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
     for (int mt = 0; mt < kKS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
 
-    // This warp's tiles are those with CTA-local index t = pres (mod kWP).
+    // This warp's ring fills are those with CTA-local index t = pres (mod kWP). A fill
+    // holds kPPT consecutive pages of the portion (two for fp8 caches, so a stage moves
+    // as many bytes as a 16-bit page).
+    const int nfill = (npg + kPPT - 1) / kPPT;
     const int first = int(((pres - k) % kWP + kWP) % kWP);
-    for (int i = first; i < npg; i += kWP) {
+    for (int i = first; i < nfill; i += kWP) {
       const int64_t t = k + i;
       const int stage = int(t % kStages);
       const uint32_t par = uint32_t(t / kStages) & 1u;
@@ -281,76 +332,189 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
       }
       if (aborted) continue;
-      const int valid = min(kPage, ctx - (pt.p0 + i) * kPage);
       const uint32_t kb = ring_s + stage * L::kStageBytes;
-      const uint32_t vb = kb + kDB * kBoxBytes;
+      if constexpr (F8) {
+        // ---- two pages A, B (B may be absent at a portion's end: then its slots are
+        // all stale, masked below exactly like the stale slots of a partial page)
+        const int pg0 = (pt.p0 + i * kPPT) * kPage;  // first token of page A
+        const int vld[2] = {min(kPage, ctx - pg0),
+                            (i * kPPT + 1 < npg) ? min(kPage, ctx - pg0 - kPage) : 0};
+        const uint32_t kpg[2] = {kb, kb + 2 * L::kTileBytes};
+        // S^T = K * Q^T for both pages: two independent accumulation chains. One
+        // ldmatrix.x4 covers two k-steps: matrices (tokens 0-7 | 8-15) x (chunk ks |
+        // ks+1) of 16 bytes; a lane gets 4 consecutive bytes (dims) of one token.
+        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int ks = 0; ks < kKS; ks += 2) {
+          uint32_t x[2][4];
+#pragma unroll
+          for (int hp = 0; hp < 2; ++hp)
+            ptx::ldsm_x4(kpg[hp] + f8_tile_offset<D>(tok_k, ks + chunk_k), x[hp][0], x[hp][1],
+                         x[hp][2], x[hp][3]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int hp = 0; hp < 2; ++hp) {
+              uint32_t a[4];
+              ptx::Mma<T>::from_e4m3x4(x[hp][2 * h], a[0], a[2]);       // token r0
+              ptx::Mma<T>::from_e4m3x4(x[hp][2 * h + 1], a[1], a[3]);   // token r0 + 8
+              ptx::Mma<T>::run(s[hp], a, qf[ks + h][0], qf[ks + h][1]);
+            }
+          }
+        }
+        float x[2][4];
+#pragma unroll
+        for (int hp = 0; hp < 2; ++hp) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[hp][e] = s[hp][e] * p.scale_log2;
+          if (vld[hp] < kPage) {
+            if (r0 >= vld[hp]) x[hp][0] = x[hp][1] = -INFINITY;
+            if (r0 + 8 >= vld[hp]) x[hp][2] = x[hp][3] = -INFINITY;
+          }
+        }
+        // online softmax down each head column over the 32 tokens (log2 domain)
+        float c0 = fmaxf(fmaxf(x[0][0], x[0][2]), fmaxf(x[1][0], x[1][2]));
+        float c1 = fmaxf(fmaxf(x[0][1], x[0][3]), fmaxf(x[1][1], x[1][3]));
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          c0 = fmaxf(c0, __shfl_xor_sync(kFull, c0, o));
+          c1 = fmaxf(c1, __shfl_xor_sync(kFull, c1, o));
+        }
+        const float mn0 = fmaxf(m0, c0), mn1 = fmaxf(m1, c1);
+        const float al0 = ptx::exp2_approx(m0 - mn0), al1 = ptx::exp2_approx(m1 - mn1);
+        float pp[2][4];
+#pragma unroll
+        for (int hp = 0; hp < 2; ++hp) {
+          pp[hp][0] = ptx::exp2_approx(x[hp][0] - mn0);
+          pp[hp][1] = ptx::exp2_approx(x[hp][1] - mn1);
+          pp[hp][2] = ptx::exp2_approx(x[hp][2] - mn0);
+          pp[hp][3] = ptx::exp2_approx(x[hp][3] - mn1);
+        }
+        l0 = l0 * al0 + ((pp[0][0] + pp[0][2]) + (pp[1][0] + pp[1][2]));
+        l1 = l1 * al1 + ((pp[0][1] + pp[0][3]) + (pp[1][1] + pp[1][3]));
+        m0 = mn0;
+        m1 = mn1;
+        if (__any_sync(kFull, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+          for (int mt = 0; mt < kKS; ++mt) {
+            acc[mt][0] *= al0;
+            acc[mt][1] *= al1;
+            acc[mt][2] *= al0;
+            acc[mt][3] *= al1;
+          }
+        }
+        // P^T as B operands (k = token, n = head) and the token masks of the V^T
+        // fragments (tokens cq, cq+1 and cq+8, cq+9 of each page)
+        uint32_t pb[2][2], vm_lo[2], vm_hi[2];
+#pragma unroll
+        for (int hp = 0; hp < 2; ++hp) {
+          pb[hp][0] = ptx::movmatrix_trans(ptx::Mma<T>::pack(pp[hp][0], pp[hp][1]));
+          pb[hp][1] = ptx::movmatrix_trans(ptx::Mma<T>::pack(pp[hp][2], pp[hp][3]));
+          const int v = vld[hp];
+          vm_lo[hp] = (cq < v ? 0x0000ffffu : 0u) | (cq + 1 < v ? 0xffff0000u : 0u);
+          vm_hi[hp] = (cq + 8 < v ? 0x0000ffffu : 0u) | (cq + 9 < v ? 0xffff0000u : 0u);
+        }
+        // O^T += V^T * P^T over both pages. ldmatrix.x4.trans over (tokens 0-7 | 8-15) x
+        // (chunk mt | mt+1), 16-bit elements = dim pairs: a lane gets dims 2*r0, 2*r0+1
+        // of tokens cq, cq+1. After a byte permute the pairs are (tokens cq, cq+1) of
+        // dim 2*r0 and of dim 2*r0+1, so row r0 of m-tile mt is dim 16mt + 2*r0 and row
+        // r0+8 is the next dim.
+        const uint32_t vpg[2] = {kb + L::kTileBytes, kb + 3 * L::kTileBytes};
+#pragma unroll
+        for (int mt = 0; mt < kKS; mt += 2) {
+          uint32_t y[2][4];
+#pragma unroll
+          for (int hp = 0; hp < 2; ++hp)
+            ptx::ldsm_x4_trans(vpg[hp] + f8_tile_offset<D>(tok_k, mt + chunk_k), y[hp][0],
+                               y[hp][1], y[hp][2], y[hp][3]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int hp = 0; hp < 2; ++hp) {
+              uint32_t a[4];
+              ptx::Mma<T>::from_e4m3x4(ptx::prmt(y[hp][2 * h], 0u, 0x3120u), a[0], a[1]);
+              ptx::Mma<T>::from_e4m3x4(ptx::prmt(y[hp][2 * h + 1], 0u, 0x3120u), a[2], a[3]);
+              a[0] &= vm_lo[hp];
+              a[1] &= vm_lo[hp];
+              a[2] &= vm_hi[hp];
+              a[3] &= vm_hi[hp];
+              ptx::Mma<T>::run(acc[mt + h], a, pb[hp][0], pb[hp][1]);
+            }
+          }
+        }
+      } else {
+        const int valid = min(kPage, ctx - (pt.p0 + i) * kPage);
+        const uint32_t vb = kb + L::kTileBytes;
 
-      // S^T = K * Q^T  (M = 16 tokens, N = 8 heads, K = D)
-      float s[4] = {0.f, 0.f, 0.f, 0.f};
+        // S^T = K * Q^T  (M = 16 tokens, N = 8 heads, K = D)
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int ks = 0; ks < kKS; ++ks) {
-        const int chunk = (ks & 3) * 2 + chunk_k;
-        const uint32_t addr = kb + (ks >> 2) * kBoxBytes + tok_k * 128 + ((chunk ^ (tok_k & 7)) << 4);
-        uint32_t a[4];
-        ptx::ldsm_x4(addr, a[0], a[1], a[2], a[3]);
-        ptx::Mma<T>::run(s, a, qf[ks][0], qf[ks][1]);
-      }
-      float x0 = s[0] * p.scale_log2, x1 = s[1] * p.scale_log2;
-      float x2 = s[2] * p.scale_log2, x3 = s[3] * p.scale_log2;
-      if (valid < kPage) {
-        if (r0 >= valid) x0 = x1 = -INFINITY;
-        if (r0 + 8 >= valid) x2 = x3 = -INFINITY;
-      }
-      // online softmax down each head column (log2 domain)
-      float c0 = fmaxf(x0, x2), c1 = fmaxf(x1, x3);
+        for (int ks = 0; ks < kKS; ++ks) {
+          const int chunk = (ks & 3) * 2 + chunk_k;
+          const uint32_t addr =
+              kb + (ks >> 2) * kBoxBytes + tok_k * 128 + ((chunk ^ (tok_k & 7)) << 4);
+          uint32_t a[4];
+          ptx::ldsm_x4(addr, a[0], a[1], a[2], a[3]);
+          ptx::Mma<T>::run(s, a, qf[ks][0], qf[ks][1]);
+        }
+        float x0 = s[0] * p.scale_log2, x1 = s[1] * p.scale_log2;
+        float x2 = s[2] * p.scale_log2, x3 = s[3] * p.scale_log2;
+        if (valid < kPage) {
+          if (r0 >= valid) x0 = x1 = -INFINITY;
+          if (r0 + 8 >= valid) x2 = x3 = -INFINITY;
+        }
+        // online softmax down each head column (log2 domain)
+        float c0 = fmaxf(x0, x2), c1 = fmaxf(x1, x3);
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        c0 = fmaxf(c0, __shfl_xor_sync(kFull, c0, o));
-        c1 = fmaxf(c1, __shfl_xor_sync(kFull, c1, o));
-      }
-      const float mn0 = fmaxf(m0, c0), mn1 = fmaxf(m1, c1);
-      const float al0 = ptx::exp2_approx(m0 - mn0), al1 = ptx::exp2_approx(m1 - mn1);
-      const float p0 = ptx::exp2_approx(x0 - mn0), p1 = ptx::exp2_approx(x1 - mn1);
-      const float p2 = ptx::exp2_approx(x2 - mn0), p3 = ptx::exp2_approx(x3 - mn1);
-      l0 = l0 * al0 + (p0 + p2);
-      l1 = l1 * al1 + (p1 + p3);
-      m0 = mn0;
-      m1 = mn1;
-      if (__any_sync(kFull, al0 != 1.f || al1 != 1.f)) {
+        for (int o = 4; o < 32; o <<= 1) {
+          c0 = fmaxf(c0, __shfl_xor_sync(kFull, c0, o));
+          c1 = fmaxf(c1, __shfl_xor_sync(kFull, c1, o));
+        }
+        const float mn0 = fmaxf(m0, c0), mn1 = fmaxf(m1, c1);
+        const float al0 = ptx::exp2_approx(m0 - mn0), al1 = ptx::exp2_approx(m1 - mn1);
+        const float p0 = ptx::exp2_approx(x0 - mn0), p1 = ptx::exp2_approx(x1 - mn1);
+        const float p2 = ptx::exp2_approx(x2 - mn0), p3 = ptx::exp2_approx(x3 - mn1);
+        l0 = l0 * al0 + (p0 + p2);
+        l1 = l1 * al1 + (p1 + p3);
+        m0 = mn0;
+        m1 = mn1;
+        if (__any_sync(kFull, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+          for (int mt = 0; mt < kKS; ++mt) {
+            acc[mt][0] *= al0;
+            acc[mt][1] *= al1;
+            acc[mt][2] *= al0;
+            acc[mt][3] *= al1;
+          }
+        }
+        // P^T as the B operand (k = token, n = head)
+        const uint32_t pb0 = ptx::movmatrix_trans(ptx::Mma<T>::pack(p0, p1));
+        const uint32_t pb1 = ptx::movmatrix_trans(ptx::Mma<T>::pack(p2, p3));
+        // token masks for the V^T fragments (tokens cq, cq+1 and cq+8, cq+9)
+        uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
+        if (valid < kPage) {
+          vm_lo = (cq < valid ? 0x0000ffffu : 0u) | (cq + 1 < valid ? 0xffff0000u : 0u);
+          vm_hi = (cq + 8 < valid ? 0x0000ffffu : 0u) | (cq + 9 < valid ? 0xffff0000u : 0u);
+        }
+        // O^T += V^T * P^T  (M = D in 16-row tiles, N = 8 heads, K = 16 tokens)
 #pragma unroll
         for (int mt = 0; mt < kKS; ++mt) {
-          acc[mt][0] *= al0;
-          acc[mt][1] *= al1;
-          acc[mt][2] *= al0;
-          acc[mt][3] *= al1;
+          const int chunk = (mt & 3) * 2 + chunk_v;
+          const uint32_t addr =
+              vb + (mt >> 2) * kBoxBytes + tok_v * 128 + ((chunk ^ (tok_v & 7)) << 4);
+          uint32_t a[4];
+          ptx::ldsm_x4_trans(addr, a[0], a[1], a[2], a[3]);
+          a[0] &= vm_lo;
+          a[1] &= vm_lo;
+          a[2] &= vm_hi;
+          a[3] &= vm_hi;
+          ptx::Mma<T>::run(acc[mt], a, pb0, pb1);
         }
-      }
-      // P^T as the B operand (k = token, n = head)
-      const uint32_t pb0 = ptx::movmatrix_trans(ptx::Mma<T>::pack(p0, p1));
-      const uint32_t pb1 = ptx::movmatrix_trans(ptx::Mma<T>::pack(p2, p3));
-      // token masks for the V^T fragments (tokens cq, cq+1 and cq+8, cq+9)
-      uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
-      if (valid < kPage) {
-        vm_lo = (cq < valid ? 0x0000ffffu : 0u) | (cq + 1 < valid ? 0xffff0000u : 0u);
-        vm_hi = (cq + 8 < valid ? 0x0000ffffu : 0u) | (cq + 9 < valid ? 0xffff0000u : 0u);
-      }
-      // O^T += V^T * P^T  (M = D in 16-row tiles, N = 8 heads, K = 16 tokens)
-#pragma unroll
-      for (int mt = 0; mt < kKS; ++mt) {
-        const int chunk = (mt & 3) * 2 + chunk_v;
-        const uint32_t addr = vb + (mt >> 2) * kBoxBytes + tok_v * 128 + ((chunk ^ (tok_v & 7)) << 4);
-        uint32_t a[4];
-        ptx::ldsm_x4_trans(addr, a[0], a[1], a[2], a[3]);
-        a[0] &= vm_lo;
-        a[1] &= vm_lo;
-        a[2] &= vm_hi;
-        a[3] &= vm_hi;
-        ptx::Mma<T>::run(acc[mt], a, pb0, pb1);
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&empty[stage]);
     }
-    k += npg;
+    k += nfill;
 
     // ---- this warp's state -> shared memory
 #pragma unroll
@@ -358,13 +522,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       l0 += __shfl_xor_sync(kFull, l0, o);
       l1 += __shfl_xor_sync(kFull, l1, o);
     }
+    // rows r0 and r0 + 8 of m-tile mt are dims 16mt + r0 and + 8 (16-bit caches) or
+    // 16mt + 2*r0 and + 1 (fp8 caches)
+    constexpr int kRowStep = F8 ? 1 : 8;
 #pragma unroll
     for (int mt = 0; mt < kKS; ++mt) {
-      const int d = mt * 16 + r0;
+      const int d = mt * 16 + (F8 ? 2 * r0 : r0);
       mw[cq * L::kMergeStride + d] = acc[mt][0];
       mw[(cq + 1) * L::kMergeStride + d] = acc[mt][1];
-      mw[cq * L::kMergeStride + d + 8] = acc[mt][2];
-      mw[(cq + 1) * L::kMergeStride + d + 8] = acc[mt][3];
+      mw[cq * L::kMergeStride + d + kRowStep] = acc[mt][2];
+      mw[(cq + 1) * L::kMergeStride + d + kRowStep] = acc[mt][3];
     }
     if (lane < 4) {
       mw[8 * L::kMergeStride + cq] = m0;
@@ -400,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         o[0] += a.x * f; o[1] += a.y * f; o[2] += a.z * f; o[3] += a.w * f;
         o[4] += b.x * f; o[5] += b.y * f; o[6] += b.z * f; o[7] += b.w * f;
       }
-      const float inv = 1.f / lsum;
+      const float inv = p.v_scale / lsum;
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] *= inv;
       const float lse_nat = (mx + log2f(lsum)) * kLn2;
@@ -507,63 +674,77 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Map over a paged cache [num_blocks, P, Hkv, D] (16-bit), 128-byte swizzle.
-// 5-D form: dims (d mod 64, slot, d / 64, kvh, block) with box (64, P, D/64, 1, 1), so
-// one copy lands a (block, kvh) tile as D/64 swizzled [P][64] sub-tiles.
-// 4-D form: dims (d, kvh, slot, block) with box (64, 1, P, 1), one copy per 64 dims.
+// Map over a paged cache [num_blocks, P, Hkv, D] (16-bit), 128-byte swizzle: dims
+// (d mod 64, slot, d / 64, kvh, block) with box (64, P, D/64, 1, 1), so one copy lands
+// a (block, kvh) tile as D/64 swizzled [P][64] sub-tiles.
 bool encode_cache_map(CUtensorMap* map, const void* base, int64_t num_blocks, int page, int hkv,
                       int d, bool bf16) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
-#if PDA_GQA_TMA_5D
-  {
-    const cuuint64_t dims[5] = {64, cuuint64_t(page), cuuint64_t(d / 64), cuuint64_t(hkv),
-                                cuuint64_t(num_blocks)};
-    const cuuint64_t strides[4] = {cuuint64_t(hkv) * d * 2, 128, cuuint64_t(d) * 2,
-                                   cuuint64_t(page) * hkv * d * 2};
-    const cuuint32_t box[5] = {64, cuuint32_t(page), cuuint32_t(d / 64), 1, 1};
-    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5,
-              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-  }
-#endif
-  const cuuint64_t dims[4] = {cuuint64_t(d), cuuint64_t(hkv), cuuint64_t(page),
+  const cuuint64_t dims[5] = {64, cuuint64_t(page), cuuint64_t(d / 64), cuuint64_t(hkv),
                               cuuint64_t(num_blocks)};
-  const cuuint64_t strides[3] = {cuuint64_t(d) * 2, cuuint64_t(hkv) * d * 2,
+  const cuuint64_t strides[4] = {cuuint64_t(hkv) * d * 2, 128, cuuint64_t(d) * 2,
                                  cuuint64_t(page) * hkv * d * 2};
-  const cuuint32_t box[4] = {64, 1, cuuint32_t(page), 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+  const cuuint32_t box[5] = {64, cuuint32_t(page), cuuint32_t(d / 64), 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5,
             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, typename T, int NHT>
+// Map over an E4M3 cache [num_blocks, P, Hkv, D] bytes: dims (d, kvh, slot, block),
+// box (D, 1, P, 1), so one copy lands a (block, kvh) tile as P rows of D bytes, with
+// 128-byte (D = 128) or 64-byte (D = 64) swizzle.
+bool encode_cache_map_f8(CUtensorMap* map, const void* base, int64_t num_blocks, int page,
+                         int hkv, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[4] = {cuuint64_t(d), cuuint64_t(hkv), cuuint64_t(page),
+                              cuuint64_t(num_blocks)};
+  const cuuint64_t strides[3] = {cuuint64_t(d), cuuint64_t(hkv) * d, cuuint64_t(page) * hkv * d};
+  const cuuint32_t box[4] = {cuuint32_t(d), 1, cuuint32_t(page), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, typename T, int NHT, bool F8>
 int launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const GqaParams& prm, int grid,
                cudaStream_t stream) {
-  auto kern = gqa_decode_kernel<D, T, NHT>;
+  auto kern = gqa_decode_kernel<D, T, NHT, F8>;
+  using L = Layout<D, F8>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    Layout<D>::kSmemBytes);
+                                    L::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  kern<<<grid, kThreads, Layout<D>::kSmemBytes, stream>>>(tk, tv, prm);
+  kern<<<grid, kThreads, L::kSmemBytes, stream>>>(tk, tv, prm);
   return cudaGetLastError();
 }
 
-template <int D, typename T>
+template <int D, typename T, bool F8>
 int launch_d(int nht, const CUtensorMap& tk, const CUtensorMap& tv, const GqaParams& prm, int grid,
              cudaStream_t s) {
   switch (nht) {
-    case 1: return launch_one<D, T, 1>(tk, tv, prm, grid, s);
-    case 2: return launch_one<D, T, 2>(tk, tv, prm, grid, s);
-    default: return launch_one<D, T, 4>(tk, tv, prm, grid, s);
+    case 1: return launch_one<D, T, 1, F8>(tk, tv, prm, grid, s);
+    case 2: return launch_one<D, T, 2, F8>(tk, tv, prm, grid, s);
+    default: return launch_one<D, T, 4, F8>(tk, tv, prm, grid, s);
   }
+}
+
+template <bool F8>
+int launch_dt(int d, bool bf16, int nht, const CUtensorMap& tk, const CUtensorMap& tv,
+              const GqaParams& prm, int grid, cudaStream_t s) {
+  if (d == 64)
+    return bf16 ? launch_d<64, __nv_bfloat16, F8>(nht, tk, tv, prm, grid, s)
+                : launch_d<64, __half, F8>(nht, tk, tv, prm, grid, s);
+  return bf16 ? launch_d<128, __nv_bfloat16, F8>(nht, tk, tv, prm, grid, s)
+              : launch_d<128, __half, F8>(nht, tk, tv, prm, grid, s);
 }
 
 }  // namespace
@@ -594,12 +775,18 @@ int gqa_ctas_per_sm(const pda_problem&) { return kCtasPerSm; }
 int launch_gqa_decode(const Plan& plan, const GqaArgs& a, const Workspace& ws, void* stream) {
   const pda_problem& pr = plan.prob;
   const bool bf16 = pr.dtype == PDA_BF16;
+  const bool f8 = pr.kv_format == PDA_KV_FP8_E4M3;
   CUtensorMap tk, tv;
-  if (!encode_cache_map(&tk, a.k_cache, pr.num_blocks, pr.page_size, pr.num_kv_heads,
-                        pr.head_dim_qk, bf16) ||
-      !encode_cache_map(&tv, a.v_cache, pr.num_blocks, pr.page_size, pr.num_kv_heads,
-                        pr.head_dim_v, bf16))
-    return -1;
+  const bool maps_ok =
+      f8 ? encode_cache_map_f8(&tk, a.k_cache, pr.num_blocks, pr.page_size, pr.num_kv_heads,
+                               pr.head_dim_qk) &&
+               encode_cache_map_f8(&tv, a.v_cache, pr.num_blocks, pr.page_size, pr.num_kv_heads,
+                                   pr.head_dim_v)
+         : encode_cache_map(&tk, a.k_cache, pr.num_blocks, pr.page_size, pr.num_kv_heads,
+                            pr.head_dim_qk, bf16) &&
+               encode_cache_map(&tv, a.v_cache, pr.num_blocks, pr.page_size, pr.num_kv_heads,
+                                pr.head_dim_v, bf16);
+  if (!maps_ok) return -1;
   GqaParams prm{};
   prm.q = a.q;
   prm.out = a.out;
@@ -612,7 +799,8 @@ int launch_gqa_decode(const Plan& plan, const GqaArgs& a, const Workspace& ws, v
   prm.group = plan.group;
   prm.max_blocks = pr.max_blocks_per_seq;
   prm.num_blocks = pr.num_blocks;
-  prm.scale_log2 = a.scale * kLog2e;
+  prm.scale_log2 = a.scale * a.k_scale * kLog2e;
+  prm.v_scale = a.v_scale;
   prm.total_tiles = plan.total_tiles;
   prm.tiles_per_cta = plan.tiles_per_cta;
   prm.heavy_min = plan.heavy_min_pieces;
@@ -622,13 +810,8 @@ int launch_gqa_decode(const Plan& plan, const GqaArgs& a, const Workspace& ws, v
   prm.part_out = ws.part_out;
   const int nht = plan.head_subtiles <= 1 ? 1 : (plan.head_subtiles <= 2 ? 2 : 4);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int e;
-  if (pr.head_dim_qk == 64)
-    e = bf16 ? launch_d<64, __nv_bfloat16>(nht, tk, tv, prm, plan.num_ctas, s)
-             : launch_d<64, __half>(nht, tk, tv, prm, plan.num_ctas, s);
-  else
-    e = bf16 ? launch_d<128, __nv_bfloat16>(nht, tk, tv, prm, plan.num_ctas, s)
-             : launch_d<128, __half>(nht, tk, tv, prm, plan.num_ctas, s);
+  const int e = f8 ? launch_dt<true>(pr.head_dim_qk, bf16, nht, tk, tv, prm, plan.num_ctas, s)
+                  : launch_dt<false>(pr.head_dim_qk, bf16, nht, tk, tv, prm, plan.num_ctas, s);
   if (e != 0) return e;
   return launch_split_merge(plan, ws, a.out, a.lse, stream);
 }

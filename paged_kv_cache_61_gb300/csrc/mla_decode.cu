@@ -724,6 +724,10 @@ int mla_heads_per_cta(const pda_problem& p) {
 int mla_ctas_per_sm(const pda_problem&) { return 1; }
 
 bool mla_supported(const pda_problem& p, std::string* why) {
+  if (p.kv_format != PDA_KV_SAME_AS_Q) {
+    *why = "MLA decode supports 16-bit caches (kv_format PDA_KV_SAME_AS_Q)";
+    return false;
+  }
   if (!((p.head_dim_qk == 576 && p.head_dim_v == 512) ||
         (p.head_dim_qk == 320 && p.head_dim_v == 256))) {
     *why = "MLA decode supports (head_dim_qk, head_dim_v) = (576, 512) or (320, 256)";

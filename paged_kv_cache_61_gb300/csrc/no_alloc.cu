@@ -50,6 +50,8 @@ extern "C" PDA_API pda_status paged_decode_attn_no_alloc(
   if (plan == nullptr) return pda::fail(PDA_ERR_INVALID_ARG, "plan is NULL");
   if (plan->prob.kind != PDA_KIND_GQA)
     return pda::fail(PDA_ERR_INVALID_ARG, "plan was created for the other kernel kind");
+  if (plan->prob.kv_format != PDA_KV_SAME_AS_Q)
+    return pda::fail(PDA_ERR_INVALID_ARG, "this call takes 16-bit caches (kv_format PDA_KV_SAME_AS_Q)");
   if (!std::isfinite(scale)) return pda::fail(PDA_ERR_INVALID_ARG, "scale must be finite");
   if (plan->prob.batch == 0) return PDA_OK;
   if (plan->ws_bytes > size_t(PDA_NO_ALLOC_WORKSPACE_BYTES))

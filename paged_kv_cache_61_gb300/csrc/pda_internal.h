@@ -75,6 +75,8 @@ struct GqaArgs {
   float scale;
   void* out;
   float* lse;
+  float k_scale = 1.f;   // fp8 caches: per-tensor dequantization scales
+  float v_scale = 1.f;
 };
 int launch_gqa_decode(const Plan& plan, const GqaArgs& args, const Workspace& ws, void* stream);
 

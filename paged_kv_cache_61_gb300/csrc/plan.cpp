@@ -81,6 +81,8 @@ extern "C" PDA_API pda_status pda_plan_create(pda_plan** out, const pda_problem*
     return fail(PDA_ERR_INVALID_ARG, "head dims must be >= 1");
   if (p.num_sms < 0 || p.force_num_ctas < 0)
     return fail(PDA_ERR_INVALID_ARG, "num_sms and force_num_ctas must be >= 0");
+  if (p.kv_format != PDA_KV_SAME_AS_Q && p.kv_format != PDA_KV_FP8_E4M3)
+    return fail(PDA_ERR_INVALID_ARG, "kv_format must be PDA_KV_SAME_AS_Q or PDA_KV_FP8_E4M3");
   if (p.batch > 0 && ctx_host == nullptr)
     return fail(PDA_ERR_INVALID_ARG, "context_lens_host is NULL");
 
@@ -145,6 +147,28 @@ extern "C" PDA_API pda_status pda_plan_create(pda_plan** out, const pda_problem*
       const int64_t max_ctas = plan->cluster == 2 ? int64_t(pda::mla_pair_units(num_sms))
                                                   : int64_t(num_sms) * ctas_per_sm;
       q = std::max(min_tiles_per_cta, pda::cdiv(plan->total_tiles, max_ctas));
+      // Uniform batches (every GQA segment has the same S pages): give each CTA whole
+      // segments, so no segment is split and no CTA pays the split-piece fence, counter
+      // and merge. 16-bit caches: the fewest segments per CTA that fit one wave, when
+      // that adds at most half again to a CTA's tiles (B=64, ctx 1K: 2 segments per
+      // CTA, 256 CTAs, 45.9 -> 42.7 us). fp8 caches, whose CTAs are bound by their own
+      // issue rate rather than by HBM: one segment per CTA, up to two waves, so a
+      // CTA's start and end overlap the other CTA on its SM (34.1 -> 29.2 us).
+      if (p.kind == PDA_KIND_GQA && p.batch > 0) {
+        const int64_t S = pda::cdiv(ctx_host[0], p.page_size);
+        bool uniform = true;
+        for (int32_t b = 1; b < p.batch && uniform; ++b)
+          uniform = pda::cdiv(ctx_host[b], p.page_size) == S;
+        const int64_t nseg = int64_t(p.batch) * plan->segs_per_seq;
+        if (uniform && S >= min_tiles_per_cta) {
+          if (p.kv_format == PDA_KV_FP8_E4M3) {
+            if (nseg >= max_ctas && nseg <= 2 * max_ctas) q = S;
+          } else {
+            const int64_t m = pda::cdiv(nseg, max_ctas);   // segments per CTA, one wave
+            if (m * S * 2 <= q * 3) q = m * S;
+          }
+        }
+      }
     }
     q = std::max(q, pda::cdiv(plan->total_tiles, pda::kMaxCtas));
     plan->tiles_per_cta = q;

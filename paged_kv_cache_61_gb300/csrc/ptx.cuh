@@ -160,6 +160,32 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   return y;
 }
 
+// Four E4M3 bytes -> two f16x2 registers, exactly (every E4M3 value is an fp16
+// value): bytes 0,1 -> lo (byte 0 in the low half), bytes 2,3 -> hi.
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(x));
+}
+
+// f16x2 -> bf16x2 through f32; exact for values that came from E4M3 (3 mantissa bits).
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t u) {
+  uint32_t d;
+  asm("{\n\t.reg .b16 l, h;\n\t.reg .f32 fl, fh;\n\tmov.b32 {l, h}, %1;\n\t"
+      "cvt.f32.f16 fl, l;\n\tcvt.f32.f16 fh, h;\n\tcvt.rn.bf16x2.f32 %0, fh, fl;\n\t}"
+      : "=r"(d)
+      : "r"(u));
+  return d;
+}
+
+// Byte permute: result byte i = byte sel[i] of {b, a} (a = bytes 0-3).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
 template <typename T>
 struct Mma;
 
@@ -178,6 +204,10 @@ struct Mma<__half> {
     return *reinterpret_cast<uint32_t*>(&h);
   }
   __device__ __forceinline__ static __half from_float(float x) { return __float2half_rn(x); }
+  // four E4M3 bytes -> two packed pairs of this type (bytes 0,1 -> lo; 2,3 -> hi)
+  __device__ __forceinline__ static void from_e4m3x4(uint32_t x, uint32_t& lo, uint32_t& hi) {
+    e4m3x4_to_f16x2(x, lo, hi);
+  }
 };
 
 template <>
@@ -196,6 +226,12 @@ struct Mma<__nv_bfloat16> {
   }
   __device__ __forceinline__ static __nv_bfloat16 from_float(float x) {
     return __float2bfloat16_rn(x);
+  }
+  __device__ __forceinline__ static void from_e4m3x4(uint32_t x, uint32_t& lo, uint32_t& hi) {
+    uint32_t l, h;
+    e4m3x4_to_f16x2(x, l, h);
+    lo = f16x2_to_bf16x2(l);
+    hi = f16x2_to_bf16x2(h);
   }
 };
 

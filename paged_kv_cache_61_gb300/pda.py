@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libpda.so")
 PDA_OK, PDA_ERR_INVALID_ARG, PDA_ERR_UNSUPPORTED, PDA_ERR_WORKSPACE, PDA_ERR_CUDA = range(5)
 PDA_FP16, PDA_BF16 = 0, 1
 PDA_KIND_GQA, PDA_KIND_MLA = 0, 1
+PDA_KV_SAME_AS_Q, PDA_KV_FP8_E4M3 = 0, 1
 
 _lib = None
 
@@ -33,7 +34,7 @@ class Problem(ctypes.Structure):
                 ("head_dim_qk", ctypes.c_int32), ("head_dim_v", ctypes.c_int32),
                 ("page_size", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
                 ("num_blocks", ctypes.c_int64), ("num_sms", ctypes.c_int32),
-                ("force_num_ctas", ctypes.c_int32)]
+                ("force_num_ctas", ctypes.c_int32), ("kv_format", ctypes.c_int32)]
 
 
 def _declare(lib):
@@ -47,6 +48,7 @@ def _declare(lib):
         "pda_workspace_init": (I32, [P, P, P]),
         "pda_read_device_error": (I32, [P, P, ctypes.POINTER(I32)]),
         "paged_decode_attn": (I32, [P, P, P, P, P, F32, P, P, P, P, P]),
+        "paged_decode_attn_fp8": (I32, [P, P, P, F32, F32, P, P, F32, P, P, P, P, P]),
         "mla_decode": (I32, [P, P, P, P, F32, P, P, P, P, P]),
         "pda_combine_splits": (I32, [P, P, I32, I32, I32, P, I32, P, P]),
         "paged_decode_attn_no_alloc": (I32, [P, P, P, P, P, F32, P, P, P, P]),
@@ -111,10 +113,10 @@ class Plan:
     def __init__(self, *, kind: int, dtype: int, batch: int, num_q_heads: int, num_kv_heads: int,
                  head_dim_qk: int, head_dim_v: int, page_size: int, max_blocks_per_seq: int,
                  num_blocks: int, context_lens: Sequence[int], num_sms: int = 0,
-                 force_num_ctas: int = 0):
+                 force_num_ctas: int = 0, kv_format: int = PDA_KV_SAME_AS_Q):
         self.problem = Problem(kind, dtype, batch, num_q_heads, num_kv_heads, head_dim_qk,
                                head_dim_v, page_size, max_blocks_per_seq, num_blocks, num_sms,
-                               force_num_ctas)
+                               force_num_ctas, kv_format)
         ctx = (ctypes.c_int32 * max(1, len(context_lens)))(*[int(c) for c in context_lens])
         handle = ctypes.c_void_p()
         _check(lib().pda_plan_create(ctypes.byref(handle), ctypes.byref(self.problem),
@@ -162,6 +164,17 @@ def paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, scale: fl
                                    _ptr(context_lens), float(scale), _ptr(out), _ptr(lse),
                                    plan.handle, _ptr(workspace), _stream(stream)),
            "paged_decode_attn")
+
+
+def paged_decode_attn_fp8(q, k_cache, v_cache, k_scale: float, v_scale: float, block_tables,
+                          context_lens, scale: float, out, lse, plan: Plan, workspace,
+                          stream=None):
+    """paged_decode_attn over E4M3 caches (uint8 codes) with per-tensor scales."""
+    _check(lib().paged_decode_attn_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), float(k_scale),
+                                       float(v_scale), _ptr(block_tables), _ptr(context_lens),
+                                       float(scale), _ptr(out), _ptr(lse), plan.handle,
+                                       _ptr(workspace), _stream(stream)),
+           "paged_decode_attn_fp8")
 
 
 def paged_decode_attn_no_alloc(q, k_cache, v_cache, block_tables, context_lens, scale: float,

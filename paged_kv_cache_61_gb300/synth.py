@@ -301,10 +301,10 @@ def _workload16(name: str, seed: int, kv_format: Optional[str]) -> DecodeCase:
     if name == "gqa_varlen_b128":
         return make_gqa_case(batch=128, num_q_heads=64, num_kv_heads=8, head_dim=128, dtype=BF16,
                              ctx_dist="loguniform", ctx_low=16, ctx_high=32768,
-                             max_blocks_per_seq=2048, table_layout="pool", seed=seed, name=name, kv_format=kv_format)
+                             max_blocks_per_seq=2048, table_layout="pool", seed=seed, name=name,
+                             kv_format=kv_format)
     if name in ("mla_b16_ctx64k_h16", "mla_b16_ctx64k_h128",
-                "mla_r256_b16_ctx64k_h16", "mla_r256_b16_ctx64k_h128",
-             "gqa_b64_ctx1k_fp8", "gqa_b1_ctx32k_fp8"):
+                "mla_r256_b16_ctx64k_h16", "mla_r256_b16_ctx64k_h128"):
         hq = 16 if name.endswith("h16") else 128
         latent = 256 if "_r256_" in name else 512
         return make_mla_case(batch=16, num_q_heads=hq, dtype=BF16, context_lens=[65536] * 16,
@@ -315,4 +315,5 @@ def _workload16(name: str, seed: int, kv_format: Optional[str]) -> DecodeCase:
 WORKLOADS = ("gqa_tiny", "gqa_b64_ctx1k", "gqa_b1_ctx32k", "gqa_b1_ctx32k_mqa",
              "gqa_varlen_b128", "mla_b16_ctx64k_h16", "mla_b16_ctx64k_h128",
              "mla_r256_b16_ctx64k_h16", "mla_r256_b16_ctx64k_h128",
-             "gqa_b64_ctx1k_fp8", "gqa_b1_ctx32k_fp8")
+             "gqa_b64_ctx1k_fp8", "gqa_b1_ctx32k_fp8", "gqa_b1_ctx32k_mqa_fp8",
+             "gqa_varlen_b128_fp8")

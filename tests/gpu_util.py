@@ -30,7 +30,16 @@ def make_plan(case: synth.DecodeCase, force_num_ctas: int = 0) -> pda.Plan:
                     num_kv_heads=case.num_kv_heads, head_dim_qk=case.head_dim_qk,
                     head_dim_v=case.head_dim_v, page_size=case.page_size,
                     max_blocks_per_seq=case.max_blocks_per_seq, num_blocks=case.num_blocks,
-                    context_lens=case.context_lens.tolist(), force_num_ctas=force_num_ctas)
+                    context_lens=case.context_lens.tolist(), force_num_ctas=force_num_ctas,
+                    kv_format=(pda.PDA_KV_FP8_E4M3 if case.kv_format == synth.FP8_E4M3
+                               else pda.PDA_KV_SAME_AS_Q))
+
+
+def to_device_cache(case: synth.DecodeCase, arr: np.ndarray) -> torch.Tensor:
+    """A cache array on the device: E4M3 codes as uint8, 16-bit patterns as fp16/bf16."""
+    if case.kv_format == synth.FP8_E4M3:
+        return torch.from_numpy(np.ascontiguousarray(arr, dtype=np.uint8)).cuda()
+    return to_device_16(arr, case.dtype)
 
 
 class DeviceCase:
@@ -40,10 +49,10 @@ class DeviceCase:
         self.case = case
         self.q = to_device_16(case.q, case.dtype)
         if case.kind == "gqa":
-            self.k = to_device_16(case.k_cache, case.dtype)
-            self.v = to_device_16(case.v_cache, case.dtype)
+            self.k = to_device_cache(case, case.k_cache)
+            self.v = to_device_cache(case, case.v_cache)
         else:
-            self.kv = to_device_16(case.kv_cache, case.dtype)
+            self.kv = to_device_cache(case, case.kv_cache)
         self.tables = torch.from_numpy(case.block_tables).cuda()
         self.ctx = torch.from_numpy(case.context_lens).cuda()
         self.out = torch.full((case.batch, case.num_q_heads, case.head_dim_v), float("nan"),
@@ -61,7 +70,10 @@ class DeviceCase:
         c = self.case
         out = self.out if out is None else out
         lse = self.lse if isinstance(lse, str) else lse
-        if c.kind == "gqa":
+        if c.kind == "gqa" and c.kv_format == synth.FP8_E4M3:
+            pda.paged_decode_attn_fp8(self.q, self.k, self.v, c.k_scale, c.v_scale, self.tables,
+                                      self.ctx, c.scale, out, lse, self.plan, self.ws)
+        elif c.kind == "gqa":
             pda.paged_decode_attn(self.q, self.k, self.v, self.tables, self.ctx, c.scale, out, lse,
                                   self.plan, self.ws)
         else:

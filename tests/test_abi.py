@@ -130,3 +130,38 @@ def test_combine_rejects_bad_sizes():
     with pytest.raises(pda.PdaError):
         pda.combine_splits(0, 0, 4, 2, 130, 0, pda.PDA_FP16, None, stream=0)
     pda.combine_splits(0, 0, 0, 2, 128, 0, pda.PDA_FP16, None, stream=0)  # rows == 0: no-op
+
+
+def test_fp8_plans_and_calls_must_agree():
+    f8 = _plan(kv_format=pda.PDA_KV_FP8_E4M3)
+    same = _plan()
+    args = (4096, 8192, 8192)
+    # a 16-bit call with an fp8 plan, and the other way round, are refused on the host
+    with pytest.raises(pda.PdaError) as e:
+        pda.paged_decode_attn(*args, 64, 128, 0.125, 4096, None, f8, 1 << 20, stream=0)
+    assert e.value.status == pda.PDA_ERR_INVALID_ARG
+    with pytest.raises(pda.PdaError) as e:
+        pda.paged_decode_attn_fp8(*args, 1.0, 1.0, 64, 128, 0.125, 4096, None, same, 1 << 20,
+                                  stream=0)
+    assert e.value.status == pda.PDA_ERR_INVALID_ARG
+    with pytest.raises(pda.PdaError) as e:
+        pda.paged_decode_attn_no_alloc(*args, 64, 128, 0.125, 4096, None, f8, stream=0)
+    assert e.value.status == pda.PDA_ERR_INVALID_ARG
+    for ks, vs in ((float("nan"), 1.0), (1.0, float("inf"))):
+        with pytest.raises(pda.PdaError) as e:
+            pda.paged_decode_attn_fp8(*args, ks, vs, 64, 128, 0.125, 4096, None, f8, 1 << 20,
+                                      stream=0)
+        assert e.value.status == pda.PDA_ERR_INVALID_ARG
+
+
+def test_fp8_plan_validation():
+    with pytest.raises(pda.PdaError) as e:
+        _plan(kv_format=5)
+    assert e.value.status == pda.PDA_ERR_INVALID_ARG
+    with pytest.raises(pda.PdaError) as e:     # MLA has no fp8 kernel
+        _plan(kind=pda.PDA_KIND_MLA, num_q_heads=16, num_kv_heads=1, head_dim_qk=576,
+              head_dim_v=512, page_size=64, max_blocks_per_seq=2, context_lens=[5, 64],
+              kv_format=pda.PDA_KV_FP8_E4M3)
+    assert e.value.status == pda.PDA_ERR_UNSUPPORTED
+    f8 = _plan(batch=0, context_lens=[], kv_format=pda.PDA_KV_FP8_E4M3)
+    pda.paged_decode_attn_fp8(0, 0, 0, 1.0, 1.0, 0, 0, 0.125, 0, None, f8, 0, stream=0)
