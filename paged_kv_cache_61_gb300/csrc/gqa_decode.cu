@@ -695,7 +695,10 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int64_t num_blocks, in
 
 // Map over an E4M3 cache [num_blocks, P, Hkv, D] bytes: dims (d, kvh, slot, block),
 // box (D, 1, P, 1), so one copy lands a (block, kvh) tile as P rows of D bytes, with
-// 128-byte (D = 128) or 64-byte (D = 64) swizzle.
+// 128-byte (D = 128) or 64-byte (D = 64) swizzle. L2 promotion stays at 128 bytes: a
+// row is at most 128 bytes, and a 256-byte promotion fetched the next KV head's row
+// too, which only other CTAs use, often after it has left L2 (varlen batch: 1.43x the
+// algorithmic DRAM bytes).
 bool encode_cache_map_f8(CUtensorMap* map, const void* base, int64_t num_blocks, int page,
                          int hkv, int d) {
   EncodeTiledFn fn = encode_fn();
@@ -708,7 +711,7 @@ bool encode_cache_map_f8(CUtensorMap* map, const void* base, int64_t num_blocks,
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int D, typename T, int NHT, bool F8>
