@@ -192,6 +192,61 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale, page_si
 
 
 # --------------------------------------------------------------------------------------
+# multi-token queries (speculative / MTP decoding): causal, bottom-right aligned
+# ("From MHA to MLA", section 2 kernel, its CAUSAL branch: with M query rows and N keys,
+# query row m sits at position N - M + m and sees keys n <= N - M + m; FlashMLA-ETAP
+# "Supported configurations" (any seq_len_q, causal masking for multi-token queries) and
+# "Usage" (q (B, s_q, Hq, D), o (B, s_q, Hq, Dv), lse (B, Hq, s_q))).
+# --------------------------------------------------------------------------------------
+def causal_prefix(ctx: int, seq_len_q: int, i: int) -> int:
+    """Number of cached tokens query i (of seq_len_q) attends: it sits at position
+    ctx - seq_len_q + i and sees tokens 0 .. ctx - seq_len_q + i."""
+    pos = int(ctx) - int(seq_len_q) + int(i)
+    if pos < 0:
+        raise ValueError("context length must be >= seq_len_q")
+    return pos + 1
+
+
+def paged_decode_mtp(q, k_cache, v_cache, block_tables, context_lens, scale, page_size, dtype,
+                     rows=None, kv_format=None, k_scale=1.0, v_scale=1.0):
+    """GQA/MQA/MHA decode of seq_len_q query tokens per sequence, causal bottom-right.
+
+    q [B, S, Hq, D] (16-bit bits); caches, tables, lengths and fp8 arguments as for
+    paged_decode. rows: optional (b, i, h) triples to evaluate (others left NaN).
+    Returns out [B, S, Hq, Dv] and lse [B, Hq, S], float64.
+    """
+    B, S, Hq, _ = q.shape
+    Hkv = k_cache.shape[2]
+    Dv = v_cache.shape[3]
+    out = np.full((B, S, Hq, Dv), np.nan)
+    lse = np.full((B, Hq, S), np.nan)
+    wanted = None if rows is None else {(int(b), int(i), int(h)) for b, i, h in rows}
+    for b in range(B):
+        ctx = int(context_lens[b])
+        if ctx < 1:
+            raise ValueError("context length must be >= 1")
+        for kvh in range(Hkv):
+            heads = [h for h in range(Hq) if kv_head_of(h, Hq, Hkv) == kvh]
+            todo = [(i, h) for i in range(S) for h in heads
+                    if wanted is None or (b, i, h) in wanted]
+            if not todo:
+                continue
+            keys = dequantize(gather_tokens(k_cache[:, :, kvh, :], block_tables[b], ctx, page_size),
+                              dtype, kv_format, k_scale)
+            vals = dequantize(gather_tokens(v_cache[:, :, kvh, :], block_tables[b], ctx, page_size),
+                              dtype, kv_format, v_scale)
+            for i in range(S):
+                hs = [h for (ii, h) in todo if ii == i]
+                if not hs:
+                    continue
+                n = causal_prefix(ctx, S, i)
+                o, l = attend(widen(q[b, i, hs, :], dtype), keys[:n], vals[:n], scale)
+                out[b, i, hs] = o
+                lse[b, hs, i] = l
+    return out, lse
+
+
+# --------------------------------------------------------------------------------------
 # absorbed MLA decode ("From MHA to MLA", section 6; FlashMLA-ETAP "Supported configurations")
 # --------------------------------------------------------------------------------------
 def mla_decode(q, kv_cache, block_tables, context_lens, scale, page_size, dtype,
@@ -251,3 +306,34 @@ def combine_splits(partial_out: np.ndarray, partial_lse: np.ndarray):
     denom = w.sum()
     out = (w[:, None] * po).sum(axis=0) / denom
     return out, mx + np.log(denom)
+
+
+def mla_decode_mtp(q, kv_cache, block_tables, context_lens, scale, page_size, dtype,
+                   head_dim_v=512, rows=None, kv_format=None, kv_scale=1.0):
+    """Absorbed-MLA decode of seq_len_q query tokens per sequence, causal bottom-right.
+
+    q [B, S, Hq, Dqk]; the rest as for mla_decode. rows: optional (b, i, h) triples.
+    Returns out [B, S, Hq, head_dim_v] and lse [B, Hq, S], float64.
+    """
+    B, S, Hq, Dqk = q.shape
+    out = np.full((B, S, Hq, head_dim_v), np.nan)
+    lse = np.full((B, Hq, S), np.nan)
+    wanted = None if rows is None else {(int(b), int(i), int(h)) for b, i, h in rows}
+    for b in range(B):
+        ctx = int(context_lens[b])
+        if ctx < 1:
+            raise ValueError("context length must be >= 1")
+        record = None
+        for i in range(S):
+            hs = [h for h in range(Hq) if wanted is None or (b, i, h) in wanted]
+            if not hs:
+                continue
+            if record is None:
+                record = dequantize(gather_tokens(kv_cache, block_tables[b], ctx, page_size),
+                                    dtype, kv_format, kv_scale)
+            n = causal_prefix(ctx, S, i)
+            o, l = attend(widen(q[b, i, hs, :], dtype), record[:n], record[:n, :head_dim_v],
+                          scale)
+            out[b, i, hs] = o
+            lse[b, hs, i] = l
+    return out, lse

@@ -108,7 +108,8 @@ def float32_to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
 class DecodeCase:
     """One decode-attention problem in host memory (16-bit values stored as uint16 bits;
     with ``kv_format == "e4m3"`` the caches hold uint8 E4M3 codes, dequantized as
-    code * k_scale (K, or the MLA record) and code * v_scale (V)).
+    code * k_scale (K, or the MLA record) and code * v_scale (V); with seq_len_q = S > 1
+    there are S query tokens per sequence and q is [B, S, Hq, Dqk]).
 
     GQA (``kind == "gqa"``):
       q            [B, Hq, D]
@@ -141,6 +142,7 @@ class DecodeCase:
     kv_format: Optional[str] = None
     k_scale: float = 1.0
     v_scale: float = 1.0
+    seq_len_q: int = 1        # query tokens per sequence; > 1: q is [B, S, Hq, Dqk]
 
     @property
     def max_blocks_per_seq(self) -> int:
@@ -173,7 +175,7 @@ def make_gqa_case(*, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: 
                   ctx_high: int = 256, ctx_dist: str = "fixed", num_blocks: Optional[int] = None,
                   max_blocks_per_seq: Optional[int] = None, scale: Optional[float] = None,
                   seed: int = 0, name: str = "gqa", table_layout: str = "pool",
-                  kv_format: Optional[str] = None) -> DecodeCase:
+                  kv_format: Optional[str] = None, seq_len_q: int = 1) -> DecodeCase:
     """Build a GQA/MQA/MHA decode problem.
 
     ctx_dist: "fixed" (``context_lens`` given), "uniform" (integers in
@@ -194,7 +196,7 @@ def make_gqa_case(*, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: 
         ctx = np.clip(np.floor(np.exp(u)), ctx_low, ctx_high)
     else:
         raise ValueError(ctx_dist)
-    ctx = ctx.astype(np.int32)
+    ctx = np.maximum(ctx, seq_len_q).astype(np.int32)    # every query token sees itself
     pages = (ctx.astype(np.int64) + page_size - 1) // page_size
     if max_blocks_per_seq is None:
         max_blocks_per_seq = int(max(1, pages.max(initial=1)))
@@ -212,7 +214,9 @@ def make_gqa_case(*, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: 
         tables = _tables_from_pool(pool, pages, max_blocks_per_seq, None)
     else:
         raise ValueError(table_layout)
-    q = normal_16bit(r_q, (batch, num_q_heads, head_dim), dtype)
+    q_shape = (batch, num_q_heads, head_dim) if seq_len_q == 1 else \
+        (batch, seq_len_q, num_q_heads, head_dim)
+    q = normal_16bit(r_q, q_shape, dtype)
     cache_shape = (num_blocks, page_size, num_kv_heads, head_dim)
     k_scale = v_scale = 1.0
     if kv_format is None:
@@ -229,14 +233,15 @@ def make_gqa_case(*, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: 
                       num_kv_heads=num_kv_heads, head_dim_qk=head_dim, head_dim_v=head_dim,
                       page_size=page_size, num_blocks=int(num_blocks), scale=float(scale),
                       context_lens=ctx, block_tables=tables, q=q, k_cache=k, v_cache=v,
-                      kv_format=kv_format, k_scale=k_scale, v_scale=v_scale)
+                      kv_format=kv_format, k_scale=k_scale, v_scale=v_scale,
+                      seq_len_q=seq_len_q)
 
 
 def make_mla_case(*, batch: int, num_q_heads: int, dtype: str = BF16, page_size: int = 64,
                   context_lens=None, ctx_low: int = 1, ctx_high: int = 4096, ctx_dist: str = "fixed",
                   latent_dim: int = 512, rope_dim: int = 64, num_blocks: Optional[int] = None,
                   scale: Optional[float] = None, seed: int = 0, name: str = "mla",
-                  kv_format: Optional[str] = None) -> DecodeCase:
+                  kv_format: Optional[str] = None, seq_len_q: int = 1) -> DecodeCase:
     """Build an absorbed-MLA decode problem: one shared (latent_dim + rope_dim)-wide KV head."""
     r_ctx, r_tab, r_q, r_k, _ = _streams(seed)
     if ctx_dist == "fixed":
@@ -245,7 +250,7 @@ def make_mla_case(*, batch: int, num_q_heads: int, dtype: str = BF16, page_size:
         ctx = r_ctx.integers(ctx_low, ctx_high, size=batch, endpoint=True)
     else:
         raise ValueError(ctx_dist)
-    ctx = ctx.astype(np.int32)
+    ctx = np.maximum(ctx, seq_len_q).astype(np.int32)    # every query token sees itself
     pages = (ctx.astype(np.int64) + page_size - 1) // page_size
     max_blocks = int(max(1, pages.max(initial=1)))
     if num_blocks is None:
@@ -253,7 +258,9 @@ def make_mla_case(*, batch: int, num_q_heads: int, dtype: str = BF16, page_size:
     pool = r_tab.permutation(num_blocks).astype(np.int32)
     tables = _tables_from_pool(pool, pages, max_blocks, None)
     width = latent_dim + rope_dim
-    q = normal_16bit(r_q, (batch, num_q_heads, width), dtype)
+    q_shape = (batch, num_q_heads, width) if seq_len_q == 1 else \
+        (batch, seq_len_q, num_q_heads, width)
+    q = normal_16bit(r_q, q_shape, dtype)
     kv_scale = 1.0
     if kv_format is None:
         kv = normal_16bit(r_k, (num_blocks, page_size, width), dtype)
@@ -267,48 +274,52 @@ def make_mla_case(*, batch: int, num_q_heads: int, dtype: str = BF16, page_size:
                       num_kv_heads=1, head_dim_qk=width, head_dim_v=latent_dim,
                       page_size=page_size, num_blocks=int(num_blocks), scale=float(scale),
                       context_lens=ctx, block_tables=tables, q=q, kv_cache=kv,
-                      kv_format=kv_format, k_scale=kv_scale, v_scale=kv_scale)
+                      kv_format=kv_format, k_scale=kv_scale, v_scale=kv_scale,
+                      seq_len_q=seq_len_q)
 
 
 # The five decode workloads (seed 0 everywhere).
 def workload(name: str, seed: int = 0) -> DecodeCase:
-    """The named workload; a ``_fp8`` suffix gives the same workload with E4M3 caches."""
-    fmt = None
+    """The named workload. Suffixes: ``_fp8`` gives the same workload with E4M3 caches,
+    ``_mtp2`` two query tokens per sequence (causal, bottom-right aligned)."""
+    fmt, sq = None, 1
     base = name
-    if name.endswith("_fp8"):
-        fmt, base = FP8_E4M3, name[: -len("_fp8")]
-    case = _workload16(base, seed, fmt)
+    if base.endswith("_fp8"):
+        fmt, base = FP8_E4M3, base[: -len("_fp8")]
+    if base.endswith("_mtp2"):
+        sq, base = 2, base[: -len("_mtp2")]
+    case = _workload16(base, seed, fmt, sq)
     case.name = name
     return case
 
 
-def _workload16(name: str, seed: int, kv_format: Optional[str]) -> DecodeCase:
+def _workload16(name: str, seed: int, kv_format: Optional[str], seq_len_q: int) -> DecodeCase:
     if name == "gqa_tiny":
         # B=4, Hq=8, Hkv=2, D=64, fp16, PAGE=16, ctx ~ U{1..256}, tables = one permutation of 64 blocks.
         return make_gqa_case(batch=4, num_q_heads=8, num_kv_heads=2, head_dim=64, dtype=FP16,
                              ctx_dist="uniform", ctx_low=1, ctx_high=256, num_blocks=64,
                              max_blocks_per_seq=16, table_layout="permutation",
-                             scale=1.0 / 8.0, seed=seed, name=name, kv_format=kv_format)
+                             scale=1.0 / 8.0, seed=seed, name=name, kv_format=kv_format, seq_len_q=seq_len_q)
     if name == "gqa_b64_ctx1k":
         return make_gqa_case(batch=64, num_q_heads=32, num_kv_heads=8, head_dim=128, dtype=FP16,
                              context_lens=[1024] * 64, table_layout="permutation",
-                             seed=seed, name=name, kv_format=kv_format)
+                             seed=seed, name=name, kv_format=kv_format, seq_len_q=seq_len_q)
     if name in ("gqa_b1_ctx32k", "gqa_b1_ctx32k_mqa"):
         hkv = 1 if name.endswith("mqa") else 8
         return make_gqa_case(batch=1, num_q_heads=32, num_kv_heads=hkv, head_dim=128, dtype=BF16,
                              context_lens=[32768], table_layout="permutation", seed=seed,
-                             name=name, kv_format=kv_format)
+                             name=name, kv_format=kv_format, seq_len_q=seq_len_q)
     if name == "gqa_varlen_b128":
         return make_gqa_case(batch=128, num_q_heads=64, num_kv_heads=8, head_dim=128, dtype=BF16,
                              ctx_dist="loguniform", ctx_low=16, ctx_high=32768,
                              max_blocks_per_seq=2048, table_layout="pool", seed=seed, name=name,
-                             kv_format=kv_format)
+                             kv_format=kv_format, seq_len_q=seq_len_q)
     if name in ("mla_b16_ctx64k_h16", "mla_b16_ctx64k_h128",
                 "mla_r256_b16_ctx64k_h16", "mla_r256_b16_ctx64k_h128"):
         hq = 16 if name.endswith("h16") else 128
         latent = 256 if "_r256_" in name else 512
         return make_mla_case(batch=16, num_q_heads=hq, dtype=BF16, context_lens=[65536] * 16,
-                             latent_dim=latent, seed=seed, name=name, kv_format=kv_format)
+                             latent_dim=latent, seed=seed, name=name, kv_format=kv_format, seq_len_q=seq_len_q)
     raise KeyError(name)
 
 
@@ -316,4 +327,5 @@ WORKLOADS = ("gqa_tiny", "gqa_b64_ctx1k", "gqa_b1_ctx32k", "gqa_b1_ctx32k_mqa",
              "gqa_varlen_b128", "mla_b16_ctx64k_h16", "mla_b16_ctx64k_h128",
              "mla_r256_b16_ctx64k_h16", "mla_r256_b16_ctx64k_h128",
              "gqa_b64_ctx1k_fp8", "gqa_b1_ctx32k_fp8", "gqa_b1_ctx32k_mqa_fp8",
-             "gqa_varlen_b128_fp8")
+             "gqa_varlen_b128_fp8", "gqa_b64_ctx1k_mtp2", "gqa_b1_ctx32k_mtp2",
+             "mla_b16_ctx64k_h16_mtp2")

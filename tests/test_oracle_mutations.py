@@ -31,6 +31,11 @@ PIN_CALLS = [
     pins.test_fp8_scales_enter_as_score_and_value_factors,
     pins.test_fp8_needle_returns_scaled_value_code,
     pins.test_fp8_mla_equals_generic_with_one_kv_head,
+    pins.test_mtp_causal_prefix_is_bottom_right,
+    pins.test_mtp_one_token_is_single_token_decode,
+    pins.test_mtp_row_i_is_single_token_decode_over_its_prefix,
+    lambda: pins.test_mtp_matches_torch_sdpa_lower_right_causal(None),
+    pins.test_mtp_mla_equals_generic_with_one_kv_head,
 ]
 
 
@@ -102,6 +107,18 @@ def _paged_decode_swapped_scales(q, k, v, tables, ctx, scale, page, dtype, rows=
                                       v_scale, k_scale)
 
 
+def _causal_top_left(ctx, seq_len_q, i):
+    return int(i) + 1
+
+
+def _causal_ignored(ctx, seq_len_q, i):
+    return int(ctx)
+
+
+def _causal_off_by_one(ctx, seq_len_q, i):
+    return max(1, int(ctx) - int(seq_len_q) + int(i))
+
+
 MUTATIONS = {
     "lse in log2": ("attend", _attend_log2),
     "scale dropped": ("attend", _attend_no_scale),
@@ -115,6 +132,9 @@ MUTATIONS = {
     "E4M3 subnormals read as normals": ("decode_e4m3", _e4m3_no_subnormals),
     "fp8 scales ignored": ("dequantize", _dequantize_no_scale),
     "k_scale and v_scale swapped": ("paged_decode", _paged_decode_swapped_scales),
+    "causal mask aligned top-left": ("causal_prefix", _causal_top_left),
+    "causal mask ignored": ("causal_prefix", _causal_ignored),
+    "causal limit excludes the query's own token": ("causal_prefix", _causal_off_by_one),
 }
 
 

@@ -441,3 +441,97 @@ def test_fp8_mla_equals_generic_with_one_kv_head():
                                      v_scale=case.k_scale)
     np.testing.assert_allclose(out, out2, rtol=0, atol=1e-12)
     np.testing.assert_allclose(lse, lse2, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- multi-token queries
+def _mtp_case(s=2, ctx=(37, 2, 50), hq=8, hkv=2, d=64, dtype=synth.FP16, seed=6, fmt=None):
+    return synth.make_gqa_case(batch=len(ctx), num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                               dtype=dtype, context_lens=list(ctx), table_layout="permutation",
+                               num_blocks=24, max_blocks_per_seq=5, seed=seed, seq_len_q=s,
+                               kv_format=fmt)
+
+
+def _run_mtp(case, **kw):
+    return oracle.paged_decode_mtp(case.q, case.k_cache, case.v_cache, case.block_tables,
+                                   case.context_lens, case.scale, case.page_size, case.dtype,
+                                   kv_format=case.kv_format, k_scale=case.k_scale,
+                                   v_scale=case.v_scale, **kw)
+
+
+def test_mtp_causal_prefix_is_bottom_right():
+    # query i of S sits at position ctx - S + i: the last query sees the whole context
+    assert [oracle.causal_prefix(10, 3, i) for i in range(3)] == [8, 9, 10]
+    assert oracle.causal_prefix(2, 2, 0) == 1
+    with pytest.raises(ValueError):
+        oracle.causal_prefix(1, 2, 0)
+
+
+def test_mtp_one_token_is_single_token_decode():
+    case = _mtp_case(s=1)
+    single = synth.DecodeCase(**{**case.__dict__})
+    single.q = case.q
+    out, lse = _run(single)
+    case.q = case.q[:, None]
+    out1, lse1 = _run_mtp(case)
+    np.testing.assert_array_equal(out1[:, 0], out)
+    np.testing.assert_array_equal(lse1[:, :, 0], lse)
+
+
+def test_mtp_row_i_is_single_token_decode_over_its_prefix():
+    case = _mtp_case(s=3, ctx=(37, 3, 50))
+    out, lse = _run_mtp(case)
+    for i in range(3):
+        pre = synth.DecodeCase(**{**case.__dict__})
+        pre.q = np.ascontiguousarray(case.q[:, i])
+        pre.context_lens = (case.context_lens - 3 + 1 + i).astype(np.int32)
+        o, l = _run(pre)
+        np.testing.assert_allclose(out[:, i], o, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[:, :, i], l, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("fmt", [None, synth.FP8_E4M3])
+def test_mtp_matches_torch_sdpa_lower_right_causal(fmt):
+    from torch.nn.attention.bias import causal_lower_right
+    case = _mtp_case(s=2, ctx=(37, 2, 80), fmt=fmt)
+    out, lse = _run_mtp(case)
+    P, S, G = case.page_size, case.seq_len_q, case.group
+    tdt = torch.float16 if case.dtype == synth.FP16 else torch.bfloat16
+    q = torch.from_numpy(case.q.view(np.int16)).view(tdt).double()
+    if fmt == synth.FP8_E4M3:
+        k = torch.from_numpy(case.k_cache).view(torch.float8_e4m3fn).double() * case.k_scale
+        v = torch.from_numpy(case.v_cache).view(torch.float8_e4m3fn).double() * case.v_scale
+    else:
+        k = torch.from_numpy(case.k_cache.view(np.int16)).view(tdt).double()
+        v = torch.from_numpy(case.v_cache.view(np.int16)).view(tdt).double()
+    kf = k.reshape(-1, case.num_kv_heads, case.head_dim_qk)
+    vf = v.reshape(-1, case.num_kv_heads, case.head_dim_v)
+    for b in range(case.batch):
+        n = int(case.context_lens[b])
+        idx = torch.arange(n)
+        rowidx = torch.from_numpy(case.block_tables[b].astype(np.int64))[idx // P] * P + idx % P
+        kk = kf[rowidx].permute(1, 0, 2)[:, None]             # [Hkv, 1, n, D]
+        vv = vf[rowidx].permute(1, 0, 2)[:, None]
+        qq = q[b].permute(1, 0, 2).reshape(case.num_kv_heads, G, S, -1)   # [Hkv, G, S, D]
+        bias = causal_lower_right(S, n)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qq, kk.expand(-1, G, -1, -1), vv.expand(-1, G, -1, -1), attn_mask=bias,
+            scale=case.scale)
+        logits = case.scale * (qq @ kk.expand(-1, G, -1, -1).transpose(-1, -2))
+        logits = logits.masked_fill(~bias._materialize(), float("-inf"))
+        l = torch.logsumexp(logits, dim=-1)                      # [Hkv, G, S]
+        np.testing.assert_allclose(out[b], o.reshape(case.num_q_heads, S, -1).permute(1, 0, 2),
+                                   rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[b], l.reshape(case.num_q_heads, S), rtol=0, atol=1e-12)
+
+
+def test_mtp_mla_equals_generic_with_one_kv_head():
+    case = synth.make_mla_case(batch=2, num_q_heads=4, dtype=synth.BF16, context_lens=[70, 2],
+                               seed=4, seq_len_q=2)
+    out, lse = oracle.mla_decode_mtp(case.q, case.kv_cache, case.block_tables,
+                                     case.context_lens, case.scale, case.page_size, case.dtype)
+    k = case.kv_cache[:, :, None, :]
+    v = case.kv_cache[:, :, None, :512]
+    out2, lse2 = oracle.paged_decode_mtp(case.q, k, v, case.block_tables, case.context_lens,
+                                         case.scale, case.page_size, case.dtype)
+    np.testing.assert_allclose(out, out2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse2, rtol=0, atol=1e-12)
