@@ -196,7 +196,9 @@ def make_gqa_case(*, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: 
         ctx = np.clip(np.floor(np.exp(u)), ctx_low, ctx_high)
     else:
         raise ValueError(ctx_dist)
-    ctx = np.maximum(ctx, seq_len_q).astype(np.int32)    # every query token sees itself
+    if seq_len_q > 1:
+        ctx = np.maximum(ctx, seq_len_q)                   # every query token sees itself
+    ctx = ctx.astype(np.int32)
     pages = (ctx.astype(np.int64) + page_size - 1) // page_size
     if max_blocks_per_seq is None:
         max_blocks_per_seq = int(max(1, pages.max(initial=1)))
@@ -250,7 +252,9 @@ def make_mla_case(*, batch: int, num_q_heads: int, dtype: str = BF16, page_size:
         ctx = r_ctx.integers(ctx_low, ctx_high, size=batch, endpoint=True)
     else:
         raise ValueError(ctx_dist)
-    ctx = np.maximum(ctx, seq_len_q).astype(np.int32)    # every query token sees itself
+    if seq_len_q > 1:
+        ctx = np.maximum(ctx, seq_len_q)                   # every query token sees itself
+    ctx = ctx.astype(np.int32)
     pages = (ctx.astype(np.int64) + page_size - 1) // page_size
     max_blocks = int(max(1, pages.max(initial=1)))
     if num_blocks is None:
