@@ -165,7 +165,12 @@ def accounting(case):
         kv = traffic.gqa_kv_bytes(ctx, case.num_kv_heads, case.head_dim_qk, elem)
     else:
         kv = traffic.mla_kv_bytes(ctx, case.head_dim_qk, elem)
-    flops = traffic.decode_flops(ctx, case.num_q_heads, case.head_dim_qk, case.head_dim_v)
+    S = case.seq_len_q
+    if S == 1:
+        flops = traffic.decode_flops(ctx, case.num_q_heads, case.head_dim_qk, case.head_dim_v)
+    else:   # query token i attends the first c - S + 1 + i tokens (causal, bottom-right)
+        seen = [c - S + 1 + i for c in ctx for i in range(S)]
+        flops = traffic.decode_flops(seen, case.num_q_heads, case.head_dim_qk, case.head_dim_v)
     return kv, flops
 
 
@@ -176,6 +181,7 @@ def workload_config(case, rotation_copies):
            "page_size": case.page_size, "dtype": case.dtype,
            "kv_cache": ("fp8 e4m3, per-tensor scales" if case.kv_format == synth.FP8_E4M3
                         else case.dtype),
+           "seq_len_q": case.seq_len_q,
            "context_lens": ("all " + str(int(case.context_lens[0]))
                             if (case.context_lens == case.context_lens[0]).all()
                             else f"varlen sum {int(case.context_lens.sum())}"),
@@ -194,8 +200,16 @@ def oracle_sample(case, budget_s: float):
     b = 0
     while True:
         rows = [(b, h) for h in range(case.num_q_heads)]
+        rows3 = [(b, i, h) for i in range(case.seq_len_q) for h in range(case.num_q_heads)]
         elem = 1 if case.kv_format == synth.FP8_E4M3 else 2
-        if case.kind == "gqa":
+        if case.kind == "gqa" and case.seq_len_q > 1:
+            oracle.paged_decode_mtp(case.q, case.k_cache, case.v_cache, case.block_tables,
+                                    case.context_lens, case.scale, case.page_size, case.dtype,
+                                    rows=rows3, kv_format=case.kv_format, k_scale=case.k_scale,
+                                    v_scale=case.v_scale)
+            done_bytes += traffic.gqa_kv_bytes([case.context_lens[b]], case.num_kv_heads,
+                                               case.head_dim_qk, elem)
+        elif case.kind == "gqa":
             oracle.paged_decode(case.q, case.k_cache, case.v_cache, case.block_tables,
                                 case.context_lens, case.scale, case.page_size, case.dtype,
                                 rows=rows, kv_format=case.kv_format, k_scale=case.k_scale,
@@ -322,8 +336,12 @@ def run_gpu(args, workload, rank, world, local_rank):
         caches = [(kv0, None)] + [(kv0.clone(), None) for _ in range(copies - 1)]
     tables = torch.from_numpy(case.block_tables).cuda()
     ctx = torch.from_numpy(case.context_lens).cuda()
-    out = torch.empty(case.batch, case.num_q_heads, case.head_dim_v, dtype=tdt, device="cuda")
-    lse = torch.empty(case.batch, case.num_q_heads, dtype=torch.float32, device="cuda")
+    S = case.seq_len_q
+    out_shape = (case.batch, case.num_q_heads, case.head_dim_v) if S == 1 else \
+        (case.batch, S, case.num_q_heads, case.head_dim_v)
+    lse_shape = (case.batch, case.num_q_heads) if S == 1 else (case.batch, case.num_q_heads, S)
+    out = torch.empty(out_shape, dtype=tdt, device="cuda")
+    lse = torch.empty(lse_shape, dtype=torch.float32, device="cuda")
     plan = pda.Plan(kind=pda.PDA_KIND_GQA if case.kind == "gqa" else pda.PDA_KIND_MLA,
                     dtype=pda.PDA_FP16 if case.dtype == synth.FP16 else pda.PDA_BF16,
                     batch=case.batch, num_q_heads=case.num_q_heads,
@@ -331,7 +349,8 @@ def run_gpu(args, workload, rank, world, local_rank):
                     head_dim_v=case.head_dim_v, page_size=case.page_size,
                     max_blocks_per_seq=case.max_blocks_per_seq, num_blocks=case.num_blocks,
                     context_lens=case.context_lens.tolist(),
-                    kv_format=pda.PDA_KV_FP8_E4M3 if fp8 else pda.PDA_KV_SAME_AS_Q)
+                    kv_format=pda.PDA_KV_FP8_E4M3 if fp8 else pda.PDA_KV_SAME_AS_Q,
+                    seq_len_q=S)
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     pda.workspace_init(plan, ws, stream)

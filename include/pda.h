@@ -88,6 +88,11 @@ typedef struct pda_problem {
   int32_t num_sms;            /* SMs to plan for; 0 = query the current device */
   int32_t force_num_ctas;     /* 0 = automatic; > 0 = split the work over exactly this many CTAs */
   int32_t kv_format;          /* pda_kv_format of the caches (0 = same type as q) */
+  int32_t seq_len_q;          /* S, query tokens per sequence; 0 or 1 = single-token decode.
+                                 S > 1 (speculative / MTP decoding; GQA only): query token i
+                                 of sequence b sits at position ctx_b - S + i and attends to
+                                 tokens 0 .. ctx_b - S + i (causal, bottom-right aligned);
+                                 every ctx_b >= S and S * Hq / Hkv <= 32 */
 } pda_problem;
 
 typedef struct pda_plan pda_plan;  /* opaque, owned by the library */
@@ -143,15 +148,17 @@ PDA_API pda_status pda_read_device_error(void* workspace, pda_stream_t stream, i
 /*
  * GQA / MQA / MHA paged decode ("From MHA to MLA", sections 3-5; drill page,
  * sections ③-⑤).
- *   q             device [B, Hq, D]            dtype
+ *   q             device [B, Hq, D] dtype; [B, S, Hq, D] when the plan's seq_len_q S > 1
  *   k_cache       device [num_blocks, P, Hkv, D] dtype
  *   v_cache       device [num_blocks, P, Hkv, D] dtype
  *   block_tables  device [B, max_blocks_per_seq] int32; only the first
  *                 ceil(ctx_b / P) entries of row b are read
  *   context_lens  device [B] int32, equal to the plan's host copy
  *   scale         softmax scale applied to q.k (e.g. 1/sqrt(D)); finite
- *   out           device [B, Hq, D] dtype (written; rows of other sequences untouched)
- *   lse           device [B, Hq] float32 natural-log LSE of the scaled logits, or NULL
+ *   out           device [B, Hq, D] dtype ([B, S, Hq, D] when S > 1; written; rows of
+ *                 other sequences untouched)
+ *   lse           device [B, Hq] float32 natural-log LSE of the scaled logits ([B, Hq, S]
+ *                 when S > 1, FlashMLA-ETAP "Usage" order), or NULL
  *   plan          from pda_plan_create with kind PDA_KIND_GQA
  *   workspace     device, pda_plan_workspace_bytes(plan) bytes, zeroed once
  * Slots past ctx in a sequence's last page and blocks not referenced by the

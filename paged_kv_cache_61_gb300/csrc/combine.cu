@@ -10,6 +10,7 @@
 #include <cmath>
 
 #include "pda_internal.h"
+#include "tile_walk.cuh"
 
 namespace pda {
 
@@ -77,6 +78,7 @@ struct MergeParams {
   float* lse;
   int64_t tiles_per_cta;
   int32_t group, dv, num_q_heads, count;
+  int32_t heads_per_seg, seq_len_q;  // G and S of the segments' rows (row r = i*G + g)
   HeavySegment seg[kMaxHeavySegments];
 };
 
@@ -150,14 +152,14 @@ __global__ void __launch_bounds__(kMergeThreads)
       s.x += f * sm_o[r][col].x; s.y += f * sm_o[r][col].y;
       s.z += f * sm_o[r][col].z; s.w += f * sm_o[r][col].w;
     }
-    const float inv = 1.f / den;
-    const int64_t orow = int64_t(hs.b) * p.num_q_heads + int64_t(hs.seg) * p.group + j;
-    T* out = static_cast<T*>(p.out) + orow * p.dv + dofs;
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    const RowIndex ri = seg_row(hs.b, hs.seg, j, p.heads_per_seg, p.seq_len_q, p.num_q_heads);
+    T* out = static_cast<T*>(p.out) + ri.out_row * p.dv + dofs;
     out[0] = to_out<T>(s.x * inv);
     out[1] = to_out<T>(s.y * inv);
     out[2] = to_out<T>(s.z * inv);
     out[3] = to_out<T>(s.w * inv);
-    if (dchunk == 0 && col == 0 && p.lse != nullptr) p.lse[orow] = mx + logf(den);
+    if (dchunk == 0 && col == 0 && p.lse != nullptr) p.lse[ri.lse] = mx + logf(den);
   }
 }
 
@@ -186,6 +188,8 @@ int launch_split_merge(const Plan& plan, const Workspace& ws, void* out, float* 
   prm.group = plan.group;
   prm.dv = plan.prob.head_dim_v;
   prm.num_q_heads = plan.prob.num_q_heads;
+  prm.heads_per_seg = plan.heads_per_seg;
+  prm.seq_len_q = plan.seq_len_q;
   prm.count = int32_t(plan.heavy.size());
   int max_pieces = 0;
   for (size_t i = 0; i < plan.heavy.size(); ++i) {

@@ -80,6 +80,7 @@ struct GqaParams {
   const int32_t* block_tables;
   const int32_t* context_lens;
   int32_t batch, num_q_heads, num_kv_heads, group, max_blocks;
+  int32_t heads_per_kv, seq_len_q;  // G and S: a segment's rows are r = i*G + g (group = S*G)
   int64_t num_blocks;
   float scale_log2;     // softmax scale (times k_scale for fp8 caches) times log2(e)
   float v_scale;        // fp8 caches: V dequantization scale (1 for 16-bit caches)
@@ -297,7 +298,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     {
       const bool hv = jq < p.group;
       const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-          qg + (int64_t(pt.b) * p.num_q_heads + int64_t(pt.seg) * p.group + (hv ? jq : 0)) * D);
+          qg + seg_row(pt.b, pt.seg, hv ? jq : 0, p.heads_per_kv, p.seq_len_q, p.num_q_heads)
+                       .out_row * D);
 #pragma unroll
       for (int ks = 0; ks < kKS; ++ks) {
         if constexpr (F8) {
@@ -308,6 +310,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           qf[ks][1] = hv ? __ldg(qrow + (ks * 16 + 8 + cq) / 2) : 0u;
         }
       }
+    }
+
+    // Causal limits of this lane's two columns (rows hsub*8 + cq, + 1): row r = i*G + g
+    // is query token i, which sees tokens [0, ctx - S + 1 + i) (bottom-right aligned; all
+    // ctx tokens when S = 1). Padded rows take ctx.
+    int lim0 = ctx, lim1 = ctx;
+    if (p.seq_len_q > 1) {
+      const int ra = hsub * 8 + cq;
+      if (ra < p.group) lim0 = ctx - p.seq_len_q + 1 + ra / p.heads_per_kv;
+      if (ra + 1 < p.group) lim1 = ctx - p.seq_len_q + 1 + (ra + 1) / p.heads_per_kv;
     }
 
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
@@ -367,9 +379,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         for (int hp = 0; hp < 2; ++hp) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) x[hp][e] = s[hp][e] * p.scale_log2;
-          if (vld[hp] < kPage) {
-            if (r0 >= vld[hp]) x[hp][0] = x[hp][1] = -INFINITY;
-            if (r0 + 8 >= vld[hp]) x[hp][2] = x[hp][3] = -INFINITY;
+          // tokens of this page each column may see: present slots, then the causal limit
+          const int ca = min(vld[hp], lim0 - pg0 - hp * kPage);
+          const int cb = min(vld[hp], lim1 - pg0 - hp * kPage);
+          if (ca < kPage || cb < kPage) {
+            if (r0 >= ca) x[hp][0] = -INFINITY;
+            if (r0 >= cb) x[hp][1] = -INFINITY;
+            if (r0 + 8 >= ca) x[hp][2] = -INFINITY;
+            if (r0 + 8 >= cb) x[hp][3] = -INFINITY;
           }
         }
         // online softmax down each head column over the 32 tokens (log2 domain)
@@ -381,14 +398,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           c1 = fmaxf(c1, __shfl_xor_sync(kFull, c1, o));
         }
         const float mn0 = fmaxf(m0, c0), mn1 = fmaxf(m1, c1);
-        const float al0 = ptx::exp2_approx(m0 - mn0), al1 = ptx::exp2_approx(m1 - mn1);
+        // a column that has seen no token yet (causal rows of a split piece) keeps m =
+        // -inf: subtract 0 instead, so its weights stay 0 rather than NaN
+        const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = ptx::exp2_approx(m0 - ms0), al1 = ptx::exp2_approx(m1 - ms1);
         float pp[2][4];
 #pragma unroll
         for (int hp = 0; hp < 2; ++hp) {
-          pp[hp][0] = ptx::exp2_approx(x[hp][0] - mn0);
-          pp[hp][1] = ptx::exp2_approx(x[hp][1] - mn1);
-          pp[hp][2] = ptx::exp2_approx(x[hp][2] - mn0);
-          pp[hp][3] = ptx::exp2_approx(x[hp][3] - mn1);
+          pp[hp][0] = ptx::exp2_approx(x[hp][0] - ms0);
+          pp[hp][1] = ptx::exp2_approx(x[hp][1] - ms1);
+          pp[hp][2] = ptx::exp2_approx(x[hp][2] - ms0);
+          pp[hp][3] = ptx::exp2_approx(x[hp][3] - ms1);
         }
         l0 = l0 * al0 + ((pp[0][0] + pp[0][2]) + (pp[1][0] + pp[1][2]));
         l1 = l1 * al1 + ((pp[0][1] + pp[0][3]) + (pp[1][1] + pp[1][3]));
@@ -459,9 +479,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         float x0 = s[0] * p.scale_log2, x1 = s[1] * p.scale_log2;
         float x2 = s[2] * p.scale_log2, x3 = s[3] * p.scale_log2;
-        if (valid < kPage) {
-          if (r0 >= valid) x0 = x1 = -INFINITY;
-          if (r0 + 8 >= valid) x2 = x3 = -INFINITY;
+        // tokens of this page each column may see: present slots, then the causal limit
+        const int ca = min(valid, lim0 - (pt.p0 + i) * kPage);
+        const int cb = min(valid, lim1 - (pt.p0 + i) * kPage);
+        if (ca < kPage || cb < kPage) {
+          if (r0 >= ca) x0 = -INFINITY;
+          if (r0 >= cb) x1 = -INFINITY;
+          if (r0 + 8 >= ca) x2 = -INFINITY;
+          if (r0 + 8 >= cb) x3 = -INFINITY;
         }
         // online softmax down each head column (log2 domain)
         float c0 = fmaxf(x0, x2), c1 = fmaxf(x1, x3);
@@ -471,9 +496,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           c1 = fmaxf(c1, __shfl_xor_sync(kFull, c1, o));
         }
         const float mn0 = fmaxf(m0, c0), mn1 = fmaxf(m1, c1);
-        const float al0 = ptx::exp2_approx(m0 - mn0), al1 = ptx::exp2_approx(m1 - mn1);
-        const float p0 = ptx::exp2_approx(x0 - mn0), p1 = ptx::exp2_approx(x1 - mn1);
-        const float p2 = ptx::exp2_approx(x2 - mn0), p3 = ptx::exp2_approx(x3 - mn1);
+        // a column that has seen no token yet keeps m = -inf (see the fp8 path)
+        const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = ptx::exp2_approx(m0 - ms0), al1 = ptx::exp2_approx(m1 - ms1);
+        const float p0 = ptx::exp2_approx(x0 - ms0), p1 = ptx::exp2_approx(x1 - ms1);
+        const float p2 = ptx::exp2_approx(x2 - ms0), p3 = ptx::exp2_approx(x3 - ms1);
         l0 = l0 * al0 + (p0 + p2);
         l1 = l1 * al1 + (p1 + p3);
         m0 = mn0;
@@ -567,14 +594,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         o[0] += a.x * f; o[1] += a.y * f; o[2] += a.z * f; o[3] += a.w * f;
         o[4] += b.x * f; o[5] += b.y * f; o[6] += b.z * f; o[7] += b.w * f;
       }
-      const float inv = p.v_scale / lsum;
+      // lsum = 0 only for a causal row that saw no token of a split piece: its partial
+      // is O = 0, L = -inf, which the merges skip
+      const float inv = lsum > 0.f ? p.v_scale / lsum : 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] *= inv;
-      const float lse_nat = (mx + log2f(lsum)) * kLn2;
+      const float lse_nat = lsum > 0.f ? (mx + log2f(lsum)) * kLn2 : -INFINITY;
       if (whole) {
-        const int64_t orow = int64_t(pt.b) * p.num_q_heads + int64_t(pt.seg) * p.group + j;
-        *reinterpret_cast<uint4*>(outg + orow * D + dc * 8) = pack8<T>(o);
-        if (dc == 0 && p.lse != nullptr) p.lse[orow] = lse_nat;
+        const RowIndex ri = seg_row(pt.b, pt.seg, j, p.heads_per_kv, p.seq_len_q, p.num_q_heads);
+        *reinterpret_cast<uint4*>(outg + ri.out_row * D + dc * 8) = pack8<T>(o);
+        if (dc == 0 && p.lse != nullptr) p.lse[ri.lse] = lse_nat;
       } else {
         float* po = p.part_out + (slot_row + j) * D + dc * 8;
         __stcg(reinterpret_cast<float4*>(po), make_float4(o[0], o[1], o[2], o[3]));
@@ -639,9 +668,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const float inv = 1.f / den;
 #pragma unroll
             for (int e = 0; e < 8; ++e) o[e] *= inv;
-            const int64_t orow = int64_t(pt.b) * p.num_q_heads + int64_t(pt.seg) * p.group + j;
-            *reinterpret_cast<uint4*>(outg + orow * D + dc * 8) = pack8<T>(o);
-            if (dc == 0 && p.lse != nullptr) p.lse[orow] = mx + logf(den);
+            const RowIndex ri =
+                seg_row(pt.b, pt.seg, j, p.heads_per_kv, p.seq_len_q, p.num_q_heads);
+            *reinterpret_cast<uint4*>(outg + ri.out_row * D + dc * 8) = pack8<T>(o);
+            if (dc == 0 && p.lse != nullptr) p.lse[ri.lse] = mx + logf(den);
           }
           if (tid == 0) atomicExch(counter, 0);
         }
@@ -762,8 +792,9 @@ bool gqa_supported(const pda_problem& p, std::string* why) {
     return false;
   }
   const int g = p.num_q_heads / p.num_kv_heads;
-  if (g > 32) {
-    *why = "GQA decode supports up to 32 query heads per KV head";
+  const int sq = p.seq_len_q > 1 ? p.seq_len_q : 1;
+  if (int64_t(g) * sq > 32) {
+    *why = "GQA decode supports up to 32 query rows (seq_len_q * Hq / Hkv) per KV head";
     return false;
   }
   if (p.num_blocks > INT32_MAX) {
@@ -800,6 +831,8 @@ int launch_gqa_decode(const Plan& plan, const GqaArgs& a, const Workspace& ws, v
   prm.num_q_heads = pr.num_q_heads;
   prm.num_kv_heads = pr.num_kv_heads;
   prm.group = plan.group;
+  prm.heads_per_kv = plan.heads_per_seg;
+  prm.seq_len_q = plan.seq_len_q;
   prm.max_blocks = pr.max_blocks_per_seq;
   prm.num_blocks = pr.num_blocks;
   prm.scale_log2 = a.scale * a.k_scale * kLog2e;

@@ -728,6 +728,10 @@ bool mla_supported(const pda_problem& p, std::string* why) {
     *why = "MLA decode supports 16-bit caches (kv_format PDA_KV_SAME_AS_Q)";
     return false;
   }
+  if (p.seq_len_q > 1) {
+    *why = "MLA decode supports one query token per sequence (seq_len_q 0 or 1)";
+    return false;
+  }
   if (!((p.head_dim_qk == 576 && p.head_dim_v == 512) ||
         (p.head_dim_qk == 320 && p.head_dim_v == 256))) {
     *why = "MLA decode supports (head_dim_qk, head_dim_v) = (576, 512) or (320, 256)";

@@ -33,10 +33,12 @@ constexpr int kMaxCtas = 2048;
 
 struct Plan {
   pda_problem prob{};
-  int32_t group = 1;            // query heads per segment (GQA: Hq/Hkv; MLA: Hq / head groups)
+  int32_t group = 1;            // query rows per segment: S * (GQA: Hq/Hkv; MLA: heads per group)
   int32_t segs_per_seq = 1;     // segments per sequence (GQA: Hkv; MLA: head groups)
   int32_t head_subtiles = 1;    // GQA: 8-head MMA column tiles per segment
   int32_t cluster = 1;          // CTAs per work unit (2: the MLA kernel for 128-head groups)
+  int32_t seq_len_q = 1;        // query tokens per sequence (S)
+  int32_t heads_per_seg = 1;    // heads of a segment (G); its rows are the S*G (token, head) pairs
   int64_t total_tiles = 0;
   int64_t tiles_per_cta = 0;
   int32_t num_ctas = 0;         // work units (CTA pairs when cluster == 2)

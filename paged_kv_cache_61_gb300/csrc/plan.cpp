@@ -83,6 +83,8 @@ extern "C" PDA_API pda_status pda_plan_create(pda_plan** out, const pda_problem*
     return fail(PDA_ERR_INVALID_ARG, "num_sms and force_num_ctas must be >= 0");
   if (p.kv_format != PDA_KV_SAME_AS_Q && p.kv_format != PDA_KV_FP8_E4M3)
     return fail(PDA_ERR_INVALID_ARG, "kv_format must be PDA_KV_SAME_AS_Q or PDA_KV_FP8_E4M3");
+  if (p.seq_len_q < 0) return fail(PDA_ERR_INVALID_ARG, "seq_len_q must be >= 0");
+  const int32_t S = p.seq_len_q > 1 ? p.seq_len_q : 1;
   if (p.batch > 0 && ctx_host == nullptr)
     return fail(PDA_ERR_INVALID_ARG, "context_lens_host is NULL");
 
@@ -92,8 +94,9 @@ extern "C" PDA_API pda_status pda_plan_create(pda_plan** out, const pda_problem*
 
   const int64_t max_ctx = int64_t(p.max_blocks_per_seq) * p.page_size;
   for (int32_t b = 0; b < p.batch; ++b) {
-    if (ctx_host[b] < 1)
-      return fail(PDA_ERR_INVALID_ARG, "context_lens[" + std::to_string(b) + "] < 1");
+    if (ctx_host[b] < S)
+      return fail(PDA_ERR_INVALID_ARG, "context_lens[" + std::to_string(b) + "] < " +
+                                           (S > 1 ? "seq_len_q" : std::string("1")));
     if (ctx_host[b] > max_ctx)
       return fail(PDA_ERR_INVALID_ARG, "context_lens[" + std::to_string(b) +
                                            "] exceeds max_blocks_per_seq * page_size");
@@ -114,11 +117,14 @@ extern "C" PDA_API pda_status pda_plan_create(pda_plan** out, const pda_problem*
   plan->prob = p;
   plan->prob.num_sms = num_sms;
   plan->context_lens.assign(ctx_host, ctx_host + p.batch);
+  plan->prob.seq_len_q = S;
+  plan->seq_len_q = S;
 
   int ctas_per_sm;
   int64_t min_tiles_per_cta;
   if (p.kind == PDA_KIND_GQA) {
-    plan->group = p.num_q_heads / p.num_kv_heads;
+    plan->heads_per_seg = p.num_q_heads / p.num_kv_heads;
+    plan->group = S * plan->heads_per_seg;
     plan->segs_per_seq = p.num_kv_heads;
     plan->head_subtiles = (plan->group + 7) / 8;
     ctas_per_sm = pda::gqa_ctas_per_sm(p);
@@ -128,6 +134,7 @@ extern "C" PDA_API pda_status pda_plan_create(pda_plan** out, const pda_problem*
     min_tiles_per_cta = std::max<int64_t>(4, plan->group / 4 + 1);
   } else {
     plan->group = pda::mla_heads_per_cta(p);
+    plan->heads_per_seg = plan->group;
     plan->segs_per_seq = p.num_q_heads / plan->group;
     plan->head_subtiles = 1;
     plan->cluster = pda::mla_uses_pairs(p) ? 2 : 1;

@@ -11,6 +11,20 @@ namespace pda {
 
 constexpr unsigned kFullMask = 0xffffffffu;
 
+// Query rows of a segment: the S query tokens of each of its G heads, row r = i*G + g
+// for query token i and head seg*G + g (FlashMLA-ETAP "Usage": s_q * h_q / h_kv query
+// rows per KV head). q and out rows are laid out [B][S][Hq], lse [B][Hq][S]; with S = 1
+// these are the single-token layouts [B][Hq].
+struct RowIndex {
+  int64_t out_row;  // row of q and out
+  int64_t lse;      // element of lse
+};
+__device__ __forceinline__ RowIndex seg_row(int b, int seg, int r, int G, int S, int Hq) {
+  const int i = r / G;
+  const int h = seg * G + (r - i * G);
+  return {(int64_t(b) * S + i) * Hq + h, (int64_t(b) * Hq + h) * S + i};
+}
+
 // What the walk needs to know about the batch. A segment is one (sequence, KV
 // head) for GQA or one (sequence, head group) for MLA.
 struct WalkSpec {

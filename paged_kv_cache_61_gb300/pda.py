@@ -34,7 +34,8 @@ class Problem(ctypes.Structure):
                 ("head_dim_qk", ctypes.c_int32), ("head_dim_v", ctypes.c_int32),
                 ("page_size", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
                 ("num_blocks", ctypes.c_int64), ("num_sms", ctypes.c_int32),
-                ("force_num_ctas", ctypes.c_int32), ("kv_format", ctypes.c_int32)]
+                ("force_num_ctas", ctypes.c_int32), ("kv_format", ctypes.c_int32),
+                ("seq_len_q", ctypes.c_int32)]
 
 
 def _declare(lib):
@@ -113,10 +114,11 @@ class Plan:
     def __init__(self, *, kind: int, dtype: int, batch: int, num_q_heads: int, num_kv_heads: int,
                  head_dim_qk: int, head_dim_v: int, page_size: int, max_blocks_per_seq: int,
                  num_blocks: int, context_lens: Sequence[int], num_sms: int = 0,
-                 force_num_ctas: int = 0, kv_format: int = PDA_KV_SAME_AS_Q):
+                 force_num_ctas: int = 0, kv_format: int = PDA_KV_SAME_AS_Q,
+                 seq_len_q: int = 1):
         self.problem = Problem(kind, dtype, batch, num_q_heads, num_kv_heads, head_dim_qk,
                                head_dim_v, page_size, max_blocks_per_seq, num_blocks, num_sms,
-                               force_num_ctas, kv_format)
+                               force_num_ctas, kv_format, seq_len_q)
         ctx = (ctypes.c_int32 * max(1, len(context_lens)))(*[int(c) for c in context_lens])
         handle = ctypes.c_void_p()
         _check(lib().pda_plan_create(ctypes.byref(handle), ctypes.byref(self.problem),

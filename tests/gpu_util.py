@@ -32,7 +32,8 @@ def make_plan(case: synth.DecodeCase, force_num_ctas: int = 0) -> pda.Plan:
                     max_blocks_per_seq=case.max_blocks_per_seq, num_blocks=case.num_blocks,
                     context_lens=case.context_lens.tolist(), force_num_ctas=force_num_ctas,
                     kv_format=(pda.PDA_KV_FP8_E4M3 if case.kv_format == synth.FP8_E4M3
-                               else pda.PDA_KV_SAME_AS_Q))
+                               else pda.PDA_KV_SAME_AS_Q),
+                    seq_len_q=case.seq_len_q)
 
 
 def to_device_cache(case: synth.DecodeCase, arr: np.ndarray) -> torch.Tensor:
@@ -55,10 +56,12 @@ class DeviceCase:
             self.kv = to_device_cache(case, case.kv_cache)
         self.tables = torch.from_numpy(case.block_tables).cuda()
         self.ctx = torch.from_numpy(case.context_lens).cuda()
-        self.out = torch.full((case.batch, case.num_q_heads, case.head_dim_v), float("nan"),
-                              dtype=torch_dtype(case.dtype), device="cuda")
-        self.lse = torch.full((case.batch, case.num_q_heads), float("nan"), dtype=torch.float32,
-                              device="cuda")
+        S = case.seq_len_q
+        out_shape = (case.batch, case.num_q_heads, case.head_dim_v) if S == 1 else \
+            (case.batch, S, case.num_q_heads, case.head_dim_v)
+        lse_shape = (case.batch, case.num_q_heads) if S == 1 else (case.batch, case.num_q_heads, S)
+        self.out = torch.full(out_shape, float("nan"), dtype=torch_dtype(case.dtype), device="cuda")
+        self.lse = torch.full(lse_shape, float("nan"), dtype=torch.float32, device="cuda")
         self.replan(force_num_ctas)
 
     def replan(self, force_num_ctas: int = 0):
@@ -83,11 +86,15 @@ class DeviceCase:
 
 
 def compare(case, out_gpu: torch.Tensor, lse_gpu: torch.Tensor, ref_out, ref_lse, rows=None):
-    """Max-abs errors of (out, lse) over all rows or the listed (b, h) rows."""
+    """Max-abs errors of (out, lse) over all rows or the listed (b, h) / (b, i, h) rows."""
     o = out_gpu.float().cpu().numpy().astype(np.float64)
     l = lse_gpu.cpu().numpy().astype(np.float64)
     if rows is None:
         return float(np.abs(o - ref_out).max()), float(np.abs(l - ref_lse).max())
+    if len(rows[0]) == 3:                  # (b, i, h): out [B, S, Hq, Dv], lse [B, Hq, S]
+        bs, is_, hs = ([r[k] for r in rows] for k in range(3))
+        return (float(np.abs(o[bs, is_, hs] - ref_out[bs, is_, hs]).max()),
+                float(np.abs(l[bs, hs, is_] - ref_lse[bs, hs, is_]).max()))
     bs = [r[0] for r in rows]
     hs = [r[1] for r in rows]
     return (float(np.abs(o[bs, hs] - ref_out[bs, hs]).max()),

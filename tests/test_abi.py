@@ -165,3 +165,25 @@ def test_fp8_plan_validation():
     assert e.value.status == pda.PDA_ERR_UNSUPPORTED
     f8 = _plan(batch=0, context_lens=[], kv_format=pda.PDA_KV_FP8_E4M3)
     pda.paged_decode_attn_fp8(0, 0, 0, 1.0, 1.0, 0, 0, 0.125, 0, None, f8, 0, stream=0)
+
+
+def test_multi_token_plan_validation():
+    # S = 2 query tokens: every context must hold at least S tokens
+    with pytest.raises(pda.PdaError) as e:
+        _plan(seq_len_q=2, context_lens=[1, 64])
+    assert e.value.status == pda.PDA_ERR_INVALID_ARG
+    # S * G query rows per KV head are limited to 32
+    with pytest.raises(pda.PdaError) as e:
+        _plan(seq_len_q=3, num_q_heads=24, num_kv_heads=2)
+    assert e.value.status == pda.PDA_ERR_UNSUPPORTED
+    with pytest.raises(pda.PdaError) as e:
+        _plan(seq_len_q=-1)
+    assert e.value.status == pda.PDA_ERR_INVALID_ARG
+    with pytest.raises(pda.PdaError) as e:     # the MLA kernels take one query token
+        _plan(kind=pda.PDA_KIND_MLA, num_q_heads=16, num_kv_heads=1, head_dim_qk=576,
+              head_dim_v=512, page_size=64, max_blocks_per_seq=2, context_lens=[5, 64],
+              seq_len_q=2)
+    assert e.value.status == pda.PDA_ERR_UNSUPPORTED
+    # S = 2 doubles the rows of a segment, and so each split piece's partial
+    one, two = _plan(), _plan(seq_len_q=2)
+    assert two.workspace_bytes > one.workspace_bytes
