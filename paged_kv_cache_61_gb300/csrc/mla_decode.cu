@@ -78,6 +78,9 @@ struct MlaParams {
   const int32_t* block_tables;
   const int32_t* context_lens;
   int32_t batch, num_q_heads, groups, max_blocks;
+  // S query tokens per sequence: the S*Hq rows of a sequence (row R = i*Hq + h, query
+  // token i, head h) are contiguous in q and out; with S > 1 they form one head group
+  int32_t rows_per_seq, seq_len_q;
   int64_t num_blocks;
   float scale_log2;
   int64_t total_tiles, tiles_per_cta;
@@ -211,7 +214,7 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
         if (u > 0) ok = bounded_wait(q_empty, (u - 1) & 1, flags, p.err);
         if (ok) {
           ptx::mbar_arrive_expect_tx(q_full, L::kQBytes);
-          ptx::tma_load_3d(qs, &tm_q, q_full, 0, pt.b * p.num_q_heads + pt.seg * N, 0,
+          ptx::tma_load_3d(qs, &tm_q, q_full, 0, pt.b * p.rows_per_seq + pt.seg * N, 0,
                            pol_stream);
         }
       }
@@ -410,6 +413,15 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
         const bool valid = active && token < ctx && !aborted;
         float x[NC];
         load_scores(valid, x);
+        // causal rows (S > 1, one head group holding all S*Hq rows): row R = i*Hq + h,
+        // query token i, sees tokens [0, ctx - S + 1 + i). Token ctx - S + 1 + k is hidden
+        // from the rows of query tokens 0..k, i.e. rows R < (k + 1) * Hq.
+        if (valid && token >= ctx - p.seq_len_q + 1) {
+          const int cut = (token - (ctx - p.seq_len_q)) * p.num_q_heads - cb;
+#pragma unroll
+          for (int h = 0; h < NC; ++h)
+            if (h < cut) x[h] = -INFINITY;
+        }
         if (i == 0) {
           // first page of the piece: the running maximum starts at the exact column maximum
           column_max(x);
@@ -440,7 +452,8 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
               const float4 r = *reinterpret_cast<const float4*>(red + ctid * 4);
               const float mo = mused[ctid];
               const float mn = fmaxf(mo, fmaxf(fmaxf(r.x, r.y), fmaxf(r.z, r.w)));
-              alpha_s[ctid] = ptx::exp2_approx(mo - mn);
+              // a causal row that has seen no token yet has nothing to rescale
+              alpha_s[ctid] = mn == -INFINITY ? 1.f : ptx::exp2_approx(mo - mn);
               mused[ctid] = mn;
             }
             ptx::named_barrier_sync(1, kST);
@@ -479,7 +492,8 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
           float pv[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            pv[e] = ptx::exp2_approx(x[c + e] - mm[e]);
+            // m = -inf: a causal row with no token seen yet, whose scores are all -inf
+            pv[e] = ptx::exp2_approx(x[c + e] - (mm[e] == -INFINITY ? 0.f : mm[e]));
             l_reg[c + e] += pv[e];
           }
           if (active) {
@@ -537,7 +551,13 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
 
       const bool whole = (pt.p0 == 0 && pt.p1 == pt.np);
       const int slot = piece_slot(pt.seg_start, g_lo);
-      const int64_t head0 = int64_t(pt.b) * p.num_q_heads + int64_t(pt.seg) * N;
+      const int64_t head0 = int64_t(pt.b) * p.rows_per_seq + int64_t(pt.seg) * N;
+      // lse is [B][Hq][S]: row R = i*Hq + h of the sequence goes to (b*Hq + h)*S + i
+      auto lse_at = [&](int r) {
+        const int R = pt.seg * N + r;
+        const int qi = R / p.num_q_heads;
+        return (int64_t(pt.b) * p.num_q_heads + (R - qi * p.num_q_heads)) * p.seq_len_q + qi;
+      };
       const int64_t slot_row = (int64_t(blockIdx.x) * 2 + slot) * N;
 #pragma unroll
       for (int mt = 0; mt < R::kMTiles; ++mt) {
@@ -555,7 +575,8 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int h = cb + c + e;
-            const float o = v[e] / ltot[h];
+            // ltot = 0 only for a causal row that saw no token of a split piece: O = 0
+            const float o = ltot[h] > 0.f ? v[e] / ltot[h] : 0.f;
             if (whole)
               outg[(head0 + h) * kDv + d] = from_f32<T>(o);
             else
@@ -564,9 +585,10 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
         }
       }
       if (ctid < N) {
-        const float lse_nat = (mused[ctid] + log2f(ltot[ctid])) * kLn2;
+        const float lse_nat =
+            ltot[ctid] > 0.f ? (mused[ctid] + log2f(ltot[ctid])) * kLn2 : -INFINITY;
         if (whole) {
-          if (p.lse != nullptr) p.lse[head0 + ctid] = lse_nat;
+          if (p.lse != nullptr) p.lse[lse_at(ctid)] = lse_nat;
         } else {
           __stcg(p.part_lse + slot_row + ctid, lse_nat);
         }
@@ -613,7 +635,7 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
               o[1] = from_f32<T>(acc.y * inv);
               o[2] = from_f32<T>(acc.z * inv);
               o[3] = from_f32<T>(acc.w * inv);
-              if (dq == 0 && p.lse != nullptr) p.lse[head0 + j] = mx + logf(den);
+              if (dq == 0 && p.lse != nullptr) p.lse[lse_at(j)] = mx + logf(den);
             }
             if (ctid == 0) atomicExch(counter, 0);
           }
@@ -718,6 +740,7 @@ int launch_mla_dt(int dqk, int n, const CUtensorMap& tq, const CUtensorMap& tkv,
 }  // namespace
 
 int mla_heads_per_cta(const pda_problem& p) {
+  if (p.seq_len_q > 1) return p.seq_len_q * p.num_q_heads;  // all rows of a sequence
   if (mla_uses_pairs(p)) return 128;   // one 128-head group per CTA pair
   return p.num_q_heads <= 64 ? p.num_q_heads : 64;
 }
@@ -729,8 +752,11 @@ bool mla_supported(const pda_problem& p, std::string* why) {
     return false;
   }
   if (p.seq_len_q > 1) {
-    *why = "MLA decode supports one query token per sequence (seq_len_q 0 or 1)";
-    return false;
+    const int64_t rows = int64_t(p.seq_len_q) * p.num_q_heads;
+    if (!(rows == 16 || rows == 32 || rows == 64)) {
+      *why = "MLA decode of several query tokens needs seq_len_q * num_q_heads in {16, 32, 64}";
+      return false;
+    }
   }
   if (!((p.head_dim_qk == 576 && p.head_dim_v == 512) ||
         (p.head_dim_qk == 320 && p.head_dim_v == 256))) {
@@ -746,7 +772,8 @@ bool mla_supported(const pda_problem& p, std::string* why) {
     return false;
   }
   const int n = mla_heads_per_cta(p);
-  if (!(n == 16 || n == 32 || n == 64 || n == 128) || p.num_q_heads % n != 0) {
+  if (!(n == 16 || n == 32 || n == 64 || n == 128) ||
+      (p.seq_len_q <= 1 && p.num_q_heads % n != 0)) {
     *why = "MLA decode supports num_q_heads 16, 32 or a multiple of 64";
     return false;
   }
@@ -763,7 +790,8 @@ int launch_mla_decode(const Plan& plan, const MlaArgs& a, const Workspace& ws, v
   const bool bf16 = pr.dtype == PDA_BF16;
   const int n = plan.group;
   CUtensorMap tq, tkv;
-  if (!encode_mla_maps(&tq, &tkv, a.q, int64_t(pr.batch) * pr.num_q_heads, n, a.kv_cache,
+  const int sq = pr.seq_len_q > 1 ? pr.seq_len_q : 1;
+  if (!encode_mla_maps(&tq, &tkv, a.q, int64_t(pr.batch) * sq * pr.num_q_heads, n, a.kv_cache,
                        pr.num_blocks, bf16, pr.head_dim_qk))
     return -1;
   MlaParams prm{};
@@ -774,6 +802,8 @@ int launch_mla_decode(const Plan& plan, const MlaArgs& a, const Workspace& ws, v
   prm.context_lens = a.context_lens;
   prm.batch = pr.batch;
   prm.num_q_heads = pr.num_q_heads;
+  prm.rows_per_seq = sq * pr.num_q_heads;
+  prm.seq_len_q = sq;
   prm.groups = plan.segs_per_seq;
   prm.max_blocks = pr.max_blocks_per_seq;
   prm.num_blocks = pr.num_blocks;

@@ -992,7 +992,7 @@ cudaError_t pair_kernel_attributes() {
 }  // namespace
 
 bool mla_uses_pairs(const pda_problem& p) {
-  return p.head_dim_qk == kDqk && p.num_q_heads % kHeads == 0;
+  return p.head_dim_qk == kDqk && p.num_q_heads % kHeads == 0 && p.seq_len_q <= 1;
 }
 
 int mla_pair_units(int num_sms) {

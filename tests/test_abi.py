@@ -179,11 +179,13 @@ def test_multi_token_plan_validation():
     with pytest.raises(pda.PdaError) as e:
         _plan(seq_len_q=-1)
     assert e.value.status == pda.PDA_ERR_INVALID_ARG
-    with pytest.raises(pda.PdaError) as e:     # the MLA kernels take one query token
-        _plan(kind=pda.PDA_KIND_MLA, num_q_heads=16, num_kv_heads=1, head_dim_qk=576,
-              head_dim_v=512, page_size=64, max_blocks_per_seq=2, context_lens=[5, 64],
-              seq_len_q=2)
+    mla = dict(kind=pda.PDA_KIND_MLA, num_kv_heads=1, head_dim_qk=576, head_dim_v=512,
+               page_size=64, max_blocks_per_seq=2, context_lens=[5, 64], seq_len_q=2)
+    with pytest.raises(pda.PdaError) as e:     # MLA: S * Hq rows must fit one 64-row group
+        _plan(num_q_heads=64, **mla)
     assert e.value.status == pda.PDA_ERR_UNSUPPORTED
+    p = _plan(num_q_heads=16, **mla)            # 32 rows: one head group per sequence
+    assert p.num_ctas >= 1
     # S = 2 doubles the rows of a segment, and so each split piece's partial
     one, two = _plan(), _plan(seq_len_q=2)
     assert two.workspace_bytes > one.workspace_bytes

@@ -162,3 +162,47 @@ def test_full_size_workload_sampled_rows(name):
     hq = case.num_q_heads
     rows = [(b, h) for b in (0, 7, 15) for h in sorted({0, 1, hq // 2, hq - 1})]
     _assert_close(case, DeviceCase(case), rows=rows)
+
+
+# ---------------------------------------------------------------- several query tokens
+def _oracle_mtp(case, rows=None):
+    return oracle.mla_decode_mtp(case.q, case.kv_cache, case.block_tables, case.context_lens,
+                                 case.scale, case.page_size, case.dtype,
+                                 head_dim_v=case.head_dim_v, rows=rows)
+
+
+def _assert_close_mtp(case, dc, rows=None):
+    out, lse = dc.run()
+    torch.cuda.synchronize()
+    ref_out, ref_lse = _oracle_mtp(case, rows)
+    eo, el = compare(case, out, lse, ref_out, ref_lse, rows)
+    assert eo <= TOL_OUT[case.dtype], f"out max-abs error {eo}"
+    assert el <= TOL_LSE, f"lse max-abs error {el}"
+    assert pda.read_device_error(dc.ws) == 0
+
+
+@pytest.mark.parametrize("latent", [512, 256])
+@pytest.mark.parametrize("hq,s", [(16, 2), (32, 2), (16, 4), (8, 2)])
+@pytest.mark.parametrize("force", [0, 1, 3, 17])
+def test_mtp_small_cases(hq, s, force, latent):
+    # q [B, S, Hq, Dqk]: query token i sees tokens [0, ctx - S + 1 + i)
+    case = synth.make_mla_case(batch=4, num_q_heads=hq, dtype=synth.BF16,
+                               context_lens=[64 + s - 1, 65, 130, 700], latent_dim=latent,
+                               seed=5, seq_len_q=s)
+    _assert_close_mtp(case, DeviceCase(case, force_num_ctas=force))
+
+
+@pytest.mark.parametrize("ctx", [65, 129])
+def test_mtp_piece_where_a_row_sees_no_token(ctx):
+    # ctx = 64k + 1, S = 2: the last page holds one token that query token 0 may not see;
+    # one page per CTA makes that page a split piece with no token for those rows
+    case = synth.make_mla_case(batch=1, num_q_heads=16, dtype=synth.BF16, context_lens=[ctx],
+                               seed=2, seq_len_q=2)
+    for force in (ctx // 64 + 1, 0):
+        _assert_close_mtp(case, DeviceCase(case, force_num_ctas=force))
+
+
+def test_mtp_full_size_workload_sampled_rows():
+    case = synth.workload("mla_b16_ctx64k_h16_mtp2")
+    rows = [(b, i, h) for b in (0, 7, 15) for i in range(2) for h in (0, 1, 8, 15)]
+    _assert_close_mtp(case, DeviceCase(case), rows=rows)
