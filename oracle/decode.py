@@ -337,3 +337,61 @@ def mla_decode_mtp(q, kv_cache, block_tables, context_lens, scale, page_size, dt
             out[b, i, hs] = o
             lse[b, hs, i] = l
     return out, lse
+
+
+# --------------------------------------------------------------------------------------
+# appending the new tokens' keys and values ("From MHA to MLA", section 2: at decode step
+# t the new key and value are appended to the cache, and every later step rereads them;
+# section 5: logical token n lives in block block_tables[b][n // P], slot n - (n // P) * P)
+# --------------------------------------------------------------------------------------
+def encode_e4m3(x) -> np.ndarray:
+    """float32 values -> E4M3 codes: round to nearest, ties to an even mantissa, finite
+    values beyond the largest code clamp to +-448 (saturating), NaN -> 0x7F.
+
+    Written from the format's definition: the candidates are the 127 non-negative finite
+    codes 0x00..0x7E, whose values decode_e4m3 gives and which increase with the code.
+    """
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    codes = np.arange(0x7F, dtype=np.uint8)
+    values = decode_e4m3(codes)                      # 0, 2^-9, ..., 448, increasing
+    mag = np.minimum(np.abs(np.nan_to_num(x, nan=0.0)), values[-1])
+    hi = np.searchsorted(values, mag, side="left")   # first code with value >= mag
+    hi = np.minimum(hi, len(values) - 1)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = mag - values[lo]
+    d_hi = values[hi] - mag
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (codes[hi] % 2 == 0) & (hi != lo))
+    out = np.where(pick_hi, codes[hi], codes[lo]).astype(np.uint8)
+    out = np.where(mag == values[hi], codes[hi], out).astype(np.uint8)
+    sign = (np.signbit(x) & ~np.isnan(x)).astype(np.uint8) << 7
+    out = out | sign
+    return np.where(np.isnan(x), np.uint8(0x7F), out).astype(np.uint8)
+
+
+def quantize_e4m3(x_bits, dtype, scale) -> np.ndarray:
+    """16-bit values -> E4M3 codes of value / scale, the division done in float32 (as the
+    append kernel does) and rounded once to E4M3."""
+    x32 = widen(x_bits, dtype).astype(np.float32)
+    return encode_e4m3(x32 / np.float32(scale))
+
+
+def append_tokens(cache, new, block_tables, context_lens, page_size, seq_len_q=1):
+    """A copy of ``cache`` [NB, P, ...] with the new tokens written in place.
+
+    new [B, S, ...] holds the S new tokens of each sequence (already in the cache's storage
+    type); token i of sequence b is logical token n = ctx_b - S + i (ctx_b counts the new
+    tokens), stored at (block_tables[b][n // P], n % P).
+    """
+    out = np.array(cache, copy=True)
+    B = len(context_lens)
+    for b in range(B):
+        ctx = int(context_lens[b])
+        if ctx < seq_len_q:
+            raise ValueError("context length must be >= seq_len_q")
+        for i in range(seq_len_q):
+            n = ctx - seq_len_q + i
+            logical_page = n // page_size
+            slot = n - logical_page * page_size
+            phys = int(block_tables[b][logical_page])
+            out[phys, slot] = new[b, i]
+    return out

@@ -36,6 +36,10 @@ PIN_CALLS = [
     pins.test_mtp_row_i_is_single_token_decode_over_its_prefix,
     lambda: pins.test_mtp_matches_torch_sdpa_lower_right_causal(None),
     pins.test_mtp_mla_equals_generic_with_one_kv_head,
+    pins.test_e4m3_encode_closed_forms,
+    pins.test_e4m3_encode_inverts_decode_on_every_finite_code,
+    pins.test_e4m3_encode_matches_torch_float8_cast_in_range,
+    lambda: pins.test_append_puts_new_tokens_where_the_gather_reads_them(2),
 ]
 
 
@@ -119,6 +123,26 @@ def _causal_off_by_one(ctx, seq_len_q, i):
     return max(1, int(ctx) - int(seq_len_q) + int(i))
 
 
+def _encode_ties_away(x):
+    x = np.asarray(x, dtype=np.float32)
+    base = od.__dict__["_orig_encode"](x)
+    up = od.__dict__["_orig_encode"](x * np.float32(1.0 + 2.0 ** -20))   # nudge ties upward
+    return np.where(np.abs(x) > 0, up, base).astype(np.uint8)
+
+
+def _encode_truncates(x):
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    codes = np.arange(0x7F, dtype=np.uint8)
+    values = od.decode_e4m3(codes)
+    mag = np.minimum(np.abs(np.nan_to_num(x)), values[-1])
+    idx = np.searchsorted(values, mag, side="right") - 1
+    return (codes[idx] | ((x < 0).astype(np.uint8) << 7)).astype(np.uint8)
+
+
+def _append_one_slot_late(cache, new, tables, ctx, page, seq_len_q=1):
+    return od.__dict__["_orig_append"](cache, new, tables, np.asarray(ctx) + 1, page, seq_len_q)
+
+
 MUTATIONS = {
     "lse in log2": ("attend", _attend_log2),
     "scale dropped": ("attend", _attend_no_scale),
@@ -135,6 +159,9 @@ MUTATIONS = {
     "causal mask aligned top-left": ("causal_prefix", _causal_top_left),
     "causal mask ignored": ("causal_prefix", _causal_ignored),
     "causal limit excludes the query's own token": ("causal_prefix", _causal_off_by_one),
+    "E4M3 encoding rounds ties away from zero": ("encode_e4m3", _encode_ties_away),
+    "E4M3 encoding truncates": ("encode_e4m3", _encode_truncates),
+    "append writes one slot late": ("append_tokens", _append_one_slot_late),
 }
 
 
@@ -147,6 +174,8 @@ def test_mutation_is_caught_by_a_pin(name, monkeypatch):
     monkeypatch.setitem(od.__dict__, "_orig_e4m3", od.decode_e4m3)
     monkeypatch.setitem(od.__dict__, "_orig_dequantize", od.dequantize)
     monkeypatch.setitem(od.__dict__, "_orig_paged", od.paged_decode)
+    monkeypatch.setitem(od.__dict__, "_orig_encode", od.encode_e4m3)
+    monkeypatch.setitem(od.__dict__, "_orig_append", od.append_tokens)
     monkeypatch.setattr(od, func, repl)
     monkeypatch.setattr(oracle, func, repl)
     caught = []

@@ -535,3 +535,53 @@ def test_mtp_mla_equals_generic_with_one_kv_head():
                                          case.scale, case.page_size, case.dtype)
     np.testing.assert_allclose(out, out2, rtol=0, atol=1e-12)
     np.testing.assert_allclose(lse, lse2, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- appending new tokens
+def test_e4m3_encode_closed_forms():
+    x = np.array([1.0625, 1.1875, 1.0, -2.5, 500.0, -1e30, 448.0, 464.0, 2.0 ** -10,
+                  1.5 * 2.0 ** -10, 0.0, -0.0, np.nan, np.inf], dtype=np.float32)
+    want = [0x38,   # midpoint of 1.0 and 1.125: ties to the even mantissa (1.0)
+            0x3A,   # midpoint of 1.125 and 1.25: the even one is 1.25
+            0x38, 0xC2, 0x7E, 0xFE, 0x7E, 0x7E,   # +-448 saturate
+            0x00,   # 2^-10: midpoint of 0 and the smallest subnormal, ties to 0
+            0x01, 0x00, 0x80, 0x7F, 0x7E]
+    np.testing.assert_array_equal(oracle.encode_e4m3(x), np.array(want, dtype=np.uint8))
+
+
+def test_e4m3_encode_inverts_decode_on_every_finite_code():
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], dtype=np.uint8)
+    np.testing.assert_array_equal(oracle.encode_e4m3(oracle.decode_e4m3(codes)), codes)
+
+
+def test_e4m3_encode_matches_torch_float8_cast_in_range():
+    x = np.random.default_rng(1).standard_normal(100000).astype(np.float32) * 60.0
+    x = np.clip(x, -448.0, 448.0)
+    lib = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(oracle.encode_e4m3(x), lib)
+
+
+@pytest.mark.parametrize("s", [1, 2])
+def test_append_puts_new_tokens_where_the_gather_reads_them(s):
+    case = synth.make_gqa_case(batch=3, num_q_heads=8, num_kv_heads=2, head_dim=64,
+                               dtype=synth.BF16, context_lens=[37, 16, 17],
+                               table_layout="permutation", num_blocks=24, max_blocks_per_seq=5,
+                               seed=8, seq_len_q=s)
+    rng = np.random.default_rng(3)
+    new = rng.integers(0, 2 ** 16, size=(3, s, 2, 64), dtype=np.uint16)
+    out = oracle.append_tokens(case.k_cache, new, case.block_tables, case.context_lens, 16, s)
+    changed = np.zeros(out.shape[:2], dtype=bool)
+    for b, ctx in enumerate(case.context_lens):
+        got = oracle.gather_tokens(out, case.block_tables[b], int(ctx), 16)
+        np.testing.assert_array_equal(got[int(ctx) - s:], new[b])
+        np.testing.assert_array_equal(got[:int(ctx) - s],
+                                      oracle.gather_tokens(case.k_cache, case.block_tables[b],
+                                                           int(ctx) - s, 16))
+        phys, slots = oracle.token_locations(case.block_tables[b], int(ctx), 16)
+        changed[phys[-s:], slots[-s:]] = True
+    # nothing else in the pool changes
+    np.testing.assert_array_equal(out[~changed], case.k_cache[~changed])
+    # as in the drill's worked example, token 36 of a 37-token sequence is slot 4 of the
+    # block in the third table entry
+    phys, slots = oracle.token_locations(case.block_tables[0], 37, 16)
+    assert (int(phys[-1]), int(slots[-1])) == (int(case.block_tables[0][2]), 4)
