@@ -57,7 +57,8 @@ typedef enum pda_status {
   PDA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, ctx < 1, plan/kind mismatch */
   PDA_ERR_UNSUPPORTED = 2,  /* a shape or dtype this build has no kernel for */
   PDA_ERR_WORKSPACE = 3,    /* workspace missing or too small for the plan */
-  PDA_ERR_CUDA = 4          /* a CUDA runtime call failed (launch, copy, device query) */
+  PDA_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch, copy, device query) */
+  PDA_ERR_OUT_OF_BLOCKS = 5 /* the block pool has too few free blocks (nothing allocated) */
 } pda_status;
 
 typedef enum pda_dtype { PDA_FP16 = 0, PDA_BF16 = 1 } pda_dtype;
@@ -247,6 +248,67 @@ PDA_API pda_status paged_decode_attn_no_alloc(const void* q, const void* k_cache
                                               const int32_t* context_lens, float scale, void* out,
                                               float* lse, const pda_plan* plan,
                                               pda_stream_t stream);
+
+/*
+ * Append the S new tokens of every sequence to the caches ("From MHA to MLA", section 2:
+ * at each decode step the new key and value are appended to the cache; section 5: token
+ * n of sequence b lives in block block_tables[b][n / P], slot n % P). S is the plan's
+ * seq_len_q; the new tokens are sequence b's logical tokens context_lens[b] - S + i, so
+ * context_lens already counts them (the same lengths the decode call then takes).
+ *   GQA plan (pda_kv_append):
+ *     k_new, v_new    device [B, S, Hkv, D] in the plan's dtype, 16-byte aligned
+ *     k_cache, v_cache device [num_blocks, P, Hkv, D] (plan's dtype), written in place
+ *   MLA plan (pda_mla_append): kv_new [B, S, Dqk] into kv_cache [num_blocks, 64, Dqk]
+ *   block_tables, context_lens device, as for the decode calls; the entries that hold the
+ *                   new tokens must already be assigned (see pda_pool_grow)
+ *   workspace       the plan's workspace (only its error word is used)
+ * A new token whose table entry is outside [0, num_blocks), or whose position is outside
+ * the table or negative, is not written and sets bit 0 of the device error word.
+ * Asynchronous on `stream`; no other cache entry is touched.
+ */
+PDA_API pda_status pda_kv_append(const void* k_new, const void* v_new, void* k_cache,
+                                 void* v_cache, const int32_t* block_tables,
+                                 const int32_t* context_lens, const pda_plan* plan,
+                                 void* workspace, pda_stream_t stream);
+
+/* pda_kv_append into E4M3 caches (plan kv_format PDA_KV_FP8_E4M3): each value x is
+ * stored as the E4M3 code of x / scale, the division in fp32 (IEEE, round to nearest),
+ * rounded once to nearest-even and saturated to +-448 (NaN stays NaN). k_scale and
+ * v_scale (finite, nonzero) are the tensors' dequantization scales. */
+PDA_API pda_status pda_kv_append_fp8(const void* k_new, const void* v_new, void* k_cache,
+                                     void* v_cache, float k_scale, float v_scale,
+                                     const int32_t* block_tables, const int32_t* context_lens,
+                                     const pda_plan* plan, void* workspace, pda_stream_t stream);
+
+PDA_API pda_status pda_mla_append(const void* kv_new, void* kv_cache,
+                                  const int32_t* block_tables, const int32_t* context_lens,
+                                  const pda_plan* plan, void* workspace, pda_stream_t stream);
+
+/*
+ * Physical block pool behind the block tables ("From MHA to MLA", section 5: requests'
+ * logical pages map to one shared physical pool). Host memory only; one thread at a time
+ * per pool. Blocks are ids in [0, num_blocks); a new pool hands them out as 0, 1, 2, ...
+ * and a released block is handed out before the older free ones.
+ */
+typedef struct pda_block_pool pda_block_pool;  /* opaque, owned by the library */
+
+PDA_API pda_status pda_pool_create(pda_block_pool** pool, int64_t num_blocks);
+PDA_API void pda_pool_destroy(pda_block_pool* pool);
+PDA_API int64_t pda_pool_num_free(const pda_block_pool* pool);
+
+/* Grow one sequence from old_len to new_len tokens: assigns blocks to its logical pages
+ * ceil(old_len / page_size) .. ceil(new_len / page_size) - 1, writing them into the host
+ * table row (max_blocks_per_seq entries). All or nothing: PDA_ERR_OUT_OF_BLOCKS, with the
+ * row and the pool unchanged, when too few blocks are free. */
+PDA_API pda_status pda_pool_grow(pda_block_pool* pool, int32_t* table_row,
+                                 int32_t max_blocks_per_seq, int32_t page_size,
+                                 int32_t old_len, int32_t new_len);
+
+/* Return the blocks of a finished sequence (its first ceil(len / page_size) entries) to
+ * the pool and set those entries to -1. An entry that is not an in-use block of this pool,
+ * or a block listed twice, fails with PDA_ERR_INVALID_ARG and changes nothing. */
+PDA_API pda_status pda_pool_release(pda_block_pool* pool, int32_t* table_row,
+                                    int32_t page_size, int32_t len);
 
 /* Static name of a status code. */
 PDA_API const char* pda_status_string(pda_status status);

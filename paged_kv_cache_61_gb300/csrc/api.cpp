@@ -161,3 +161,69 @@ extern "C" PDA_API pda_status pda_combine_splits(const float* partial_out, const
   if (e != 0) return cuda_fail(e, "combine launch");
   return PDA_OK;
 }
+
+namespace {
+
+pda_status append_call(int kind, const void* k_new, const void* v_new, void* k_cache,
+                       void* v_cache, float k_scale, float v_scale, const int32_t* block_tables,
+                       const int32_t* context_lens, const pda_plan* plan, void* workspace,
+                       pda_stream_t stream) {
+  if (plan == nullptr) return fail(PDA_ERR_INVALID_ARG, "plan is NULL");
+  if (plan->prob.kind != kind)
+    return fail(PDA_ERR_INVALID_ARG, "plan was created for the other kernel kind");
+  if (plan->prob.batch == 0) return PDA_OK;
+  const bool gqa = kind == PDA_KIND_GQA;
+  if (k_new == nullptr || k_cache == nullptr || (gqa && (v_new == nullptr || v_cache == nullptr)) ||
+      block_tables == nullptr || context_lens == nullptr)
+    return fail(PDA_ERR_INVALID_ARG, "a required tensor pointer is NULL");
+  if (!aligned(k_new, 16) || !aligned(k_cache, 16) ||
+      (gqa && (!aligned(v_new, 16) || !aligned(v_cache, 16))))
+    return fail(PDA_ERR_INVALID_ARG, "new values and caches must start on a 16-byte boundary");
+  if (!aligned(block_tables, 4) || !aligned(context_lens, 4))
+    return fail(PDA_ERR_INVALID_ARG, "block_tables and context_lens must be 4-byte aligned");
+  if (workspace == nullptr) return fail(PDA_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(workspace, 256))
+    return fail(PDA_ERR_WORKSPACE, "workspace must start on a 256-byte boundary");
+  pda::AppendArgs args{k_new, v_new, k_cache, v_cache, block_tables, context_lens, k_scale,
+                       v_scale};
+  const int e = pda::launch_append(*plan, args, pda::workspace_views(*plan, workspace), stream);
+  if (e != 0) return cuda_fail(e, "append launch");
+  return PDA_OK;
+}
+
+}  // namespace
+
+extern "C" PDA_API pda_status pda_kv_append(const void* k_new, const void* v_new, void* k_cache,
+                                            void* v_cache, const int32_t* block_tables,
+                                            const int32_t* context_lens, const pda_plan* plan,
+                                            void* workspace, pda_stream_t stream) {
+  pda::clear_error();
+  if (plan != nullptr && plan->prob.kv_format != PDA_KV_SAME_AS_Q)
+    return fail(PDA_ERR_INVALID_ARG, "the plan's caches are fp8: call pda_kv_append_fp8");
+  return append_call(PDA_KIND_GQA, k_new, v_new, k_cache, v_cache, 1.f, 1.f, block_tables,
+                     context_lens, plan, workspace, stream);
+}
+
+extern "C" PDA_API pda_status pda_kv_append_fp8(const void* k_new, const void* v_new,
+                                                void* k_cache, void* v_cache, float k_scale,
+                                                float v_scale, const int32_t* block_tables,
+                                                const int32_t* context_lens,
+                                                const pda_plan* plan, void* workspace,
+                                                pda_stream_t stream) {
+  pda::clear_error();
+  if (plan != nullptr && plan->prob.kv_format != PDA_KV_FP8_E4M3)
+    return fail(PDA_ERR_INVALID_ARG, "the plan's caches are not fp8: call pda_kv_append");
+  if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || k_scale == 0.f || v_scale == 0.f)
+    return fail(PDA_ERR_INVALID_ARG, "k_scale and v_scale must be finite and nonzero");
+  return append_call(PDA_KIND_GQA, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                     block_tables, context_lens, plan, workspace, stream);
+}
+
+extern "C" PDA_API pda_status pda_mla_append(const void* kv_new, void* kv_cache,
+                                             const int32_t* block_tables,
+                                             const int32_t* context_lens, const pda_plan* plan,
+                                             void* workspace, pda_stream_t stream) {
+  pda::clear_error();
+  return append_call(PDA_KIND_MLA, kv_new, nullptr, kv_cache, nullptr, 1.f, 1.f, block_tables,
+                     context_lens, plan, workspace, stream);
+}

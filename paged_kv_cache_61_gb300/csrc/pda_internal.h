@@ -93,6 +93,20 @@ struct MlaArgs {
 };
 int launch_mla_decode(const Plan& plan, const MlaArgs& args, const Workspace& ws, void* stream);
 
+// Append the S new tokens of each sequence to the caches (append.cu). GQA: k_new/v_new
+// [B][S][Hkv][D] into k_cache/v_cache; MLA: k_new [B][S][Dqk] into k_cache (v unused).
+struct AppendArgs {
+  const void* k_new;
+  const void* v_new;
+  void* k_cache;
+  void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  float k_scale = 1.f;
+  float v_scale = 1.f;
+};
+int launch_append(const Plan& plan, const AppendArgs& args, const Workspace& ws, void* stream);
+
 // Merge the pieces of the plan's heavy segments (launched after a decode kernel on the
 // same stream, overlapping its tail through programmatic dependent launch).
 int launch_split_merge(const Plan& plan, const Workspace& ws, void* out, float* lse, void* stream);

@@ -55,6 +55,7 @@ extern "C" PDA_API const char* pda_status_string(pda_status s) {
     case PDA_ERR_UNSUPPORTED: return "PDA_ERR_UNSUPPORTED";
     case PDA_ERR_WORKSPACE: return "PDA_ERR_WORKSPACE";
     case PDA_ERR_CUDA: return "PDA_ERR_CUDA";
+    case PDA_ERR_OUT_OF_BLOCKS: return "PDA_ERR_OUT_OF_BLOCKS";
   }
   return "PDA_ERR_UNKNOWN";
 }

@@ -14,7 +14,8 @@ from typing import Optional, Sequence
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpda.so")
 
-PDA_OK, PDA_ERR_INVALID_ARG, PDA_ERR_UNSUPPORTED, PDA_ERR_WORKSPACE, PDA_ERR_CUDA = range(5)
+(PDA_OK, PDA_ERR_INVALID_ARG, PDA_ERR_UNSUPPORTED, PDA_ERR_WORKSPACE, PDA_ERR_CUDA,
+ PDA_ERR_OUT_OF_BLOCKS) = range(6)
 PDA_FP16, PDA_BF16 = 0, 1
 PDA_KIND_GQA, PDA_KIND_MLA = 0, 1
 PDA_KV_SAME_AS_Q, PDA_KV_FP8_E4M3 = 0, 1
@@ -53,6 +54,14 @@ def _declare(lib):
         "mla_decode": (I32, [P, P, P, P, F32, P, P, P, P, P]),
         "pda_combine_splits": (I32, [P, P, I32, I32, I32, P, I32, P, P]),
         "paged_decode_attn_no_alloc": (I32, [P, P, P, P, P, F32, P, P, P, P]),
+        "pda_kv_append": (I32, [P, P, P, P, P, P, P, P, P]),
+        "pda_kv_append_fp8": (I32, [P, P, P, P, F32, F32, P, P, P, P, P]),
+        "pda_mla_append": (I32, [P, P, P, P, P, P, P]),
+        "pda_pool_create": (I32, [ctypes.POINTER(P), I64]),
+        "pda_pool_destroy": (None, [P]),
+        "pda_pool_num_free": (I64, [P]),
+        "pda_pool_grow": (I32, [P, P, I32, I32, I32, I32]),
+        "pda_pool_release": (I32, [P, P, I32, I32]),
         "pda_status_string": (ctypes.c_char_p, [I32]),
         "pda_last_error": (ctypes.c_char_p, []),
     }
@@ -60,7 +69,6 @@ def _declare(lib):
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    del I64
 
 
 def lib():
@@ -200,3 +208,69 @@ def combine_splits(partial_out, partial_lse, rows: int, num_splits: int, head_di
     _check(lib().pda_combine_splits(_ptr(partial_out), _ptr(partial_lse), rows, num_splits,
                                     head_dim_v, _ptr(out), out_dtype, _ptr(lse), _stream(stream)),
            "pda_combine_splits")
+
+
+def kv_append(k_new, v_new, k_cache, v_cache, block_tables, context_lens, plan: Plan, workspace,
+              stream=None):
+    """Write the S new tokens of each sequence into 16-bit GQA caches (see include/pda.h)."""
+    _check(lib().pda_kv_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                               _ptr(block_tables), _ptr(context_lens), plan.handle,
+                               _ptr(workspace), _stream(stream)), "pda_kv_append")
+
+
+def kv_append_fp8(k_new, v_new, k_cache, v_cache, k_scale: float, v_scale: float, block_tables,
+                  context_lens, plan: Plan, workspace, stream=None):
+    """kv_append into E4M3 caches: codes of value / scale."""
+    _check(lib().pda_kv_append_fp8(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                   float(k_scale), float(v_scale), _ptr(block_tables),
+                                   _ptr(context_lens), plan.handle, _ptr(workspace),
+                                   _stream(stream)), "pda_kv_append_fp8")
+
+
+def mla_append(kv_new, kv_cache, block_tables, context_lens, plan: Plan, workspace, stream=None):
+    """Write the S new MLA records of each sequence into the latent cache."""
+    _check(lib().pda_mla_append(_ptr(kv_new), _ptr(kv_cache), _ptr(block_tables),
+                                _ptr(context_lens), plan.handle, _ptr(workspace),
+                                _stream(stream)), "pda_mla_append")
+
+
+class BlockPool:
+    """Owns a ``pda_block_pool``: the free list of physical blocks behind block tables.
+
+    Table rows are int32 numpy arrays (host memory) that the calls update in place.
+    """
+
+    def __init__(self, num_blocks: int):
+        handle = ctypes.c_void_p()
+        _check(lib().pda_pool_create(ctypes.byref(handle), int(num_blocks)), "pda_pool_create")
+        self.handle = handle
+
+    @property
+    def num_free(self) -> int:
+        return int(lib().pda_pool_num_free(self.handle))
+
+    @staticmethod
+    def _row(row):
+        import numpy as np
+        if not (isinstance(row, np.ndarray) and row.dtype == np.int32 and row.flags.c_contiguous):
+            raise ValueError("table rows must be contiguous int32 numpy arrays")
+        return row.ctypes.data
+
+    def grow(self, table_row, page_size: int, old_len: int, new_len: int):
+        _check(lib().pda_pool_grow(self.handle, self._row(table_row), int(table_row.shape[0]),
+                                   int(page_size), int(old_len), int(new_len)), "pda_pool_grow")
+
+    def release(self, table_row, page_size: int, length: int):
+        _check(lib().pda_pool_release(self.handle, self._row(table_row), int(page_size),
+                                      int(length)), "pda_pool_release")
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib().pda_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
