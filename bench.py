@@ -277,6 +277,9 @@ def run_reference(args, workload):
     print(json.dumps(line))
 
 
+# decode steps that append each sequence's new token first (see run_gpu)
+STEP_WORKLOADS = ("gqa_b64_ctx1k_step", "gqa_b64_ctx1k_fp8_step", "mla_b16_ctx64k_h16_step")
+
 METRIC = "paged decode attn achieved HBM GB/s (% of GB300 peak), μs/step; MLA TFLOPS"
 
 
@@ -314,7 +317,11 @@ def run_gpu(args, workload, rank, world, local_rank):
     dist = None
     if world > 1:
         import torch.distributed as dist
-    case = synth.workload(workload, seed=rank)
+    # "<workload>_step": each step first appends one new token per sequence (the last of
+    # its context) through the append call, then decodes: a serving step's cache work
+    with_append = workload.endswith("_step")
+    case = synth.workload(workload[: -len("_step")] if with_append else workload, seed=rank)
+    case.name = workload
     kv_bytes, flops = accounting(case)
     tdt = torch.float16 if case.dtype == synth.FP16 else torch.bfloat16
 
@@ -355,8 +362,26 @@ def run_gpu(args, workload, rank, world, local_rank):
     stream = torch.cuda.current_stream()
     pda.workspace_init(plan, ws, stream)
 
+    new_shape = ((case.batch, S, case.num_kv_heads, case.head_dim_qk) if case.kind == "gqa"
+                 else (case.batch, S, case.head_dim_qk))
+    gen = torch.Generator(device="cuda").manual_seed(rank)
+    k_new = torch.randn(new_shape, generator=gen, device="cuda").to(tdt)
+    v_new = torch.randn(new_shape, generator=gen, device="cuda").to(tdt)
+
+    def append(i, tables_, ctx_, kn=k_new, vn=v_new):
+        kc, vc = caches[i % copies]
+        if case.kind == "gqa" and fp8:
+            pda.kv_append_fp8(kn, vn, kc, vc, case.k_scale, case.v_scale, tables_, ctx_, plan,
+                              ws, stream)
+        elif case.kind == "gqa":
+            pda.kv_append(kn, vn, kc, vc, tables_, ctx_, plan, ws, stream)
+        else:
+            pda.mla_append(kn, kc, tables_, ctx_, plan, ws, stream)
+
     def step(i, q_=q, out_=out, lse_=lse, tables_=tables, ctx_=ctx):
         kc, vc = caches[i % copies]
+        if with_append:
+            append(i, tables_, ctx_)
         if case.kind == "gqa" and fp8:
             pda.paged_decode_attn_fp8(q_, kc, vc, case.k_scale, case.v_scale, tables_, ctx_,
                                       case.scale, out_, lse_, plan, ws, stream)
@@ -427,8 +452,14 @@ def run_gpu(args, workload, rank, world, local_rank):
     q_d, tables_d, ctx_d = torch.empty_like(q), torch.empty_like(tables), torch.empty_like(ctx)
     h2d = q_h.numel() * q_h.element_size() + tables_h.numel() * 4 + ctx_h.numel() * 4
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+    kn_h, vn_h = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
+    if with_append:                          # the new tokens' K/V come from the host too
+        h2d += 2 * kn_h.numel() * kn_h.element_size()
 
     def e2e_step(i):
+        if with_append:
+            k_new.copy_(kn_h, non_blocking=True)
+            v_new.copy_(vn_h, non_blocking=True)
         q_d.copy_(q_h, non_blocking=True)
         tables_d.copy_(tables_h, non_blocking=True)
         ctx_d.copy_(ctx_h, non_blocking=True)
@@ -448,7 +479,7 @@ def run_gpu(args, workload, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
-    launches_per_step = 1 + (1 if _has_merge(plan, case) else 0)
+    launches_per_step = 1 + (1 if _has_merge(plan, case) else 0) + (1 if with_append else 0)
     pk, pk_src = peaks()
     # The kernel time the roofline divides by: the timed region's time per step. A step
     # is one decode launch, plus one split-merge launch when the plan has heavily split
@@ -482,8 +513,8 @@ def run_gpu(args, workload, rank, world, local_rank):
     roof["traffic"] = recorded_traffic(workload, kernel_kind(case))
     roof["algorithmic_bytes_per_launch"] = kv_bytes
     roof["mean_launch_us"] = mean_launch_ms * 1e3
-    roof["scope"] = ("decode kernel + split-merge kernel per step" if launches_per_step > 1
-                     else "decode kernel, one launch per step")
+    roof["scope"] = (("append kernel + " if with_append else "") + "decode kernel" +
+                     (" + split-merge kernel" if _has_merge(plan, case) else "") + " per step")
     roof["event_us_per_call"] = statistics.median(per_launch_ms) * 1e3
 
     cpu = None if args.no_cpu_baseline else cpu_baseline(workload)
@@ -511,7 +542,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=synth.WORKLOADS)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=synth.WORKLOADS + STEP_WORKLOADS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
