@@ -86,8 +86,11 @@ template <typename T, int COLS>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_heavy_kernel(const __grid_constant__ MergeParams p) {
   constexpr int kLanes = kMergeThreads / COLS;
-  // Wait until the decode grid that wrote the pieces has completed (programmatic
-  // dependent launch lets this grid be scheduled while that one drains).
+  // Let the next decode grid on the stream be scheduled early (its consumers wait for
+  // this grid to complete before they touch q, out, lse or the workspace), then wait
+  // until the decode grid that wrote the pieces has completed (programmatic dependent
+  // launch lets this grid be scheduled while that one drains).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ float sm_m[kLanes][COLS];
   __shared__ float sm_l[kLanes][COLS];
@@ -169,7 +172,9 @@ cudaError_t launch_merge_t(int cols, const cudaLaunchConfig_t& base, const Merge
   cfg.gridDim = dim3(unsigned(prm.count * prm.group * (prm.dv / (4 * cols))));
   switch (cols) {
     case 8: return cudaLaunchKernelEx(&cfg, merge_heavy_kernel<T, 8>, prm);
+    case 16: return cudaLaunchKernelEx(&cfg, merge_heavy_kernel<T, 16>, prm);
     case 32: return cudaLaunchKernelEx(&cfg, merge_heavy_kernel<T, 32>, prm);
+    case 64: return cudaLaunchKernelEx(&cfg, merge_heavy_kernel<T, 64>, prm);
     default: return cudaLaunchKernelEx(&cfg, merge_heavy_kernel<T, 128>, prm);
   }
 }
@@ -199,10 +204,13 @@ int launch_split_merge(const Plan& plan, const Workspace& ws, void* out, float* 
         (h.seg_start + h.np - 1) / plan.tiles_per_cta - h.seg_start / plan.tiles_per_cta + 1;
     max_pieces = std::max(max_pieces, int(pieces));
   }
-  // float4 columns per CTA: wide rows with few pieces, narrow rows with many
-  int cols = max_pieces >= 64 ? 8 : (max_pieces >= 16 ? 32 : 128);
-  cols = std::min(cols, prm.dv / 4);
-  if (cols != 8 && cols != 32 && cols != 128) cols = 8;
+  // float4 columns per CTA: the widest rows for which the CTA's piece lanes
+  // (kMergeThreads / cols of them, 4 loads each in flight) cover every piece in one round
+  // of loads; rows narrower than that with more pieces than 4 * kMergeThreads / 8
+  int cols = 128;
+  while (cols > 8 && 4 * (kMergeThreads / cols) < max_pieces) cols /= 2;
+  while (cols > prm.dv / 4) cols /= 2;
+  if (cols < 8 || (prm.dv / 4) % cols != 0) cols = 8;
   cudaLaunchConfig_t cfg{};
   cfg.blockDim = dim3(kMergeThreads);
   cfg.dynamicSmemBytes = 0;

@@ -266,6 +266,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
 
   // ============================== consumer warps ==============================
+  // The grid may start while the previous kernel on the stream drains (programmatic
+  // dependent launch; only this library's decode and split-merge kernels allow that).
+  // The producers above only read the caches, tables and lengths, which no such kernel
+  // writes; the consumers read q and write out, lse and the workspace, so they wait here
+  // until the previous grid has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int hsub = warp % NHT;
   const int pres = warp / NHT;
   const int tid = threadIdx.x;  // 0..127 among consumers
@@ -756,7 +762,18 @@ int launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const GqaParams& pr
                                     L::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  kern<<<grid, kThreads, L::kSmemBytes, stream>>>(tk, tv, prm);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tk, tv, prm);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
