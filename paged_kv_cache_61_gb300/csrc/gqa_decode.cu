@@ -84,6 +84,10 @@ struct GqaParams {
   int64_t num_blocks;
   float scale_log2;     // softmax scale (times k_scale for fp8 caches) times log2(e)
   float v_scale;        // fp8 caches: V dequantization scale (1 for 16-bit caches)
+  // fp8 caches: 0 = separate K and V maps; 1 = one map whose last dimension (extent 2,
+  // stride |v - k|) selects K then V, so one copy lands a page's K and V tiles; 2 = the
+  // same with V first (v_cache below k_cache)
+  int32_t kv_pair;
   int64_t total_tiles, tiles_per_cta;
   int32_t heavy_min;  // split segments with more pieces are merged by the split-merge kernel
   int32_t* err;
@@ -230,7 +234,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           // lane c copies tensor c & 1 (K, V) of page c >> 1 into [K A][V A][K B][V B].
           // fp8: box (D bytes, 1 kvh, 16 slots, 1 block); 16-bit: box (64 d, 16 slots,
           // D/64 d-blocks, 1 kvh, 1 block), landing as D/64 swizzled [16][64] sub-tiles.
-          if (lane < (two ? 4 : 2)) {
+          if (F8 && p.kv_pair != 0) {
+            // fp8, one map over both caches: lane c copies page c's K and V tiles at once
+            if (lane < (two ? 2 : 1)) {
+              uint8_t* dst = ring + stage * L::kStageBytes + lane * 2 * L::kTileBytes;
+              ptx::tma_load_5d(dst, &tm_k, &full[stage], 0, pt.seg, 0, lane ? phys2 : phys, 0,
+                               policy);
+            }
+          } else if (lane < (two ? 4 : 2)) {
             const CUtensorMap* map = (lane & 1) ? &tm_v : &tm_k;
             uint8_t* dst = ring + stage * L::kStageBytes + lane * L::kTileBytes;
             const int32_t ph = (lane >> 1) ? phys2 : phys;
@@ -357,7 +368,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int pg0 = (pt.p0 + i * kPPT) * kPage;  // first token of page A
         const int vld[2] = {min(kPage, ctx - pg0),
                             (i * kPPT + 1 < npg) ? min(kPage, ctx - pg0 - kPage) : 0};
-        const uint32_t kpg[2] = {kb, kb + 2 * L::kTileBytes};
+        // a page's two tiles: K then V, or V then K when one map reads V first
+        const uint32_t koff = p.kv_pair == 2 ? L::kTileBytes : 0;
+        const uint32_t voff = p.kv_pair == 2 ? 0 : L::kTileBytes;
+        const uint32_t kpg[2] = {kb + koff, kb + 2 * L::kTileBytes + koff};
         // S^T = K * Q^T for both pages: two independent accumulation chains. One
         // ldmatrix.x4 covers two k-steps: matrices (tokens 0-7 | 8-15) x (chunk ks |
         // ks+1) of 16 bytes; a lane gets 4 consecutive bytes (dims) of one token.
@@ -445,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // of tokens cq, cq+1. After a byte permute the pairs are (tokens cq, cq+1) of
         // dim 2*r0 and of dim 2*r0+1, so row r0 of m-tile mt is dim 16mt + 2*r0 and row
         // r0+8 is the next dim.
-        const uint32_t vpg[2] = {kb + L::kTileBytes, kb + 3 * L::kTileBytes};
+        const uint32_t vpg[2] = {kb + voff, kb + 2 * L::kTileBytes + voff};
 #pragma unroll
         for (int mt = 0; mt < kKS; mt += 2) {
           uint32_t y[2][4];
@@ -750,6 +764,33 @@ bool encode_cache_map_f8(CUtensorMap* map, const void* base, int64_t num_blocks,
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// One map over both E4M3 caches: dims (d, kvh, slot, block, tensor) where the tensor
+// dimension (extent 2) steps from the lower of the two cache addresses to the other, so
+// one copy of box (D, 1, P, 1, 2) lands a page's two tiles back to back. Only
+// coordinates 0 and 1 of that dimension are ever read, i.e. the two caches themselves.
+bool encode_cache_pair_f8(CUtensorMap* map, const void* k, const void* v, int64_t num_blocks,
+                          int page, int hkv, int d, int32_t* order) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const uintptr_t ka = reinterpret_cast<uintptr_t>(k), va = reinterpret_cast<uintptr_t>(v);
+  const uintptr_t lo = ka < va ? ka : va, gap = ka < va ? va - ka : ka - va;
+  const uint64_t cache_bytes = uint64_t(num_blocks) * page * hkv * d;
+  if (gap < cache_bytes || gap % 16 != 0 || gap >= (uint64_t(1) << 40)) return false;
+  const cuuint64_t dims[5] = {cuuint64_t(d), cuuint64_t(hkv), cuuint64_t(page),
+                              cuuint64_t(num_blocks), 2};
+  const cuuint64_t strides[4] = {cuuint64_t(d), cuuint64_t(hkv) * d,
+                                 cuuint64_t(page) * hkv * d, cuuint64_t(gap)};
+  const cuuint32_t box[5] = {cuuint32_t(d), 1, cuuint32_t(page), 1, 2};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  if (fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, reinterpret_cast<void*>(lo), dims, strides, box,
+         estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  *order = ka < va ? 1 : 2;
+  return true;
+}
+
 template <int D, typename T, int NHT, bool F8>
 int launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const GqaParams& prm, int grid,
                cudaStream_t stream) {
@@ -839,6 +880,17 @@ int launch_gqa_decode(const Plan& plan, const GqaArgs& a, const Workspace& ws, v
                                 pr.head_dim_v, bf16);
   if (!maps_ok) return -1;
   GqaParams prm{};
+  // fp8: when one map can span both caches, a page's K and V come in one copy (the
+  // producer's copy issue, not HBM, bounds the fp8 kernel)
+  if (f8) {
+    CUtensorMap pair;
+    int32_t order = 0;
+    if (encode_cache_pair_f8(&pair, a.k_cache, a.v_cache, pr.num_blocks, pr.page_size,
+                             pr.num_kv_heads, pr.head_dim_qk, &order)) {
+      tk = pair;
+      prm.kv_pair = order;
+    }
+  }
   prm.q = a.q;
   prm.out = a.out;
   prm.lse = a.lse;

@@ -168,3 +168,28 @@ def test_full_size_workload_sampled_rows(name):
     bs = sorted({0, case.batch // 2, case.batch - 1})
     rows = [(b, h) for b in bs for h in sorted({0, 1, hq // 2, hq - 1})]
     _assert_close(case, DeviceCase(case), rows=rows)
+
+
+@pytest.mark.parametrize("layout", ["v_below_k", "one_buffer", "same_buffer"])
+def test_cache_placements(layout):
+    # The fp8 path reads a page's K and V with one copy through a map spanning both caches
+    # when it can: K below V, V below K (its tiles land in the other order), K and V as
+    # halves of one [2, ...] buffer; with K and V the same buffer it uses separate maps.
+    case = _case(synth.BF16, 128, 16, 2, [300, 17, 64], seed=12)
+    if layout == "same_buffer":
+        case.v_cache = case.k_cache.copy()
+        case.v_scale = case.k_scale
+    dc = DeviceCase(case)
+    k = torch.from_numpy(case.k_cache).cuda()
+    v = torch.from_numpy(case.v_cache).cuda()
+    if layout == "v_below_k":
+        both = torch.empty((2,) + k.shape, dtype=torch.uint8, device="cuda")
+        both[0].copy_(v)
+        both[1].copy_(k)
+        dc.v, dc.k = both[0], both[1]
+    elif layout == "one_buffer":
+        both = torch.stack([k, v])
+        dc.k, dc.v = both[0], both[1]
+    else:
+        dc.k = dc.v = k
+    _assert_close(case, dc)
