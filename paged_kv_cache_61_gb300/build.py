@@ -20,6 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpda.so")
 SOURCES = ["plan.cpp", "api.cpp", "gqa_decode.cu", "combine.cu", "mla_decode.cu", "mla_pair.cu",
+           "mla_rows.cu",
            "no_alloc.cu", "append.cu", "pool.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

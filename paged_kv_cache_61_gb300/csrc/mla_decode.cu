@@ -34,6 +34,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "mla_maps.h"
 #include "pda_internal.h"
 #include "ptx.cuh"
 #include "tile_walk.cuh"
@@ -264,7 +265,8 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
     // One thread polls for whichever MMA group is ready and issues it: the scores of
     // the next page (its data, q and an S^T buffer are ready) or the PV of the oldest
     // page whose P^T is written. PV never waits behind the next page's load, so the
-    // stage it frees is refilled as early as possible.
+    // stage it frees is refilled as early as possible. The polls are non-blocking tests
+    // (a try_wait may suspend the thread while another group is ready).
     constexpr uint32_t kIdQK = ptx::umma_idesc_f16(64, N, 0, 0, kBf16);
     constexpr uint32_t kIdPV = ptx::umma_idesc_f16(128, N, 1, 1, kBf16);
     const uint32_t kv_s = ptx::smem_addr(kv);
@@ -274,7 +276,7 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
       int u = 0, i = 0, npg = 0;
       bool have = false, need_q = false, qk_done = false;
       uint32_t first_bits = 0;   // bit (t & 31): page t is the first of its piece
-      uint64_t last_progress = ptx::globaltimer();
+      ptx::Watchdog watchdog;
       while (true) {
         bool progress = false;
         if (!qk_done && (!have || i == npg)) {
@@ -291,9 +293,9 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
         if (!qk_done && i < npg) {
           const int s = t_qk & 1;          // S^T buffer
           const int kst = t_qk % KS;       // ring stage
-          const bool ready = (!need_q || ptx::mbar_try_wait(q_full, u & 1)) &&
-                             ptx::mbar_try_wait(&kv_full[kst], (t_qk / KS) & 1) &&
-                             (t_qk < 2 || ptx::mbar_try_wait(&s_free[s], ((t_qk >> 1) - 1) & 1));
+          const bool ready = (!need_q || ptx::mbar_test_wait(q_full, u & 1)) &&
+                             ptx::mbar_test_wait(&kv_full[kst], (t_qk / KS) & 1) &&
+                             (t_qk < 2 || ptx::mbar_test_wait(&s_free[s], ((t_qk >> 1) - 1) & 1));
           if (ready) {
             need_q = false;
             ptx::tc_fence_after();
@@ -318,7 +320,7 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
             progress = true;
           }
         }
-        if (t_pv < t_qk && ptx::mbar_try_wait(&p_full[t_pv & 1], (t_pv >> 1) & 1)) {
+        if (t_pv < t_qk && ptx::mbar_test_wait(&p_full[t_pv & 1], (t_pv >> 1) & 1)) {
           ptx::tc_fence_after();
           const bool first = (first_bits >> (t_pv & 31)) & 1u;
           const uint32_t st = kv_s + (t_pv % KS) * kPageBytes;
@@ -340,8 +342,8 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
         }
         if (qk_done && t_pv == t_qk) break;
         if (progress) {
-          last_progress = ptx::globaltimer();
-        } else if (flags[0] || ptx::globaltimer() - last_progress > ptx::kWaitLimitNs) {
+          watchdog.progress();
+        } else if (flags[0] || watchdog.expired()) {
           flags[0] = 1;
           atomicOr(p.err, 2);
           break;
@@ -654,7 +656,10 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
   }
 }
 
+}  // namespace
+
 // ------------------------------------------------------------------ host side
+namespace {
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -676,10 +681,8 @@ EncodeTiledFn mla_encode_fn() {
   return fn;
 }
 
-// With S = dqk / 64 sub-tiles per record (9 for 576, 5 for 320):
-// q [rows, dqk]: dims (d mod 64, row, d / 64), box (64, N, S) -> S [N][64] sub-tiles.
-// kv [blocks, 64, dqk]: dims (d mod 64, slot, d / 64, block), box (64, 64, S, 1) ->
-// S [64][64] sub-tiles per page. Both with 128-byte swizzle.
+}  // namespace
+
 bool encode_mla_maps(CUtensorMap* tq, CUtensorMap* tkv, const void* q, int64_t rows, int n,
                      const void* kv, int64_t num_blocks, bool bf16, int dqk) {
   EncodeTiledFn fn = mla_encode_fn();
@@ -704,6 +707,8 @@ bool encode_mla_maps(CUtensorMap* tq, CUtensorMap* tkv, const void* q, int64_t r
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 template <int N, int DQK, typename T>
 int launch_mla_n(const CUtensorMap& tq, const CUtensorMap& tkv, const MlaParams& prm, int grid,
@@ -742,6 +747,7 @@ int launch_mla_dt(int dqk, int n, const CUtensorMap& tq, const CUtensorMap& tkv,
 int mla_heads_per_cta(const pda_problem& p) {
   if (p.seq_len_q > 1) return p.seq_len_q * p.num_q_heads;  // all rows of a sequence
   if (mla_uses_pairs(p)) return 128;   // one 128-head group per CTA pair
+  if (mla_uses_rows(p)) return 128;    // one 128-head group per CTA, heads on M
   return p.num_q_heads <= 64 ? p.num_q_heads : 64;
 }
 int mla_ctas_per_sm(const pda_problem&) { return 1; }
@@ -786,6 +792,7 @@ bool mla_supported(const pda_problem& p, std::string* why) {
 
 int launch_mla_decode(const Plan& plan, const MlaArgs& a, const Workspace& ws, void* stream) {
   if (plan.cluster == 2) return launch_mla_pair(plan, a, ws, stream);
+  if (mla_uses_rows(plan.prob)) return launch_mla_rows(plan, a, ws, stream);
   const pda_problem& pr = plan.prob;
   const bool bf16 = pr.dtype == PDA_BF16;
   const int n = plan.group;

@@ -312,7 +312,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t ph_qk = 0;
       bool have = false, need_q = false, qk_done = false;
       uint32_t first_bits = 0;   // bit (t & 31): page t is the first of its piece
-      uint64_t last_progress = ptx::globaltimer();
+      ptx::Watchdog watchdog;
       while (true) {
         bool progress = false;
         if (!qk_done && (!have || i == npg)) {
@@ -327,9 +327,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         if (!qk_done && i < npg) {
-          const bool ready = (!need_q || ptx::mbar_try_wait(q_full, u & 1)) &&
-                             ptx::mbar_try_wait(&kv_full[st_qk], ph_qk) &&
-                             (t_qk == 0 || ptx::mbar_try_wait(s_free, (t_qk - 1) & 1));
+          const bool ready = (!need_q || ptx::mbar_test_wait(q_full, u & 1)) &&
+                             ptx::mbar_test_wait(&kv_full[st_qk], ph_qk) &&
+                             (t_qk == 0 || ptx::mbar_test_wait(s_free, (t_qk - 1) & 1));
           if (ready) {
             if (need_q) ++u;
             need_q = false;
@@ -360,7 +360,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             progress = true;
           }
         }
-        if (t_pv < t_qk && ptx::mbar_try_wait(&p_full[t_pv & 1], (t_pv >> 1) & 1)) {
+        if (t_pv < t_qk && ptx::mbar_test_wait(&p_full[t_pv & 1], (t_pv >> 1) & 1)) {
           ptx::tc_fence_after();
           const bool first = (first_bits >> (t_pv & 31)) & 1u;
           const uint32_t stg = kv_s + st_pv * kStageBytes;
@@ -383,8 +383,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (qk_done && t_pv == t_qk) break;
         if (progress) {
-          last_progress = ptx::globaltimer();
-        } else if (flags[0] || ptx::globaltimer() - last_progress > ptx::kWaitLimitNs) {
+          watchdog.progress();
+        } else if (flags[0] || watchdog.expired()) {
           flags[0] = 1;
           atomicOr(p.err, 2);
           break;
@@ -623,7 +623,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // this warp's 8 KB staging block: [token half][32 rows][32 fp32]
       const uint32_t sblk = ptx::smem_addr(sstg) + uint32_t(gw) * (32 * kPage * 4);
       const uint32_t srow = sblk + uint32_t(lane) * (kHalfTok * 4);
-      uint64_t last = ptx::globaltimer();
+      ptx::Watchdog watchdog;
       while (t < total) {
         if (flags[0]) aborted = true;
         aborted = __any_sync(kFullMask, aborted);
@@ -709,8 +709,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         if (progress) {
-          last = ptx::globaltimer();
-        } else if (ptx::globaltimer() - last > ptx::kWaitLimitNs) {
+          watchdog.progress();
+        } else if (watchdog.expired()) {
           if (lane == 0) {
             flags[0] = 1;
             atomicOr(p.err, 2);
@@ -782,18 +782,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0 && !aborted) ptx::mbar_arrive_remote_relaxed(remote(&xs_free[b2]));
           const int nv = nvalid - kHalfTok * pos;   // valid tokens of this half
+          // The largest scaled score is the scale times the largest raw score (scale >= 0)
+          // or the smallest (scale < 0); masked tokens take no part in it.
+          const float sc = p.scale_log2;
+          const bool neg = sc < 0.f;
           if (nv < kHalfTok) {
 #pragma unroll
             for (int j = 0; j < kHalfTok; ++j)
-              if (j >= nv) v[j] = -INFINITY;
+              if (j >= nv) v[j] = neg ? INFINITY : -INFINITY;
           }
           float smax = v[0];
+          if (neg) {
 #pragma unroll
-          for (int j = 1; j < kHalfTok; ++j) smax = fmaxf(smax, v[j]);
-          // the head's maximum over both halves (the two warps agree on every decision)
+            for (int j = 1; j < kHalfTok; ++j) smax = fminf(smax, v[j]);
+          } else {
+#pragma unroll
+            for (int j = 1; j < kHalfTok; ++j) smax = fmaxf(smax, v[j]);
+          }
+          // the head's extreme over both halves (the two warps agree on every decision)
           hmx[pos * kOwnHeads + r] = smax;
           ptx::named_barrier_sync(pair_bar, 64);
-          const float mx = fmaxf(hmx[r], hmx[kOwnHeads + r]) * p.scale_log2;
+          const float ext = neg ? fminf(hmx[r], hmx[kOwnHeads + r])
+                                : fmaxf(hmx[r], hmx[kOwnHeads + r]);
+          const float mx = ext * sc;
           float alpha = 1.f;
           bool need = false;
           if (i == 0) {
@@ -812,8 +823,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           float lsum = 0.f, lqsum = 0.f;
 #pragma unroll
           for (int j = 0; j < kHalfTok / 2; ++j) {
-            const float p0 = ptx::exp2_approx(fmaf(v[2 * j], p.scale_log2, -m));
-            const float p1 = ptx::exp2_approx(fmaf(v[2 * j + 1], p.scale_log2, -m));
+            float p0 = ptx::exp2_approx(fmaf(v[2 * j], sc, -m));
+            float p1 = ptx::exp2_approx(fmaf(v[2 * j + 1], sc, -m));
+            if (nv < kHalfTok) {   // masked tokens weigh 0 (whatever the scale's sign)
+              if (2 * j >= nv) p0 = 0.f;
+              if (2 * j + 1 >= nv) p1 = 0.f;
+            }
             pk[j] = pack2<T>(p0, p1);
             lsum += p0 + p1;
             lqsum += sum2<T>(pk[j]);

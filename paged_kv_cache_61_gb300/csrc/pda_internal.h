@@ -128,6 +128,11 @@ bool mla_uses_pairs(const pda_problem& p);
 int mla_pair_units(int num_sms);   // co-resident CTA pairs (falls back to num_sms / 2)
 int launch_mla_pair(const Plan& plan, const MlaArgs& args, const Workspace& ws, void* stream);
 
+// MLA with the 320-wide record and head groups of 128: one group per CTA, the heads on
+// the MMA's M axis (mla_rows.cu).
+bool mla_uses_rows(const pda_problem& p);
+int launch_mla_rows(const Plan& plan, const MlaArgs& args, const Workspace& ws, void* stream);
+
 }  // namespace pda
 
 // The opaque handle of the C ABI is the planner's record.

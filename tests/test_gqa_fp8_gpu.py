@@ -67,6 +67,16 @@ def test_small_cases(dtype, d, hq, hkv, ctx, force):
     _assert_close(case, DeviceCase(case, force_num_ctas=force))
 
 
+@pytest.mark.parametrize("k_scale", [-0.02, 0.0])
+def test_negative_and_zero_k_scale(k_scale):
+    # k_scale folds into the softmax scale: a negative one flips the scores' order, zero
+    # gives uniform weights
+    case = _case(synth.BF16, 128, 16, 2, [300, 17, 64, 1], seed=13)
+    case.k_scale = k_scale
+    for force in (0, 5):
+        _assert_close(case, DeviceCase(case, force_num_ctas=force))
+
+
 def test_tiny_workload():
     case = synth.workload("gqa_tiny_fp8")
     _assert_close(case, DeviceCase(case))

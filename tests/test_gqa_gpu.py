@@ -71,6 +71,16 @@ def test_small_cases(dtype, d, hq, hkv, ctx, force):
     _assert_close(case, DeviceCase(case, force_num_ctas=force))
 
 
+@pytest.mark.parametrize("scale", [-0.09, 0.0])
+@pytest.mark.parametrize("hkv", [8, 1])
+def test_negative_and_zero_scale(scale, hkv):
+    # any finite scale: negative (the scores' order flips) or zero (uniform weights)
+    case = _case(synth.FP16, 128, 32, hkv, [300, 17, 64, 1], seed=14)
+    case.scale = scale
+    for force in (0, 5):
+        _assert_close(case, DeviceCase(case, force_num_ctas=force))
+
+
 def test_split_count_invariance():
     case = _case(synth.BF16, 128, 32, 8, [4000, 70, 1500])
     ref = _oracle(case)

@@ -54,6 +54,18 @@ def test_small_cases(hq, force, latent):
 
 @pytest.mark.parametrize("latent", [512, 256])
 @pytest.mark.parametrize("hq", [16, 128])
+@pytest.mark.parametrize("scale", [-0.07, 0.0])
+def test_negative_and_zero_scale(hq, latent, scale):
+    # the softmax takes any finite scale: negative (the row maximum of the scaled scores
+    # is scale times the smallest raw score) and zero (uniform weights over the context)
+    case = _case(hq, [1, 64, 65, 700], latent=latent)
+    case.scale = scale
+    for force in (0, 3):
+        _assert_close(case, DeviceCase(case, force_num_ctas=force))
+
+
+@pytest.mark.parametrize("latent", [512, 256])
+@pytest.mark.parametrize("hq", [16, 128])
 def test_fp16(hq, latent):
     case = _case(hq, [200, 64, 1], dtype=synth.FP16, latent=latent)
     _assert_close(case, DeviceCase(case))
@@ -123,20 +135,22 @@ def test_rope_needle_is_bit_exact(hq, latent):
                 assert np.array_equal(got[b, h], case.kv_cache[blk, t % 64, :latent]), (force, b, h)
 
 
-def test_ctx1_returns_latent_of_token0():
-    case = _case(128, [1, 1])
+@pytest.mark.parametrize("latent", [512, 256])
+def test_ctx1_returns_latent_of_token0(latent):
+    case = _case(128, [1, 1], latent=latent)
     dc = DeviceCase(case)
     out, _ = _assert_close(case, dc)
     got = device_bits(out)
     for b in range(2):
         blk = int(case.block_tables[b, 0])
         for h in range(128):
-            assert np.array_equal(got[b, h], case.kv_cache[blk, 0, :512])
+            assert np.array_equal(got[b, h], case.kv_cache[blk, 0, :latent])
 
 
+@pytest.mark.parametrize("latent", [512, 256])
 @pytest.mark.parametrize("hq", [32, 128])
-def test_poisoned_stale_slots_and_table_entries(hq):
-    case = _case(hq, [70, 129, 5])
+def test_poisoned_stale_slots_and_table_entries(hq, latent):
+    case = _case(hq, [70, 129, 5], latent=latent)
     out0, lse0 = DeviceCase(case).run()
     torch.cuda.synchronize()
     kv, tab = case.kv_cache.copy(), case.block_tables.copy()
