@@ -40,8 +40,11 @@ from paged_kv_cache_61_gb300 import synth, traffic  # noqa: E402
 DEFAULT_WORKLOAD = "gqa_b64_ctx1k"
 L2_BYTES = 129 * 2 ** 20
 KERNEL_SOURCES = {"gqa": ["gqa_decode.cu", "ptx.cuh", "tile_walk.cuh"],
-                  "mla": ["mla_decode.cu", "ptx.cuh", "tile_walk.cuh"],
-                  "mla_pair": ["mla_pair.cu", "ptx.cuh", "ptx_cluster.cuh", "tile_walk.cuh"]}
+                  "mla": ["mla_decode.cu", "ptx.cuh", "ptx_ext.cuh", "tile_walk.cuh"],
+                  "mla_pair": ["mla_pair.cu", "ptx.cuh", "ptx_ext.cuh", "ptx_cluster.cuh",
+                               "tile_walk.cuh"],
+                  "mla_rows": ["mla_rows.cu", "ptx.cuh", "ptx_ext.cuh", "ptx_cluster.cuh",
+                               "tile_walk.cuh"]}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -71,12 +74,17 @@ def kernel_hash(kind: str) -> str:
 
 
 def kernel_kind(case) -> str:
-    """Which decode kernel a case runs on (576-wide MLA records with head groups of 128 use
-    the two-CTA kernel; every other MLA shape the single-CTA one)."""
+    """Which decode kernel a case runs on. MLA with head groups of 128 (one query token):
+    the two-CTA kernel for the 576-wide record, the heads-on-M kernel for the 320-wide one;
+    every other MLA shape the 64-head kernel."""
     if case.kind == "gqa":
         return "gqa"
-    pair = case.head_dim_qk == 576 and case.num_q_heads % 128 == 0
-    return "mla_pair" if pair else "mla"
+    if case.num_q_heads % 128 == 0 and case.seq_len_q <= 1:
+        if case.head_dim_qk == 576:
+            return "mla_pair"
+        if case.head_dim_qk == 320:
+            return "mla_rows"
+    return "mla"
 
 
 def recorded_traffic(workload: str, kind: str):

@@ -37,6 +37,7 @@
 #include "mla_maps.h"
 #include "pda_internal.h"
 #include "ptx.cuh"
+#include "ptx_ext.cuh"
 #include "tile_walk.cuh"
 
 namespace pda {

@@ -40,6 +40,7 @@
 
 #include "pda_internal.h"
 #include "ptx.cuh"
+#include "ptx_ext.cuh"
 #include "ptx_cluster.cuh"
 #include "tile_walk.cuh"
 

@@ -33,6 +33,7 @@
 #include "mla_maps.h"
 #include "pda_internal.h"
 #include "ptx.cuh"
+#include "ptx_ext.cuh"
 #include "ptx_cluster.cuh"
 #include "tile_walk.cuh"
 
@@ -202,9 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============================== MMA issuer ==============================
     // One thread issues whichever MMA group is ready, PV first: the PV of the oldest page
     // whose P is written, the scores of the next page (its data and q ready, the previous
-    // page's S read). It polls with non-blocking tests and reads the global timer only
-    // while idle: a timer read per issued group left the tensor pipe idle ~800 cycles of
-    // a page's ~2600.
+    // page's S read). The MMAs of a group go out back to back: any other work between
+    // them (a barrier test costs about as much as an MMA) leaves the tensor pipe idle.
     constexpr uint32_t kIdQK = ptx::umma_idesc_f16(kRows, kPage, 0, 0, kBf16);
     constexpr uint32_t kIdPV = ptx::umma_idesc_f16(kRows, kDv, 0, 1, kBf16);
     const uint32_t kv_s = ptx::smem_addr(kv);
