@@ -524,6 +524,7 @@ def run_gpu(args, workload, rank, world, local_rank):
     roof["scope"] = (("append kernel + " if with_append else "") + "decode kernel" +
                      (" + split-merge kernel" if _has_merge(plan, case) else "") + " per step")
     roof["event_us_per_call"] = statistics.median(per_launch_ms) * 1e3
+    roof["event_us_per_call_min"] = min(per_launch_ms) * 1e3
 
     cpu = None if args.no_cpu_baseline else cpu_baseline(workload)
     line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
