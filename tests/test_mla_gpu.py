@@ -71,11 +71,12 @@ def test_fp16(hq, latent):
     _assert_close(case, DeviceCase(case))
 
 
-@pytest.mark.parametrize("hq", [128, 192])
+@pytest.mark.parametrize("hq", [128, 192, 256])
 @pytest.mark.parametrize("force", [0, 2, 5])
 def test_rank256_several_head_groups_ragged_batch(hq, force):
-    # the 320-wide record runs 64-head groups on single CTAs: several groups per
-    # sequence, ragged last pages, a one-token sequence, split sequences
+    # the 320-wide record: head groups of 128 on one CTA each (Hq = 128, 256: one or two
+    # groups per sequence), 64-head groups otherwise (Hq = 192: three); ragged last pages,
+    # a one-token sequence, split sequences
     case = _case(hq, [1, 65, 127, 128, 129, 1000, 3000], seed=11, latent=256)
     _assert_close(case, DeviceCase(case, force_num_ctas=force))
 
