@@ -74,13 +74,13 @@ def kernel_hash(kind: str) -> str:
 
 
 def kernel_kind(case) -> str:
-    """Which decode kernel a case runs on. MLA with head groups of 128 (one query token):
-    the two-CTA kernel for the 576-wide record, the heads-on-M kernel for the 320-wide one;
-    every other MLA shape the 64-head kernel."""
+    """Which decode kernel a case runs on. MLA with head counts a multiple of 128: the
+    two-CTA kernel for the 576-wide record (one query token), the heads-on-M kernel for the
+    320-wide one; every other MLA shape the 64-head kernel."""
     if case.kind == "gqa":
         return "gqa"
-    if case.num_q_heads % 128 == 0 and case.seq_len_q <= 1:
-        if case.head_dim_qk == 576:
+    if case.num_q_heads % 128 == 0:
+        if case.head_dim_qk == 576 and case.seq_len_q <= 1:
             return "mla_pair"
         if case.head_dim_qk == 320:
             return "mla_rows"

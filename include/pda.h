@@ -90,10 +90,11 @@ typedef struct pda_problem {
   int32_t force_num_ctas;     /* 0 = automatic; > 0 = split the work over exactly this many CTAs */
   int32_t kv_format;          /* pda_kv_format of the caches (0 = same type as q) */
   int32_t seq_len_q;          /* S, query tokens per sequence; 0 or 1 = single-token decode.
-                                 S > 1 (speculative / MTP decoding; GQA only): query token i
-                                 of sequence b sits at position ctx_b - S + i and attends to
+                                 S > 1 (speculative / MTP decoding): query token i of
+                                 sequence b sits at position ctx_b - S + i and attends to
                                  tokens 0 .. ctx_b - S + i (causal, bottom-right aligned);
-                                 every ctx_b >= S and S * Hq / Hkv <= 32 */
+                                 every ctx_b >= S. GQA: S * Hq / Hkv <= 32. MLA (16-bit
+                                 records): S * Hq in {16, 32, 64}, or Hq a multiple of 64 */
 } pda_problem;
 
 typedef struct pda_plan pda_plan;  /* opaque, owned by the library */
@@ -190,12 +191,15 @@ PDA_API pda_status paged_decode_attn_fp8(const void* q, const void* k_cache, con
  * per token of Dqk = head_dim_qk values, Dv = head_dim_v latent then 64 rope,
  * with (Dqk, Dv) = (576, 512) (kv_lora_rank 512) or (320, 256) (kv_lora_rank
  * 256). Scores use all Dqk values, values are the first Dv.
- *   q             device [B, Hq, Dqk] dtype (absorbed content query then rope query)
+ *   q             device [B, Hq, Dqk] dtype (absorbed content query then rope query);
+ *                 [B, S, Hq, Dqk] when the plan's seq_len_q S > 1
  *   kv_cache      device [num_blocks, 64, Dqk] dtype (one KV head)
  *   block_tables, context_lens, scale, plan (kind PDA_KIND_MLA), workspace: as above
- *   out           device [B, Hq, Dv] dtype
- *   lse           device [B, Hq] float32 or NULL
- * Hq: 16, 32 or a multiple of 64.
+ *   out           device [B, Hq, Dv] dtype; [B, S, Hq, Dv] when S > 1
+ *   lse           device [B, Hq] float32 or NULL; [B, Hq, S] when S > 1
+ * Hq: 16, 32 or a multiple of 64. With S > 1: S * Hq in {16, 32, 64}, or Hq a multiple
+ * of 64 (the heads of each query token are then separate head groups, each reading the
+ * sequence's pages).
  */
 PDA_API pda_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_tables,
                       const int32_t* context_lens, float scale, void* out, float* lse,

@@ -79,6 +79,8 @@ struct MergeParams {
   int64_t tiles_per_cta;
   int32_t group, dv, num_q_heads, count;
   int32_t heads_per_seg, seq_len_q;  // G and S of the segments' rows (row r = i*G + g)
+  // MLA: segment seg holds rows R = seg*group + r of the sequence's S*Hq rows (R = i*Hq + h)
+  int32_t mla_rows;
   HeavySegment seg[kMaxHeavySegments];
 };
 
@@ -156,7 +158,16 @@ __global__ void __launch_bounds__(kMergeThreads)
       s.z += f * sm_o[r][col].z; s.w += f * sm_o[r][col].w;
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
-    const RowIndex ri = seg_row(hs.b, hs.seg, j, p.heads_per_seg, p.seq_len_q, p.num_q_heads);
+    RowIndex ri;
+    if (p.mla_rows) {
+      const int R = hs.seg * p.group + j;
+      const int qi = R / p.num_q_heads;
+      const int h = R - qi * p.num_q_heads;
+      ri = {(int64_t(hs.b) * p.seq_len_q + qi) * p.num_q_heads + h,
+            (int64_t(hs.b) * p.num_q_heads + h) * p.seq_len_q + qi};
+    } else {
+      ri = seg_row(hs.b, hs.seg, j, p.heads_per_seg, p.seq_len_q, p.num_q_heads);
+    }
     T* out = static_cast<T*>(p.out) + ri.out_row * p.dv + dofs;
     out[0] = to_out<T>(s.x * inv);
     out[1] = to_out<T>(s.y * inv);
@@ -195,6 +206,7 @@ int launch_split_merge(const Plan& plan, const Workspace& ws, void* out, float* 
   prm.num_q_heads = plan.prob.num_q_heads;
   prm.heads_per_seg = plan.heads_per_seg;
   prm.seq_len_q = plan.seq_len_q;
+  prm.mla_rows = plan.prob.kind == PDA_KIND_MLA ? 1 : 0;
   prm.count = int32_t(plan.heavy.size());
   int max_pieces = 0;
   for (size_t i = 0; i < plan.heavy.size(); ++i) {

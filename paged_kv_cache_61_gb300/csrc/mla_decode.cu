@@ -424,11 +424,11 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
         const bool valid = active && token < ctx && !aborted;
         float x[NC];
         load_scores(valid, x);
-        // causal rows (S > 1, one head group holding all S*Hq rows): row R = i*Hq + h,
+        // causal rows (S > 1): row R = i*Hq + h of the sequence (R = seg*N + column),
         // query token i, sees tokens [0, ctx - S + 1 + i). Token ctx - S + 1 + k is hidden
         // from the rows of query tokens 0..k, i.e. rows R < (k + 1) * Hq.
         if (valid && token >= ctx - p.seq_len_q + 1) {
-          const int cut = (token - (ctx - p.seq_len_q)) * p.num_q_heads - cb;
+          const int cut = (token - (ctx - p.seq_len_q)) * p.num_q_heads - pt.seg * N - cb;
 #pragma unroll
           for (int h = 0; h < NC; ++h)
             if (h < cut) x[h] = -INFINITY;
@@ -754,7 +754,11 @@ int launch_mla_dt(int dqk, int n, const CUtensorMap& tq, const CUtensorMap& tkv,
 }  // namespace
 
 int mla_heads_per_cta(const pda_problem& p) {
-  if (p.seq_len_q > 1) return p.seq_len_q * p.num_q_heads;  // all rows of a sequence
+  if (p.seq_len_q > 1) {
+    const int64_t rows = int64_t(p.seq_len_q) * p.num_q_heads;
+    if (rows <= 64) return int(rows);          // all rows of a sequence in one group
+    return mla_uses_rows(p) ? 128 : 64;        // groups of one query token's heads
+  }
   if (mla_uses_pairs(p)) return 128;   // one 128-head group per CTA pair
   if (mla_uses_rows(p)) return 128;    // one 128-head group per CTA, heads on M
   return p.num_q_heads <= 64 ? p.num_q_heads : 64;
@@ -768,8 +772,9 @@ bool mla_supported(const pda_problem& p, std::string* why) {
   }
   if (p.seq_len_q > 1) {
     const int64_t rows = int64_t(p.seq_len_q) * p.num_q_heads;
-    if (!(rows == 16 || rows == 32 || rows == 64)) {
-      *why = "MLA decode of several query tokens needs seq_len_q * num_q_heads in {16, 32, 64}";
+    if (!(rows == 16 || rows == 32 || rows == 64 || (rows > 64 && p.num_q_heads % 64 == 0))) {
+      *why = "MLA decode of several query tokens needs seq_len_q * num_q_heads in {16, 32, 64} "
+             "or num_q_heads a multiple of 64";
       return false;
     }
   }

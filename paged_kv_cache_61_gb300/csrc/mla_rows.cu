@@ -75,6 +75,9 @@ struct RowsParams {
   const int32_t* block_tables;
   const int32_t* context_lens;
   int32_t batch, num_q_heads, groups, max_blocks;
+  // S query tokens per sequence: its S*Hq rows (row R = i*Hq + h) are contiguous in q and
+  // out, in groups of 128 rows (128 heads of one token; S*Hq / 128 groups per sequence)
+  int32_t rows_per_seq, seq_len_q;
   int64_t num_blocks;
   float scale_log2;
   int64_t total_tiles, tiles_per_cta;
@@ -307,6 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Portion pt = walker_next(walk, spec, g_hi);
       const int npg = pt.p1 - pt.p0;
       const int ctx = __ldg(p.context_lens + pt.b);
+      // this group's query token qi sees tokens [0, ctx - S + 1 + qi) (all of them, S = 1)
+      const int qi = pt.seg * kRows / p.num_q_heads;
+      const int lim = ctx - p.seq_len_q + 1 + qi;
       float m = -INFINITY;   // maximum in use (log2 units)
       float l = 0.f;         // softmax denominator relative to m
 
@@ -315,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const uint4* qrow = reinterpret_cast<const uint4*>(
             static_cast<const T*>(p.q) +
-            (int64_t(pt.b) * p.num_q_heads + int64_t(pt.seg) * kRows + h) * kDqk);
+            (int64_t(pt.b) * p.rows_per_seq + int64_t(pt.seg) * kRows + h) * kDqk);
 #pragma unroll
         for (int c0 = 0; c0 < kDqk / 32; c0 += 5) {
           uint4 v[20];
@@ -356,70 +362,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         // max, paired f32 FMA and add): the MMA-issuing thread shares an SM sub-partition
         // with one of these warps, and FMA-pipe work there slows the MMA issue (a page's
         // MMAs took ~2600 cycles beside the scalar version, 1300 alone).
-        // Tokens past ctx (last page only) get no weight; every page has a valid token 0.
-        const int nvalid = min(kPage, ctx - (pt.p0 + i) * kPage);
-        const float sc = p.scale_log2;
-        // the page's maximum scaled score: scale times the largest raw score (scale >= 0)
-        // or the smallest (scale < 0)
-        float mr;
-        if (nvalid == kPage) {
-          if (sc >= 0.f) {
-            float a = ptx::max3(x[0], x[1], x[2]), b = ptx::max3(x[3], x[4], x[5]);
-#pragma unroll
-            for (int j = 6; j < kPage - 2; j += 4) {
-              a = ptx::max3(a, x[j], x[j + 1]);
-              b = ptx::max3(b, x[j + 2], x[j + 3]);
-            }
-            mr = ptx::max3(a, b, fmaxf(x[kPage - 2], x[kPage - 1]));
-          } else {
-            float a = ptx::min3(x[0], x[1], x[2]), b = ptx::min3(x[3], x[4], x[5]);
-#pragma unroll
-            for (int j = 6; j < kPage - 2; j += 4) {
-              a = ptx::min3(a, x[j], x[j + 1]);
-              b = ptx::min3(b, x[j + 2], x[j + 3]);
-            }
-            mr = ptx::min3(a, b, fminf(x[kPage - 2], x[kPage - 1]));
-          }
-        } else {
-          mr = x[0];
-#pragma unroll
-          for (int j = 1; j < kPage; ++j)
-            if (j < nvalid) mr = sc >= 0.f ? fmaxf(mr, x[j]) : fminf(mr, x[j]);
-        }
-        const float mx = mr * sc;
-        // lazy maximum: set on a piece's first page, raised only when a score exceeds the
-        // maximum in use by 2^8 (the common factor cancels in O / l)
-        const float mn = (i == 0 || mx > m + kRescaleLog2) ? mx : m;
-        const float alpha = i == 0 ? 1.f : ptx::exp2_approx(m - mn);
-        m = mn;
-        // exponent arguments x * scale - m, two per instruction
-        const uint64_t sc2 = ptx::f2_pack(sc, sc);
-        const uint64_t nm2 = ptx::f2_pack(-mn, -mn);
-#pragma unroll
-        for (int j = 0; j < kPage; j += 2)
-          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(x[j], x[j + 1]), sc2, nm2), x[j], x[j + 1]);
-        if (nvalid < kPage) {
-#pragma unroll
-          for (int j = 1; j < kPage; ++j)
-            if (j >= nvalid) x[j] = -INFINITY;
-        }
+        // Tokens from lim on get no weight. A page past lim (S > 1: the last page for an
+        // earlier query token) leaves the row unchanged with P = 0; once one is, so are the
+        // piece's later pages.
+        const int nvalid = min(kPage, lim - (pt.p0 + i) * kPage);
         uint32_t pk[kPage / 2];
-        uint64_t sum_a = ptx::f2_pack(0.f, 0.f), sum_b = sum_a;
+        float alpha = 1.f;
+        if (nvalid <= 0) {
 #pragma unroll
-        for (int j = 0; j < kPage; j += 4) {
-          const float p0 = ptx::exp2_approx(x[j]);
-          const float p1 = ptx::exp2_approx(x[j + 1]);
-          const float p2 = ptx::exp2_approx(x[j + 2]);
-          const float p3 = ptx::exp2_approx(x[j + 3]);
-          sum_a = ptx::f2_add(sum_a, ptx::f2_pack(p0, p1));
-          sum_b = ptx::f2_add(sum_b, ptx::f2_pack(p2, p3));
-          pk[j / 2] = ptx::Mma<T>::pack(p0, p1);
-          pk[j / 2 + 1] = ptx::Mma<T>::pack(p2, p3);
+          for (int c = 0; c < kPage / 2; ++c) pk[c] = 0u;
+        } else {
+          const float sc = p.scale_log2;
+          // the page's maximum scaled score: scale times the largest raw score (scale >= 0)
+          // or the smallest (scale < 0)
+          float mr;
+          if (nvalid == kPage) {
+            if (sc >= 0.f) {
+              float a = ptx::max3(x[0], x[1], x[2]), b = ptx::max3(x[3], x[4], x[5]);
+#pragma unroll
+              for (int j = 6; j < kPage - 2; j += 4) {
+                a = ptx::max3(a, x[j], x[j + 1]);
+                b = ptx::max3(b, x[j + 2], x[j + 3]);
+              }
+              mr = ptx::max3(a, b, fmaxf(x[kPage - 2], x[kPage - 1]));
+            } else {
+              float a = ptx::min3(x[0], x[1], x[2]), b = ptx::min3(x[3], x[4], x[5]);
+#pragma unroll
+              for (int j = 6; j < kPage - 2; j += 4) {
+                a = ptx::min3(a, x[j], x[j + 1]);
+                b = ptx::min3(b, x[j + 2], x[j + 3]);
+              }
+              mr = ptx::min3(a, b, fminf(x[kPage - 2], x[kPage - 1]));
+            }
+          } else {
+            mr = x[0];
+#pragma unroll
+            for (int j = 1; j < kPage; ++j)
+              if (j < nvalid) mr = sc >= 0.f ? fmaxf(mr, x[j]) : fminf(mr, x[j]);
+          }
+          const float mx = mr * sc;
+          // lazy maximum: set on a piece's first page, raised only when a score exceeds the
+          // maximum in use by 2^8 (the common factor cancels in O / l)
+          const float mn = (i == 0 || mx > m + kRescaleLog2) ? mx : m;
+          alpha = i == 0 ? 1.f : ptx::exp2_approx(m - mn);
+          m = mn;
+          // exponent arguments x * scale - m, two per instruction
+          const uint64_t sc2 = ptx::f2_pack(sc, sc);
+          const uint64_t nm2 = ptx::f2_pack(-mn, -mn);
+#pragma unroll
+          for (int j = 0; j < kPage; j += 2)
+            ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(x[j], x[j + 1]), sc2, nm2), x[j], x[j + 1]);
+          if (nvalid < kPage) {
+#pragma unroll
+            for (int j = 1; j < kPage; ++j)
+              if (j >= nvalid) x[j] = -INFINITY;
+          }
+          uint64_t sum_a = ptx::f2_pack(0.f, 0.f), sum_b = sum_a;
+#pragma unroll
+          for (int j = 0; j < kPage; j += 4) {
+            const float p0 = ptx::exp2_approx(x[j]);
+            const float p1 = ptx::exp2_approx(x[j + 1]);
+            const float p2 = ptx::exp2_approx(x[j + 2]);
+            const float p3 = ptx::exp2_approx(x[j + 3]);
+            sum_a = ptx::f2_add(sum_a, ptx::f2_pack(p0, p1));
+            sum_b = ptx::f2_add(sum_b, ptx::f2_pack(p2, p3));
+            pk[j / 2] = ptx::Mma<T>::pack(p0, p1);
+            pk[j / 2 + 1] = ptx::Mma<T>::pack(p2, p3);
+          }
+          float s0, s1, s2, s3;
+          ptx::f2_unpack(sum_a, s0, s1);
+          ptx::f2_unpack(sum_b, s2, s3);
+          l = l * alpha + ((s0 + s1) + (s2 + s3));
         }
-        float s0, s1, s2, s3;
-        ptx::f2_unpack(sum_a, s0, s1);
-        ptx::f2_unpack(sum_b, s2, s3);
-        l = l * alpha + ((s0 + s1) + (s2 + s3));
 
         // P and O hold page t-1 until its PV completes (the previous piece's end already
         // waited for it when i == 0).
@@ -447,14 +461,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tmem_st16(t_lane + kColP + 16, *reinterpret_cast<float(*)[16]>(pk + 16));
           ptx::tmem_st_wait();
         }
-        // Slots past ctx in the last page: P is 0 there, but 0 * (whatever the slot holds,
-        // NaN included) must not reach O, so their V rows (the first four sub-tiles) are
+        // Slots from lim on: P is 0 there, but 0 * (whatever a slot past ctx holds, NaN
+        // included) must not reach O, so their V rows (the first four sub-tiles) are
         // cleared; the score MMAs have consumed the page.
         if (nvalid < kPage) {
+          const int nz = max(nvalid, 0);
           uint8_t* stg = kv + (t % kStages) * kPageBytes;
-          const int n16 = (kPage - nvalid) * (kDv / 8);   // 16-byte pieces to clear
+          const int n16 = (kPage - nz) * (kDv / 8);   // 16-byte pieces to clear
           for (int idx = ctid; idx < n16; idx += kST) {
-            const int r = nvalid + idx / (kDv / 8);
+            const int r = nz + idx / (kDv / 8);
             const int rem = idx % (kDv / 8);
             *reinterpret_cast<uint4*>(stg + (rem >> 3) * kSubBytes + r * 128 + (rem & 7) * 16) =
                 make_uint4(0u, 0u, 0u, 0u);
@@ -474,7 +489,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       const bool whole = (pt.p0 == 0 && pt.p1 == pt.np);
       const int slot = piece_slot(pt.seg_start, g_lo);
-      const int64_t head0 = int64_t(pt.b) * p.num_q_heads + int64_t(pt.seg) * kRows;
+      const int64_t head0 = int64_t(pt.b) * p.rows_per_seq + int64_t(pt.seg) * kRows;
+      // lse is [B][Hq][S]: row R = i*Hq + h of the sequence goes to (b*Hq + h)*S + i
+      auto lse_at = [&](int r) {
+        const int R = pt.seg * kRows + r;
+        const int i = R / p.num_q_heads;
+        return (int64_t(pt.b) * p.num_q_heads + (R - i * p.num_q_heads)) * p.seq_len_q + i;
+      };
       const int64_t slot_row = (int64_t(blockIdx.x) * 2 + slot) * kRows;
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 2
@@ -511,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float lse_nat = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
       if (whole) {
-        if (p.lse != nullptr) p.lse[head0 + h] = lse_nat;
+        if (p.lse != nullptr) p.lse[lse_at(h)] = lse_nat;
       } else {
         __stcg(p.part_lse + slot_row + h, lse_nat);
       }
@@ -561,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               o[1] = cvt_out<T>(acc.y * iv);
               o[2] = cvt_out<T>(acc.z * iv);
               o[3] = cvt_out<T>(acc.w * iv);
-              if (dq == 0 && p.lse != nullptr) p.lse[head0 + j] = mxp + logf(den);
+              if (dq == 0 && p.lse != nullptr) p.lse[lse_at(j)] = mxp + logf(den);
             }
             if (ctid == 0) atomicExch(counter, 0);
           }
@@ -596,15 +617,15 @@ int launch_rows_t(const CUtensorMap& tkv, const RowsParams& prm, int grid, cudaS
 }  // namespace
 
 bool mla_uses_rows(const pda_problem& p) {
-  return p.head_dim_qk == kDqk && p.head_dim_v == kDv && p.num_q_heads % kRows == 0 &&
-         p.seq_len_q <= 1;
+  return p.head_dim_qk == kDqk && p.head_dim_v == kDv && p.num_q_heads % kRows == 0;
 }
 
 int launch_mla_rows(const Plan& plan, const MlaArgs& a, const Workspace& ws, void* stream) {
   const pda_problem& pr = plan.prob;
   const bool bf16 = pr.dtype == PDA_BF16;
   CUtensorMap tq, tkv;   // q is read row by row; only the cache map is passed
-  if (!encode_mla_maps(&tq, &tkv, a.q, int64_t(pr.batch) * pr.num_q_heads, kRows, a.kv_cache,
+  const int sq = pr.seq_len_q > 1 ? pr.seq_len_q : 1;
+  if (!encode_mla_maps(&tq, &tkv, a.q, int64_t(pr.batch) * sq * pr.num_q_heads, kRows, a.kv_cache,
                        pr.num_blocks, bf16, kDqk))
     return -1;
   RowsParams prm{};
@@ -615,6 +636,8 @@ int launch_mla_rows(const Plan& plan, const MlaArgs& a, const Workspace& ws, voi
   prm.context_lens = a.context_lens;
   prm.batch = pr.batch;
   prm.num_q_heads = pr.num_q_heads;
+  prm.rows_per_seq = sq * pr.num_q_heads;
+  prm.seq_len_q = sq;
   prm.groups = plan.segs_per_seq;
   prm.max_blocks = pr.max_blocks_per_seq;
   prm.num_blocks = pr.num_blocks;

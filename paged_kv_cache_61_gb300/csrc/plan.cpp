@@ -134,9 +134,12 @@ extern "C" PDA_API pda_status pda_plan_create(pda_plan** out, const pda_problem*
     // 32-head MQA group on a 32K sequence this is also the fastest count in a sweep).
     min_tiles_per_cta = std::max<int64_t>(4, plan->group / 4 + 1);
   } else {
-    plan->group = pda::mla_heads_per_cta(p);          // rows per head group
-    plan->heads_per_seg = S > 1 ? p.num_q_heads : plan->group;
-    plan->segs_per_seq = S > 1 ? 1 : p.num_q_heads / plan->group;
+    // The S*Hq query rows of a sequence (row R = i*Hq + h: query token i, head h) form
+    // groups of n consecutive rows: all of them (S*Hq <= 64), or n heads of one token.
+    const int n = pda::mla_heads_per_cta(p);
+    plan->group = n;
+    plan->heads_per_seg = std::min(n, p.num_q_heads);
+    plan->segs_per_seq = int32_t(int64_t(S) * p.num_q_heads / n);
     plan->head_subtiles = 1;
     plan->cluster = pda::mla_uses_pairs(p) ? 2 : 1;
     ctas_per_sm = pda::mla_ctas_per_sm(p);

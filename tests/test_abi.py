@@ -181,11 +181,19 @@ def test_multi_token_plan_validation():
     assert e.value.status == pda.PDA_ERR_INVALID_ARG
     mla = dict(kind=pda.PDA_KIND_MLA, num_kv_heads=1, head_dim_qk=576, head_dim_v=512,
                page_size=64, max_blocks_per_seq=2, context_lens=[5, 64], seq_len_q=2)
-    with pytest.raises(pda.PdaError) as e:     # MLA: S * Hq rows must fit one 64-row group
-        _plan(num_q_heads=64, **mla)
+    # MLA: the S * Hq rows of a sequence form one group when there are at most 64, else
+    # groups of one query token's heads, which needs Hq a multiple of 64
+    with pytest.raises(pda.PdaError) as e:
+        _plan(num_q_heads=48, **mla)
     assert e.value.status == pda.PDA_ERR_UNSUPPORTED
     p = _plan(num_q_heads=16, **mla)            # 32 rows: one head group per sequence
     assert p.num_ctas >= 1
+    for hq, dqk in ((64, 576), (128, 576), (128, 320)):
+        p = _plan(num_q_heads=hq, **{**mla, "head_dim_qk": dqk, "head_dim_v": dqk - 64,
+                                     "force_num_ctas": 1})
+        # accepted: 2 groups of 64 rows (Hq=64), 4 of 64 (576 record, Hq=128) or 2 of 128
+        # (320 record, Hq=128) per sequence
+        assert p.num_ctas == 1 and p.workspace_bytes > 0
     # S = 2 doubles the rows of a segment, and so each split piece's partial
     one, two = _plan(), _plan(seq_len_q=2)
     assert two.workspace_bytes > one.workspace_bytes

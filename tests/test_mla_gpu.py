@@ -197,27 +197,36 @@ def _assert_close_mtp(case, dc, rows=None):
 
 
 @pytest.mark.parametrize("latent", [512, 256])
-@pytest.mark.parametrize("hq,s", [(16, 2), (32, 2), (16, 4), (8, 2)])
+@pytest.mark.parametrize("hq,s", [(16, 2), (32, 2), (16, 4), (8, 2), (64, 2), (128, 2)])
 @pytest.mark.parametrize("force", [0, 1, 3, 17])
 def test_mtp_small_cases(hq, s, force, latent):
-    # q [B, S, Hq, Dqk]: query token i sees tokens [0, ctx - S + 1 + i)
+    # q [B, S, Hq, Dqk]: query token i sees tokens [0, ctx - S + 1 + i). Up to 64 rows
+    # (S * Hq) form one head group per sequence; more form groups of one token's heads
+    # (64 per group, or 128 on the heads-on-M kernel for the 320 record)
     case = synth.make_mla_case(batch=4, num_q_heads=hq, dtype=synth.BF16,
                                context_lens=[64 + s - 1, 65, 130, 700], latent_dim=latent,
                                seed=5, seq_len_q=s)
     _assert_close_mtp(case, DeviceCase(case, force_num_ctas=force))
 
 
+@pytest.mark.parametrize("hq,latent", [(16, 512), (128, 512), (128, 256)])
 @pytest.mark.parametrize("ctx", [65, 129])
-def test_mtp_piece_where_a_row_sees_no_token(ctx):
+def test_mtp_piece_where_a_row_sees_no_token(ctx, hq, latent):
     # ctx = 64k + 1, S = 2: the last page holds one token that query token 0 may not see;
-    # one page per CTA makes that page a split piece with no token for those rows
-    case = synth.make_mla_case(batch=1, num_q_heads=16, dtype=synth.BF16, context_lens=[ctx],
-                               seed=2, seq_len_q=2)
-    for force in (ctx // 64 + 1, 0):
+    # one page per CTA makes that page a split piece with no token for those rows (with
+    # Hq = 128, a whole head group's piece)
+    case = synth.make_mla_case(batch=1, num_q_heads=hq, dtype=synth.BF16, context_lens=[ctx],
+                               seed=2, seq_len_q=2, latent_dim=latent)
+    # head groups per sequence: all 2 * Hq rows (<= 64), else groups of one token's heads
+    groups = 1 if 2 * hq <= 64 else 2 * hq // (128 if latent == 256 else 64)
+    for force in ((ctx // 64 + 1) * groups, 0):
         _assert_close_mtp(case, DeviceCase(case, force_num_ctas=force))
 
 
-def test_mtp_full_size_workload_sampled_rows():
-    case = synth.workload("mla_b16_ctx64k_h16_mtp2")
-    rows = [(b, i, h) for b in (0, 7, 15) for i in range(2) for h in (0, 1, 8, 15)]
+@pytest.mark.parametrize("name", ["mla_b16_ctx64k_h16_mtp2", "mla_b16_ctx64k_h128_mtp2",
+                                  "mla_r256_b16_ctx64k_h128_mtp2"])
+def test_mtp_full_size_workload_sampled_rows(name):
+    case = synth.workload(name)
+    hq = case.num_q_heads
+    rows = [(b, i, h) for b in (0, 7, 15) for i in range(2) for h in sorted({0, 1, 8, hq - 1})]
     _assert_close_mtp(case, DeviceCase(case), rows=rows)
