@@ -3,7 +3,9 @@
 //
 // What it computes: as the 64-head kernel ("From MHA to MLA", section 6; FlashMLA-ETAP
 // "Supported configurations", (320, 256)): score(h, j) = scale * <q_h, rec_j>, value
-// rec_j[:256], output [B, Hq, 256] and fp32 LSE.
+// rec_j[:256], output [B, Hq, 256] and fp32 LSE. With S query tokens (FlashMLA-ETAP
+// "Usage": seq_len_q, causal) a group holds the 128 heads of one token i, which sees
+// tokens [0, ctx - S + 1 + i); q and out are [B, S, Hq, .], lse [B, Hq, S].
 //
 // How: the 320-wide record lets one SM hold a whole 128-head group, so every page is
 // read once (the 64-head kernel splits 128 heads into two groups that each read it):
