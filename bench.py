@@ -386,10 +386,10 @@ def run_gpu(args, workload, rank, world, local_rank):
         else:
             pda.mla_append(kn, kc, tables_, ctx_, plan, ws, stream)
 
-    def step(i, q_=q, out_=out, lse_=lse, tables_=tables, ctx_=ctx):
+    def step(i, q_=q, out_=out, lse_=lse, tables_=tables, ctx_=ctx, kn_=k_new, vn_=v_new):
         kc, vc = caches[i % copies]
         if with_append:
-            append(i, tables_, ctx_)
+            append(i, tables_, ctx_, kn=kn_, vn=vn_)
         if case.kind == "gqa" and fp8:
             pda.paged_decode_attn_fp8(q_, kc, vc, case.k_scale, case.v_scale, tables_, ctx_,
                                       case.scale, out_, lse_, plan, ws, stream)
@@ -450,30 +450,43 @@ def run_gpu(args, workload, rank, world, local_rank):
     if rank != 0:
         return
 
-    # ---- end to end through the C ABI: pinned host inputs in, outputs back, every step
+    # ---- end to end through the C ABI: pinned host inputs in, outputs back, every step.
+    # A step's inputs (q, block tables, context lengths, and the new tokens' K/V of the
+    # _step workloads) travel as one pinned host buffer, one copy in; its outputs (out,
+    # lse) are views of one device buffer, one copy out. The decode call reads and writes
+    # those views, as a caller batching its transfers would.
     e2e_steps = min(args.steps, 500)
-    q_h = q.cpu().pin_memory()
-    tables_h = tables.cpu().pin_memory()
-    ctx_h = ctx.cpu().pin_memory()
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    q_d, tables_d, ctx_d = torch.empty_like(q), torch.empty_like(tables), torch.empty_like(ctx)
-    h2d = q_h.numel() * q_h.element_size() + tables_h.numel() * 4 + ctx_h.numel() * 4
-    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
-    kn_h, vn_h = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
-    if with_append:                          # the new tokens' K/V come from the host too
-        h2d += 2 * kn_h.numel() * kn_h.element_size()
+    ins = [q, tables, ctx] + ([k_new, v_new] if with_append else [])
+    outs = [out, lse]
+
+    def packed(tensors):
+        offs, n = [], 0
+        for t in tensors:                    # 16-byte aligned, end to end
+            offs.append(n)
+            n += -(-t.numel() * t.element_size() // 16) * 16
+        return offs, n
+
+    def view(buf, off, like):
+        nbytes = like.numel() * like.element_size()
+        return buf[off:off + nbytes].view(like.dtype).view(like.shape)
+
+    in_offs, h2d = packed(ins)
+    out_offs, d2h = packed(outs)
+    in_h = torch.empty(h2d, dtype=torch.uint8).pin_memory()
+    in_d = torch.empty(h2d, dtype=torch.uint8, device="cuda")
+    res_h = torch.empty(d2h, dtype=torch.uint8).pin_memory()
+    res_d = torch.empty(d2h, dtype=torch.uint8, device="cuda")
+    for t, off in zip(ins, in_offs):
+        view(in_h, off, t).copy_(t.cpu())
+    d_in = [view(in_d, off, t) for t, off in zip(ins, in_offs)]
+    out_v, lse_v = (view(res_d, off, t) for t, off in zip(outs, out_offs))
+    kn_v, vn_v = (d_in[3], d_in[4]) if with_append else (k_new, v_new)
 
     def e2e_step(i):
-        if with_append:
-            k_new.copy_(kn_h, non_blocking=True)
-            v_new.copy_(vn_h, non_blocking=True)
-        q_d.copy_(q_h, non_blocking=True)
-        tables_d.copy_(tables_h, non_blocking=True)
-        ctx_d.copy_(ctx_h, non_blocking=True)
-        step(i, q_=q_d, tables_=tables_d, ctx_=ctx_d)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        in_d.copy_(in_h, non_blocking=True)
+        step(i, q_=d_in[0], out_=out_v, lse_=lse_v, tables_=d_in[1], ctx_=d_in[2], kn_=kn_v,
+             vn_=vn_v)
+        res_h.copy_(res_d, non_blocking=True)
 
     for i in range(3):
         e2e_step(i)
@@ -535,8 +548,10 @@ def run_gpu(args, workload, rank, world, local_rank):
             "config": workload_config(case, copies), "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                    "path": "pinned host q/block_tables/context_lens -> device, C-ABI decode, "
-                            "out/lse -> pinned host, every step; caches resident in HBM"},
+                    "path": "one pinned host buffer (q, block_tables, context_lens"
+                            + (", new K/V" if with_append else "") + ") -> device, C-ABI "
+                            "decode into one device buffer (out, lse) -> pinned host, every "
+                            "step, eager launches; caches resident in HBM"},
             "gpu_launches": args.steps * launches_per_step, "clocks": clocks,
             "timing": "value: K steps captured in one CUDA graph and replayed (device events); "
                       "roofline: device events around each call",
