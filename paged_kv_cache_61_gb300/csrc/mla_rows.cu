@@ -14,9 +14,8 @@
 //  * Warp 1 issues from one thread S[128 heads x 64 tokens] = q * K^T (20 MMAs M=128,
 //    N=64, K=16) and O[128 x 256] += P * V (4 MMAs M=128, N=256, V read in place from the
 //    page's first four sub-tiles, MN-major). q and P, the A operands, sit in tensor
-//    memory: an MMA whose A comes from shared memory reads it there every time, and with
-//    both operands in shared memory the 20 score MMAs took twice as long as the page's
-//    HBM time.
+//    memory, which leaves shared memory (80 KB of q, 16 KB of P) to the page ring; the
+//    MMAs take as long with A in shared memory.
 //  * Warps 2-5 own one head each per thread (TMEM lane = head). At the start of a piece
 //    each thread puts its head's q row into tensor memory. Per page the row's 64 scores
 //    come out of TMEM, the online softmax runs in the thread without any reduction (lazy
