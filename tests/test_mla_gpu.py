@@ -197,7 +197,8 @@ def _assert_close_mtp(case, dc, rows=None):
 
 
 @pytest.mark.parametrize("latent", [512, 256])
-@pytest.mark.parametrize("hq,s", [(16, 2), (32, 2), (16, 4), (8, 2), (64, 2), (128, 2)])
+@pytest.mark.parametrize("hq,s", [(16, 2), (32, 2), (16, 4), (8, 2), (64, 2), (128, 2), (64, 3),
+                                  (128, 3)])
 @pytest.mark.parametrize("force", [0, 1, 3, 17])
 def test_mtp_small_cases(hq, s, force, latent):
     # q [B, S, Hq, Dqk]: query token i sees tokens [0, ctx - S + 1 + i). Up to 64 rows
