@@ -204,3 +204,23 @@ def test_multi_token_plan_validation():
     # S = 2 doubles the rows of a segment, and so each split piece's partial
     one, two = _plan(), _plan(seq_len_q=2)
     assert two.workspace_bytes > one.workspace_bytes
+
+
+@pytest.mark.parametrize("hkv,ctas,splits", [(8, 256, 32), (1, 256, 256)])
+def test_planner_cuts_a_long_segment_into_equal_pieces(hkv, ctas, splits):
+    # B=1, ctx 32K (2048 pages of 16 tokens), 152 SMs: pieces of 2048 / k pages, so every
+    # CTA range lies inside one segment. Hkv=8: the natural share is 54 pages, and 64-page
+    # pieces are within a quarter above it. MQA: the share is 9 pages (the G/4 + 1 floor)
+    # with no divisor of 2048 in 9..11, so 8-page pieces, which still fit one wave.
+    p = _plan(batch=1, num_q_heads=32, num_kv_heads=hkv, head_dim_qk=128, head_dim_v=128,
+              page_size=16, max_blocks_per_seq=2048, num_blocks=2048, context_lens=[32768],
+              num_sms=152)
+    assert p.num_ctas == ctas and p.num_splits(0) == splits
+
+
+def test_planner_gives_whole_segments_to_a_uniform_batch():
+    # B=64, ctx 1024, Hkv=8: 512 segments of 64 pages, two whole segments per CTA
+    p = _plan(batch=64, num_q_heads=32, num_kv_heads=8, head_dim_qk=128, head_dim_v=128,
+              page_size=16, max_blocks_per_seq=64, num_blocks=4096, context_lens=[1024] * 64,
+              num_sms=152)
+    assert p.num_ctas == 256 and all(p.num_splits(b) == 1 for b in range(64))
