@@ -40,6 +40,8 @@ PIN_CALLS = [
     pins.test_e4m3_encode_inverts_decode_on_every_finite_code,
     pins.test_e4m3_encode_matches_torch_float8_cast_in_range,
     lambda: pins.test_append_puts_new_tokens_where_the_gather_reads_them(2),
+    pins.test_e4m3_quantize_divides_once_in_float32,
+    pins.test_e4m3_quantize_matches_torch_float32_division_and_cast,
 ]
 
 
@@ -139,6 +141,25 @@ def _encode_truncates(x):
     return (codes[idx] | ((x < 0).astype(np.uint8) << 7)).astype(np.uint8)
 
 
+def _quantize_divides_in_float64(x_bits, dtype, scale):
+    # the exact float64 quotient rounded once to E4M3 (no float32 step in between)
+    x = od.widen(x_bits, dtype) / float(scale)
+    codes = np.arange(0x7F, dtype=np.uint8)
+    values = od.decode_e4m3(codes)
+    mag = np.minimum(np.abs(x), values[-1])
+    hi = np.minimum(np.searchsorted(values, mag, side="left"), len(values) - 1)
+    lo = np.maximum(hi - 1, 0)
+    d_lo, d_hi = mag - values[lo], values[hi] - mag
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (codes[hi] % 2 == 0))
+    out = np.where(pick_hi, codes[hi], codes[lo]).astype(np.uint8)
+    return (out | (np.signbit(x).astype(np.uint8) << 7)).astype(np.uint8)
+
+
+def _quantize_times_reciprocal(x_bits, dtype, scale):
+    x32 = od.widen(x_bits, dtype).astype(np.float32)
+    return od.encode_e4m3(x32 * (np.float32(1.0) / np.float32(scale)))
+
+
 def _append_one_slot_late(cache, new, tables, ctx, page, seq_len_q=1):
     return od.__dict__["_orig_append"](cache, new, tables, np.asarray(ctx) + 1, page, seq_len_q)
 
@@ -162,6 +183,9 @@ MUTATIONS = {
     "E4M3 encoding rounds ties away from zero": ("encode_e4m3", _encode_ties_away),
     "E4M3 encoding truncates": ("encode_e4m3", _encode_truncates),
     "append writes one slot late": ("append_tokens", _append_one_slot_late),
+    "E4M3 quantization divides in float64": ("quantize_e4m3", _quantize_divides_in_float64),
+    "E4M3 quantization multiplies by the reciprocal": ("quantize_e4m3",
+                                                       _quantize_times_reciprocal),
 }
 
 

@@ -561,6 +561,47 @@ def test_e4m3_encode_matches_torch_float8_cast_in_range():
     np.testing.assert_array_equal(oracle.encode_e4m3(x), lib)
 
 
+def test_e4m3_quantize_divides_once_in_float32():
+    # An fp8 cache stores one byte per value ("Attention Kernel Variants", KV-cache table,
+    # fp8 row; pitfall 5); the stored code is that of x / scale with the division done in
+    # IEEE float32 and rounded once more to E4M3. Each pair below is worked out by hand.
+    bf = lambda x: synth.float32_to_bits(np.array([x], np.float32), synth.BF16)
+    f16 = lambda x: synth.float32_to_bits(np.array([x], np.float32), synth.FP16)
+    cases = [
+        # 3 / 0.25 = 12 exactly: exponent 3 (field 10), mantissa 1.5 (field 4) -> 0x54
+        (bf(3.0), synth.BF16, 0.25, 0x54),
+        # 5.46875 / 3.5 = 1.5625 exactly, the midpoint of 1.5 (0x3C) and 1.625 (0x3D): ties
+        # go to the even mantissa, 0x3C. Multiplying by the float32 reciprocal of 3.5
+        # instead gives 1.5625001..., above the midpoint, hence 0x3D.
+        (bf(5.46875), synth.BF16, 3.5, 0x3C),
+        # 1.77 as a float32 is 1.76999998...; 5.53125 / that = 3.12500003..., which float32
+        # rounds to 3.125 (the excess is below half a float32 step at 3.125, 1.2e-7).
+        # 3.125 is the midpoint of 3.0 (0x44, even) and 3.25 (0x45) -> 0x44; the exact
+        # quotient, rounded once, would give 0x45.
+        (bf(5.53125), synth.BF16, float(np.float32(1.77)), 0x44),
+        # scale = float32 0x3EFA38E4 (0.48871529...): -6.59765625 / scale = -13.49999996...
+        # exactly, -13.5 in float32: the midpoint of 13 (odd mantissa 5) and 14 (even,
+        # 6) -> 14, sign set: 0xD6; the exact quotient rounds to -13, 0xD5.
+        (f16(-6.59765625), synth.FP16, float(np.uint32(0x3EFA38E4).view(np.float32)), 0xD6),
+    ]
+    for bits, dtype, scale, want in cases:
+        got = int(oracle.quantize_e4m3(bits, dtype, scale)[0])
+        assert got == want, (bits, scale, hex(got), hex(want))
+
+
+def test_e4m3_quantize_matches_torch_float32_division_and_cast():
+    # library cross-check: torch's float32 division, then its float8_e4m3fn cast (in range)
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal(50000).astype(np.float32) * 3
+    bits = synth.float32_to_bits(x, synth.BF16)
+    for scale in (np.float32(1.77), np.float32(0.0123), np.float32(3.5), np.float32(0.37)):
+        xw = synth.bits_to_float32(bits, synth.BF16)
+        q32 = torch.from_numpy(xw) / torch.tensor(scale, dtype=torch.float32)
+        q32 = q32.clamp(-448.0, 448.0)
+        lib = q32.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        np.testing.assert_array_equal(oracle.quantize_e4m3(bits, synth.BF16, float(scale)), lib)
+
+
 @pytest.mark.parametrize("s", [1, 2])
 def test_append_puts_new_tokens_where_the_gather_reads_them(s):
     case = synth.make_gqa_case(batch=3, num_q_heads=8, num_kv_heads=2, head_dim=64,
