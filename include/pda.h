@@ -235,16 +235,20 @@ PDA_API pda_status pda_combine_splits(const float* partial_out, const float* par
  * GPU which loads this library keeps until the process exits. The call
  * allocates nothing and calls no allocating routine:
  *  - the first call on a device looks up that device's address of the array
- *    (once per device, with that device current); make that first call before
- *    any stream capture;
- *  - each call clears the array's counters and error word on `stream` before
- *    its kernel runs;
+ *    (once per device, with that device current) and keeps it for the life of
+ *    the process; make that first call before any stream capture. The kept
+ *    address is not valid after cudaDeviceReset on that device: a process that
+ *    resets a device must not use this call (or its error reader) there again;
+ *  - each call clears the array's merge counters on `stream` before its kernel
+ *    runs; the split pieces need no clearing (they are written before read);
  *  - every call shares the one array, so calls that can overlap on the GPU
  *    (different streams, or several host threads) race and give wrong results;
  *    issue them on one stream, or serialize them;
  *  - a plan whose workspace exceeds the array (pda_plan_workspace_bytes(plan) >
  *    PDA_NO_ALLOC_WORKSPACE_BYTES) is rejected with PDA_ERR_WORKSPACE.
- * Device-side errors (the word pda_read_device_error reads) are not reported.
+ * Device-side errors (a block id outside the pool, a timed-out wait: the codes of
+ * pda_read_device_error) accumulate in the array's own error word across calls
+ * until pda_no_alloc_read_device_error reads and clears it.
  */
 #define PDA_NO_ALLOC_WORKSPACE_BYTES (16u << 20)
 PDA_API pda_status paged_decode_attn_no_alloc(const void* q, const void* k_cache,
@@ -252,6 +256,16 @@ PDA_API pda_status paged_decode_attn_no_alloc(const void* q, const void* k_cache
                                               const int32_t* context_lens, float scale, void* out,
                                               float* lse, const pda_plan* plan,
                                               pda_stream_t stream);
+
+/*
+ * Read and clear the device error word of paged_decode_attn_no_alloc's library array
+ * on the current device (synchronizes `stream`). *code as for pda_read_device_error:
+ * 0 = no error; bit 0: a block-table entry of a read page was outside [0, num_blocks)
+ * (that page was read as zeros); bit 1: a pipeline wait timed out and the kernel
+ * abandoned its work. Like the decode call it allocates nothing, and it has no
+ * counterpart in the sources this library follows.
+ */
+PDA_API pda_status pda_no_alloc_read_device_error(pda_stream_t stream, int32_t* code);
 
 /*
  * Append the S new tokens of every sequence to the caches ("From MHA to MLA", section 2:

@@ -103,7 +103,8 @@ struct MlaLayout {
   static constexpr int kMused = kRed + 64 * 4 * 4;     // running maximum per head (log2 units)
   static constexpr int kAlpha = kMused + 64 * 4;       // rescale factor per head
   static constexpr int kLtot = kAlpha + 64 * 4;        // softmax denominator per head
-  static constexpr int kBar = kLtot + 64 * 4;
+  static constexpr int kLqtot = kLtot + 64 * 4;        // sum of the rounded weights per head
+  static constexpr int kBar = kLqtot + 64 * 4;
   static constexpr int kBarCount = 2 * R::kStages + 20;
   static constexpr int kSmem = 1024 + kBar + kBarCount * 8 + 64;
   static_assert(kSmem <= 232448, "fits the 227 KB of dynamic shared memory per block");
@@ -152,6 +153,7 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
   float* mused = reinterpret_cast<float*>(base + L::kMused);
   float* alpha_s = reinterpret_cast<float*>(base + L::kAlpha);
   float* ltot = reinterpret_cast<float*>(base + L::kLtot);
+  float* lqtot = reinterpret_cast<float*>(base + L::kLqtot);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::kBar);
   // Page t sits in ring stage t % KS (its P^T in that stage's rope sub-tile).
   uint64_t* kv_full = bars + 0;        // [KS]
@@ -381,7 +383,10 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
     const int ctid = threadIdx.x - 64;     // 0 .. kST-1
     const uint32_t t_lane = tmem + (uint32_t(32 * sp) << 16);
     T* outg = static_cast<T*>(p.out);
-    float l_reg[NC];
+    // per head: the sum of the weights (for the LSE) and the sum of the weights as
+    // rounded for the PV product (O is divided by the latter, so the output is a convex
+    // combination of value rows whatever the rounding of P)
+    float l_reg[NC], lq_reg[NC];
     bool aborted = false;
     int t = 0;
 
@@ -414,7 +419,7 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
       const int npg = pt.p1 - pt.p0;
       const int ctx = __ldg(p.context_lens + pt.b);
 #pragma unroll
-      for (int h = 0; h < NC; ++h) l_reg[h] = 0.f;
+      for (int h = 0; h < NC; ++h) l_reg[h] = lq_reg[h] = 0.f;
 
       for (int i = 0; i < npg; ++i, ++t) {
         if (!aborted && !bounded_wait(&s_full[t & 1], (t >> 1) & 1, flags, p.err)) aborted = true;
@@ -469,7 +474,10 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
             }
             ptx::named_barrier_sync(1, kST);
 #pragma unroll
-            for (int h = 0; h < NC; ++h) l_reg[h] *= alpha_s[cb + h];
+            for (int h = 0; h < NC; ++h) {
+              l_reg[h] *= alpha_s[cb + h];
+              lq_reg[h] *= alpha_s[cb + h];
+            }
             // O^T holds the pages up to t-1: wait for their PV, then rescale it in TMEM
             if (!aborted && !bounded_wait(&pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, flags, p.err))
               aborted = true;
@@ -507,12 +515,21 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
             pv[e] = ptx::exp2_approx(x[c + e] - (mm[e] == -INFINITY ? 0.f : mm[e]));
             l_reg[c + e] += pv[e];
           }
+          uint4 w;
+          w.x = ptx::Mma<T>::pack(pv[0], pv[1]);
+          w.y = ptx::Mma<T>::pack(pv[2], pv[3]);
+          w.z = ptx::Mma<T>::pack(pv[4], pv[5]);
+          w.w = ptx::Mma<T>::pack(pv[6], pv[7]);
+          {
+            float r[8];
+            ptx::Mma<T>::unpack(w.x, r[0], r[1]);
+            ptx::Mma<T>::unpack(w.y, r[2], r[3]);
+            ptx::Mma<T>::unpack(w.z, r[4], r[5]);
+            ptx::Mma<T>::unpack(w.w, r[6], r[7]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) lq_reg[c + e] += r[e];
+          }
           if (active) {
-            uint4 w;
-            w.x = ptx::Mma<T>::pack(pv[0], pv[1]);
-            w.y = ptx::Mma<T>::pack(pv[2], pv[3]);
-            w.z = ptx::Mma<T>::pack(pv[4], pv[5]);
-            w.w = ptx::Mma<T>::pack(pv[6], pv[7]);
             const int chunk = (cb + c) / 8;
             *reinterpret_cast<uint4*>(pbuf + row * 128 + ((chunk ^ (row & 7)) << 4)) = w;
           }
@@ -555,6 +572,19 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
         ltot[ctid] = (r.x + r.y) + (r.z + r.w);
       }
       ptx::named_barrier_sync(1, kST);
+#pragma unroll
+      for (int h = 0; h < NC; ++h) {
+        float v = lq_reg[h];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) v += __shfl_xor_sync(kFullMask, v, o);
+        if (lane == (h & 31)) red[(cb + h) * 4 + sp] = v;
+      }
+      ptx::named_barrier_sync(1, kST);
+      if (ctid < N) {
+        const float4 r = *reinterpret_cast<const float4*>(red + ctid * 4);
+        lqtot[ctid] = (r.x + r.y) + (r.z + r.w);
+      }
+      ptx::named_barrier_sync(1, kST);
       if (!aborted && !bounded_wait(&pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, flags, p.err))
         aborted = true;
       aborted = __any_sync(kFullMask, aborted);
@@ -587,7 +617,7 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
           for (int e = 0; e < 16; ++e) {
             const int h = cb + c + e;
             // ltot = 0 only for a causal row that saw no token of a split piece: O = 0
-            const float o = ltot[h] > 0.f ? v[e] / ltot[h] : 0.f;
+            const float o = ltot[h] > 0.f ? v[e] / lqtot[h] : 0.f;
             if (whole)
               outg[(head0 + h) * kDv + d] = from_f32<T>(o);
             else

@@ -316,6 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int lim = ctx - p.seq_len_q + 1 + qi;
       float m = -INFINITY;   // maximum in use (log2 units)
       float l = 0.f;         // softmax denominator relative to m
+      // the same sum over the weights as rounded for the PV product: O is divided by it,
+      // so the output is a convex combination of value rows whatever the rounding of P
+      float lq = 0.f;
 
       // This head's q row into TMEM (dims 2c, 2c+1 in column c). The MMAs that read the
       // previous piece's q have completed: the previous piece ended waiting for its last PV.
@@ -418,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 1; j < kPage; ++j)
               if (j >= nvalid) x[j] = -INFINITY;
           }
-          uint64_t sum_a = ptx::f2_pack(0.f, 0.f), sum_b = sum_a;
+          uint64_t sum_a = ptx::f2_pack(0.f, 0.f), sum_b = sum_a, sq_a = sum_a, sq_b = sum_a;
 #pragma unroll
           for (int j = 0; j < kPage; j += 4) {
             const float p0 = ptx::exp2_approx(x[j]);
@@ -429,11 +432,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             sum_b = ptx::f2_add(sum_b, ptx::f2_pack(p2, p3));
             pk[j / 2] = ptx::Mma<T>::pack(p0, p1);
             pk[j / 2 + 1] = ptx::Mma<T>::pack(p2, p3);
+            float r0, r1, r2, r3;
+            ptx::Mma<T>::unpack(pk[j / 2], r0, r1);
+            ptx::Mma<T>::unpack(pk[j / 2 + 1], r2, r3);
+            sq_a = ptx::f2_add(sq_a, ptx::f2_pack(r0, r1));
+            sq_b = ptx::f2_add(sq_b, ptx::f2_pack(r2, r3));
           }
           float s0, s1, s2, s3;
           ptx::f2_unpack(sum_a, s0, s1);
           ptx::f2_unpack(sum_b, s2, s3);
           l = l * alpha + ((s0 + s1) + (s2 + s3));
+          ptx::f2_unpack(sq_a, s0, s1);
+          ptx::f2_unpack(sq_b, s2, s3);
+          lq = lq * alpha + ((s0 + s1) + (s2 + s3));
         }
 
         // P and O hold page t-1 until its PV completes (the previous piece's end already
@@ -498,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return (int64_t(pt.b) * p.num_q_heads + (R - i * p.num_q_heads)) * p.seq_len_q + i;
       };
       const int64_t slot_row = (int64_t(blockIdx.x) * 2 + slot) * kRows;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? 1.f / lq : 0.f;
 #pragma unroll 2
       for (int c = 0; c < kDv; c += 16) {
         float v[16];

@@ -67,9 +67,12 @@ extern "C" PDA_API pda_status paged_decode_attn_no_alloc(
     return pda::fail(PDA_ERR_CUDA, std::string("looking up the library workspace: ") +
                                        cudaGetErrorString(e));
   }
-  // The error word and the merge counters must start at zero; the split pieces are
-  // always written before they are read.
-  e = cudaMemsetAsync(ws, 0, plan->ws_part_lse, stream);
+  // The merge counters must start at zero (a kernel that gave up on a timed-out wait
+  // may have left one behind); the split pieces are always written before they are
+  // read. The error word is not cleared: it collects the device errors of every call
+  // until pda_no_alloc_read_device_error reads it.
+  e = cudaMemsetAsync(static_cast<unsigned char*>(ws) + plan->ws_counters, 0,
+                      plan->ws_part_lse - plan->ws_counters, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return pda::fail(PDA_ERR_CUDA, std::string("clearing the library workspace: ") +
@@ -78,4 +81,18 @@ extern "C" PDA_API pda_status paged_decode_attn_no_alloc(
   // Same validation and launch as paged_decode_attn, on the library's array.
   return paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, scale, out, lse, plan,
                            ws, stream);
+}
+
+extern "C" PDA_API pda_status pda_no_alloc_read_device_error(pda_stream_t stream, int32_t* code) {
+  pda::clear_error();
+  if (code == nullptr) return pda::fail(PDA_ERR_INVALID_ARG, "code must be non-NULL");
+  void* ws = nullptr;
+  cudaError_t e = pda::workspace_address(&ws);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return pda::fail(PDA_ERR_CUDA, std::string("looking up the library workspace: ") +
+                                       cudaGetErrorString(e));
+  }
+  // Every plan keeps its error word at the start of the workspace.
+  return pda_read_device_error(ws, stream, code);
 }

@@ -204,6 +204,12 @@ struct Mma<__half> {
     return *reinterpret_cast<uint32_t*>(&h);
   }
   __device__ __forceinline__ static __half from_float(float x) { return __float2half_rn(x); }
+  // the two values of a packed pair, exactly, as fp32
+  __device__ __forceinline__ static void unpack(uint32_t w, float& lo, float& hi) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+    lo = f.x;
+    hi = f.y;
+  }
   // four E4M3 bytes -> two packed pairs of this type (bytes 0,1 -> lo; 2,3 -> hi)
   __device__ __forceinline__ static void from_e4m3x4(uint32_t x, uint32_t& lo, uint32_t& hi) {
     e4m3x4_to_f16x2(x, lo, hi);
@@ -226,6 +232,11 @@ struct Mma<__nv_bfloat16> {
   }
   __device__ __forceinline__ static __nv_bfloat16 from_float(float x) {
     return __float2bfloat16_rn(x);
+  }
+  // the two values of a packed pair, exactly, as fp32 (a bf16 is the high half of an fp32)
+  __device__ __forceinline__ static void unpack(uint32_t w, float& lo, float& hi) {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xffff0000u);
   }
   __device__ __forceinline__ static void from_e4m3x4(uint32_t x, uint32_t& lo, uint32_t& hi) {
     uint32_t l, h;

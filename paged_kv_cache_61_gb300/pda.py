@@ -54,6 +54,7 @@ def _declare(lib):
         "mla_decode": (I32, [P, P, P, P, F32, P, P, P, P, P]),
         "pda_combine_splits": (I32, [P, P, I32, I32, I32, P, I32, P, P]),
         "paged_decode_attn_no_alloc": (I32, [P, P, P, P, P, F32, P, P, P, P]),
+        "pda_no_alloc_read_device_error": (I32, [P, P]),
         "pda_kv_append": (I32, [P, P, P, P, P, P, P, P, P]),
         "pda_kv_append_fp8": (I32, [P, P, P, P, F32, F32, P, P, P, P, P]),
         "pda_mla_append": (I32, [P, P, P, P, P, P, P]),
@@ -194,6 +195,14 @@ def paged_decode_attn_no_alloc(q, k_cache, v_cache, block_tables, context_lens, 
                                             _ptr(block_tables), _ptr(context_lens), float(scale),
                                             _ptr(out), _ptr(lse), plan.handle, _stream(stream)),
            "paged_decode_attn_no_alloc")
+
+
+def no_alloc_read_device_error(stream=None) -> int:
+    """Read and clear the error word of paged_decode_attn_no_alloc's library array."""
+    code = ctypes.c_int32(0)
+    _check(lib().pda_no_alloc_read_device_error(_stream(stream), ctypes.byref(code)),
+           "pda_no_alloc_read_device_error")
+    return int(code.value)
 
 
 def mla_decode(q, kv_cache, block_tables, context_lens, scale: float, out, lse, plan: Plan,
