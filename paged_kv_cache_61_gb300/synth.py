@@ -175,7 +175,8 @@ def make_gqa_case(*, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: 
                   ctx_high: int = 256, ctx_dist: str = "fixed", num_blocks: Optional[int] = None,
                   max_blocks_per_seq: Optional[int] = None, scale: Optional[float] = None,
                   seed: int = 0, name: str = "gqa", table_layout: str = "pool",
-                  kv_format: Optional[str] = None, seq_len_q: int = 1) -> DecodeCase:
+                  kv_format: Optional[str] = None, seq_len_q: int = 1,
+                  with_caches: bool = True) -> DecodeCase:
     """Build a GQA/MQA/MHA decode problem.
 
     ctx_dist: "fixed" (``context_lens`` given), "uniform" (integers in
@@ -185,6 +186,8 @@ def make_gqa_case(*, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: 
     pool of exactly sum(pages) blocks (unused entries = UNUSED_ENTRY);
     "permutation" reshapes one random permutation of ``num_blocks`` ids into
     the [B, max_blocks_per_seq] table (every entry is a valid, distinct id).
+    with_caches=False leaves the caches out (None): lengths, tables and q are the same
+    draws either way, since every array has its own random stream.
     """
     r_ctx, r_tab, r_q, r_k, r_v = _streams(seed)
     if ctx_dist == "fixed":
@@ -221,7 +224,9 @@ def make_gqa_case(*, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: 
     q = normal_16bit(r_q, q_shape, dtype)
     cache_shape = (num_blocks, page_size, num_kv_heads, head_dim)
     k_scale = v_scale = 1.0
-    if kv_format is None:
+    if not with_caches:
+        k = v = None
+    elif kv_format is None:
         k = normal_16bit(r_k, cache_shape, dtype)
         v = normal_16bit(r_v, cache_shape, dtype)
     elif kv_format == FP8_E4M3:
@@ -243,8 +248,10 @@ def make_mla_case(*, batch: int, num_q_heads: int, dtype: str = BF16, page_size:
                   context_lens=None, ctx_low: int = 1, ctx_high: int = 4096, ctx_dist: str = "fixed",
                   latent_dim: int = 512, rope_dim: int = 64, num_blocks: Optional[int] = None,
                   scale: Optional[float] = None, seed: int = 0, name: str = "mla",
-                  kv_format: Optional[str] = None, seq_len_q: int = 1) -> DecodeCase:
-    """Build an absorbed-MLA decode problem: one shared (latent_dim + rope_dim)-wide KV head."""
+                  kv_format: Optional[str] = None, seq_len_q: int = 1,
+                  with_caches: bool = True) -> DecodeCase:
+    """Build an absorbed-MLA decode problem: one shared (latent_dim + rope_dim)-wide KV head.
+    with_caches=False leaves the cache out (None), as for make_gqa_case."""
     r_ctx, r_tab, r_q, r_k, _ = _streams(seed)
     if ctx_dist == "fixed":
         ctx = np.asarray(context_lens, dtype=np.int64).reshape(batch)
@@ -266,7 +273,9 @@ def make_mla_case(*, batch: int, num_q_heads: int, dtype: str = BF16, page_size:
         (batch, seq_len_q, num_q_heads, width)
     q = normal_16bit(r_q, q_shape, dtype)
     kv_scale = 1.0
-    if kv_format is None:
+    if not with_caches:
+        kv = None
+    elif kv_format is None:
         kv = normal_16bit(r_k, (num_blocks, page_size, width), dtype)
     elif kv_format == FP8_E4M3:
         kv, kv_scale = normal_e4m3(r_k, (num_blocks, page_size, width))
@@ -283,47 +292,48 @@ def make_mla_case(*, batch: int, num_q_heads: int, dtype: str = BF16, page_size:
 
 
 # The five decode workloads (seed 0 everywhere).
-def workload(name: str, seed: int = 0) -> DecodeCase:
+def workload(name: str, seed: int = 0, with_caches: bool = True) -> DecodeCase:
     """The named workload. Suffixes: ``_fp8`` gives the same workload with E4M3 caches,
-    ``_mtp2`` two query tokens per sequence (causal, bottom-right aligned)."""
+    ``_mtp2`` two query tokens per sequence (causal, bottom-right aligned).
+    with_caches=False: the same lengths, tables and q, without the caches."""
     fmt, sq = None, 1
     base = name
     if base.endswith("_fp8"):
         fmt, base = FP8_E4M3, base[: -len("_fp8")]
     if base.endswith("_mtp2"):
         sq, base = 2, base[: -len("_mtp2")]
-    case = _workload16(base, seed, fmt, sq)
+    case = _workload16(base, seed, fmt, sq, with_caches)
     case.name = name
     return case
 
 
-def _workload16(name: str, seed: int, kv_format: Optional[str], seq_len_q: int) -> DecodeCase:
+def _workload16(name: str, seed: int, kv_format: Optional[str], seq_len_q: int,
+                with_caches: bool = True) -> DecodeCase:
+    kw = dict(seed=seed, name=name, kv_format=kv_format, seq_len_q=seq_len_q,
+              with_caches=with_caches)
     if name == "gqa_tiny":
         # B=4, Hq=8, Hkv=2, D=64, fp16, PAGE=16, ctx ~ U{1..256}, tables = one permutation of 64 blocks.
         return make_gqa_case(batch=4, num_q_heads=8, num_kv_heads=2, head_dim=64, dtype=FP16,
                              ctx_dist="uniform", ctx_low=1, ctx_high=256, num_blocks=64,
                              max_blocks_per_seq=16, table_layout="permutation",
-                             scale=1.0 / 8.0, seed=seed, name=name, kv_format=kv_format, seq_len_q=seq_len_q)
+                             scale=1.0 / 8.0, **kw)
     if name == "gqa_b64_ctx1k":
         return make_gqa_case(batch=64, num_q_heads=32, num_kv_heads=8, head_dim=128, dtype=FP16,
-                             context_lens=[1024] * 64, table_layout="permutation",
-                             seed=seed, name=name, kv_format=kv_format, seq_len_q=seq_len_q)
+                             context_lens=[1024] * 64, table_layout="permutation", **kw)
     if name in ("gqa_b1_ctx32k", "gqa_b1_ctx32k_mqa"):
         hkv = 1 if name.endswith("mqa") else 8
         return make_gqa_case(batch=1, num_q_heads=32, num_kv_heads=hkv, head_dim=128, dtype=BF16,
-                             context_lens=[32768], table_layout="permutation", seed=seed,
-                             name=name, kv_format=kv_format, seq_len_q=seq_len_q)
+                             context_lens=[32768], table_layout="permutation", **kw)
     if name == "gqa_varlen_b128":
         return make_gqa_case(batch=128, num_q_heads=64, num_kv_heads=8, head_dim=128, dtype=BF16,
                              ctx_dist="loguniform", ctx_low=16, ctx_high=32768,
-                             max_blocks_per_seq=2048, table_layout="pool", seed=seed, name=name,
-                             kv_format=kv_format, seq_len_q=seq_len_q)
+                             max_blocks_per_seq=2048, table_layout="pool", **kw)
     if name in ("mla_b16_ctx64k_h16", "mla_b16_ctx64k_h128",
                 "mla_r256_b16_ctx64k_h16", "mla_r256_b16_ctx64k_h128"):
         hq = 16 if name.endswith("h16") else 128
         latent = 256 if "_r256_" in name else 512
         return make_mla_case(batch=16, num_q_heads=hq, dtype=BF16, context_lens=[65536] * 16,
-                             latent_dim=latent, seed=seed, name=name, kv_format=kv_format, seq_len_q=seq_len_q)
+                             latent_dim=latent, **kw)
     raise KeyError(name)
 
 
