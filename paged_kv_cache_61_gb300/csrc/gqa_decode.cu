@@ -278,11 +278,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
   // ============================== consumer warps ==============================
   // The grid may start while the previous kernel on the stream drains (programmatic
-  // dependent launch; only this library's decode and split-merge kernels allow that).
-  // The producers above only read the caches, tables and lengths, which no such kernel
-  // writes; the consumers read q and write out, lse and the workspace, so they wait here
-  // until the previous grid has completed.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // dependent launch; only this library's decode and split-merge kernels allow that, and
+  // any other predecessor, the caller's kernels included, has completed before this grid
+  // starts). None of those kernels writes q, the caches, the tables or the lengths, so
+  // the consumers read them and attend to their pages at once; they write out, lse and
+  // the workspace, which the previous grid may still be reading or writing, only after
+  // the griddepcontrol.wait at the end of each portion's page loop.
   const int hsub = warp % NHT;
   const int pres = warp / NHT;
   const int tid = threadIdx.x;  // 0..127 among consumers
@@ -562,6 +563,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (lane == 0) ptx::mbar_arrive(&empty[stage]);
     }
     k += nfill;
+    // the previous grid on the stream has completed from here on (returns at once after
+    // the first portion)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // ---- this warp's state -> shared memory
 #pragma unroll
