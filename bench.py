@@ -387,8 +387,7 @@ def whole_job_rate(units_per_rank_step: float, world: int, ms_per_step: float) -
 
 def _has_merge(plan, case):
     """Whether a decode call on this plan also launches the split-merge kernel."""
-    return plan.num_ctas > 0 and max(plan.num_splits(b) for b in range(case.batch)) > max(
-        4, -(-plan.num_ctas // 64))
+    return plan.num_launches > 1
 
 
 def rotation_copies(kv_bytes: int) -> int:

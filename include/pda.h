@@ -131,6 +131,11 @@ PDA_API int32_t pda_plan_num_ctas(const pda_plan* plan);
  * share one of its (KV head or head group) segments. 1 = computed by one CTA. */
 PDA_API int32_t pda_plan_num_splits(const pda_plan* plan, int32_t b);
 
+/* Kernel launches one decode call makes with this plan: 1, or 2 when heavily split
+ * segments are merged by a separate split-merge kernel after the decode kernel. (An
+ * append call is one more launch of its own.) */
+PDA_API int32_t pda_plan_num_launches(const pda_plan* plan);
+
 /*
  * Zero a workspace before its first use with any plan. The decode calls leave
  * the workspace's counters at zero when they complete, so this is needed once

@@ -872,29 +872,34 @@ int launch_gqa_decode(const Plan& plan, const GqaArgs& a, const Workspace& ws, v
   const pda_problem& pr = plan.prob;
   const bool bf16 = pr.dtype == PDA_BF16;
   const bool f8 = pr.kv_format == PDA_KV_FP8_E4M3;
-  CUtensorMap tk, tv;
-  const bool maps_ok =
-      f8 ? encode_cache_map_f8(&tk, a.k_cache, pr.num_blocks, pr.page_size, pr.num_kv_heads,
-                               pr.head_dim_qk) &&
-               encode_cache_map_f8(&tv, a.v_cache, pr.num_blocks, pr.page_size, pr.num_kv_heads,
-                                   pr.head_dim_v)
-         : encode_cache_map(&tk, a.k_cache, pr.num_blocks, pr.page_size, pr.num_kv_heads,
-                            pr.head_dim_qk, bf16) &&
-               encode_cache_map(&tv, a.v_cache, pr.num_blocks, pr.page_size, pr.num_kv_heads,
-                                pr.head_dim_v, bf16);
-  if (!maps_ok) return -1;
-  GqaParams prm{};
-  // fp8: when one map can span both caches, a page's K and V come in one copy (the
-  // producer's copy issue, not HBM, bounds the fp8 kernel)
-  if (f8) {
-    CUtensorMap pair;
-    int32_t order = 0;
-    if (encode_cache_pair_f8(&pair, a.k_cache, a.v_cache, pr.num_blocks, pr.page_size,
-                             pr.num_kv_heads, pr.head_dim_qk, &order)) {
-      tk = pair;
-      prm.kv_pair = order;
+  CUtensorMap m[2];
+  int32_t kv_pair = 0;
+  const bool maps_ok = plan.map_cache.get(a.k_cache, a.v_cache, m, &kv_pair,
+                                          [&](CUtensorMap* t, int32_t* order) {
+    const bool ok =
+        f8 ? encode_cache_map_f8(&t[0], a.k_cache, pr.num_blocks, pr.page_size,
+                                 pr.num_kv_heads, pr.head_dim_qk) &&
+                 encode_cache_map_f8(&t[1], a.v_cache, pr.num_blocks, pr.page_size,
+                                     pr.num_kv_heads, pr.head_dim_v)
+           : encode_cache_map(&t[0], a.k_cache, pr.num_blocks, pr.page_size, pr.num_kv_heads,
+                              pr.head_dim_qk, bf16) &&
+                 encode_cache_map(&t[1], a.v_cache, pr.num_blocks, pr.page_size,
+                                  pr.num_kv_heads, pr.head_dim_v, bf16);
+    // fp8: when one map can span both caches, a page's K and V come in one copy (the
+    // producer's copy issue, not HBM, bounds the fp8 kernel)
+    if (ok && f8) {
+      CUtensorMap pair;
+      if (encode_cache_pair_f8(&pair, a.k_cache, a.v_cache, pr.num_blocks, pr.page_size,
+                               pr.num_kv_heads, pr.head_dim_qk, order))
+        t[0] = pair;
     }
-  }
+    return ok;
+  });
+  if (!maps_ok) return -1;
+  const CUtensorMap& tk = m[0];
+  const CUtensorMap& tv = m[1];
+  GqaParams prm{};
+  prm.kv_pair = kv_pair;
   prm.q = a.q;
   prm.out = a.out;
   prm.lse = a.lse;

@@ -840,11 +840,15 @@ int launch_mla_decode(const Plan& plan, const MlaArgs& a, const Workspace& ws, v
   const pda_problem& pr = plan.prob;
   const bool bf16 = pr.dtype == PDA_BF16;
   const int n = plan.group;
-  CUtensorMap tq, tkv;
+  CUtensorMap m[2];
   const int sq = pr.seq_len_q > 1 ? pr.seq_len_q : 1;
-  if (!encode_mla_maps(&tq, &tkv, a.q, int64_t(pr.batch) * sq * pr.num_q_heads, n, a.kv_cache,
-                       pr.num_blocks, bf16, pr.head_dim_qk))
+  if (!plan.map_cache.get(a.q, a.kv_cache, m, nullptr, [&](CUtensorMap* t, int32_t*) {
+        return encode_mla_maps(&t[0], &t[1], a.q, int64_t(pr.batch) * sq * pr.num_q_heads, n,
+                               a.kv_cache, pr.num_blocks, bf16, pr.head_dim_qk);
+      }))
     return -1;
+  const CUtensorMap& tq = m[0];
+  const CUtensorMap& tkv = m[1];
   MlaParams prm{};
   prm.q = a.q;
   prm.out = a.out;

@@ -691,7 +691,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (++i == cur.p1 - cur.p0) {
               // end of the piece: the owner's (m, l, lq) of this head, then the output
               if (!aborted && !bounded_wait_cluster(fin_full, u & 1, flags, p.err)) aborted = true;
-              const float4 f = aborted ? make_float4(0.f, 1.f, 1.f, 0.f) : fin_in[r];
+              // acquire load: the relaxed arrive on fin_free below comes after it
+              const float4 f = aborted ? make_float4(0.f, 1.f, 1.f, 0.f)
+                                       : ptx::ld_shared_v4_acquire(ptx::smem_addr(fin_in + r));
               __syncwarp();
               if (lane == 0 && !aborted) ptx::mbar_arrive_remote_relaxed(remote(fin_free));
               if (relay_lead && !aborted) ptx::mbar_arrive_expect_tx(fin_full, kFinBytes);  // next piece
@@ -773,8 +775,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t xr = xs_s + b2 * kXsBytes + pos * kXsHalfBytes + row_off;
 #pragma unroll
           for (int j = 0; j < kHalfTok / 4; ++j) {
+            // acquire loads: the relaxed arrive on the peer's xs_free below comes after them
             const float4 x = aborted ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                     : ptx::ld_shared_v4(xr + ((uint32_t(j) ^ swz) << 4));
+                                     : ptx::ld_shared_v4_acquire(xr + ((uint32_t(j) ^ swz) << 4));
             v[4 * j] += x.x;
             v[4 * j + 1] += x.y;
             v[4 * j + 2] += x.z;
@@ -1031,8 +1034,13 @@ int mla_pair_units(int num_sms) {
 int launch_mla_pair(const Plan& plan, const MlaArgs& a, const Workspace& ws, void* stream) {
   const pda_problem& pr = plan.prob;
   const bool bf16 = pr.dtype == PDA_BF16;
-  CUtensorMap tkl, tkr;
-  if (!encode_pair_maps(&tkl, &tkr, a.kv_cache, pr.num_blocks, bf16)) return -1;
+  CUtensorMap m[2];
+  if (!plan.map_cache.get(a.kv_cache, nullptr, m, nullptr, [&](CUtensorMap* t, int32_t*) {
+        return encode_pair_maps(&t[0], &t[1], a.kv_cache, pr.num_blocks, bf16);
+      }))
+    return -1;
+  const CUtensorMap& tkl = m[0];
+  const CUtensorMap& tkr = m[1];
   PairParams prm{};
   prm.q = a.q;
   prm.out = a.out;

@@ -635,11 +635,14 @@ bool mla_uses_rows(const pda_problem& p) {
 int launch_mla_rows(const Plan& plan, const MlaArgs& a, const Workspace& ws, void* stream) {
   const pda_problem& pr = plan.prob;
   const bool bf16 = pr.dtype == PDA_BF16;
-  CUtensorMap tq, tkv;   // q is read row by row; only the cache map is passed
+  CUtensorMap m[2];   // q is read row by row; only the cache map is passed
   const int sq = pr.seq_len_q > 1 ? pr.seq_len_q : 1;
-  if (!encode_mla_maps(&tq, &tkv, a.q, int64_t(pr.batch) * sq * pr.num_q_heads, kRows, a.kv_cache,
-                       pr.num_blocks, bf16, kDqk))
+  if (!plan.map_cache.get(a.q, a.kv_cache, m, nullptr, [&](CUtensorMap* t, int32_t*) {
+        return encode_mla_maps(&t[0], &t[1], a.q, int64_t(pr.batch) * sq * pr.num_q_heads,
+                               kRows, a.kv_cache, pr.num_blocks, bf16, kDqk);
+      }))
     return -1;
+  const CUtensorMap& tkv = m[1];
   RowsParams prm{};
   prm.q = a.q;
   prm.out = a.out;

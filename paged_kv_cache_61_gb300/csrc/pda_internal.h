@@ -1,8 +1,12 @@
 // Internal declarations shared by the host side (plan.cpp, api.cpp) and the kernel launchers.
 #pragma once
 
+#include <cuda.h>
+
 #include <cstddef>
 #include <cstdint>
+#include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -31,6 +35,36 @@ struct HeavySegment {
 constexpr int kMaxHeavySegments = 64;
 constexpr int kMaxCtas = 2048;
 
+// The TMA descriptors of the last call, keyed by the tensors they address: a plan's
+// shapes are fixed, so a call on the same buffers (the caches, and q for the MLA kernels)
+// reuses them instead of encoding them again.
+struct MapCache {
+  std::mutex mu;
+  bool valid = false;
+  const void* key[2] = {nullptr, nullptr};
+  int32_t extra = 0;
+  CUtensorMap maps[2];
+
+  // Fill out[0..1] (and *extra) from the cache, or from encode(out, extra) when the keys
+  // differ; returns false (and caches nothing) when encode fails.
+  template <typename F>
+  bool get(const void* k0, const void* k1, CUtensorMap* out, int32_t* extra_out, F encode) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!(valid && key[0] == k0 && key[1] == k1)) {
+      valid = false;
+      int32_t x = 0;
+      if (!encode(maps, &x)) return false;
+      key[0] = k0;
+      key[1] = k1;
+      extra = x;
+      valid = true;
+    }
+    std::memcpy(out, maps, sizeof(maps));
+    if (extra_out != nullptr) *extra_out = extra;
+    return true;
+  }
+};
+
 struct Plan {
   pda_problem prob{};
   int32_t group = 1;            // query rows per segment: S * (GQA: Hq/Hkv; MLA: heads per group)
@@ -52,6 +86,7 @@ struct Plan {
   size_t ws_part_lse = 0;   // float [num_ctas * 2 * group]
   size_t ws_part_out = 0;   // float [num_ctas * 2 * group * head_dim_v]
   size_t ws_bytes = 0;
+  mutable MapCache map_cache;   // TMA descriptors of the last call's buffers
 };
 
 // Error reporting (thread-local last error string).

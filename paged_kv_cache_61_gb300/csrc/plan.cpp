@@ -130,8 +130,9 @@ extern "C" PDA_API pda_status pda_plan_create(pda_plan** out, const pda_problem*
     plan->head_subtiles = (plan->group + 7) / 8;
     ctas_per_sm = pda::gqa_ctas_per_sm(p);
     // A split piece writes a 4·G·D-byte fp32 partial and reads 64·D bytes per tile: at
-    // least G/4 + 1 tiles keep the partial under a quarter of what the piece reads (for a
-    // 32-head MQA group on a 32K sequence this is also the fastest count in a sweep).
+    // least G/4 + 1 tiles keep the partial under a quarter of what the piece reads. (A
+    // starting floor: the cap on pieces per segment below and the aligned-piece search
+    // may raise or lower a CTA's share from there.)
     min_tiles_per_cta = std::max<int64_t>(4, plan->group / 4 + 1);
   } else {
     // The S*Hq query rows of a sequence (row R = i*Hq + h: query token i, head h) form
@@ -146,9 +147,19 @@ extern "C" PDA_API pda_status pda_plan_create(pda_plan** out, const pda_problem*
     min_tiles_per_cta = 2;
   }
 
-  int64_t pages_total = 0;
-  for (int32_t b = 0; b < p.batch; ++b) pages_total += pda::cdiv(ctx_host[b], p.page_size);
+  int64_t pages_total = 0, pages_max = 0;
+  for (int32_t b = 0; b < p.batch; ++b) {
+    pages_total += pda::cdiv(ctx_host[b], p.page_size);
+    pages_max = std::max<int64_t>(pages_max, pda::cdiv(ctx_host[b], p.page_size));
+  }
   plan->total_tiles = pages_total * plan->segs_per_seq;
+  // GQA: at most 32 pieces per segment. Every piece adds a partial to the split merge,
+  // which runs after the decode grid; with consumers that attend before waiting for the
+  // previous grid, a sweep of forced CTA counts on B=1, ctx 32K put the fastest plans at
+  // 32 pieces per segment or fewer: MQA 12.3 us at 256 pieces -> 7.2 us at 32; Hq/Hkv =
+  // 16 (two segments) 11.5 -> 6.5 us at 32; Hkv=8 unchanged at 32.
+  if (p.kind == PDA_KIND_GQA)
+    min_tiles_per_cta = std::max<int64_t>(min_tiles_per_cta, pda::cdiv(pages_max, 32));
 
   if (plan->total_tiles > 0) {
     int64_t q;
@@ -258,6 +269,11 @@ extern "C" PDA_API size_t pda_plan_workspace_bytes(const pda_plan* plan) {
 }
 
 extern "C" PDA_API int32_t pda_plan_num_ctas(const pda_plan* plan) { return plan ? plan->num_ctas : 0; }
+
+extern "C" PDA_API int32_t pda_plan_num_launches(const pda_plan* plan) {
+  if (plan == nullptr || plan->num_ctas == 0) return 0;
+  return plan->heavy.empty() ? 1 : 2;
+}
 
 extern "C" PDA_API int32_t pda_plan_num_splits(const pda_plan* plan, int32_t b) {
   if (plan == nullptr || b < 0 || b >= plan->prob.batch) return 0;

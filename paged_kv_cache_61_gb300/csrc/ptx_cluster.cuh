@@ -51,9 +51,11 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t rbar) {
 }
 
 // Arrive on an mbarrier of a peer CTA with no ordering of this thread's earlier memory
-// accesses: for signalling that a buffer the peer writes has been read (the loads have
-// returned their values before the arrive is issued), without waiting for this thread's
-// own outstanding stores to the peer.
+// accesses: for signalling that a buffer the peer writes has been read, without waiting
+// for this thread's own outstanding stores to the peer (release semantics would). The
+// callers read the buffer with acquire loads (ld_shared_v4_acquire), which keep every
+// later operation, this arrive included, after the loads, and a __syncwarp between every
+// lane's loads and the one lane's arrive orders the other lanes' loads before it too.
 __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t rbar) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar)
                : "memory");
@@ -70,6 +72,18 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
       : "r"(smem_addr(bar)), "r"(parity)
       : "memory");
   return done != 0;
+}
+
+// A shared-memory load with acquire semantics at cluster scope: no later memory operation
+// of this thread (a relaxed remote arrive that tells the peer the buffer may be
+// overwritten, in particular) is performed before this load.
+__device__ __forceinline__ float4 ld_shared_v4_acquire(uint32_t saddr) {
+  float4 v;
+  asm volatile("ld.acquire.cluster.shared::cta.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(saddr)
+               : "memory");
+  return v;
 }
 
 __device__ __forceinline__ float4 ld_shared_v4(uint32_t saddr) {

@@ -47,6 +47,7 @@ def _declare(lib):
         "pda_plan_workspace_bytes": (SZ, [P]),
         "pda_plan_num_ctas": (I32, [P]),
         "pda_plan_num_splits": (I32, [P, I32]),
+        "pda_plan_num_launches": (I32, [P]),
         "pda_workspace_init": (I32, [P, P, P]),
         "pda_read_device_error": (I32, [P, P, ctypes.POINTER(I32)]),
         "paged_decode_attn": (I32, [P, P, P, P, P, F32, P, P, P, P, P]),
@@ -141,6 +142,11 @@ class Plan:
     @property
     def num_ctas(self) -> int:
         return int(lib().pda_plan_num_ctas(self.handle))
+
+    @property
+    def num_launches(self) -> int:
+        """Kernel launches of one decode call (2 when a split-merge kernel follows)."""
+        return int(lib().pda_plan_num_launches(self.handle))
 
     def num_splits(self, b: int) -> int:
         return int(lib().pda_plan_num_splits(self.handle, b))

@@ -206,16 +206,31 @@ def test_multi_token_plan_validation():
     assert two.workspace_bytes > one.workspace_bytes
 
 
-@pytest.mark.parametrize("hkv,ctas,splits", [(8, 256, 32), (1, 256, 256)])
+@pytest.mark.parametrize("hkv,ctas,splits", [(8, 256, 32), (2, 64, 32), (1, 32, 32)])
 def test_planner_cuts_a_long_segment_into_equal_pieces(hkv, ctas, splits):
     # B=1, ctx 32K (2048 pages of 16 tokens), 152 SMs: pieces of 2048 / k pages, so every
-    # CTA range lies inside one segment. Hkv=8: the natural share is 54 pages, and 64-page
-    # pieces are within a quarter above it. MQA: the share is 9 pages (the G/4 + 1 floor)
-    # with no divisor of 2048 in 9..11, so 8-page pieces, which still fit one wave.
+    # CTA range lies inside one segment, and at most 32 pieces per segment. Hkv=8: the
+    # natural share is 54 pages, and 64-page pieces are within a quarter above it. Hkv=2
+    # and MQA: the share is raised to 64 pages (32 pieces per segment).
     p = _plan(batch=1, num_q_heads=32, num_kv_heads=hkv, head_dim_qk=128, head_dim_v=128,
               page_size=16, max_blocks_per_seq=2048, num_blocks=2048, context_lens=[32768],
               num_sms=152)
     assert p.num_ctas == ctas and p.num_splits(0) == splits
+    # pieces beyond the in-kernel merge's four go to the split-merge kernel
+    assert p.num_launches == 2
+
+
+def test_planner_merges_few_pieces_in_kernel():
+    # a uniform batch cut into whole segments needs one launch; a sequence cut into a few
+    # pieces is merged by its last piece, in the same launch
+    p = _plan(batch=64, num_q_heads=32, num_kv_heads=8, head_dim_qk=128, head_dim_v=128,
+              page_size=16, max_blocks_per_seq=64, num_blocks=4096, context_lens=[1024] * 64,
+              num_sms=152)
+    assert p.num_launches == 1
+    p = _plan(batch=1, num_q_heads=32, num_kv_heads=8, head_dim_qk=128, head_dim_v=128,
+              page_size=16, max_blocks_per_seq=2048, num_blocks=2048, context_lens=[32768],
+              num_sms=152, force_num_ctas=24)
+    assert 2 <= p.num_splits(0) <= 4 and p.num_launches == 1
 
 
 def test_planner_gives_whole_segments_to_a_uniform_batch():

@@ -175,7 +175,8 @@ def test_poisoned_stale_slots_and_table_entries(hq, latent):
 def test_full_size_workload_sampled_rows(name):
     case = synth.workload(name)
     hq = case.num_q_heads
-    rows = [(b, h) for b in (0, 7, 15) for h in sorted({0, 1, hq // 2, hq - 1})]
+    # every head of six sequences: the oracle's cost is the gather of each sequence
+    rows = [(b, h) for b in (0, 3, 7, 8, 12, 15) for h in range(hq)]
     _assert_close(case, DeviceCase(case), rows=rows)
 
 
@@ -229,5 +230,5 @@ def test_mtp_piece_where_a_row_sees_no_token(ctx, hq, latent):
 def test_mtp_full_size_workload_sampled_rows(name):
     case = synth.workload(name)
     hq = case.num_q_heads
-    rows = [(b, i, h) for b in (0, 7, 15) for i in range(2) for h in sorted({0, 1, 8, hq - 1})]
+    rows = [(b, i, h) for b in (0, 3, 7, 8, 12, 15) for i in range(2) for h in range(hq)]
     _assert_close_mtp(case, DeviceCase(case), rows=rows)

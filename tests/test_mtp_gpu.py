@@ -118,6 +118,5 @@ def test_full_size_workload_sampled_rows(name):
     case = synth.workload(name)
     hq = case.num_q_heads
     bs = sorted({0, case.batch // 2, case.batch - 1})
-    rows = [(b, i, h) for b in bs for i in range(case.seq_len_q)
-            for h in sorted({0, 1, hq // 2, hq - 1})]
+    rows = [(b, i, h) for b in bs for i in range(case.seq_len_q) for h in range(hq)]
     _assert_close(case, DeviceCase(case), rows=rows)
