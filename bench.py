@@ -47,7 +47,7 @@ from paged_kv_cache_61_gb300 import synth, traffic  # noqa: E402
 DEFAULT_WORKLOAD = "gqa_b64_ctx1k"
 # the other decode workloads of the default run, with their role
 PER_CONFIG = ("gqa_tiny", "gqa_b1_ctx32k", "gqa_b1_ctx32k_mqa", "gqa_varlen_b128",
-              "mla_b16_ctx64k_h16", "mla_b16_ctx64k_h128")
+              "mla_b16_ctx64k_h16", "mla_b16_ctx64k_h128", "mla_b16_ctx64k_h16_fp8")
 L2_BYTES = 129 * 2 ** 20
 KERNEL_SOURCES = {"gqa": ["gqa_decode.cu", "ptx.cuh", "tile_walk.cuh"],
                   "mla": ["mla_decode.cu", "ptx.cuh", "ptx_ext.cuh", "tile_walk.cuh"],
@@ -492,6 +492,9 @@ def time_config(args, workload, rank, world, dist, sampler, e2e=False, steps=Non
         elif case.kind == "gqa":
             pda.paged_decode_attn(q_, kc, vc, tables_, ctx_, case.scale, out_, lse_, plan, ws,
                                   stream)
+        elif fp8:
+            pda.mla_decode_fp8(q_, kc, case.k_scale, tables_, ctx_, case.scale, out_, lse_, plan,
+                               ws, stream)
         else:
             pda.mla_decode(q_, kc, tables_, ctx_, case.scale, out_, lse_, plan, ws, stream)
 

@@ -211,6 +211,22 @@ PDA_API pda_status mla_decode(const void* q, const void* kv_cache, const int32_t
                       const pda_plan* plan, void* workspace, pda_stream_t stream);
 
 /*
+ * mla_decode over an E4M3 record cache ("Attention Kernel Variants: MQA, GQA, and MLA",
+ * KV-cache arithmetic table: the DeepSeek-V3 MLA row with an fp8 latent, 34.3 KiB per
+ * token; plan created with kv_format PDA_KV_FP8_E4M3).
+ *   kv_cache   device [num_blocks, 64, Dqk] uint8 E4M3 codes, 16-byte aligned
+ *   kv_scale   the record's per-tensor dequantization scale (finite): rec = e4m3(code) * kv_scale,
+ *              for the scores (all Dqk values) and the values (the first Dv) alike
+ * Every other argument, and the result, as for mla_decode (q, out in the plan's 16-bit
+ * dtype). Supported: seq_len_q * num_q_heads in {16, 32}. A stale slot or an unused block
+ * may hold any code, NaN included.
+ */
+PDA_API pda_status mla_decode_fp8(const void* q, const void* kv_cache, float kv_scale,
+                                  const int32_t* block_tables, const int32_t* context_lens,
+                                  float scale, void* out, float* lse, const pda_plan* plan,
+                                  void* workspace, pda_stream_t stream);
+
+/*
  * Flash-Decoding combine on its own ("From MHA to MLA", section 4): for each
  * of `rows` rows, merge `num_splits` locally normalized partial outputs:
  *   L = max_s L_s + ln sum_s exp(L_s - max_s L_s),   out = sum_s exp(L_s - L) O_s

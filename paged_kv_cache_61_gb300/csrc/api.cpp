@@ -120,24 +120,53 @@ extern "C" PDA_API pda_status paged_decode_attn_fp8(const void* q, const void* k
                   lse, plan, workspace, stream);
 }
 
-extern "C" PDA_API pda_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_tables,
-                                 const int32_t* context_lens, float scale, void* out, float* lse,
-                                 const pda_plan* plan, void* workspace, pda_stream_t stream) {
-  pda::clear_error();
+namespace {
+
+pda_status mla_call(const void* q, const void* kv_cache, float kv_scale,
+                    const int32_t* block_tables, const int32_t* context_lens, float scale,
+                    void* out, float* lse, const pda_plan* plan, void* workspace,
+                    pda_stream_t stream) {
   pda_status st = check_common(plan, PDA_KIND_MLA, q, block_tables, context_lens, scale, out,
                                workspace);
   if (st != PDA_OK || plan->prob.batch == 0) return st;
+  if (!std::isfinite(kv_scale)) return fail(PDA_ERR_INVALID_ARG, "kv_scale must be finite");
   if (kv_cache == nullptr) return fail(PDA_ERR_INVALID_ARG, "kv_cache must be non-NULL");
   if (!aligned(kv_cache, 16))
     return fail(PDA_ERR_INVALID_ARG, "kv_cache must start on a 16-byte boundary");
   if (lse != nullptr && !aligned(lse, 4))
     return fail(PDA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
-  pda::MlaArgs args{q, kv_cache, block_tables, context_lens, scale, out, lse};
+  pda::MlaArgs args{q, kv_cache, block_tables, context_lens, scale, out, lse, kv_scale};
   const int e = pda::launch_mla_decode(*plan, args, pda::workspace_views(*plan, workspace),
                                        stream);
   if (e == -1) return fail(PDA_ERR_INVALID_ARG, "could not build the TMA descriptor of the cache");
   if (e != 0) return cuda_fail(e, "MLA decode launch");
   return PDA_OK;
+}
+
+}  // namespace
+
+extern "C" PDA_API pda_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_tables,
+                                 const int32_t* context_lens, float scale, void* out, float* lse,
+                                 const pda_plan* plan, void* workspace, pda_stream_t stream) {
+  pda::clear_error();
+  if (plan != nullptr && plan->prob.kv_format != PDA_KV_SAME_AS_Q)
+    return fail(PDA_ERR_INVALID_ARG,
+                "the plan's cache is fp8: call mla_decode_fp8 with its scale");
+  return mla_call(q, kv_cache, 1.f, block_tables, context_lens, scale, out, lse, plan, workspace,
+                  stream);
+}
+
+extern "C" PDA_API pda_status mla_decode_fp8(const void* q, const void* kv_cache, float kv_scale,
+                                             const int32_t* block_tables,
+                                             const int32_t* context_lens, float scale, void* out,
+                                             float* lse, const pda_plan* plan, void* workspace,
+                                             pda_stream_t stream) {
+  pda::clear_error();
+  if (plan != nullptr && plan->prob.kv_format != PDA_KV_FP8_E4M3)
+    return fail(PDA_ERR_INVALID_ARG,
+                "the plan's cache is not fp8 (kv_format PDA_KV_FP8_E4M3): call mla_decode");
+  return mla_call(q, kv_cache, kv_scale, block_tables, context_lens, scale, out, lse, plan,
+                  workspace, stream);
 }
 
 extern "C" PDA_API pda_status pda_combine_splits(const float* partial_out, const float* partial_lse,

@@ -69,6 +69,14 @@ struct SoftmaxWarps {
   static constexpr int kThreads = 64 + 32 * kWarps;
   static constexpr int kCols = N / (kWarps / 4);   // head columns per softmax thread
 };
+// E4M3 caches add converter warps after the softmax warps (groups of 16 or 32 rows): one
+// per sub-partition beside 16 heads' four softmax warps, two beside 32 heads' eight (more
+// would cap the registers of every warp below what the softmax warps use).
+template <int N, bool F8>
+struct Roles {
+  static constexpr int kConvWarps = F8 ? (N == 16 ? 4 : 2) : 0;
+  static constexpr int kThreads = SoftmaxWarps<N>::kThreads + 32 * kConvWarps;
+};
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.f;           // lazy-max slack (log2 units)
@@ -84,7 +92,8 @@ struct MlaParams {
   // token i, head h) are contiguous in q and out; with S > 1 they form one head group
   int32_t rows_per_seq, seq_len_q;
   int64_t num_blocks;
-  float scale_log2;
+  float scale_log2;   // softmax scale (times the record scale for E4M3 caches) times log2(e)
+  float v_scale;      // E4M3 caches: the record's dequantization scale (1 for 16-bit caches)
   int64_t total_tiles, tiles_per_cta;
   int32_t heavy_min;
   int32_t* err;
@@ -93,9 +102,12 @@ struct MlaParams {
   float* part_out;
 };
 
-template <int N, int DQK>
+template <int N, int DQK, bool F8 = false>
 struct MlaLayout {
   using R = Rec<DQK>;
+  // E4M3 caches with the two-stage ring (576 record): one page of codes beside the ring,
+  // so the next page's copy lands while the ring's stages are busy
+  static constexpr bool kSepCodes = F8 && R::kStages == 2;
   static constexpr int kQBytes = R::kSubTiles * N * 128;  // q as K-major [N][64] sub-tiles
   static constexpr int kKV = 0;
   static constexpr int kQ = kKV + R::kStages * R::kPageBytes;
@@ -104,8 +116,9 @@ struct MlaLayout {
   static constexpr int kAlpha = kMused + 64 * 4;       // rescale factor per head
   static constexpr int kLtot = kAlpha + 64 * 4;        // softmax denominator per head
   static constexpr int kLqtot = kLtot + 64 * 4;        // sum of the rounded weights per head
-  static constexpr int kBar = kLqtot + 64 * 4;
-  static constexpr int kBarCount = 2 * R::kStages + 20;
+  static constexpr int kCodes = (kLqtot + 64 * 4 + 1023) / 1024 * 1024;   // [page of codes]
+  static constexpr int kBar = kCodes + (kSepCodes ? DQK * 64 : 0);
+  static constexpr int kBarCount = 2 * R::kStages + 24;
   static constexpr int kSmem = 1024 + kBar + kBarCount * 8 + 64;
   static_assert(kSmem <= 232448, "fits the 227 KB of dynamic shared memory per block");
   // TMEM columns: S^T double-buffered at [0, 2N), O^T d-tile mt at 2N + mt*N
@@ -133,18 +146,23 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
   return __float2bfloat16_rn(x);
 }
 
-template <int N, int DQK, typename T>
-__global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
+template <int N, int DQK, typename T, bool F8>
+__global__ void __launch_bounds__(Roles<N, F8>::kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_kv, const MlaParams p) {
-  using L = MlaLayout<N, DQK>;
+  using L = MlaLayout<N, DQK, F8>;
   using R = Rec<DQK>;
   constexpr int kDv = R::kDv;
   constexpr int kSubTiles = R::kSubTiles;
   constexpr int kPageBytes = R::kPageBytes;
   constexpr int kRopeSub = R::kRopeSub;
   constexpr int KS = R::kStages;
-  constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+  // The MMAs' operand type: q's type for 16-bit caches. For E4M3 caches the codes become
+  // fp16 (exact, one conversion per two codes), and q (converted in shared memory once per
+  // piece, exact for |q| in [2^-14, 65504]) and P follow, since both operands of one MMA
+  // share a type; the output keeps q's type.
+  using TM = typename std::conditional<F8, __half, T>::type;
+  constexpr bool kBf16 = std::is_same<TM, __nv_bfloat16>::value;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   uint8_t* kv = base + L::kKV;
@@ -169,6 +187,15 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
   // [0] abort, [1] last piece, [2..9] softmax-warp votes (5 slots)
   volatile int* flags = reinterpret_cast<volatile int*>(bars + 2 * KS + 10);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * KS + 16);
+  // E4M3 caches: a page's codes have landed in the upper half of its stage (the converters
+  // then arrive on kv_full once the stage holds the 16-bit record)
+  uint64_t* kv_f8 = bars + 2 * KS + 17;   // [KS]
+  // separate code page (L::kSepCodes): kv_f8[0] = the page of codes has landed, kv_f8[1] =
+  // the converters have read it
+  constexpr bool kSep = L::kSepCodes;
+  uint8_t* codes_buf = base + L::kCodes;
+  uint64_t* q_cvt = bars + 2 * KS + 17 + KS;   // E4M3 caches: q is in the MMAs' type
+  constexpr int kConvWarps = Roles<N, F8>::kConvWarps;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -179,11 +206,13 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < KS; ++s) {
-      ptx::mbar_init(&kv_full[s], 1);
+      ptx::mbar_init(&kv_full[s], F8 ? kConvWarps : 1);
       ptx::mbar_init(&kv_empty[s], 1);
+      ptx::mbar_init(&kv_f8[s], (kSep && s == 1) ? kConvWarps : 1);
     }
     ptx::mbar_init(q_full, 1);
     ptx::mbar_init(q_empty, 1);
+    ptx::mbar_init(q_cvt, kConvWarps > 0 ? kConvWarps : 1);
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&s_full[b], 1);
       ptx::mbar_init(&s_free[b], SoftmaxWarps<N>::kWarps);
@@ -232,13 +261,26 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
           int good = 1;
           if (lane == 0) {
             const int s = t % KS;
-            if (!bounded_wait(&kv_empty[s], ((t / KS) & 1) ^ 1, flags, p.err)) {
+            // the separate code page waits for the converters to have read the previous
+            // page (they wait for the ring stage); otherwise the stage itself must be free
+            if (kSep ? (t > 0 && !bounded_wait(&kv_f8[1], (t - 1) & 1, flags, p.err))
+                     : !bounded_wait(&kv_empty[s], ((t / KS) & 1) ^ 1, flags, p.err)) {
               good = 0;
             } else {
               if (phys < 0 || int64_t(phys) >= p.num_blocks) atomicOr(p.err, 1);
-              ptx::mbar_arrive_expect_tx(&kv_full[s], kPageBytes);
-              ptx::tma_load_4d(kv + s * kPageBytes, &tm_kv, &kv_full[s], 0, 0, 0, phys,
-                               pol_stream);
+              if constexpr (kSep) {
+                ptx::mbar_arrive_expect_tx(&kv_f8[0], kPageBytes / 2);
+                ptx::tma_load_4d(codes_buf, &tm_kv, &kv_f8[0], 0, 0, 0, phys, pol_stream);
+              } else if constexpr (F8) {
+                // the page's E4M3 codes, [sub-tile][64 tokens][64 B], into the stage's upper half
+                ptx::mbar_arrive_expect_tx(&kv_f8[s], kPageBytes / 2);
+                ptx::tma_load_4d(kv + s * kPageBytes + kPageBytes / 2, &tm_kv, &kv_f8[s], 0, 0,
+                                 0, phys, pol_stream);
+              } else {
+                ptx::mbar_arrive_expect_tx(&kv_full[s], kPageBytes);
+                ptx::tma_load_4d(kv + s * kPageBytes, &tm_kv, &kv_full[s], 0, 0, 0, phys,
+                                 pol_stream);
+              }
               // Two-stage ring (576 record): the page that reuses this stage next goes to
               // L2 now; its load is issued only when this page's PV has freed the stage, and
               // then reads L2, not HBM (B=16, ctx 64K, Hq=16: 281.5 -> 274.1 us). The
@@ -257,11 +299,21 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
     }
     // Leave no copy in flight: the last fill of each stage and of q (bounded).
     if (lane == 0) {
-      for (int k = 1; k <= KS && t - k >= 0; ++k) {
-        const int tt = t - k;
-        const uint64_t t0 = ptx::globaltimer();
-        while (!ptx::mbar_try_wait(&kv_full[tt % KS], (tt / KS) & 1) &&
-               ptx::globaltimer() - t0 < ptx::kWaitLimitNs) {
+      uint64_t* tma_bar = F8 ? kv_f8 : kv_full;   // completed by the copies themselves
+      if (kSep) {
+        if (t > 0) {
+          const uint64_t t0 = ptx::globaltimer();
+          while (!ptx::mbar_try_wait(&kv_f8[0], (t - 1) & 1) &&
+                 ptx::globaltimer() - t0 < ptx::kWaitLimitNs) {
+          }
+        }
+      } else {
+        for (int k = 1; k <= KS && t - k >= 0; ++k) {
+          const int tt = t - k;
+          const uint64_t t0 = ptx::globaltimer();
+          while (!ptx::mbar_try_wait(&tma_bar[tt % KS], (tt / KS) & 1) &&
+                 ptx::globaltimer() - t0 < ptx::kWaitLimitNs) {
+          }
         }
       }
       if (u > 0) {
@@ -304,7 +356,7 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
         if (!qk_done && i < npg) {
           const int s = t_qk & 1;          // S^T buffer
           const int kst = t_qk % KS;       // ring stage
-          const bool ready = (!need_q || ptx::mbar_test_wait(q_full, u & 1)) &&
+          const bool ready = (!need_q || ptx::mbar_test_wait(F8 ? q_cvt : q_full, u & 1)) &&
                              ptx::mbar_test_wait(&kv_full[kst], (t_qk / KS) & 1) &&
                              (t_qk < 2 || ptx::mbar_test_wait(&s_free[s], ((t_qk >> 1) - 1) & 1));
           if (ready) {
@@ -370,6 +422,95 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
       }
     }
     __syncwarp();
+  } else if (F8 && warp >= 2 + SoftmaxWarps<N>::kWarps) {
+    // ============================== E4M3 converters ==============================
+    // A page's E4M3 codes land in the upper half of its stage as kSubTiles blocks of
+    // [64 tokens][64 bytes]; the converter warps rewrite the stage in place as the 16-bit
+    // record the MMAs read: kSubTiles 128-byte-swizzled [64 tokens][64 dims] sub-tiles,
+    // the layout the 16-bit cache's TMA map gives. Codes convert exactly (cvt.rn.f16x2.e4m3x2;
+    // bf16 through f32); the record scale is applied to the scores and the output instead.
+    // With the codes in the stage's upper half (the four-stage ring of the 320 record),
+    // sub-tile k is written over bytes [8K k, 8K k + 8K), which reach the codes from
+    // k = kFirstOverlap on, and there only blocks j <= k: each sub-tile is read into
+    // registers first, and from kFirstOverlap on the converters meet at a named barrier
+    // between reading and writing, so every block is read before anything overwrites it.
+    // The barrier count never depends on an abort, so the warps always meet. (The 576
+    // record's two-stage ring keeps the codes in a page of their own instead.)
+    constexpr int kCT = 32 * (kConvWarps > 0 ? kConvWarps : 1);
+    constexpr int kPer = (kPage * 4) / kCT;      // 16-byte code chunks per thread per sub-tile
+    // the first sub-tile whose 16-bit bytes reach the codes in the stage's upper half
+    constexpr int kFirstOverlap = (kPageBytes / 2) / kSubBytes;
+    const int ct = threadIdx.x - SoftmaxWarps<N>::kThreads;
+    bool aborted = false;
+    int t = 0, u = 0;
+    while (walk.g < g_hi) {
+      const Portion pt = walker_next(walk, spec, g_hi);
+      // this piece's q in the MMAs' type: bf16 -> fp16 in place (16 bytes at a time)
+      if (!aborted && !bounded_wait(q_full, u & 1, flags, p.err)) aborted = true;
+      if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        if (!aborted) {
+          for (int i = ct; i < L::kQBytes / 16; i += kCT) {
+            uint4* w = reinterpret_cast<uint4*>(qs) + i;
+            uint4 v = *w;
+            uint32_t* e = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float lo = __uint_as_float(e[k] << 16), hi = __uint_as_float(e[k] & 0xffff0000u);
+              e[k] = ptx::Mma<__half>::pack(lo, hi);
+            }
+            *w = v;
+          }
+        }
+      }
+      ptx::fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(q_cvt);
+      ++u;
+      for (int i = pt.p0; i < pt.p1; ++i, ++t) {
+        const int s = t % KS;
+        if (kSep) {
+          // the page's codes have landed, and the ring stage is free (PV of page t - KS)
+          if (!aborted && !bounded_wait(&kv_f8[0], t & 1, flags, p.err)) aborted = true;
+          if (!aborted && !bounded_wait(&kv_empty[s], ((t / KS) & 1) ^ 1, flags, p.err))
+            aborted = true;
+        } else if (!aborted && !bounded_wait(&kv_f8[s], (t / KS) & 1, flags, p.err)) {
+          aborted = true;
+        }
+        uint8_t* stg = kv + s * kPageBytes;
+        const uint8_t* codes = kSep ? codes_buf : stg + kPageBytes / 2;
+#pragma unroll 1
+        for (int k = 0; k < kSubTiles; ++k) {
+          uint4 x[kPer];
+#pragma unroll
+          for (int c = 0; c < kPer; ++c) {
+            const int idx = ct + c * kCT;          // row idx / 4, 16-byte piece idx % 4
+            x[c] = aborted ? make_uint4(0u, 0u, 0u, 0u)
+                           : *reinterpret_cast<const uint4*>(codes + k * (kPage * 64) +
+                                                             (idx >> 2) * 64 + (idx & 3) * 16);
+          }
+          if (!kSep && k >= kFirstOverlap) ptx::named_barrier_sync(2, kCT);
+#pragma unroll
+          for (int c = 0; c < kPer; ++c) {
+            const int idx = ct + c * kCT;
+            const int r = idx >> 2, m = idx & 3;
+            uint4 w0, w1;
+            ptx::Mma<TM>::from_e4m3x4(x[c].x, w0.x, w0.y);
+            ptx::Mma<TM>::from_e4m3x4(x[c].y, w0.z, w0.w);
+            ptx::Mma<TM>::from_e4m3x4(x[c].z, w1.x, w1.y);
+            ptx::Mma<TM>::from_e4m3x4(x[c].w, w1.z, w1.w);
+            uint8_t* row = stg + k * kSubBytes + r * 128;
+            *reinterpret_cast<uint4*>(row + (((2 * m) ^ (r & 7)) << 4)) = w0;
+            *reinterpret_cast<uint4*>(row + (((2 * m + 1) ^ (r & 7)) << 4)) = w1;
+          }
+        }
+        ptx::fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          if (kSep) ptx::mbar_arrive(&kv_f8[1]);   // the code page may be refilled
+          ptx::mbar_arrive(&kv_full[s]);
+        }
+      }
+    }
   } else {
     // ============================== softmax / epilogue warps ==============================
     constexpr int kSW = SoftmaxWarps<N>::kWarps;
@@ -516,16 +657,16 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
             l_reg[c + e] += pv[e];
           }
           uint4 w;
-          w.x = ptx::Mma<T>::pack(pv[0], pv[1]);
-          w.y = ptx::Mma<T>::pack(pv[2], pv[3]);
-          w.z = ptx::Mma<T>::pack(pv[4], pv[5]);
-          w.w = ptx::Mma<T>::pack(pv[6], pv[7]);
+          w.x = ptx::Mma<TM>::pack(pv[0], pv[1]);
+          w.y = ptx::Mma<TM>::pack(pv[2], pv[3]);
+          w.z = ptx::Mma<TM>::pack(pv[4], pv[5]);
+          w.w = ptx::Mma<TM>::pack(pv[6], pv[7]);
           {
             float r[8];
-            ptx::Mma<T>::unpack(w.x, r[0], r[1]);
-            ptx::Mma<T>::unpack(w.y, r[2], r[3]);
-            ptx::Mma<T>::unpack(w.z, r[4], r[5]);
-            ptx::Mma<T>::unpack(w.w, r[6], r[7]);
+            ptx::Mma<TM>::unpack(w.x, r[0], r[1]);
+            ptx::Mma<TM>::unpack(w.y, r[2], r[3]);
+            ptx::Mma<TM>::unpack(w.z, r[4], r[5]);
+            ptx::Mma<TM>::unpack(w.w, r[6], r[7]);
 #pragma unroll
             for (int e = 0; e < 8; ++e) lq_reg[c + e] += r[e];
           }
@@ -617,7 +758,7 @@ __global__ void __launch_bounds__(SoftmaxWarps<N>::kThreads, 1)
           for (int e = 0; e < 16; ++e) {
             const int h = cb + c + e;
             // ltot = 0 only for a causal row that saw no token of a split piece: O = 0
-            const float o = ltot[h] > 0.f ? v[e] / lqtot[h] : 0.f;
+            const float o = ltot[h] > 0.f ? v[e] * p.v_scale / lqtot[h] : 0.f;
             if (whole)
               outg[(head0 + h) * kDv + d] = from_f32<T>(o);
             else
@@ -747,38 +888,56 @@ bool encode_mla_maps(CUtensorMap* tq, CUtensorMap* tkv, const void* q, int64_t r
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// E4M3 record cache [blocks, 64, dqk] bytes: dims (d mod 64, slot, d / 64, block), box
+// (64, 64, S, 1), no swizzle: S blocks of [64 tokens][64 bytes] per page.
+bool encode_mla_cache_f8(CUtensorMap* tkv, const void* kv, int64_t num_blocks, int dqk) {
+  EncodeTiledFn fn = mla_encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t kDqk = cuuint64_t(dqk);
+  const cuuint64_t kdims[4] = {64, kPage, cuuint64_t(dqk / 64), cuuint64_t(num_blocks)};
+  const cuuint64_t kstr[3] = {kDqk, 64, cuuint64_t(kPage) * kDqk};
+  const cuuint32_t kbox[4] = {64, kPage, cuuint32_t(dqk / 64), 1};
+  const cuuint32_t e4[4] = {1, 1, 1, 1};
+  return fn(tkv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(kv), kdims, kstr, kbox, e4,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 namespace {
 
-template <int N, int DQK, typename T>
+template <int N, int DQK, typename T, bool F8>
 int launch_mla_n(const CUtensorMap& tq, const CUtensorMap& tkv, const MlaParams& prm, int grid,
                  cudaStream_t stream) {
-  auto kern = mla_decode_kernel<N, DQK, T>;
-  using L = MlaLayout<N, DQK>;
+  auto kern = mla_decode_kernel<N, DQK, T, F8>;
+  using L = MlaLayout<N, DQK, F8>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  kern<<<grid, SoftmaxWarps<N>::kThreads, L::kSmem, stream>>>(tq, tkv, prm);
+  kern<<<grid, Roles<N, F8>::kThreads, L::kSmem, stream>>>(tq, tkv, prm);
   return cudaGetLastError();
 }
 
 template <int DQK, typename T>
-int launch_mla_t(int n, const CUtensorMap& tq, const CUtensorMap& tkv, const MlaParams& prm,
-                 int grid, cudaStream_t s) {
+int launch_mla_t(int n, bool f8, const CUtensorMap& tq, const CUtensorMap& tkv,
+                 const MlaParams& prm, int grid, cudaStream_t s) {
+  if (f8)   // E4M3 caches: groups of 16 or 32 rows (mla_supported)
+    return n == 16 ? launch_mla_n<16, DQK, T, true>(tq, tkv, prm, grid, s)
+                   : launch_mla_n<32, DQK, T, true>(tq, tkv, prm, grid, s);
   switch (n) {
-    case 16: return launch_mla_n<16, DQK, T>(tq, tkv, prm, grid, s);
-    case 32: return launch_mla_n<32, DQK, T>(tq, tkv, prm, grid, s);
-    default: return launch_mla_n<64, DQK, T>(tq, tkv, prm, grid, s);
+    case 16: return launch_mla_n<16, DQK, T, false>(tq, tkv, prm, grid, s);
+    case 32: return launch_mla_n<32, DQK, T, false>(tq, tkv, prm, grid, s);
+    default: return launch_mla_n<64, DQK, T, false>(tq, tkv, prm, grid, s);
   }
 }
 
 template <typename T>
-int launch_mla_dt(int dqk, int n, const CUtensorMap& tq, const CUtensorMap& tkv,
+int launch_mla_dt(int dqk, int n, bool f8, const CUtensorMap& tq, const CUtensorMap& tkv,
                   const MlaParams& prm, int grid, cudaStream_t s) {
-  return dqk == 320 ? launch_mla_t<320, T>(n, tq, tkv, prm, grid, s)
-                    : launch_mla_t<576, T>(n, tq, tkv, prm, grid, s);
+  return dqk == 320 ? launch_mla_t<320, T>(n, f8, tq, tkv, prm, grid, s)
+                    : launch_mla_t<576, T>(n, f8, tq, tkv, prm, grid, s);
 }
 
 }  // namespace
@@ -796,8 +955,14 @@ int mla_heads_per_cta(const pda_problem& p) {
 int mla_ctas_per_sm(const pda_problem&) { return 1; }
 
 bool mla_supported(const pda_problem& p, std::string* why) {
-  if (p.kv_format != PDA_KV_SAME_AS_Q) {
-    *why = "MLA decode supports 16-bit caches (kv_format PDA_KV_SAME_AS_Q)";
+  if (p.kv_format == PDA_KV_FP8_E4M3) {
+    const int64_t rows = int64_t(p.seq_len_q > 1 ? p.seq_len_q : 1) * p.num_q_heads;
+    if (rows != 16 && rows != 32) {
+      *why = "MLA decode over E4M3 caches supports seq_len_q * num_q_heads in {16, 32}";
+      return false;
+    }
+  } else if (p.kv_format != PDA_KV_SAME_AS_Q) {
+    *why = "MLA decode supports 16-bit or E4M3 caches";
     return false;
   }
   if (p.seq_len_q > 1) {
@@ -839,12 +1004,14 @@ int launch_mla_decode(const Plan& plan, const MlaArgs& a, const Workspace& ws, v
   if (mla_uses_rows(plan.prob)) return launch_mla_rows(plan, a, ws, stream);
   const pda_problem& pr = plan.prob;
   const bool bf16 = pr.dtype == PDA_BF16;
+  const bool f8 = pr.kv_format == PDA_KV_FP8_E4M3;
   const int n = plan.group;
   CUtensorMap m[2];
   const int sq = pr.seq_len_q > 1 ? pr.seq_len_q : 1;
   if (!plan.map_cache.get(a.q, a.kv_cache, m, nullptr, [&](CUtensorMap* t, int32_t*) {
         return encode_mla_maps(&t[0], &t[1], a.q, int64_t(pr.batch) * sq * pr.num_q_heads, n,
-                               a.kv_cache, pr.num_blocks, bf16, pr.head_dim_qk);
+                               a.kv_cache, pr.num_blocks, bf16, pr.head_dim_qk) &&
+               (!f8 || encode_mla_cache_f8(&t[1], a.kv_cache, pr.num_blocks, pr.head_dim_qk));
       }))
     return -1;
   const CUtensorMap& tq = m[0];
@@ -862,7 +1029,8 @@ int launch_mla_decode(const Plan& plan, const MlaArgs& a, const Workspace& ws, v
   prm.groups = plan.segs_per_seq;
   prm.max_blocks = pr.max_blocks_per_seq;
   prm.num_blocks = pr.num_blocks;
-  prm.scale_log2 = a.scale * kLog2e;
+  prm.scale_log2 = a.scale * a.kv_scale * kLog2e;
+  prm.v_scale = a.kv_scale;
   prm.total_tiles = plan.total_tiles;
   prm.tiles_per_cta = plan.tiles_per_cta;
   prm.heavy_min = plan.heavy_min_pieces;
@@ -872,8 +1040,8 @@ int launch_mla_decode(const Plan& plan, const MlaArgs& a, const Workspace& ws, v
   prm.part_out = ws.part_out;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int dqk = pr.head_dim_qk;
-  const int e = bf16 ? launch_mla_dt<__nv_bfloat16>(dqk, n, tq, tkv, prm, plan.num_ctas, s)
-                     : launch_mla_dt<__half>(dqk, n, tq, tkv, prm, plan.num_ctas, s);
+  const int e = bf16 ? launch_mla_dt<__nv_bfloat16>(dqk, n, f8, tq, tkv, prm, plan.num_ctas, s)
+                     : launch_mla_dt<__half>(dqk, n, f8, tq, tkv, prm, plan.num_ctas, s);
   if (e != 0) return e;
   return launch_split_merge(plan, ws, a.out, a.lse, stream);
 }

@@ -636,18 +636,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             s_rem = np.p1 - np.p0;
             load_q(np);
           }
-          const int rdy = (lane == 0) ? int(aborted || ptx::mbar_try_wait(s_full, ts & 1)) : 0;
+          // ready: the page's scores exist, and the peer's owners have read page ts-2 from
+          // the buffer this page goes to. Both are polled, never waited for here: this warp
+          // must keep taking in the peer's P rows meanwhile (the peer's owners wait for this
+          // CTA's PV of a page two back, which waits for those rows).
+          const int b2 = ts & 1;
+          const uint32_t par2 = uint32_t(ts >> 1) & 1;
+          const int rdy = (lane == 0) ? int(aborted ||
+                                            (ptx::mbar_try_wait(s_full, ts & 1) &&
+                                             ptx::mbar_try_wait_cluster(&xs_free[b2], par2 ^ 1)))
+                                      : 0;
           if (__shfl_sync(kFullMask, rdy, 0)) {
-            const int b2 = ts & 1;
-            const uint32_t par2 = uint32_t(ts >> 1) & 1;
             float v[kPage];
             read_s(ts, 0, v);
-            // the peer's owners have read page ts-2 from the buffer this page goes to
-            int ok = 1;
-            if (lane == 0 && !aborted &&
-                !bounded_wait_cluster(&xs_free[b2], par2 ^ 1, flags, p.err))
-              ok = 0;
-            if (!__shfl_sync(kFullMask, ok, 0)) aborted = true;
             // both half-rows through this warp's staging block (its previous page's copies
             // have long been read), then one copy per half
             if (lane == 0) ptx::bulk_wait_read_all();
@@ -1011,7 +1012,8 @@ cudaError_t pair_kernel_attributes() {
 }  // namespace
 
 bool mla_uses_pairs(const pda_problem& p) {
-  return p.head_dim_qk == kDqk && p.num_q_heads % kHeads == 0 && p.seq_len_q <= 1;
+  return p.head_dim_qk == kDqk && p.num_q_heads % kHeads == 0 && p.seq_len_q <= 1 &&
+         p.kv_format == PDA_KV_SAME_AS_Q;
 }
 
 int mla_pair_units(int num_sms) {

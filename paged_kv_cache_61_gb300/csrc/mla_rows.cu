@@ -629,7 +629,8 @@ int launch_rows_t(const CUtensorMap& tkv, const RowsParams& prm, int grid, cudaS
 }  // namespace
 
 bool mla_uses_rows(const pda_problem& p) {
-  return p.head_dim_qk == kDqk && p.head_dim_v == kDv && p.num_q_heads % kRows == 0;
+  return p.head_dim_qk == kDqk && p.head_dim_v == kDv && p.num_q_heads % kRows == 0 &&
+         p.kv_format == PDA_KV_SAME_AS_Q;
 }
 
 int launch_mla_rows(const Plan& plan, const MlaArgs& a, const Workspace& ws, void* stream) {

@@ -125,6 +125,7 @@ struct MlaArgs {
   float scale;
   void* out;
   float* lse;
+  float kv_scale = 1.f;   // E4M3 caches: the record's dequantization scale
 };
 int launch_mla_decode(const Plan& plan, const MlaArgs& args, const Workspace& ws, void* stream);
 

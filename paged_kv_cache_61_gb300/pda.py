@@ -53,6 +53,7 @@ def _declare(lib):
         "paged_decode_attn": (I32, [P, P, P, P, P, F32, P, P, P, P, P]),
         "paged_decode_attn_fp8": (I32, [P, P, P, F32, F32, P, P, F32, P, P, P, P, P]),
         "mla_decode": (I32, [P, P, P, P, F32, P, P, P, P, P]),
+        "mla_decode_fp8": (I32, [P, P, F32, P, P, F32, P, P, P, P, P]),
         "pda_combine_splits": (I32, [P, P, I32, I32, I32, P, I32, P, P]),
         "paged_decode_attn_no_alloc": (I32, [P, P, P, P, P, F32, P, P, P, P]),
         "pda_no_alloc_read_device_error": (I32, [P, P]),
@@ -216,6 +217,15 @@ def mla_decode(q, kv_cache, block_tables, context_lens, scale: float, out, lse, 
     _check(lib().mla_decode(_ptr(q), _ptr(kv_cache), _ptr(block_tables), _ptr(context_lens),
                             float(scale), _ptr(out), _ptr(lse), plan.handle, _ptr(workspace),
                             _stream(stream)), "mla_decode")
+
+
+def mla_decode_fp8(q, kv_cache, kv_scale: float, block_tables, context_lens, scale: float, out,
+                   lse, plan: Plan, workspace, stream=None):
+    """mla_decode over an E4M3 record cache (uint8 codes) with its per-tensor scale."""
+    _check(lib().mla_decode_fp8(_ptr(q), _ptr(kv_cache), float(kv_scale), _ptr(block_tables),
+                                _ptr(context_lens), float(scale), _ptr(out), _ptr(lse),
+                                plan.handle, _ptr(workspace), _stream(stream)),
+           "mla_decode_fp8")
 
 
 def combine_splits(partial_out, partial_lse, rows: int, num_splits: int, head_dim_v: int, out,

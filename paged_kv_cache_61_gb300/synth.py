@@ -343,4 +343,5 @@ WORKLOADS = ("gqa_tiny", "gqa_b64_ctx1k", "gqa_b1_ctx32k", "gqa_b1_ctx32k_mqa",
              "gqa_b64_ctx1k_fp8", "gqa_b1_ctx32k_fp8", "gqa_b1_ctx32k_mqa_fp8",
              "gqa_varlen_b128_fp8", "gqa_b64_ctx1k_mtp2", "gqa_b1_ctx32k_mtp2",
              "gqa_b64_ctx1k_mtp2_fp8", "mla_b16_ctx64k_h16_mtp2", "mla_b16_ctx64k_h128_mtp2",
-             "mla_r256_b16_ctx64k_h128_mtp2")
+             "mla_r256_b16_ctx64k_h128_mtp2", "mla_b16_ctx64k_h16_fp8",
+             "mla_r256_b16_ctx64k_h16_fp8")

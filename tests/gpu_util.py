@@ -79,6 +79,9 @@ class DeviceCase:
         elif c.kind == "gqa":
             pda.paged_decode_attn(self.q, self.k, self.v, self.tables, self.ctx, c.scale, out, lse,
                                   self.plan, self.ws)
+        elif c.kv_format == synth.FP8_E4M3:
+            pda.mla_decode_fp8(self.q, self.kv, c.k_scale, self.tables, self.ctx, c.scale, out,
+                               lse, self.plan, self.ws)
         else:
             pda.mla_decode(self.q, self.kv, self.tables, self.ctx, c.scale, out, lse, self.plan,
                            self.ws)

@@ -158,11 +158,29 @@ def test_fp8_plan_validation():
     with pytest.raises(pda.PdaError) as e:
         _plan(kv_format=5)
     assert e.value.status == pda.PDA_ERR_INVALID_ARG
-    with pytest.raises(pda.PdaError) as e:     # MLA has no fp8 kernel
-        _plan(kind=pda.PDA_KIND_MLA, num_q_heads=16, num_kv_heads=1, head_dim_qk=576,
-              head_dim_v=512, page_size=64, max_blocks_per_seq=2, context_lens=[5, 64],
-              kv_format=pda.PDA_KV_FP8_E4M3)
-    assert e.value.status == pda.PDA_ERR_UNSUPPORTED
+    mla = dict(kind=pda.PDA_KIND_MLA, num_kv_heads=1, head_dim_qk=576, head_dim_v=512,
+               page_size=64, max_blocks_per_seq=2, context_lens=[5, 64],
+               kv_format=pda.PDA_KV_FP8_E4M3)
+    # E4M3 record caches: groups of 16 or 32 query rows; larger head counts are refused
+    for hq in (16, 32):
+        assert _plan(num_q_heads=hq, **mla).num_ctas >= 1
+    assert _plan(num_q_heads=16, seq_len_q=2, **mla).num_ctas >= 1
+    for hq in (64, 128):
+        with pytest.raises(pda.PdaError) as e:
+            _plan(num_q_heads=hq, **mla)
+        assert e.value.status == pda.PDA_ERR_UNSUPPORTED
+    # the fp8 call needs an fp8 plan, the 16-bit call a 16-bit one, the scale is finite
+    f8m = _plan(num_q_heads=16, **mla)
+    m16 = _plan(num_q_heads=16, **{**mla, "kv_format": pda.PDA_KV_SAME_AS_Q})
+    margs = (4096, 8192, 64, 128, 0.07, 4096, None)
+    with pytest.raises(pda.PdaError) as e:
+        pda.mla_decode(*margs, f8m, 1 << 20, stream=0)
+    assert e.value.status == pda.PDA_ERR_INVALID_ARG
+    for plan, ks in ((m16, 1.0), (f8m, float("nan"))):
+        with pytest.raises(pda.PdaError) as e:
+            pda.mla_decode_fp8(4096, 8192, ks, 64, 128, 0.07, 4096, None, plan, 1 << 20,
+                               stream=0)
+        assert e.value.status == pda.PDA_ERR_INVALID_ARG
     f8 = _plan(batch=0, context_lens=[], kv_format=pda.PDA_KV_FP8_E4M3)
     pda.paged_decode_attn_fp8(0, 0, 0, 1.0, 1.0, 0, 0, 0.125, 0, None, f8, 0, stream=0)
 
