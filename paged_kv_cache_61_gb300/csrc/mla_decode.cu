@@ -946,7 +946,8 @@ int mla_heads_per_cta(const pda_problem& p) {
   if (p.seq_len_q > 1) {
     const int64_t rows = int64_t(p.seq_len_q) * p.num_q_heads;
     if (rows <= 64) return int(rows);          // all rows of a sequence in one group
-    return mla_uses_rows(p) ? 128 : 64;        // groups of one query token's heads
+    // groups of one query token's heads: 128 on the heads-on-M and two-CTA kernels
+    return (mla_uses_rows(p) || mla_uses_pairs(p)) ? 128 : 64;
   }
   if (mla_uses_pairs(p)) return 128;   // one 128-head group per CTA pair
   if (mla_uses_rows(p)) return 128;    // one 128-head group per CTA, heads on M

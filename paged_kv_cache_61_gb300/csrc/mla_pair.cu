@@ -111,6 +111,9 @@ struct PairParams {
   const int32_t* block_tables;
   const int32_t* context_lens;
   int32_t batch, num_q_heads, groups, max_blocks;
+  // S query tokens per sequence: rows R = i*Hq + h (query token i, head h) are contiguous in
+  // q and out; head group seg holds rows [128 seg, 128 seg + 128), all of one query token
+  int32_t rows_per_seq, seq_len_q;
   int64_t num_blocks;
   float scale_log2;
   int64_t total_tiles, tiles_per_cta;
@@ -432,7 +435,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // q_r rows of this warp's heads into tensor memory (latent dims in columns [0, 128),
     // rope dims in [128, 144)); the two owner warps of a sub-partition split the chunks
     auto load_q = [&](const Portion& pq) __attribute__((always_inline)) {
-      const T* qrow = qg + (int64_t(pq.b) * p.num_q_heads + int64_t(pq.seg) * kHeads + h) * kDqk;
+      const T* qrow = qg + (int64_t(pq.b) * p.rows_per_seq + int64_t(pq.seg) * kHeads + h) * kDqk;
       const int c_lo = owner ? (pos == 0 ? 0 : 5) : 0;
       const int c_hi = owner ? (pos == 0 ? 5 : 9) : 9;
 #pragma unroll
@@ -497,14 +500,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ptx::tmem_st_wait();
       }
     };
+    // lse is [B][Hq][S]: row R = i*Hq + hh of the sequence goes to (b*Hq + hh)*S + i
+    auto lse_at = [&](const Portion& pc, int row) __attribute__((always_inline)) -> int64_t {
+      const int R = pc.seg * kHeads + row;
+      const int qi = R / p.num_q_heads;
+      return (int64_t(pc.b) * p.num_q_heads + (R - qi * p.num_q_heads)) * p.seq_len_q + qi;
+    };
     // normalise columns [c0, c0 + n) of this head's row of O_r by 1/lq and write them out
+    // (lq = 0: a causal head group that saw no token of a split piece; its O is 0)
     auto write_out = [&](const Portion& pc, float lq_tot, float lse_nat, int c0, int n,
                          bool write_lse) __attribute__((always_inline)) {
       const bool whole = (pc.p0 == 0 && pc.p1 == pc.np);
       const int slot = piece_slot(pc.seg_start, g_lo);
-      const int64_t head_row = int64_t(pc.b) * p.num_q_heads + int64_t(pc.seg) * kHeads + h;
+      const int64_t head_row = int64_t(pc.b) * p.rows_per_seq + int64_t(pc.seg) * kHeads + h;
       const int64_t slot_row = (pair * 2 + slot) * kHeads + h;
-      const float inv = 1.f / lq_tot;
+      const float inv = lq_tot > 0.f ? 1.f / lq_tot : 0.f;
 #pragma unroll 2
       for (int c = c0; c < c0 + n; c += 16) {
         float o16[16];
@@ -539,7 +549,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (write_lse) {
         if (whole) {
-          if (owner && p.lse != nullptr) p.lse[head_row] = lse_nat;
+          if (owner && p.lse != nullptr) p.lse[lse_at(pc, h)] = lse_nat;
         } else {
           // each CTA stores the LSE of all 128 heads (its owners' values and the peer's,
           // received at the end of the piece), so each half's merge finds them once its own
@@ -569,7 +579,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ptx::named_barrier_sync(1, kMergeThreads);
           if (flags[1]) {
             __threadfence();
-            const int64_t head0 = int64_t(pc.b) * p.num_q_heads + int64_t(pc.seg) * kHeads;
+            const int64_t head0 = int64_t(pc.b) * p.rows_per_seq + int64_t(pc.seg) * kHeads;
             for (int idx = mtid; idx < kHeads * (kHalfDv / 4); idx += kMergeThreads) {
               const int j = idx / (kHalfDv / 4);
               const int dq = idx - j * (kHalfDv / 4);
@@ -597,7 +607,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               w.x = pack2<T>(acc.x * dinv, acc.y * dinv);
               w.y = pack2<T>(acc.z * dinv, acc.w * dinv);
               *reinterpret_cast<uint2*>(outg + (head0 + j) * kDv + int(rank) * kHalfDv + dq * 4) = w;
-              if (rank == 0 && dq == 0 && p.lse != nullptr) p.lse[head0 + j] = mxl + logf(den);
+              if (rank == 0 && dq == 0 && p.lse != nullptr) p.lse[lse_at(pc, j)] = mxl + logf(den);
             }
             if (mtid == 0) atomicExch(counter, 0);
           }
@@ -762,7 +772,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       while (true) {
         const int npg = cur.p1 - cur.p0;
-        const int ctx = __ldg(p.context_lens + cur.b);
+        // this head group's query token qi sees tokens [0, ctx - S + 1 + qi) (all of them
+        // with S = 1); a page past that limit (the last page, for an earlier token) adds
+        // nothing, and a piece made only of such pages ends with l = 0, LSE = -inf
+        const int qi = cur.seg * kHeads / p.num_q_heads;
+        const int ctx = __ldg(p.context_lens + cur.b) - p.seq_len_q + 1 + qi;
         for (int i = 0; i < npg; ++i, ++t) {
           const int b2 = t & 1;
           const uint32_t par2 = uint32_t(t >> 1) & 1;
@@ -1012,7 +1026,7 @@ cudaError_t pair_kernel_attributes() {
 }  // namespace
 
 bool mla_uses_pairs(const pda_problem& p) {
-  return p.head_dim_qk == kDqk && p.num_q_heads % kHeads == 0 && p.seq_len_q <= 1 &&
+  return p.head_dim_qk == kDqk && p.num_q_heads % kHeads == 0 &&
          p.kv_format == PDA_KV_SAME_AS_Q;
 }
 
@@ -1051,6 +1065,8 @@ int launch_mla_pair(const Plan& plan, const MlaArgs& a, const Workspace& ws, voi
   prm.context_lens = a.context_lens;
   prm.batch = pr.batch;
   prm.num_q_heads = pr.num_q_heads;
+  prm.seq_len_q = pr.seq_len_q > 1 ? pr.seq_len_q : 1;
+  prm.rows_per_seq = prm.seq_len_q * pr.num_q_heads;
   prm.groups = plan.segs_per_seq;
   prm.max_blocks = pr.max_blocks_per_seq;
   prm.num_blocks = pr.num_blocks;

@@ -209,13 +209,13 @@ def test_multi_token_plan_validation():
     for hq, dqk in ((64, 576), (128, 576), (128, 320)):
         p = _plan(num_q_heads=hq, **{**mla, "head_dim_qk": dqk, "head_dim_v": dqk - 64,
                                      "force_num_ctas": 1})
-        # accepted: 2 groups of 64 rows (Hq=64), 4 of 64 (576 record, Hq=128) or 2 of 128
-        # (320 record, Hq=128) per sequence
+        # accepted: 2 groups of 64 rows (Hq=64) or 2 of 128 (Hq=128: the two-CTA kernel for
+        # the 576 record, heads-on-M for the 320 one) per sequence
         assert p.num_ctas == 1 and p.workspace_bytes > 0
     # one tile per CTA (force_num_ctas above the tile count) makes num_ctas the tile count,
     # pages x head groups per sequence: ctx 5 and 64 are one 64-token page each
-    for hq, dqk, groups in ((16, 576, 1), (64, 576, 2), (128, 576, 4), (128, 320, 2),
-                            (256, 320, 4)):
+    for hq, dqk, groups in ((16, 576, 1), (64, 576, 2), (128, 576, 2), (128, 320, 2),
+                            (256, 320, 4), (256, 576, 4)):
         p = _plan(num_q_heads=hq, **{**mla, "head_dim_qk": dqk, "head_dim_v": dqk - 64,
                                      "force_num_ctas": 1000})
         assert p.num_ctas == 2 * groups, (hq, dqk)

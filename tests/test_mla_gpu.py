@@ -219,8 +219,9 @@ def test_mtp_piece_where_a_row_sees_no_token(ctx, hq, latent):
     # Hq = 128, a whole head group's piece)
     case = synth.make_mla_case(batch=1, num_q_heads=hq, dtype=synth.BF16, context_lens=[ctx],
                                seed=2, seq_len_q=2, latent_dim=latent)
-    # head groups per sequence: all 2 * Hq rows (<= 64), else groups of one token's heads
-    groups = 1 if 2 * hq <= 64 else 2 * hq // (128 if latent == 256 else 64)
+    # head groups per sequence: all 2 * Hq rows (<= 64), else groups of one token's 128
+    # heads (the two-CTA kernel for the 576 record, heads-on-M for the 320 one)
+    groups = 1 if 2 * hq <= 64 else 2 * hq // 128
     for force in ((ctx // 64 + 1) * groups, 0):
         _assert_close_mtp(case, DeviceCase(case, force_num_ctas=force))
 
