@@ -487,8 +487,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int valid = min(kPage, ctx - (pt.p0 + i) * kPage);
         const uint32_t vb = kb + L::kTileBytes;
 
-        // S^T = K * Q^T  (M = 16 tokens, N = 8 heads, K = D)
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        // S^T = K * Q^T  (M = 16 tokens, N = 8 heads, K = D), as two independent chains
+        // over the even and odd k-steps (half the dependent MMA latency per page)
+        float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int ks = 0; ks < kKS; ++ks) {
           const int chunk = (ks & 3) * 2 + chunk_k;
@@ -496,8 +497,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
               kb + (ks >> 2) * kBoxBytes + tok_k * 128 + ((chunk ^ (tok_k & 7)) << 4);
           uint32_t a[4];
           ptx::ldsm_x4(addr, a[0], a[1], a[2], a[3]);
-          ptx::Mma<T>::run(s, a, qf[ks][0], qf[ks][1]);
+          ptx::Mma<T>::run((ks & 1) ? s2 : s, a, qf[ks][0], qf[ks][1]);
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[e] += s2[e];
         float x0 = s[0] * p.scale_log2, x1 = s[1] * p.scale_log2;
         float x2 = s[2] * p.scale_log2, x3 = s[3] * p.scale_log2;
         // tokens of this page each column may see: present slots, then the causal limit
