@@ -93,8 +93,11 @@ typedef struct pda_problem {
                                  S > 1 (speculative / MTP decoding): query token i of
                                  sequence b sits at position ctx_b - S + i and attends to
                                  tokens 0 .. ctx_b - S + i (causal, bottom-right aligned);
-                                 every ctx_b >= S. GQA: S * Hq / Hkv <= 32. MLA (16-bit
-                                 records): S * Hq in {16, 32, 64}, or Hq a multiple of 64 */
+                                 every ctx_b >= S. GQA: S * Hq / Hkv <= 1024 (a KV
+                                 head's rows beyond 32 are computed in equal chunks of
+                                 at most 32 rows, each of which reads the KV head's
+                                 pages). MLA (16-bit records): S * Hq in {16, 32, 64},
+                                 or Hq a multiple of 64 */
 } pda_problem;
 
 typedef struct pda_plan pda_plan;  /* opaque, owned by the library */

@@ -78,7 +78,9 @@ struct MergeParams {
   float* lse;
   int64_t tiles_per_cta;
   int32_t group, dv, num_q_heads, count;
-  int32_t heads_per_seg, seq_len_q;  // G and S of the segments' rows (row r = i*G + g)
+  int32_t heads_per_seg, seq_len_q;  // G and S of a KV head's rows (row r = i*G + g)
+  // GQA: segment seg is KV head seg / row_chunks, rows (seg % row_chunks) * group + j
+  int32_t row_chunks;
   // MLA: segment seg holds rows R = seg*group + r of the sequence's S*Hq rows (R = i*Hq + h)
   int32_t mla_rows;
   HeavySegment seg[kMaxHeavySegments];
@@ -104,6 +106,10 @@ __global__ void __launch_bounds__(kMergeThreads)
   w /= chunks;
   const int j = w % p.group;
   const HeavySegment hs = p.seg[w / p.group];
+  // GQA: the last row chunk of a KV head may hold fewer than `group` rows
+  const int kvh = hs.seg / p.row_chunks;
+  const int r = (hs.seg - kvh * p.row_chunks) * p.group + j;
+  if (!p.mla_rows && r >= p.heads_per_seg * p.seq_len_q) return;
   const int64_t q = p.tiles_per_cta;
   const int64_t c0 = hs.seg_start / q;
   const int n = int((hs.seg_start + hs.np - 1) / q - c0 + 1);
@@ -166,7 +172,7 @@ __global__ void __launch_bounds__(kMergeThreads)
       ri = {(int64_t(hs.b) * p.seq_len_q + qi) * p.num_q_heads + h,
             (int64_t(hs.b) * p.num_q_heads + h) * p.seq_len_q + qi};
     } else {
-      ri = seg_row(hs.b, hs.seg, j, p.heads_per_seg, p.seq_len_q, p.num_q_heads);
+      ri = seg_row(hs.b, kvh, r, p.heads_per_seg, p.seq_len_q, p.num_q_heads);
     }
     T* out = static_cast<T*>(p.out) + ri.out_row * p.dv + dofs;
     out[0] = to_out<T>(s.x * inv);
@@ -206,6 +212,7 @@ int launch_split_merge(const Plan& plan, const Workspace& ws, void* out, float* 
   prm.num_q_heads = plan.prob.num_q_heads;
   prm.heads_per_seg = plan.heads_per_seg;
   prm.seq_len_q = plan.seq_len_q;
+  prm.row_chunks = plan.row_chunks;
   prm.mla_rows = plan.prob.kind == PDA_KIND_MLA ? 1 : 0;
   prm.count = int32_t(plan.heavy.size());
   int max_pieces = 0;

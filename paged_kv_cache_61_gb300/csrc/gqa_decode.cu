@@ -80,7 +80,10 @@ struct GqaParams {
   const int32_t* block_tables;
   const int32_t* context_lens;
   int32_t batch, num_q_heads, num_kv_heads, group, max_blocks;
-  int32_t heads_per_kv, seq_len_q;  // G and S: a segment's rows are r = i*G + g (group = S*G)
+  int32_t heads_per_kv, seq_len_q;  // G and S: a KV head's rows are r = i*G + g
+  // A KV head's S*G rows form row_chunks segments of `group` rows (the last one may hold
+  // fewer): segment seg is KV head seg / row_chunks, rows (seg % row_chunks) * group + j.
+  int32_t row_chunks, segs_per_seq;
   int64_t num_blocks;
   float scale_log2;     // softmax scale (times k_scale for fp8 caches) times log2(e)
   float v_scale;        // fp8 caches: V dequantization scale (1 for 16-bit caches)
@@ -174,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   __syncthreads();
 
-  const WalkSpec spec{p.context_lens, p.batch, p.num_kv_heads, kPage};
+  const WalkSpec spec{p.context_lens, p.batch, p.segs_per_seq, kPage};
   Walker walk;
   walker_init(walk, spec, g_lo, lane);
 
@@ -195,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     bool ok = true;
     while (ok && walk.g < g_hi) {
       const Portion pt = walker_next(walk, spec, g_hi);
+      const int kvh = pt.seg / p.row_chunks;
       const int32_t* row = p.block_tables + int64_t(pt.b) * p.max_blocks;
       int32_t next = (pt.p0 + lane < pt.p1) ? __ldg(row + pt.p0 + lane) : 0;
       for (int base = pt.p0; ok && base < pt.p1; base += 32) {
@@ -238,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             // fp8, one map over both caches: lane c copies page c's K and V tiles at once
             if (lane < (two ? 2 : 1)) {
               uint8_t* dst = ring + stage * L::kStageBytes + lane * 2 * L::kTileBytes;
-              ptx::tma_load_5d(dst, &tm_k, &full[stage], 0, pt.seg, 0, lane ? phys2 : phys, 0,
+              ptx::tma_load_5d(dst, &tm_k, &full[stage], 0, kvh, 0, lane ? phys2 : phys, 0,
                                policy);
             }
           } else if (lane < (two ? 4 : 2)) {
@@ -246,9 +250,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             uint8_t* dst = ring + stage * L::kStageBytes + lane * L::kTileBytes;
             const int32_t ph = (lane >> 1) ? phys2 : phys;
             if constexpr (F8)
-              ptx::tma_load_4d(dst, map, &full[stage], 0, pt.seg, 0, ph, policy);
+              ptx::tma_load_4d(dst, map, &full[stage], 0, kvh, 0, ph, policy);
             else
-              ptx::tma_load_5d(dst, map, &full[stage], 0, 0, 0, pt.seg, ph, policy);
+              ptx::tma_load_5d(dst, map, &full[stage], 0, 0, 0, kvh, ph, policy);
           }
           filled |= 1u << stage;
           if (++stage == kStages) {
@@ -305,6 +309,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const Portion pt = walker_next(walk, spec, g_hi);
     const int ctx = __ldg(p.context_lens + pt.b);
     const int npg = pt.p1 - pt.p0;
+    // the segment's KV head, its first row and its row count
+    const int kvh = pt.seg / p.row_chunks;
+    const int rbase = (pt.seg - kvh * p.row_chunks) * p.group;
+    const int nrows = min(p.group, p.heads_per_kv * p.seq_len_q - rbase);
 
     // Q^T as the B operand (k = head dim, n = head): lane holds head hsub*8 + lane/4.
     // fp8 caches: the K fragment of a lane holds 4 consecutive dims of a token (one
@@ -314,10 +322,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int jq = hsub * 8 + r0;
     uint32_t qf[kKS][2];
     {
-      const bool hv = jq < p.group;
+      const bool hv = jq < nrows;
       const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-          qg + seg_row(pt.b, pt.seg, hv ? jq : 0, p.heads_per_kv, p.seq_len_q, p.num_q_heads)
-                       .out_row * D);
+          qg + seg_row(pt.b, kvh, rbase + (hv ? jq : 0), p.heads_per_kv, p.seq_len_q,
+                       p.num_q_heads).out_row * D);
 #pragma unroll
       for (int ks = 0; ks < kKS; ++ks) {
         if constexpr (F8) {
@@ -330,14 +338,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
     }
 
-    // Causal limits of this lane's two columns (rows hsub*8 + cq, + 1): row r = i*G + g
-    // is query token i, which sees tokens [0, ctx - S + 1 + i) (bottom-right aligned; all
-    // ctx tokens when S = 1). Padded rows take ctx.
+    // Causal limits of this lane's two columns (segment rows hsub*8 + cq, + 1): row
+    // r = i*G + g of the KV head is query token i, which sees tokens [0, ctx - S + 1 + i)
+    // (bottom-right aligned; all ctx tokens when S = 1). Padded rows take ctx.
     int lim0 = ctx, lim1 = ctx;
     if (p.seq_len_q > 1) {
       const int ra = hsub * 8 + cq;
-      if (ra < p.group) lim0 = ctx - p.seq_len_q + 1 + ra / p.heads_per_kv;
-      if (ra + 1 < p.group) lim1 = ctx - p.seq_len_q + 1 + (ra + 1) / p.heads_per_kv;
+      if (ra < nrows) lim0 = ctx - p.seq_len_q + 1 + (rbase + ra) / p.heads_per_kv;
+      if (ra + 1 < nrows) lim1 = ctx - p.seq_len_q + 1 + (rbase + ra + 1) / p.heads_per_kv;
     }
 
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
@@ -600,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int slot = piece_slot(pt.seg_start, g_lo);
     const int64_t slot_row = (int64_t(blockIdx.x) * 2 + slot) * p.group;
     constexpr int kChunks = D / 8;
-    for (int idx = tid; idx < p.group * kChunks; idx += kConsumerWarps * 32) {
+    for (int idx = tid; idx < nrows * kChunks; idx += kConsumerWarps * 32) {
       const int j = idx / kChunks;
       const int dc = idx - j * kChunks;
       const int hs = j >> 3, n = j & 7;
@@ -628,7 +636,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       for (int e = 0; e < 8; ++e) o[e] *= inv;
       const float lse_nat = lsum > 0.f ? (mx + log2f(lsum)) * kLn2 : -INFINITY;
       if (whole) {
-        const RowIndex ri = seg_row(pt.b, pt.seg, j, p.heads_per_kv, p.seq_len_q, p.num_q_heads);
+        const RowIndex ri =
+            seg_row(pt.b, kvh, rbase + j, p.heads_per_kv, p.seq_len_q, p.num_q_heads);
         *reinterpret_cast<uint4*>(outg + ri.out_row * D + dc * 8) = pack8<T>(o);
         if (dc == 0 && p.lse != nullptr) p.lse[ri.lse] = lse_nat;
       } else {
@@ -648,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (pieces <= p.heavy_min) {
         __threadfence();
         ptx::named_barrier_sync(1, kConsumerWarps * 32);
-        int32_t* counter = p.counters + int64_t(pt.b) * p.num_kv_heads + pt.seg;
+        int32_t* counter = p.counters + int64_t(pt.b) * p.segs_per_seq + pt.seg;
         if (tid == 0) {
           const int prev = aborted ? -1 : atomicAdd(counter, 1);
           flags[1] = (prev == pieces - 1) ? 1 : 0;
@@ -656,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         ptx::named_barrier_sync(1, kConsumerWarps * 32);
         if (flags[1]) {
           __threadfence();
-          for (int idx = tid; idx < p.group * kChunks; idx += kConsumerWarps * 32) {
+          for (int idx = tid; idx < nrows * kChunks; idx += kConsumerWarps * 32) {
             const int j = idx / kChunks;
             const int dc = idx - j * kChunks;
             // online merge over the pieces, four at a time with independent loads
@@ -696,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
             for (int e = 0; e < 8; ++e) o[e] *= inv;
             const RowIndex ri =
-                seg_row(pt.b, pt.seg, j, p.heads_per_kv, p.seq_len_q, p.num_q_heads);
+                seg_row(pt.b, kvh, rbase + j, p.heads_per_kv, p.seq_len_q, p.num_q_heads);
             *reinterpret_cast<uint4*>(outg + ri.out_row * D + dc * 8) = pack8<T>(o);
             if (dc == 0 && p.lse != nullptr) p.lse[ri.lse] = mx + logf(den);
           }
@@ -858,8 +867,13 @@ bool gqa_supported(const pda_problem& p, std::string* why) {
   }
   const int g = p.num_q_heads / p.num_kv_heads;
   const int sq = p.seq_len_q > 1 ? p.seq_len_q : 1;
-  if (int64_t(g) * sq > 32) {
-    *why = "GQA decode supports up to 32 query rows (seq_len_q * Hq / Hkv) per KV head";
+  if (int64_t(g) * sq > kMaxRowsPerKvHead) {
+    *why = "GQA decode supports up to " + std::to_string(kMaxRowsPerKvHead) +
+           " query rows (seq_len_q * Hq / Hkv) per KV head";
+    return false;
+  }
+  if (int64_t(p.num_kv_heads) * ((int64_t(g) * sq + 31) / 32) > INT32_MAX) {
+    *why = "Hkv times the row chunks per KV head must fit in int32";
     return false;
   }
   if (p.num_blocks > INT32_MAX) {
@@ -913,6 +927,8 @@ int launch_gqa_decode(const Plan& plan, const GqaArgs& a, const Workspace& ws, v
   prm.num_kv_heads = pr.num_kv_heads;
   prm.group = plan.group;
   prm.heads_per_kv = plan.heads_per_seg;
+  prm.row_chunks = plan.row_chunks;
+  prm.segs_per_seq = plan.segs_per_seq;
   prm.seq_len_q = plan.seq_len_q;
   prm.max_blocks = pr.max_blocks_per_seq;
   prm.num_blocks = pr.num_blocks;

@@ -27,13 +27,15 @@ namespace pda {
 // are merged by the stand-alone split-merge kernel that follows the decode kernel.
 struct HeavySegment {
   int32_t b;          // sequence
-  int32_t seg;        // KV head (GQA) or head group (MLA)
+  int32_t seg;        // segment: KV head and row chunk (GQA) or head group (MLA)
   int32_t np;         // pages of the sequence
   int32_t pad;
   int64_t seg_start;  // flattened index of the segment's first tile
 };
 constexpr int kMaxHeavySegments = 64;
 constexpr int kMaxCtas = 2048;
+// GQA: query rows (S * Hq / Hkv) per KV head; more than 32 are cut into row chunks
+constexpr int kMaxRowsPerKvHead = 1024;
 
 // The TMA descriptors of the last call, keyed by the tensors they address: a plan's
 // shapes are fixed, so a call on the same buffers (the caches, and q for the MLA kernels)
@@ -67,8 +69,9 @@ struct MapCache {
 
 struct Plan {
   pda_problem prob{};
-  int32_t group = 1;            // query rows per segment: S * (GQA: Hq/Hkv; MLA: heads per group)
-  int32_t segs_per_seq = 1;     // segments per sequence (GQA: Hkv; MLA: head groups)
+  int32_t group = 1;            // query rows per segment (GQA: a chunk of S * Hq/Hkv; MLA: heads per group)
+  int32_t segs_per_seq = 1;     // segments per sequence (GQA: Hkv * row_chunks; MLA: head groups)
+  int32_t row_chunks = 1;       // GQA: segments per KV head (its S*G rows cut into chunks of group)
   int32_t head_subtiles = 1;    // GQA: 8-head MMA column tiles per segment
   int32_t cluster = 1;          // CTAs per work unit (2: the MLA kernel for 128-head groups)
   int32_t seq_len_q = 1;        // query tokens per sequence (S)

@@ -124,9 +124,16 @@ extern "C" PDA_API pda_status pda_plan_create(pda_plan** out, const pda_problem*
   int ctas_per_sm;
   int64_t min_tiles_per_cta;
   if (p.kind == PDA_KIND_GQA) {
+    // A KV head's S*G query rows go to one segment when they fit the kernel's four
+    // 8-column MMA tiles (32 rows); more rows are cut into row_chunks segments of equal
+    // size, each of which reads the KV head's pages (the chunks of one head are
+    // neighbours in the tile order, so their CTAs read the same pages at about the same
+    // time and the repeated reads are served by L2).
     plan->heads_per_seg = p.num_q_heads / p.num_kv_heads;
-    plan->group = S * plan->heads_per_seg;
-    plan->segs_per_seq = p.num_kv_heads;
+    const int64_t rows = int64_t(S) * plan->heads_per_seg;
+    plan->row_chunks = int32_t(pda::cdiv(rows, 32));
+    plan->group = int32_t(pda::cdiv(rows, plan->row_chunks));
+    plan->segs_per_seq = p.num_kv_heads * plan->row_chunks;
     plan->head_subtiles = (plan->group + 7) / 8;
     ctas_per_sm = pda::gqa_ctas_per_sm(p);
     // A split piece writes a 4·G·D-byte fp32 partial and reads 64·D bytes per tile: at

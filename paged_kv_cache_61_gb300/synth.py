@@ -320,9 +320,11 @@ def _workload16(name: str, seed: int, kv_format: Optional[str], seq_len_q: int,
     if name == "gqa_b64_ctx1k":
         return make_gqa_case(batch=64, num_q_heads=32, num_kv_heads=8, head_dim=128, dtype=FP16,
                              context_lens=[1024] * 64, table_layout="permutation", **kw)
-    if name in ("gqa_b1_ctx32k", "gqa_b1_ctx32k_mqa"):
-        hkv = 1 if name.endswith("mqa") else 8
-        return make_gqa_case(batch=1, num_q_heads=32, num_kv_heads=hkv, head_dim=128, dtype=BF16,
+    if name in ("gqa_b1_ctx32k", "gqa_b1_ctx32k_mqa", "gqa_b1_ctx32k_mqa_h64"):
+        # _mqa: one KV head; _mqa_h64: one KV head shared by 64 query heads
+        hkv = 1 if "_mqa" in name else 8
+        hq = 64 if name.endswith("_h64") else 32
+        return make_gqa_case(batch=1, num_q_heads=hq, num_kv_heads=hkv, head_dim=128, dtype=BF16,
                              context_lens=[32768], table_layout="permutation", **kw)
     if name == "gqa_varlen_b128":
         return make_gqa_case(batch=128, num_q_heads=64, num_kv_heads=8, head_dim=128, dtype=BF16,
@@ -338,6 +340,7 @@ def _workload16(name: str, seed: int, kv_format: Optional[str], seq_len_q: int,
 
 
 WORKLOADS = ("gqa_tiny", "gqa_b64_ctx1k", "gqa_b1_ctx32k", "gqa_b1_ctx32k_mqa",
+             "gqa_b1_ctx32k_mqa_h64", "gqa_b1_ctx32k_mqa_h64_fp8",
              "gqa_varlen_b128", "mla_b16_ctx64k_h16", "mla_b16_ctx64k_h128",
              "mla_r256_b16_ctx64k_h16", "mla_r256_b16_ctx64k_h128",
              "gqa_b64_ctx1k_fp8", "gqa_b1_ctx32k_fp8", "gqa_b1_ctx32k_mqa_fp8",

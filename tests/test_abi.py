@@ -58,7 +58,7 @@ def _plan(**kw):
     (dict(kind=9), pda.PDA_ERR_INVALID_ARG),
     (dict(head_dim_qk=96, head_dim_v=96), pda.PDA_ERR_UNSUPPORTED),
     (dict(page_size=32, context_lens=[5, 5]), pda.PDA_ERR_UNSUPPORTED),
-    (dict(num_q_heads=128, num_kv_heads=2), pda.PDA_ERR_UNSUPPORTED),     # G = 64
+    (dict(num_q_heads=2050, num_kv_heads=2), pda.PDA_ERR_UNSUPPORTED),    # G = 1025
     (dict(batch=-1), pda.PDA_ERR_INVALID_ARG),
 ])
 def test_plan_rejects_bad_problems(kw, status):
@@ -190,9 +190,9 @@ def test_multi_token_plan_validation():
     with pytest.raises(pda.PdaError) as e:
         _plan(seq_len_q=2, context_lens=[1, 64])
     assert e.value.status == pda.PDA_ERR_INVALID_ARG
-    # S * G query rows per KV head are limited to 32
+    # S * G query rows per KV head are limited to 1024
     with pytest.raises(pda.PdaError) as e:
-        _plan(seq_len_q=3, num_q_heads=24, num_kv_heads=2)
+        _plan(seq_len_q=3, num_q_heads=684, num_kv_heads=2)
     assert e.value.status == pda.PDA_ERR_UNSUPPORTED
     with pytest.raises(pda.PdaError) as e:
         _plan(seq_len_q=-1)
@@ -222,6 +222,28 @@ def test_multi_token_plan_validation():
     # S = 2 doubles the rows of a segment, and so each split piece's partial
     one, two = _plan(), _plan(seq_len_q=2)
     assert two.workspace_bytes > one.workspace_bytes
+
+
+@pytest.mark.parametrize("hq,hkv,s,chunks", [
+    (64, 1, 1, 2),      # MQA with 64 heads: chunks of 32 rows
+    (96, 2, 1, 2),      # G = 48: chunks of 24
+    (40, 1, 1, 2),      # G = 40: chunks of 20
+    (22, 2, 3, 2),      # S * G = 33: chunks of 17 and 16
+    (128, 1, 2, 8),     # 256 rows: chunks of 32
+    (32, 1, 1, 1),      # 32 rows: one segment per KV head
+    (12, 2, 5, 1),      # S * G = 30
+])
+def test_planner_cuts_many_rows_into_chunks(hq, hkv, s, chunks):
+    # more than 32 query rows per KV head: the rows are cut into equal chunks, each a
+    # segment that reads the KV head's pages. With one page per CTA the CTA count is the
+    # tile count: pages x Hkv x chunks (ctx 5 and 64 are 1 + 4 pages of 16 tokens).
+    p = _plan(num_q_heads=hq, num_kv_heads=hkv, seq_len_q=s, context_lens=[max(5, s), 64],
+              force_num_ctas=1000)
+    assert p.num_ctas == 5 * hkv * chunks
+    rows = s * hq // hkv
+    group = -(-rows // chunks)
+    # workspace: two split slots of `group` rows (fp32 LSE + 64 fp32 dims) per CTA
+    assert p.workspace_bytes >= p.num_ctas * 2 * group * 4 * 65
 
 
 @pytest.mark.parametrize("hkv,ctas,splits", [(8, 256, 32), (2, 64, 32), (1, 32, 32)])
