@@ -47,7 +47,8 @@ from paged_kv_cache_61_gb300 import synth, traffic  # noqa: E402
 DEFAULT_WORKLOAD = "gqa_b64_ctx1k"
 # the other decode workloads of the default run, with their role
 PER_CONFIG = ("gqa_tiny", "gqa_b1_ctx32k", "gqa_b1_ctx32k_mqa", "gqa_varlen_b128",
-              "mla_b16_ctx64k_h16", "mla_b16_ctx64k_h128", "mla_b16_ctx64k_h16_fp8")
+              "mla_b16_ctx64k_h16", "mla_b16_ctx64k_h128", "gqa_b64_ctx1k_fp8",
+              "mla_b16_ctx64k_h16_fp8")
 L2_BYTES = 129 * 2 ** 20
 KERNEL_SOURCES = {"gqa": ["gqa_decode.cu", "ptx.cuh", "tile_walk.cuh"],
                   "mla": ["mla_decode.cu", "ptx.cuh", "ptx_ext.cuh", "tile_walk.cuh"],

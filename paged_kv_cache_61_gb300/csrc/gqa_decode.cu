@@ -38,6 +38,7 @@
 
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include "pda_internal.h"
 #include "ptx.cuh"
@@ -139,12 +140,28 @@ __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
   return r;
 }
 
+// A packed pair of q's type as a pair of the MMAs' type (the same bits when they agree).
+template <typename T, typename TM>
+__device__ __forceinline__ uint32_t to_mma_pair(uint32_t w) {
+  if constexpr (std::is_same_v<T, TM>) {
+    return w;
+  } else {
+    float lo, hi;
+    ptx::Mma<T>::unpack(w, lo, hi);
+    return ptx::Mma<TM>::pack(lo, hi);
+  }
+}
+
 // ------------------------------------------------------------------ the kernel
 template <int D, typename T, int NHT, bool F8>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const GqaParams p) {
   using L = Layout<D, F8>;
+  // the MMAs' operand type: q's type, except over E4M3 caches, whose codes convert to
+  // fp16 in one instruction per pair (to bf16 it takes three more); q is then converted
+  // to fp16 as it is loaded (exact for |q| in [2^-14, 65504])
+  using TM = std::conditional_t<F8, __half, T>;
   constexpr int kStages = L::kStages;
   constexpr int kPPT = L::kPPT;
   constexpr int kWP = kConsumerWarps / NHT;  // consumer warps sharing one head subtile
@@ -329,8 +346,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
       for (int ks = 0; ks < kKS; ++ks) {
         if constexpr (F8) {
-          qf[ks][0] = hv ? __ldg(qrow + (ks * 16 + 2 * cq) / 2) : 0u;
-          qf[ks][1] = hv ? __ldg(qrow + (ks * 16 + 2 * cq + 2) / 2) : 0u;
+          qf[ks][0] = hv ? to_mma_pair<T, TM>(__ldg(qrow + (ks * 16 + 2 * cq) / 2)) : 0u;
+          qf[ks][1] = hv ? to_mma_pair<T, TM>(__ldg(qrow + (ks * 16 + 2 * cq + 2) / 2)) : 0u;
         } else {
           qf[ks][0] = hv ? __ldg(qrow + (ks * 16 + cq) / 2) : 0u;
           qf[ks][1] = hv ? __ldg(qrow + (ks * 16 + 8 + cq) / 2) : 0u;
@@ -397,9 +414,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
             for (int hp = 0; hp < 2; ++hp) {
               uint32_t a[4];
-              ptx::Mma<T>::from_e4m3x4(x[hp][2 * h], a[0], a[2]);       // token r0
-              ptx::Mma<T>::from_e4m3x4(x[hp][2 * h + 1], a[1], a[3]);   // token r0 + 8
-              ptx::Mma<T>::run(s[hp], a, qf[ks + h][0], qf[ks + h][1]);
+              ptx::Mma<TM>::from_e4m3x4(x[hp][2 * h], a[0], a[2]);       // token r0
+              ptx::Mma<TM>::from_e4m3x4(x[hp][2 * h + 1], a[1], a[3]);   // token r0 + 8
+              ptx::Mma<TM>::run(s[hp], a, qf[ks + h][0], qf[ks + h][1]);
             }
           }
         }
@@ -457,8 +474,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         uint32_t pb[2][2], vm_lo[2], vm_hi[2];
 #pragma unroll
         for (int hp = 0; hp < 2; ++hp) {
-          pb[hp][0] = ptx::movmatrix_trans(ptx::Mma<T>::pack(pp[hp][0], pp[hp][1]));
-          pb[hp][1] = ptx::movmatrix_trans(ptx::Mma<T>::pack(pp[hp][2], pp[hp][3]));
+          pb[hp][0] = ptx::movmatrix_trans(ptx::Mma<TM>::pack(pp[hp][0], pp[hp][1]));
+          pb[hp][1] = ptx::movmatrix_trans(ptx::Mma<TM>::pack(pp[hp][2], pp[hp][3]));
           const int v = vld[hp];
           vm_lo[hp] = (cq < v ? 0x0000ffffu : 0u) | (cq + 1 < v ? 0xffff0000u : 0u);
           vm_hi[hp] = (cq + 8 < v ? 0x0000ffffu : 0u) | (cq + 9 < v ? 0xffff0000u : 0u);
@@ -481,13 +498,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
             for (int hp = 0; hp < 2; ++hp) {
               uint32_t a[4];
-              ptx::Mma<T>::from_e4m3x4(ptx::prmt(y[hp][2 * h], 0u, 0x3120u), a[0], a[1]);
-              ptx::Mma<T>::from_e4m3x4(ptx::prmt(y[hp][2 * h + 1], 0u, 0x3120u), a[2], a[3]);
+              ptx::Mma<TM>::from_e4m3x4(ptx::prmt(y[hp][2 * h], 0u, 0x3120u), a[0], a[1]);
+              ptx::Mma<TM>::from_e4m3x4(ptx::prmt(y[hp][2 * h + 1], 0u, 0x3120u), a[2], a[3]);
               a[0] &= vm_lo[hp];
               a[1] &= vm_lo[hp];
               a[2] &= vm_hi[hp];
               a[3] &= vm_hi[hp];
-              ptx::Mma<T>::run(acc[mt + h], a, pb[hp][0], pb[hp][1]);
+              ptx::Mma<TM>::run(acc[mt + h], a, pb[hp][0], pb[hp][1]);
             }
           }
         }

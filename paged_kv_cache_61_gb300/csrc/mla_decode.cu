@@ -427,8 +427,8 @@ __global__ void __launch_bounds__(Roles<N, F8>::kThreads, 1)
     // A page's E4M3 codes land in the upper half of its stage as kSubTiles blocks of
     // [64 tokens][64 bytes]; the converter warps rewrite the stage in place as the 16-bit
     // record the MMAs read: kSubTiles 128-byte-swizzled [64 tokens][64 dims] sub-tiles,
-    // the layout the 16-bit cache's TMA map gives. Codes convert exactly (cvt.rn.f16x2.e4m3x2;
-    // bf16 through f32); the record scale is applied to the scores and the output instead.
+    // the layout the 16-bit cache's TMA map gives. Codes convert exactly to fp16
+    // (cvt.rn.f16x2.e4m3x2); the record scale is applied to the scores and the output instead.
     // With the codes in the stage's upper half (the four-stage ring of the 320 record),
     // sub-tile k is written over bytes [8K k, 8K k + 8K), which reach the codes from
     // k = kFirstOverlap on, and there only blocks j <= k: each sub-tile is read into
@@ -494,10 +494,10 @@ __global__ void __launch_bounds__(Roles<N, F8>::kThreads, 1)
             const int idx = ct + c * kCT;
             const int r = idx >> 2, m = idx & 3;
             uint4 w0, w1;
-            ptx::Mma<TM>::from_e4m3x4(x[c].x, w0.x, w0.y);
-            ptx::Mma<TM>::from_e4m3x4(x[c].y, w0.z, w0.w);
-            ptx::Mma<TM>::from_e4m3x4(x[c].z, w1.x, w1.y);
-            ptx::Mma<TM>::from_e4m3x4(x[c].w, w1.z, w1.w);
+            ptx::e4m3x4_to_f16x2(x[c].x, w0.x, w0.y);
+            ptx::e4m3x4_to_f16x2(x[c].y, w0.z, w0.w);
+            ptx::e4m3x4_to_f16x2(x[c].z, w1.x, w1.y);
+            ptx::e4m3x4_to_f16x2(x[c].w, w1.z, w1.w);
             uint8_t* row = stg + k * kSubBytes + r * 128;
             *reinterpret_cast<uint4*>(row + (((2 * m) ^ (r & 7)) << 4)) = w0;
             *reinterpret_cast<uint4*>(row + (((2 * m + 1) ^ (r & 7)) << 4)) = w1;

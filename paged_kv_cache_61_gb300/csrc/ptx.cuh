@@ -169,16 +169,6 @@ __device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t x, uint32_t& lo, uint32
       : "r"(x));
 }
 
-// f16x2 -> bf16x2 through f32; exact for values that came from E4M3 (3 mantissa bits).
-__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t u) {
-  uint32_t d;
-  asm("{\n\t.reg .b16 l, h;\n\t.reg .f32 fl, fh;\n\tmov.b32 {l, h}, %1;\n\t"
-      "cvt.f32.f16 fl, l;\n\tcvt.f32.f16 fh, h;\n\tcvt.rn.bf16x2.f32 %0, fh, fl;\n\t}"
-      : "=r"(d)
-      : "r"(u));
-  return d;
-}
-
 // Byte permute: result byte i = byte sel[i] of {b, a} (a = bytes 0-3).
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
@@ -237,12 +227,6 @@ struct Mma<__nv_bfloat16> {
   __device__ __forceinline__ static void unpack(uint32_t w, float& lo, float& hi) {
     lo = __uint_as_float(w << 16);
     hi = __uint_as_float(w & 0xffff0000u);
-  }
-  __device__ __forceinline__ static void from_e4m3x4(uint32_t x, uint32_t& lo, uint32_t& hi) {
-    uint32_t l, h;
-    e4m3x4_to_f16x2(x, l, h);
-    lo = f16x2_to_bf16x2(l);
-    hi = f16x2_to_bf16x2(h);
   }
 };
 
