@@ -788,11 +788,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!aborted && !bounded_wait_cluster(&xs_full[b2], par2, flags, p.err)) aborted = true;
           if (owner_lead && !aborted) ptx::mbar_arrive_expect_tx(&xs_full[b2], kXsBytes);  // page t+2
           const uint32_t xr = xs_s + b2 * kXsBytes + pos * kXsHalfBytes + row_off;
+          // The peer overwrites this buffer once it sees the relaxed arrive on xs_free below.
+          // The loads are plain shared-memory loads, not acquire loads: every loaded value is
+          // added into v before the warp barrier, and lane 0 issues the arrive after that
+          // barrier, so each lane's loads have returned their data before the arrive is
+          // issued and no later write by the peer can reach them. (The PTX memory model
+          // alone would ask for acquire loads or a release arrive here: acquire loads cost
+          // 410.5 against 399.8 us per step at B=16, ctx 64K, and a release arrive, which
+          // also waits for this thread's outstanding stores to the peer, ~70 us.)
 #pragma unroll
           for (int j = 0; j < kHalfTok / 4; ++j) {
-            // acquire loads: the relaxed arrive on the peer's xs_free below comes after them
             const float4 x = aborted ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                     : ptx::ld_shared_v4_acquire(xr + ((uint32_t(j) ^ swz) << 4));
+                                     : ptx::ld_shared_v4(xr + ((uint32_t(j) ^ swz) << 4));
             v[4 * j] += x.x;
             v[4 * j + 1] += x.y;
             v[4 * j + 2] += x.z;

@@ -52,10 +52,10 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t rbar) {
 
 // Arrive on an mbarrier of a peer CTA with no ordering of this thread's earlier memory
 // accesses: for signalling that a buffer the peer writes has been read, without waiting
-// for this thread's own outstanding stores to the peer (release semantics would). The
-// callers read the buffer with acquire loads (ld_shared_v4_acquire), which keep every
-// later operation, this arrive included, after the loads, and a __syncwarp between every
-// lane's loads and the one lane's arrive orders the other lanes' loads before it too.
+// for this thread's own outstanding stores to the peer (release semantics would). Each
+// caller says how its reads of the buffer come before the arrive: acquire loads
+// (ld_shared_v4_acquire), which keep every later operation after them, or loads whose
+// values are consumed before a __syncwarp that precedes the one lane's arrive.
 __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t rbar) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar)
                : "memory");
