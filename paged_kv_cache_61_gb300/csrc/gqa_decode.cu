@@ -11,12 +11,13 @@
 //  * Persistent-free, equal-work CTAs: the plan gives every CTA the same number
 //    of (sequence, KV head, page) tiles in one flattened list, so one wave of
 //    CTAs covers any batch mix (uniform, one 32K sequence, varlen).
-//  * A producer warp walks the CTA's tiles, reads the block table 32 entries
-//    at a time and issues TMA tile loads (4-D map over [block, slot, kvh, d],
-//    coordinates (d, kvh, 0, phys): the 64-bit address is formed by the TMA
-//    unit, so no 32-bit product phys*stride exists) of each page's K and V into
-//    a ring of shared-memory stages with 128-byte swizzle.
-//  * Four consumer warps take pages round-robin (by CTA-local tile index, so a
+//  * Two producer warps walk the CTA's tiles and take the ring fills alternately;
+//    each reads the block table 32 entries at a time and issues TMA tile loads
+//    (maps over [block, slot, kvh, d], coordinates (d, kvh, phys): the 64-bit
+//    address is formed by the TMA unit, so no 32-bit product phys*stride exists)
+//    of each page's K and V into a ring of shared-memory stages with 128-byte
+//    swizzle. A stage holds one page, or two (fp8 caches; 25-32 rows per segment).
+//  * Four consumer warps take stages round-robin (by CTA-local fill index, so a
 //    ring stage always has the same consumers). Each page is one m16n8k16
 //    tile in the transposed ("keys on M") orientation the FlashMLA-ETAP README
 //    describes for Hopper WGMMA, here on warp MMA: S^T[16 tokens x 8 heads] =
@@ -105,11 +106,17 @@ struct GqaParams {
 // 16-bit tile, and a ring stage holds two consecutive pages ([K A][V A][K B][V B]), so
 // a stage carries as many bytes as a 16-bit one and the per-stage costs (producer
 // issue, barrier waits, the softmax reductions) are paid once per two pages.
-template <int D, bool F8>
+// 16-bit caches with four head subtiles (25-32 rows per segment) take two pages per stage
+// as well, in half as many stages: each consumer warp then owns one subtile and walks
+// every page, and two pages per step give its chain of dependent MMAs, shuffles and
+// exponentials twice the independent work (B=1, ctx 32K, MQA: 7.01 -> 5.78 us). With
+// fewer rows the warps share a subtile's pages, and one page per stage is faster (B=64,
+// ctx 1K: 37.98 against 38.69 us with two).
+template <int D, bool F8, int NHT>
 struct Layout {
   static constexpr int kDBlocks = D / 64;
-  static constexpr int kPPT = F8 ? 2 : 1;                  // pages per ring fill
-  static constexpr int kStages = F8 ? kStagesF8 : kStages16;
+  static constexpr int kPPT = (F8 || NHT == 4) ? 2 : 1;    // pages per ring fill
+  static constexpr int kStages = F8 ? kStagesF8 : (kPPT == 2 ? kStages16 / 2 : kStages16);
   static constexpr int kTileBytes = F8 ? kPage * D : kDBlocks * kBoxBytes;  // page, tensor
   static constexpr int kStageBytes = 2 * kPPT * kTileBytes;
   static constexpr int kMergeStride = D + 4;  // floats per head row; +4 spreads banks
@@ -157,7 +164,7 @@ template <int D, typename T, int NHT, bool F8>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const GqaParams p) {
-  using L = Layout<D, F8>;
+  using L = Layout<D, F8, NHT>;
   // the MMAs' operand type: q's type, except over E4M3 caches, whose codes convert to
   // fp16 in one instruction per pair (to bf16 it takes three more); q is then converted
   // to fp16 as it is loaded (exact for |q| in [2^-14, 65504])
@@ -372,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
     // This warp's ring fills are those with CTA-local index t = pres (mod kWP). A fill
     // holds kPPT consecutive pages of the portion (two for fp8 caches, so a stage moves
-    // as many bytes as a 16-bit page).
+    // as many bytes as a 16-bit page; two for 16-bit caches with four head subtiles).
     const int nfill = (npg + kPPT - 1) / kPPT;
     const int first = int(((pres - k) % kWP + kWP) % kWP);
     for (int i = first; i < nfill; i += kWP) {
@@ -506,6 +513,97 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
               a[3] &= vm_hi[hp];
               ptx::Mma<TM>::run(acc[mt + h], a, pb[hp][0], pb[hp][1]);
             }
+          }
+        }
+      } else if constexpr (kPPT == 2) {
+        // ---- two 16-bit pages A, B (B may be absent at a portion's end: its slots are
+        // then all stale and masked like the stale slots of a partial page)
+        const int pg0 = (pt.p0 + i * kPPT) * kPage;
+        const int vld[2] = {min(kPage, ctx - pg0),
+                            (i * kPPT + 1 < npg) ? min(kPage, ctx - pg0 - kPage) : 0};
+        const uint32_t kpg[2] = {kb, kb + 2 * L::kTileBytes};
+        const uint32_t vpg[2] = {kb + L::kTileBytes, kb + 3 * L::kTileBytes};
+        // S^T = K * Q^T for both pages: four independent accumulation chains (page x
+        // parity of the k-step)
+        float s[2][2][4] = {};
+#pragma unroll
+        for (int ks = 0; ks < kKS; ++ks) {
+          const int chunk = (ks & 3) * 2 + chunk_k;
+          const uint32_t off = (ks >> 2) * kBoxBytes + tok_k * 128 + ((chunk ^ (tok_k & 7)) << 4);
+#pragma unroll
+          for (int hp = 0; hp < 2; ++hp) {
+            uint32_t a[4];
+            ptx::ldsm_x4(kpg[hp] + off, a[0], a[1], a[2], a[3]);
+            ptx::Mma<T>::run(s[hp][ks & 1], a, qf[ks][0], qf[ks][1]);
+          }
+        }
+        float x[2][4];
+#pragma unroll
+        for (int hp = 0; hp < 2; ++hp) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[hp][e] = (s[hp][0][e] + s[hp][1][e]) * p.scale_log2;
+          const int ca = min(vld[hp], lim0 - pg0 - hp * kPage);
+          const int cb = min(vld[hp], lim1 - pg0 - hp * kPage);
+          if (ca < kPage || cb < kPage) {
+            if (r0 >= ca) x[hp][0] = -INFINITY;
+            if (r0 >= cb) x[hp][1] = -INFINITY;
+            if (r0 + 8 >= ca) x[hp][2] = -INFINITY;
+            if (r0 + 8 >= cb) x[hp][3] = -INFINITY;
+          }
+        }
+        float c0 = fmaxf(fmaxf(x[0][0], x[0][2]), fmaxf(x[1][0], x[1][2]));
+        float c1 = fmaxf(fmaxf(x[0][1], x[0][3]), fmaxf(x[1][1], x[1][3]));
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          c0 = fmaxf(c0, __shfl_xor_sync(kFull, c0, o));
+          c1 = fmaxf(c1, __shfl_xor_sync(kFull, c1, o));
+        }
+        const float mn0 = fmaxf(m0, c0), mn1 = fmaxf(m1, c1);
+        const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = ptx::exp2_approx(m0 - ms0), al1 = ptx::exp2_approx(m1 - ms1);
+        float pp[2][4];
+#pragma unroll
+        for (int hp = 0; hp < 2; ++hp) {
+          pp[hp][0] = ptx::exp2_approx(x[hp][0] - ms0);
+          pp[hp][1] = ptx::exp2_approx(x[hp][1] - ms1);
+          pp[hp][2] = ptx::exp2_approx(x[hp][2] - ms0);
+          pp[hp][3] = ptx::exp2_approx(x[hp][3] - ms1);
+        }
+        l0 = l0 * al0 + ((pp[0][0] + pp[0][2]) + (pp[1][0] + pp[1][2]));
+        l1 = l1 * al1 + ((pp[0][1] + pp[0][3]) + (pp[1][1] + pp[1][3]));
+        m0 = mn0;
+        m1 = mn1;
+        if (__any_sync(kFull, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+          for (int mt = 0; mt < kKS; ++mt) {
+            acc[mt][0] *= al0;
+            acc[mt][1] *= al1;
+            acc[mt][2] *= al0;
+            acc[mt][3] *= al1;
+          }
+        }
+        uint32_t pb[2][2], vm_lo[2], vm_hi[2];
+#pragma unroll
+        for (int hp = 0; hp < 2; ++hp) {
+          pb[hp][0] = ptx::movmatrix_trans(ptx::Mma<T>::pack(pp[hp][0], pp[hp][1]));
+          pb[hp][1] = ptx::movmatrix_trans(ptx::Mma<T>::pack(pp[hp][2], pp[hp][3]));
+          const int v = vld[hp];
+          vm_lo[hp] = (cq < v ? 0x0000ffffu : 0u) | (cq + 1 < v ? 0xffff0000u : 0u);
+          vm_hi[hp] = (cq + 8 < v ? 0x0000ffffu : 0u) | (cq + 9 < v ? 0xffff0000u : 0u);
+        }
+#pragma unroll
+        for (int mt = 0; mt < kKS; ++mt) {
+          const int chunk = (mt & 3) * 2 + chunk_v;
+          const uint32_t off = (mt >> 2) * kBoxBytes + tok_v * 128 + ((chunk ^ (tok_v & 7)) << 4);
+#pragma unroll
+          for (int hp = 0; hp < 2; ++hp) {
+            uint32_t a[4];
+            ptx::ldsm_x4_trans(vpg[hp] + off, a[0], a[1], a[2], a[3]);
+            a[0] &= vm_lo[hp];
+            a[1] &= vm_lo[hp];
+            a[2] &= vm_hi[hp];
+            a[3] &= vm_hi[hp];
+            ptx::Mma<T>::run(acc[mt], a, pb[hp][0], pb[hp][1]);
           }
         }
       } else {
@@ -828,7 +926,7 @@ template <int D, typename T, int NHT, bool F8>
 int launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const GqaParams& prm, int grid,
                cudaStream_t stream) {
   auto kern = gqa_decode_kernel<D, T, NHT, F8>;
-  using L = Layout<D, F8>;
+  using L = Layout<D, F8, NHT>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {

@@ -130,8 +130,9 @@ def test_ctx1_returns_first_value_row_exactly():
             assert np.array_equal(got[b, h], case.v_cache[blk, 0, h // 4])
 
 
-def test_poisoned_stale_slots_unused_blocks_and_table_entries():
-    case = _case(synth.FP16, 128, 32, 8, [37, 100, 5, 250], layout="permutation")
+@pytest.mark.parametrize("hkv", [8, 1])   # one page per ring stage; two (32-row segments)
+def test_poisoned_stale_slots_unused_blocks_and_table_entries(hkv):
+    case = _case(synth.FP16, 128, 32, hkv, [37, 100, 5, 250, 17], layout="permutation")
     clean = DeviceCase(case)
     out0, lse0 = _assert_close(case, clean)
     out0 = device_bits(out0)
