@@ -544,6 +544,7 @@ def time_config(args, workload, rank, world, dist, sampler, e2e=False, steps=Non
     replay_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     ms_per_step = reduce_step_time(statistics.median(replay_ms) / K, dist, "cuda")
     clocks = sampler.summary(t_win0, t_win1) if sampler else None
+    isolated_us = isolated_step_us(step, K, stream, torch)
     launches_per_step = 1 + (1 if _has_merge(plan, case) else 0) + (1 if with_append else 0)
 
     pk, pk_src = peaks()
@@ -581,6 +582,7 @@ def time_config(args, workload, rank, world, dist, sampler, e2e=False, steps=Non
                "median": statistics.median(replay_ms) / K * 1e3,
                "min": min(replay_ms) / K * 1e3, "max": max(replay_ms) / K * 1e3},
            "roofline": roof, "clocks": clocks, "launches_per_step": launches_per_step,
+           "isolated_us_per_step": isolated_us,
            "copies": copies, "kv_bytes": kv_bytes, "flops": flops,
            "plan": {"num_ctas": plan.num_ctas,
                     "max_splits": max(plan.num_splits(b) for b in range(case.batch))}}
@@ -590,6 +592,37 @@ def time_config(args, workload, rank, world, dist, sampler, e2e=False, steps=Non
                               kv_bytes, flops)
     del graph, caches
     return rec
+
+
+def isolated_step_us(step, K, stream, torch):
+    """Device time of one step on its own, outside the timed window (information only).
+
+    In the timed graph a decode grid may start while the step before it drains: the
+    library's decode and split-merge kernels allow programmatic dependent launch, so
+    consecutive steps overlap, as consecutive calls do when nothing else runs between them.
+    Here every step is preceded by a one-element kernel, after which a grid starts only
+    once everything before it has completed; the same K of those kernels alone are timed
+    as well and subtracted."""
+    sep = torch.zeros(1, device="cuda")
+    g_iso, g_sep = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_iso, stream=stream):
+        for i in range(K):
+            sep.add_(1.0)
+            step(i)
+    with torch.cuda.graph(g_sep, stream=stream):
+        for i in range(K):
+            sep.add_(1.0)
+    t_iso, t_sep = [], []
+    for _ in range(5):
+        for g, acc in ((g_iso, t_iso), (g_sep, t_sep)):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            acc.append(e0.elapsed_time(e1))
+    del g_iso, g_sep
+    return (statistics.median(t_iso) - statistics.median(t_sep)) / K * 1e3
 
 
 def time_e2e(args, case, step, stream, ins, out, lse, with_append, kv_bytes, flops):
@@ -689,6 +722,7 @@ def config_entry(rec, cpu):
          "tflops": rec["flops"] / (rec["ms_per_step"] * 1e-3) / 1e12,
          "steps_per_replay": rec["steps"], "replays": rec["replays"],
          "replay_us_per_step": rec["replay_us_per_step"],
+         "isolated_us_per_step": rec["isolated_us_per_step"],
          "roofline": roof, "frac_of_slower_roof": roof.get("frac_of_slower_roof", roof["frac"]),
          "clocks": rec["clocks"], "plan": rec["plan"],
          "l2": f"steps rotate over {min(rec['copies'], rec['steps'])} copies of the caches "
@@ -744,9 +778,13 @@ def run_gpu(args, workload, rank, world, local_rank):
             "roofline": head["roofline"], "cpu_baseline": cpu, "e2e": head["e2e"],
             "gpu_launches": args.steps * head["launches_per_step"], "clocks": head["clocks"],
             "replays": head["replays"], "replay_us_per_step": head["replay_us_per_step"],
+            "isolated_us_per_step": head["isolated_us_per_step"],
             "timing": "value: K steps captured in one CUDA graph, replayed R times (device "
-                      "events per replay, median); roofline.event_us_per_call: events around "
-                      "each eager call",
+                      "events per replay, median); consecutive steps overlap through "
+                      "programmatic dependent launch. isolated_us_per_step: each step after a "
+                      "one-element kernel that lets no grid start early (that kernel's own "
+                      "time subtracted), outside the timed window; roofline.event_us_per_call: "
+                      "events around each eager call",
             "plan": head["plan"], "per_config": per_config}
     print(json.dumps(line))
 

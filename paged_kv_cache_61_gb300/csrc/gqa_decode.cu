@@ -54,9 +54,8 @@ constexpr int kConsumerWarps = 4;
 // Two producer warps take the ring fills alternately: one warp's per-fill chain (barrier
 // wait, expect-tx, tensor-copy issue) took longer than the consumers needed per fill.
 constexpr int kProducerWarps = 2;
-constexpr int kThreads = (kConsumerWarps + kProducerWarps) * 32;
 // Ring stages: a multiple of the consumer warps, so stage s is only ever read by
-// the warps whose tiles are t = s (mod kConsumerWarps / NHT), each of which takes
+// the warps whose fills are t = s (mod consumer warps / NHT), each of which takes
 // every fill of that stage in order (the parity waits rely on this).
 #ifndef PDA_GQA_STAGES
 #define PDA_GQA_STAGES 8
@@ -64,6 +63,21 @@ constexpr int kThreads = (kConsumerWarps + kProducerWarps) * 32;
 #ifndef PDA_GQA_CTAS_PER_SM
 #define PDA_GQA_CTAS_PER_SM 2
 #endif
+#ifndef PDA_GQA_WIDE32
+#define PDA_GQA_WIDE32 1
+#endif
+// Warp roles. Segments of 25-32 rows on 16-bit caches (four head subtiles) run eight
+// consumer warps, two per subtile taking alternate stages, in one CTA per SM: with four,
+// one warp per subtile walks every page of the CTA's range, and a single long sequence
+// (MQA) then waits on that one warp's chain of dependent MMAs and shuffles per page.
+// B=1, ctx 32K, MQA: a step on its own 26.1 -> 21.1 us (back to back unchanged, 5.8 us);
+// B=64, ctx 1K, MQA 12.06 -> 11.20 us back to back.
+template <int NHT, bool F8>
+struct Roles {
+  static constexpr int kConsumer = (PDA_GQA_WIDE32 && !F8 && NHT == 4) ? 8 : kConsumerWarps;
+  static constexpr int kThreads = (kConsumer + kProducerWarps) * 32;
+  static constexpr int kCtasPerSm = kConsumer == 8 ? 1 : PDA_GQA_CTAS_PER_SM;
+};
 #ifndef PDA_GQA_STAGES_F8
 #define PDA_GQA_STAGES_F8 8
 #endif
@@ -116,16 +130,18 @@ template <int D, bool F8, int NHT>
 struct Layout {
   static constexpr int kDBlocks = D / 64;
   static constexpr int kPPT = (F8 || NHT == 4) ? 2 : 1;    // pages per ring fill
-  static constexpr int kStages = F8 ? kStagesF8 : (kPPT == 2 ? kStages16 / 2 : kStages16);
+  static constexpr int kCW = Roles<NHT, F8>::kConsumer;     // consumer warps
+  static constexpr int kStages =
+      F8 ? kStagesF8 : (kPPT == 2 && kCW == 4 ? kStages16 / 2 : kStages16);
   static constexpr int kTileBytes = F8 ? kPage * D : kDBlocks * kBoxBytes;  // page, tensor
   static constexpr int kStageBytes = 2 * kPPT * kTileBytes;
   static constexpr int kMergeStride = D + 4;  // floats per head row; +4 spreads banks
   static constexpr int kMergeWarpFloats = 8 * kMergeStride + 16;
   static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kMergeBytes = kConsumerWarps * kMergeWarpFloats * 4;
+  static constexpr int kMergeBytes = kCW * kMergeWarpFloats * 4;
   static constexpr int kBarBytes = 2 * kStages * 8 + 16;
   static constexpr int kSmemBytes = 1024 + kRingBytes + kMergeBytes + kBarBytes;
-  static_assert(kStages % kConsumerWarps == 0, "each stage needs a fixed set of consumer warps");
+  static_assert(kStages % kCW == 0, "each stage needs a fixed set of consumer warps");
 };
 
 // Byte offset of 16-byte chunk `ch` of row `r` in a swizzled fp8 tile of 16 rows of D
@@ -161,7 +177,7 @@ __device__ __forceinline__ uint32_t to_mma_pair(uint32_t w) {
 
 // ------------------------------------------------------------------ the kernel
 template <int D, typename T, int NHT, bool F8>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+__global__ void __launch_bounds__(Roles<NHT, F8>::kThreads, Roles<NHT, F8>::kCtasPerSm)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const GqaParams p) {
   using L = Layout<D, F8, NHT>;
@@ -171,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   using TM = std::conditional_t<F8, __half, T>;
   constexpr int kStages = L::kStages;
   constexpr int kPPT = L::kPPT;
-  constexpr int kWP = kConsumerWarps / NHT;  // consumer warps sharing one head subtile
+  constexpr int kWP = L::kCW / NHT;  // consumer warps sharing one head subtile
   constexpr int kKS = D / 16;                // k-steps of S^T and m-tiles of O^T
 
   extern __shared__ uint8_t smem_raw[];
@@ -205,11 +221,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   Walker walk;
   walker_init(walk, spec, g_lo, lane);
 
-  if (warp >= kConsumerWarps) {
+  if (warp >= L::kCW) {
     // ============================== producer warps ==============================
     // Both walk every fill of the CTA's range; producer pw issues the fills f with
     // f = pw (mod kProducerWarps) and skips the others.
-    const int pw = warp - kConsumerWarps;
+    const int pw = warp - L::kCW;
     if (lane == 0) {
       ptx::prefetch_tensormap(&tm_k);
       ptx::prefetch_tensormap(&tm_v);
@@ -716,14 +732,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       mw[8 * L::kMergeStride + 8 + cq] = l0;
       mw[8 * L::kMergeStride + 8 + cq + 1] = l1;
     }
-    ptx::named_barrier_sync(1, kConsumerWarps * 32);
+    ptx::named_barrier_sync(1, L::kCW * 32);
 
     // ---- merge the warps of each head subtile; write final rows or this CTA's split slot
     const bool whole = (pt.p0 == 0 && pt.p1 == pt.np);
     const int slot = piece_slot(pt.seg_start, g_lo);
     const int64_t slot_row = (int64_t(blockIdx.x) * 2 + slot) * p.group;
     constexpr int kChunks = D / 8;
-    for (int idx = tid; idx < nrows * kChunks; idx += kConsumerWarps * 32) {
+    for (int idx = tid; idx < nrows * kChunks; idx += L::kCW * 32) {
       const int j = idx / kChunks;
       const int dc = idx - j * kChunks;
       const int hs = j >> 3, n = j & 7;
@@ -771,16 +787,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const int pieces = int(c1 - c0 + 1);
       if (pieces <= p.heavy_min) {
         __threadfence();
-        ptx::named_barrier_sync(1, kConsumerWarps * 32);
+        ptx::named_barrier_sync(1, L::kCW * 32);
         int32_t* counter = p.counters + int64_t(pt.b) * p.segs_per_seq + pt.seg;
         if (tid == 0) {
           const int prev = aborted ? -1 : atomicAdd(counter, 1);
           flags[1] = (prev == pieces - 1) ? 1 : 0;
         }
-        ptx::named_barrier_sync(1, kConsumerWarps * 32);
+        ptx::named_barrier_sync(1, L::kCW * 32);
         if (flags[1]) {
           __threadfence();
-          for (int idx = tid; idx < nrows * kChunks; idx += kConsumerWarps * 32) {
+          for (int idx = tid; idx < nrows * kChunks; idx += L::kCW * 32) {
             const int j = idx / kChunks;
             const int dc = idx - j * kChunks;
             // online merge over the pieces, four at a time with independent loads
@@ -829,7 +845,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
     }
     // the merge area is rewritten by the next portion
-    ptx::named_barrier_sync(1, kConsumerWarps * 32);
+    ptx::named_barrier_sync(1, L::kCW * 32);
   }
 }
 
@@ -936,7 +952,7 @@ int launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const GqaParams& pr
   if (attr_err != cudaSuccess) return attr_err;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(unsigned(grid));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(Roles<NHT, F8>::kThreads);
   cfg.dynamicSmemBytes = L::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -998,7 +1014,14 @@ bool gqa_supported(const pda_problem& p, std::string* why) {
   return true;
 }
 
-int gqa_ctas_per_sm(const pda_problem&) { return kCtasPerSm; }
+int gqa_ctas_per_sm(const pda_problem& p) {
+  // the launcher's head-subtile count of a segment (rows in chunks of at most 32)
+  const int64_t rows = int64_t(p.seq_len_q > 1 ? p.seq_len_q : 1) * (p.num_q_heads / p.num_kv_heads);
+  const int64_t group = (rows + (rows + 31) / 32 - 1) / ((rows + 31) / 32);
+  const bool four = (group + 7) / 8 > 2;
+  const bool f8 = p.kv_format == PDA_KV_FP8_E4M3;
+  return four ? (f8 ? Roles<4, true>::kCtasPerSm : Roles<4, false>::kCtasPerSm) : kCtasPerSm;
+}
 
 int launch_gqa_decode(const Plan& plan, const GqaArgs& a, const Workspace& ws, void* stream) {
   const pda_problem& pr = plan.prob;
