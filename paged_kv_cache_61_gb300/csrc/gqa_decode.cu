@@ -66,15 +66,15 @@ constexpr int kProducerWarps = 2;
 #ifndef PDA_GQA_WIDE32
 #define PDA_GQA_WIDE32 1
 #endif
-// Warp roles. Segments of 25-32 rows on 16-bit caches (four head subtiles) run eight
-// consumer warps, two per subtile taking alternate stages, in one CTA per SM: with four,
-// one warp per subtile walks every page of the CTA's range, and a single long sequence
-// (MQA) then waits on that one warp's chain of dependent MMAs and shuffles per page.
-// B=1, ctx 32K, MQA: a step on its own 26.1 -> 21.1 us (back to back unchanged, 5.8 us);
-// B=64, ctx 1K, MQA 12.06 -> 11.20 us back to back.
+// Warp roles. Segments of 25-32 rows (four head subtiles) run eight consumer warps, two
+// per subtile taking alternate stages, in one CTA per SM: with four, one warp per subtile
+// walks every page of the CTA's range, and a single long sequence (MQA) then waits on that
+// one warp's chain of dependent MMAs and shuffles per page. B=1, ctx 32K, MQA: a step on
+// its own 26.1 -> 21.1 us with 16-bit caches, 29.1 -> 24.0 us with fp8 (back to back
+// unchanged, 5.8 and 6.8 us); B=64, ctx 1K, MQA 12.06 -> 11.20 us back to back.
 template <int NHT, bool F8>
 struct Roles {
-  static constexpr int kConsumer = (PDA_GQA_WIDE32 && !F8 && NHT == 4) ? 8 : kConsumerWarps;
+  static constexpr int kConsumer = (PDA_GQA_WIDE32 && NHT == 4) ? 8 : kConsumerWarps;
   static constexpr int kThreads = (kConsumer + kProducerWarps) * 32;
   static constexpr int kCtasPerSm = kConsumer == 8 ? 1 : PDA_GQA_CTAS_PER_SM;
 };
@@ -1019,8 +1019,7 @@ int gqa_ctas_per_sm(const pda_problem& p) {
   const int64_t rows = int64_t(p.seq_len_q > 1 ? p.seq_len_q : 1) * (p.num_q_heads / p.num_kv_heads);
   const int64_t group = (rows + (rows + 31) / 32 - 1) / ((rows + 31) / 32);
   const bool four = (group + 7) / 8 > 2;
-  const bool f8 = p.kv_format == PDA_KV_FP8_E4M3;
-  return four ? (f8 ? Roles<4, true>::kCtasPerSm : Roles<4, false>::kCtasPerSm) : kCtasPerSm;
+  return four ? Roles<4, false>::kCtasPerSm : kCtasPerSm;
 }
 
 int launch_gqa_decode(const Plan& plan, const GqaArgs& a, const Workspace& ws, void* stream) {
