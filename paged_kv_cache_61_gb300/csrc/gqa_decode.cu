@@ -17,11 +17,12 @@
 //    address is formed by the TMA unit, so no 32-bit product phys*stride exists)
 //    of each page's K and V into a ring of shared-memory stages with 128-byte
 //    swizzle. A stage holds one page, or two (fp8 caches; 25-32 rows per segment).
-//  * Four consumer warps take stages round-robin (by CTA-local fill index, so a
-//    ring stage always has the same consumers). Each page is one m16n8k16
-//    tile in the transposed ("keys on M") orientation the FlashMLA-ETAP README
-//    describes for Hopper WGMMA, here on warp MMA: S^T[16 tokens x 8 heads] =
-//    K * Q^T, so a group of 4 heads wastes half an MMA instead of 3/4 of one.
+//  * Four consumer warps (eight for 25-32 rows per segment) take stages round-robin
+//    (by CTA-local fill index, so a ring stage always has the same consumers).
+//    Each page is one m16n8k16 tile in the transposed ("keys on M") orientation
+//    the FlashMLA-ETAP README describes for Hopper WGMMA, here on warp MMA:
+//    S^T[16 tokens x 8 heads] = K * Q^T, so a group of 4 heads wastes half an MMA
+//    instead of 3/4 of one.
 //    The online softmax runs down each column (head) with three shuffles;
 //    P^T is turned into the B fragment of O^T += V^T * P^T with movmatrix.
 //  * Stale slots of a partial last page are removed by selects on the scores
@@ -121,11 +122,12 @@ struct GqaParams {
 // a stage carries as many bytes as a 16-bit one and the per-stage costs (producer
 // issue, barrier waits, the softmax reductions) are paid once per two pages.
 // 16-bit caches with four head subtiles (25-32 rows per segment) take two pages per stage
-// as well, in half as many stages: each consumer warp then owns one subtile and walks
-// every page, and two pages per step give its chain of dependent MMAs, shuffles and
-// exponentials twice the independent work (B=1, ctx 32K, MQA: 7.01 -> 5.78 us). With
-// fewer rows the warps share a subtile's pages, and one page per stage is faster (B=64,
-// ctx 1K: 37.98 against 38.69 us with two).
+// as well: a consumer warp owns one subtile and walks every other stage of the range, and
+// two pages per step give its chain of dependent MMAs, shuffles and exponentials twice
+// the independent work (B=1, ctx 32K, MQA with four consumer warps and four stages: 7.01
+// -> 5.78 us; the eight consumer warps of Roles take eight such stages). With fewer rows
+// the warps share a subtile's pages, and one page per stage is faster (B=64, ctx 1K:
+// 37.98 against 38.69 us with two).
 template <int D, bool F8, int NHT>
 struct Layout {
   static constexpr int kDBlocks = D / 64;
