@@ -73,7 +73,7 @@ constexpr int kProducerWarps = 2;
 // one warp's chain of dependent MMAs and shuffles per page. B=1, ctx 32K, MQA: a step on
 // its own 26.1 -> 21.1 us with 16-bit caches, 29.1 -> 24.0 us with fp8 (back to back
 // unchanged, 5.8 and 6.8 us); B=64, ctx 1K, MQA 12.06 -> 11.20 us back to back.
-template <int NHT, bool F8>
+template <int NHT>
 struct Roles {
   static constexpr int kConsumer = (PDA_GQA_WIDE32 && NHT == 4) ? 8 : kConsumerWarps;
   static constexpr int kThreads = (kConsumer + kProducerWarps) * 32;
@@ -132,7 +132,7 @@ template <int D, bool F8, int NHT>
 struct Layout {
   static constexpr int kDBlocks = D / 64;
   static constexpr int kPPT = (F8 || NHT == 4) ? 2 : 1;    // pages per ring fill
-  static constexpr int kCW = Roles<NHT, F8>::kConsumer;     // consumer warps
+  static constexpr int kCW = Roles<NHT>::kConsumer;     // consumer warps
   static constexpr int kStages =
       F8 ? kStagesF8 : (kPPT == 2 && kCW == 4 ? kStages16 / 2 : kStages16);
   static constexpr int kTileBytes = F8 ? kPage * D : kDBlocks * kBoxBytes;  // page, tensor
@@ -179,7 +179,7 @@ __device__ __forceinline__ uint32_t to_mma_pair(uint32_t w) {
 
 // ------------------------------------------------------------------ the kernel
 template <int D, typename T, int NHT, bool F8>
-__global__ void __launch_bounds__(Roles<NHT, F8>::kThreads, Roles<NHT, F8>::kCtasPerSm)
+__global__ void __launch_bounds__(Roles<NHT>::kThreads, Roles<NHT>::kCtasPerSm)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const GqaParams p) {
   using L = Layout<D, F8, NHT>;
@@ -954,7 +954,7 @@ int launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const GqaParams& pr
   if (attr_err != cudaSuccess) return attr_err;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(unsigned(grid));
-  cfg.blockDim = dim3(Roles<NHT, F8>::kThreads);
+  cfg.blockDim = dim3(Roles<NHT>::kThreads);
   cfg.dynamicSmemBytes = L::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -1021,7 +1021,7 @@ int gqa_ctas_per_sm(const pda_problem& p) {
   const int64_t rows = int64_t(p.seq_len_q > 1 ? p.seq_len_q : 1) * (p.num_q_heads / p.num_kv_heads);
   const int64_t group = (rows + (rows + 31) / 32 - 1) / ((rows + 31) / 32);
   const bool four = (group + 7) / 8 > 2;
-  return four ? Roles<4, false>::kCtasPerSm : kCtasPerSm;
+  return four ? Roles<4>::kCtasPerSm : kCtasPerSm;
 }
 
 int launch_gqa_decode(const Plan& plan, const GqaArgs& a, const Workspace& ws, void* stream) {
