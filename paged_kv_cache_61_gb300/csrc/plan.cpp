@@ -217,6 +217,26 @@ extern "C" PDA_API pda_status pda_plan_create(pda_plan** out, const pda_problem*
             if (m * S * 2 <= q * 3) q = m * S;
           }
         }
+        // At most one tile per SM the step is latency bound, and a split-merge launch
+        // after the decode grid costs more than the extra pieces save: raise the share
+        // until every segment has no more pieces than the decode kernel merges itself
+        // (B=4, ctx U{1..256}, Hkv=2: 18 CTAs and a merge launch 8.95 us, 12 CTAs and
+        // one launch 6.06 us).
+        if (plan->total_tiles <= num_sms) {
+          auto max_pieces = [&](int64_t share) {
+            int64_t worst = 1, start = 0;
+            for (int32_t b = 0; b < p.batch; ++b) {
+              const int64_t np = pda::cdiv(ctx_host[b], p.page_size);
+              for (int32_t s = 0; s < plan->segs_per_seq; ++s) {
+                const int64_t s0 = start + s * np;
+                worst = std::max(worst, (s0 + np - 1) / share - s0 / share + 1);
+              }
+              start += np * plan->segs_per_seq;
+            }
+            return worst;
+          };
+          while (max_pieces(q) > 4) ++q;
+        }
       }
     }
     q = std::max(q, pda::cdiv(plan->total_tiles, pda::kMaxCtas));

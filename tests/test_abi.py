@@ -273,6 +273,21 @@ def test_planner_merges_few_pieces_in_kernel():
     assert 2 <= p.num_splits(0) <= 4 and p.num_launches == 1
 
 
+def test_planner_keeps_a_tiny_problem_in_one_launch():
+    # at most one tile per SM (B=4, ctx up to 242, Hkv=2: 72 tiles): the share is raised
+    # until no segment has more pieces than the decode kernel merges itself
+    lens = [206, 242, 2, 81]
+    p = _plan(batch=4, num_q_heads=8, num_kv_heads=2, head_dim_qk=64, head_dim_v=64,
+              page_size=16, max_blocks_per_seq=16, num_blocks=64, context_lens=lens,
+              num_sms=152)
+    assert p.num_launches == 1 and max(p.num_splits(b) for b in range(4)) <= 4
+    # a forced CTA count is kept as asked, merge launch included
+    f = _plan(batch=4, num_q_heads=8, num_kv_heads=2, head_dim_qk=64, head_dim_v=64,
+              page_size=16, max_blocks_per_seq=16, num_blocks=64, context_lens=lens,
+              num_sms=152, force_num_ctas=36)
+    assert f.num_ctas == 36 and f.num_launches == 2
+
+
 def test_planner_gives_whole_segments_to_a_uniform_batch():
     # B=64, ctx 1024, Hkv=8: 512 segments of 64 pages, two whole segments per CTA
     p = _plan(batch=64, num_q_heads=32, num_kv_heads=8, head_dim_qk=128, head_dim_v=128,

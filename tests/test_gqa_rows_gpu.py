@@ -85,14 +85,14 @@ def test_long_sequence_goes_through_the_split_merge(hq, hkv, s):
 def test_chunks_agree_with_single_segment_heads():
     # The first 32 heads of a 64-head MQA problem form its first row chunk, which is the
     # whole of a 32-head problem on the same caches, lengths and tables. With the same
-    # piece boundaries (automatic plans: the share is 9 pages either way; or one page per
+    # piece boundaries (a share of 9 pages either way: 14 and 7 CTAs; or one page per
     # CTA) the two compute those rows with the same arithmetic: bit-identical outputs.
     big = _case(synth.BF16, 128, 64, 1, [900, 40, 3], seed=5)
     small = synth.DecodeCase(**{**big.__dict__})
     small.q = big.q[:, :32].copy()
     small.num_q_heads = 32
     pages = sum((int(c) + 15) // 16 for c in big.context_lens)
-    for f_big, f_small in ((0, 0), (2 * pages, pages)):
+    for f_big, f_small in ((14, 7), (2 * pages, pages)):
         db, ds = DeviceCase(big, force_num_ctas=f_big), DeviceCase(small, force_num_ctas=f_small)
         assert db.plan.num_splits(0) == ds.plan.num_splits(0) > 1
         ob, lb = db.run()
