@@ -322,9 +322,21 @@ PDA_API pda_status pda_kv_append_fp8(const void* k_new, const void* v_new, void*
                                      const int32_t* block_tables, const int32_t* context_lens,
                                      const pda_plan* plan, void* workspace, pda_stream_t stream);
 
+/* pda_mla_append takes plans of 16-bit record caches (kv_format PDA_KV_SAME_AS_Q); an
+ * E4M3 plan is refused with PDA_ERR_INVALID_ARG. */
 PDA_API pda_status pda_mla_append(const void* kv_new, void* kv_cache,
                                   const int32_t* block_tables, const int32_t* context_lens,
                                   const pda_plan* plan, void* workspace, pda_stream_t stream);
+
+/* pda_mla_append into an E4M3 record cache (MLA plan with kv_format PDA_KV_FP8_E4M3, the
+ * variants page's fp8 latent): kv_new [B, S, Dqk] in the plan's dtype is stored as the
+ * E4M3 codes of x / kv_scale into kv_cache [num_blocks, 64, Dqk] bytes, with the
+ * quantization of pda_kv_append_fp8. kv_scale (finite, nonzero) is the record cache's
+ * dequantization scale, the one mla_decode_fp8 takes. */
+PDA_API pda_status pda_mla_append_fp8(const void* kv_new, void* kv_cache, float kv_scale,
+                                      const int32_t* block_tables, const int32_t* context_lens,
+                                      const pda_plan* plan, void* workspace,
+                                      pda_stream_t stream);
 
 /*
  * Physical block pool behind the block tables ("From MHA to MLA", section 5: requests'

@@ -253,6 +253,22 @@ extern "C" PDA_API pda_status pda_mla_append(const void* kv_new, void* kv_cache,
                                              const int32_t* context_lens, const pda_plan* plan,
                                              void* workspace, pda_stream_t stream) {
   pda::clear_error();
+  if (plan != nullptr && plan->prob.kv_format != PDA_KV_SAME_AS_Q)
+    return fail(PDA_ERR_INVALID_ARG, "the plan's record cache is fp8: call pda_mla_append_fp8");
   return append_call(PDA_KIND_MLA, kv_new, nullptr, kv_cache, nullptr, 1.f, 1.f, block_tables,
                      context_lens, plan, workspace, stream);
+}
+
+extern "C" PDA_API pda_status pda_mla_append_fp8(const void* kv_new, void* kv_cache,
+                                                 float kv_scale, const int32_t* block_tables,
+                                                 const int32_t* context_lens,
+                                                 const pda_plan* plan, void* workspace,
+                                                 pda_stream_t stream) {
+  pda::clear_error();
+  if (plan != nullptr && plan->prob.kv_format != PDA_KV_FP8_E4M3)
+    return fail(PDA_ERR_INVALID_ARG, "the plan's record cache is not fp8: call pda_mla_append");
+  if (!std::isfinite(kv_scale) || kv_scale == 0.f)
+    return fail(PDA_ERR_INVALID_ARG, "kv_scale must be finite and nonzero");
+  return append_call(PDA_KIND_MLA, kv_new, nullptr, kv_cache, nullptr, kv_scale, 1.f,
+                     block_tables, context_lens, plan, workspace, stream);
 }

@@ -59,6 +59,7 @@ def _declare(lib):
         "pda_no_alloc_read_device_error": (I32, [P, P]),
         "pda_kv_append": (I32, [P, P, P, P, P, P, P, P, P]),
         "pda_kv_append_fp8": (I32, [P, P, P, P, F32, F32, P, P, P, P, P]),
+        "pda_mla_append_fp8": (I32, [P, P, F32, P, P, P, P, P]),
         "pda_mla_append": (I32, [P, P, P, P, P, P, P]),
         "pda_pool_create": (I32, [ctypes.POINTER(P), I64]),
         "pda_pool_destroy": (None, [P]),
@@ -257,6 +258,14 @@ def mla_append(kv_new, kv_cache, block_tables, context_lens, plan: Plan, workspa
     _check(lib().pda_mla_append(_ptr(kv_new), _ptr(kv_cache), _ptr(block_tables),
                                 _ptr(context_lens), plan.handle, _ptr(workspace),
                                 _stream(stream)), "pda_mla_append")
+
+
+def mla_append_fp8(kv_new, kv_cache, kv_scale: float, block_tables, context_lens, plan: Plan,
+                   workspace, stream=None):
+    """mla_append into an E4M3 record cache (uint8 codes of value / kv_scale)."""
+    _check(lib().pda_mla_append_fp8(_ptr(kv_new), _ptr(kv_cache), float(kv_scale),
+                                    _ptr(block_tables), _ptr(context_lens), plan.handle,
+                                    _ptr(workspace), _stream(stream)), "pda_mla_append_fp8")
 
 
 class BlockPool:

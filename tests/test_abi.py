@@ -181,6 +181,15 @@ def test_fp8_plan_validation():
             pda.mla_decode_fp8(4096, 8192, ks, 64, 128, 0.07, 4096, None, plan, 1 << 20,
                                stream=0)
         assert e.value.status == pda.PDA_ERR_INVALID_ARG
+    # appends: the 16-bit record append refuses an fp8 plan (it would store codes with a
+    # scale of 1), the fp8 one a 16-bit plan and a scale that is not finite or is zero
+    with pytest.raises(pda.PdaError) as e:
+        pda.mla_append(4096, 8192, 64, 128, f8m, 1 << 20, stream=0)
+    assert e.value.status == pda.PDA_ERR_INVALID_ARG
+    for plan, ks in ((m16, 1.0), (f8m, float("inf")), (f8m, 0.0)):
+        with pytest.raises(pda.PdaError) as e:
+            pda.mla_append_fp8(4096, 8192, ks, 64, 128, plan, 1 << 20, stream=0)
+        assert e.value.status == pda.PDA_ERR_INVALID_ARG
     f8 = _plan(batch=0, context_lens=[], kv_format=pda.PDA_KV_FP8_E4M3)
     pda.paged_decode_attn_fp8(0, 0, 0, 1.0, 1.0, 0, 0, 0.125, 0, None, f8, 0, stream=0)
 

@@ -88,6 +88,43 @@ def test_mla_append_is_bit_exact(latent, s):
         case.kv_cache, new, case.block_tables, case.context_lens, 64, s))
 
 
+@pytest.mark.parametrize("latent", [512, 256])
+@pytest.mark.parametrize("s", [1, 2])
+def test_mla_fp8_append_quantizes_like_the_oracle_and_decodes(latent, s):
+    # E4M3 record cache (the variants page's fp8 latent): the appended records are the
+    # oracle's codes of value / kv_scale, bit for bit, and the decode that follows reads them
+    case = synth.make_mla_case(batch=3, num_q_heads=16, dtype=synth.BF16,
+                               context_lens=[64 + s, 65, 700], latent_dim=latent, seed=3,
+                               seq_len_q=s, kv_format=synth.FP8_E4M3)
+    dc = DeviceCase(case)
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((3, s, latent + 64)).astype(np.float32)
+    # rope dims far above 448 * kv_scale (saturated codes) on a record whose latent is
+    # clipped to |x| <= 2: its score may dominate, and an output near 4 would round in bf16
+    # by more than the 1e-2 tolerance
+    x[0, 0, :latent] = np.clip(x[0, 0, :latent], -2.0, 2.0)
+    x[0, 0, latent:] *= 1000.0
+    x[1, -1, :128] *= 1e-4                      # E4M3 subnormals and zeros
+    new = synth.float32_to_bits(x, synth.BF16)
+    pda.mla_append_fp8(to_device_16(new, synth.BF16), dc.kv, case.k_scale, dc.tables, dc.ctx,
+                       dc.plan, dc.ws)
+    torch.cuda.synchronize()
+    codes = oracle.quantize_e4m3(new, synth.BF16, case.k_scale)
+    assert (codes & 0x7F == 0x7E).any() and ((codes & 0x78) == 0).sum() > 16
+    want = oracle.append_tokens(case.kv_cache, codes, case.block_tables, case.context_lens,
+                                64, s)
+    np.testing.assert_array_equal(_bits(dc.kv), want)
+    assert pda.read_device_error(dc.ws) == 0
+    out, lse = dc.run()
+    torch.cuda.synchronize()
+    fn = oracle.mla_decode_mtp if s > 1 else oracle.mla_decode
+    ref_out, ref_lse = fn(case.q, want, case.block_tables, case.context_lens, case.scale, 64,
+                          case.dtype, head_dim_v=latent, kv_format=synth.FP8_E4M3,
+                          kv_scale=case.k_scale)
+    assert np.abs(out.float().cpu().numpy() - ref_out).max() <= TOL_OUT[case.dtype]
+    assert np.abs(lse.cpu().numpy() - ref_lse).max() <= TOL_LSE
+
+
 def test_bad_table_entry_is_flagged_and_skipped():
     case = synth.make_gqa_case(batch=3, num_q_heads=4, num_kv_heads=1, head_dim=64,
                                dtype=synth.FP16, context_lens=[20, 33, 5], seed=7)
