@@ -59,7 +59,8 @@ KERNEL_SOURCES = {"gqa": ["gqa_decode.cu", "ptx.cuh", "tile_walk.cuh"],
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 METRIC = "paged decode attn achieved HBM GB/s (% of GB300 peak), μs/step; MLA TFLOPS"
 # decode steps that append each sequence's new token first (see time_config)
-STEP_WORKLOADS = ("gqa_b64_ctx1k_step", "gqa_b64_ctx1k_fp8_step", "mla_b16_ctx64k_h16_step")
+STEP_WORKLOADS = ("gqa_b64_ctx1k_step", "gqa_b64_ctx1k_fp8_step", "mla_b16_ctx64k_h16_step",
+                  "mla_b16_ctx64k_h16_fp8_step")
 
 
 # ---------------------------------------------------------------- helpers
@@ -480,6 +481,8 @@ def time_config(args, workload, rank, world, dist, sampler, e2e=False, steps=Non
                               ws, stream)
         elif case.kind == "gqa":
             pda.kv_append(kn, vn, kc, vc, tables_, ctx_, plan, ws, stream)
+        elif fp8:
+            pda.mla_append_fp8(kn, kc, case.k_scale, tables_, ctx_, plan, ws, stream)
         else:
             pda.mla_append(kn, kc, tables_, ctx_, plan, ws, stream)
 
