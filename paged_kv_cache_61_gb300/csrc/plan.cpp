@@ -136,8 +136,9 @@ extern "C" PDA_API pda_status pda_plan_create(pda_plan** out, const pda_problem*
     plan->segs_per_seq = p.num_kv_heads * plan->row_chunks;
     plan->head_subtiles = (plan->group + 7) / 8;
     ctas_per_sm = pda::gqa_ctas_per_sm(p);
-    // A split piece writes a 4·G·D-byte fp32 partial and reads 64·D bytes per tile: at
-    // least G/4 + 1 tiles keep the partial under a quarter of what the piece reads. (A
+    // A split piece writes a 4·group·D-byte fp32 partial (group: the segment's rows) and
+    // reads 64·D bytes per tile: at least group/4 + 1 tiles keep the partial under a
+    // quarter of what the piece reads. (A
     // starting floor: the cap on pieces per segment below and the aligned-piece search
     // may raise or lower a CTA's share from there.)
     min_tiles_per_cta = std::max<int64_t>(4, plan->group / 4 + 1);
